@@ -112,14 +112,26 @@ def stream_f64(seed, stream, B, pos0, T, H, D, heads=None, batches=None) -> np.n
     return bf16_bits_to_f64(stream_bits(seed, stream, B, pos0, T, H, D, heads, batches))
 
 
-def head_stream_f64(seed, stream, b, head, pos0, T, D, chunk=1 << 16) -> np.ndarray:
-    """float64 [T, D] of one (batch, head), generated chunk by chunk (long contexts)."""
+def head_stream_f64(seed, stream, b, head, pos0, T, D, chunk=1 << 16, workers=1) -> np.ndarray:
+    """float64 [T, D] of one (batch, head), generated chunk by chunk (long contexts).
+
+    ``workers`` > 1 generates chunks on that many threads (numpy releases the GIL)."""
     out = np.empty((T, D), dtype=np.float64)
-    for c0 in range(0, T, chunk):
+
+    def one(c0):
         c1 = min(T, c0 + chunk)
         keys = element_keys(seed, stream, b, (pos0 + np.arange(c0, c1))[:, None], head,
                             np.arange(D)[None, :])
         out[c0:c1] = bf16_bits_to_f64(f32_to_bf16_bits(keys_to_f32(keys)))
+
+    starts = list(range(0, T, chunk))
+    if workers > 1 and len(starts) > 1:
+        from concurrent.futures import ThreadPoolExecutor
+        with ThreadPoolExecutor(workers) as ex:
+            list(ex.map(one, starts))
+    else:
+        for c0 in starts:
+            one(c0)
     return out
 
 

@@ -1,0 +1,173 @@
+/*
+ * duo_attn.h -- C ABI of a GB300 (sm_103a) library for mixed-head causal attention
+ * in long-context serving: retrieval heads over a full KV cache, streaming heads
+ * over a sink + ring-buffer cache.
+ *
+ * What the operations compute (sources are the pages this library restates):
+ *
+ *   DuoAttention README (mit-han-lab/duo-attention), Abstract: a few attention heads
+ *   ("retrieval heads") need full attention over every token and keep a full KV
+ *   cache; the others ("streaming heads") look mostly at the attention sinks and
+ *   the recent tokens and keep a constant-size cache. With S = sink_size and
+ *   R = recent_size (quick start: S = 64, R = 256), query position i of a head sees
+ *   key position j when
+ *       retrieval:  j <= i
+ *       streaming:  j <= i  and  (j < S  or  i - j < R)
+ *   and the output is softmax(q.k / sqrt(head_dim)) over the visible keys, times v.
+ *
+ *   vLLM issue "Could you support Attention Sink?", block tables and its option 3:
+ *   sink tokens stay in their own slots and later tokens wrap around a circular
+ *   buffer, so nothing is ever moved. Token t is stored in slot t if t < S, else in
+ *   slot S + ((t - S) mod R).
+ *
+ *   transformers pull request "[WIP] Dynamic length in static cache": a decode step
+ *   attends only to the positions written so far, never to the unused capacity.
+ *
+ * Conventions for every call:
+ *   - All tensors are caller-owned device memory (e.g. torch tensors); the library
+ *     allocates no device memory and never synchronises the device, except in
+ *     duo_device_error().
+ *   - bf16 means IEEE-754 binary16 "brain float" (torch.bfloat16). Tensors are dense
+ *     and row-major in the index order written; base addresses must be 16-byte
+ *     aligned.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *     Every kernel runs on it, asynchronously to the host.
+ *   - Arguments are checked on the host before any launch. On an error nothing is
+ *     written, the cache length is unchanged, the status is returned and
+ *     duo_last_error() describes it.
+ *   - A handle holds host state only; it may be used from one host thread at a
+ *     time. The device is the one current when duo_create ran.
+ */
+#ifndef DUO_ATTN_H_
+#define DUO_ATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  DUO_OK = 0,
+  DUO_ERR_INVALID_ARG = 1,    /* null pointer, bad size, misaligned address */
+  DUO_ERR_UNSUPPORTED = 2,    /* a shape the kernels do not implement (see duo_config) */
+  DUO_ERR_CAPACITY = 3,       /* the append would exceed max_seq_len */
+  DUO_ERR_CUDA = 4,           /* a CUDA runtime or driver call failed (launch error) */
+  DUO_ERR_DEVICE_TIMEOUT = 5, /* a kernel gave up a bounded wait (see duo_device_error) */
+  DUO_ERR_WORKSPACE = 6       /* decode workspace missing or smaller than required */
+} duo_status;
+
+/* Head kinds, one per KV head. A query head h uses KV head h / (num_q_heads /
+ * num_kv_heads) and inherits its kind. */
+#define DUO_STREAMING 0
+#define DUO_RETRIEVAL 1
+
+typedef struct {
+  int32_t batch;        /* B >= 1 */
+  int32_t num_q_heads;  /* Hq, a multiple of num_kv_heads, Hq / Hkv in {1, 2, 4, 8} */
+  int32_t num_kv_heads; /* Hkv, 1 ... 128 */
+  int32_t head_dim;     /* D in {64, 128} */
+  int32_t sink_size;    /* S >= 0 */
+  int32_t recent_size;  /* R >= 1 (R = 0 would leave a query with no key) */
+  int64_t max_seq_len;  /* capacity of each retrieval head's cache, in tokens */
+} duo_config;
+
+typedef struct duo_handle duo_handle;
+
+/* The caches of one layer. All pointers are device pointers owned by the caller.
+ *   k_full, v_full : bf16 [B, n_ret, max_seq_len, D]; row t of retrieval head r holds
+ *                    token t for t < n. Rows >= n are never read.
+ *   k_sr, v_sr     : bf16 [B, n_str, S + R, D]; the sink slots then the ring slots of
+ *                    each streaming head.
+ *   pos            : int32 [B, S + R]; the token position held by each slot, -1 if
+ *                    empty. Shared by all streaming heads of a sequence.
+ *   n              : tokens appended so far (the same for every sequence of the batch).
+ * n_ret / n_str are the numbers of retrieval / streaming KV heads; a pointer whose
+ * count is zero may be NULL. The compact order of heads of one kind is increasing
+ * KV-head index (see duo_classify_heads). Initialise a cache with duo_cache_reset. */
+typedef struct {
+  void* k_full;
+  void* v_full;
+  void* k_sr;
+  void* v_sr;
+  int32_t* pos;
+  int64_t n;
+} duo_kv_cache;
+
+/* Per-head retrieval/streaming mask (host only, no device work).
+ * is_retrieval[Hkv]: nonzero = retrieval. Writes kind_index[h] = the index of KV head
+ * h among the heads of its kind (its plane in k_full/v_full or k_sr/v_sr), and
+ * *n_retrieval. Source: the DuoAttention README's quick start turns trained per-head
+ * gate values into a binary retrieval/streaming choice per head. */
+duo_status duo_classify_heads(const uint8_t* is_retrieval, int32_t num_kv_heads, int32_t* kind_index,
+                              int32_t* n_retrieval);
+
+/* Create a handle for one layer shape and head mask (host arrays, copied). */
+duo_status duo_create(const duo_config* config, const uint8_t* is_retrieval, duo_handle** out);
+void duo_destroy(duo_handle* handle);
+
+/* Empty the cache: pos[] := -1 on `stream`, cache->n := 0. */
+duo_status duo_cache_reset(duo_handle* handle, duo_kv_cache* cache, void* stream);
+
+/* Append T >= 1 new tokens at positions n ... n+T-1 and set cache->n += T.
+ * k_new, v_new: bf16 [B, T, Hkv, D] (token-major, as a fused QKV projection emits).
+ * Retrieval heads: rows n ... n+T-1 of k_full/v_full. Streaming heads: each token goes
+ * to slot t (t < S) or S + ((t - S) mod R); of the tokens of one call only those still
+ * held when the call ends are written (t < S, or t >= n+T-R), so the result equals T
+ * single-token appends and no slot is written twice. pos[] is updated to match.
+ * DUO_ERR_CAPACITY if n + T > max_seq_len (nothing written). */
+duo_status duo_kv_append(duo_handle* handle, duo_kv_cache* cache, const void* k_new, const void* v_new, int32_t T,
+                         void* stream);
+
+/* Prefill attention of T >= 1 new tokens at positions n ... n+T-1 (n = cache->n, the
+ * cache state BEFORE these tokens are appended; n = 0 for a one-shot prefill, n > 0
+ * for a chunk of a chunked prefill against the growing cache).
+ * q: bf16 [B, T, Hq, D]; k, v: bf16 [B, T, Hkv, D] of the same tokens; o: bf16
+ * [B, T, Hq, D]. A retrieval head attends to cache rows [0, n) and to the new tokens;
+ * a streaming head to what its sink + ring cache holds and to the new tokens, each
+ * with the visibility rule above. Scale 1/sqrt(D) is applied in fp32 to the fp32
+ * product; softmax and accumulation are fp32; o is rounded to nearest even.
+ * The cache is not modified: call duo_kv_append(k, v) afterwards.
+ * Fully masked key tiles are skipped, so a streaming head costs O((S + R) * T). */
+duo_status duo_attn_prefill(duo_handle* handle, const duo_kv_cache* cache, const void* q, const void* k,
+                            const void* v, int32_t T, void* o, void* stream);
+
+/* As duo_attn_prefill, restricted to the query heads whose KV head kind bit is set in
+ * kind_mask (bit 0 = streaming, bit 1 = retrieval). Rows of o for other heads are not
+ * written. Used to time the retrieval heads alone. */
+duo_status duo_attn_prefill_select(duo_handle* handle, const duo_kv_cache* cache, const void* q, const void* k,
+                                   const void* v, int32_t T, void* o, int32_t kind_mask, void* stream);
+
+/* Bytes of device workspace duo_attn_decode needs for a cache of n tokens. */
+size_t duo_decode_workspace_size(const duo_handle* handle, int64_t n);
+
+/* One decode step for the token at position p = cache->n - 1, which must already have
+ * been appended (duo_kv_append with T = 1). q: bf16 [B, Hq, D]; o: bf16 [B, Hq, D].
+ * Reads rows [0, n) of each retrieval head and the valid slots of each streaming head
+ * (each slot checked against pos[] and the visibility rule), every K/V byte once per
+ * KV head for all its query heads. The keys are split over the GPU's SMs; partial
+ * softmaxes (o, max, sum) go to `workspace` and are merged by log-sum-exp.
+ * workspace: device memory of at least duo_decode_workspace_size(handle, n) bytes,
+ * 256-byte aligned. It keeps per-head counters that each call leaves at zero; the
+ * library clears them itself the first time it sees a workspace address and after any
+ * error. Calls sharing one workspace must be ordered on the GPU (same stream). */
+duo_status duo_attn_decode(duo_handle* handle, const duo_kv_cache* cache, const void* q, void* o, void* workspace,
+                           size_t workspace_bytes, void* stream);
+
+/* Synchronises the device, then returns (and clears) the OR of the error codes that
+ * kernels of this library recorded when a bounded wait ran out; 0 = none. Sets
+ * *code and returns DUO_ERR_DEVICE_TIMEOUT if it is nonzero. */
+duo_status duo_device_error(uint32_t* code);
+
+/* Message describing the last error of the calling host thread ("" if none). */
+const char* duo_last_error(void);
+
+/* Short name of a status code. */
+const char* duo_status_string(duo_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DUO_ATTN_H_ */

@@ -1,0 +1,96 @@
+"""GB300-native mixed-head causal attention (retrieval + streaming heads) for long-context serving.
+
+The product is the C ABI in ``include/duo_attn.h``, implemented by
+``libduo_attn.so`` (hand-written sm_103a kernels). This package holds its thin
+ctypes binding (``_lib``, the same entry-point names), ``DuoLayer`` -- a small
+owner of the torch tensors one layer's caches live in -- and the algorithmic
+work counters used to report throughput (``workload``).
+"""
+
+from __future__ import annotations
+
+from . import _lib
+from ._lib import (DUO_RETRIEVAL, DUO_STREAMING, DuoError, duo_attn_decode, duo_attn_prefill,  # noqa: F401
+                   duo_attn_prefill_select, duo_cache_reset, duo_classify_heads, duo_create,
+                   duo_decode_workspace_size, duo_destroy, duo_device_error, duo_kv_append, duo_last_error)
+
+
+class DuoLayer:
+    """Caches of one attention layer in torch device memory plus a library handle.
+
+    k_full/v_full: bf16 [B, n_ret, max_seq_len, D]; k_sr/v_sr: bf16 [B, n_str, S+R, D];
+    pos: int32 [B, S+R]; ``n`` tokens appended so far. ``workspace`` is the decode
+    workspace (zero-filled once)."""
+
+    def __init__(self, batch, num_q_heads, num_kv_heads, head_dim, sink_size, recent_size, max_seq_len,
+                 is_retrieval, device="cuda"):
+        import torch
+        self.B, self.Hq, self.Hkv, self.D = batch, num_q_heads, num_kv_heads, head_dim
+        self.S, self.R, self.cap = sink_size, recent_size, max_seq_len
+        self.is_retrieval = [1 if x else 0 for x in is_retrieval]
+        self.kind_index, self.n_ret = duo_classify_heads(self.is_retrieval)
+        self.n_str = num_kv_heads - self.n_ret
+        self.device = torch.device(device)
+        with torch.cuda.device(self.device):
+            self.handle = duo_create(batch, num_q_heads, num_kv_heads, head_dim, sink_size, recent_size,
+                                     max_seq_len, self.is_retrieval)
+        bf = dict(dtype=torch.bfloat16, device=self.device)
+        SR = sink_size + recent_size
+        self.k_full = torch.empty((batch, self.n_ret, max_seq_len if self.n_ret else 0, head_dim), **bf)
+        self.v_full = torch.empty_like(self.k_full)
+        self.k_sr = torch.empty((batch, self.n_str, SR, head_dim), **bf)
+        self.v_sr = torch.empty_like(self.k_sr)
+        self.pos = torch.empty((batch, SR), dtype=torch.int32, device=self.device)
+        ws = duo_decode_workspace_size(self.handle, 1)
+        self.workspace = torch.zeros(((ws + 255) // 256) * 256, dtype=torch.uint8, device=self.device)
+        self.cache = _lib.duo_kv_cache(self.k_full.data_ptr() if self.n_ret else None,
+                                       self.v_full.data_ptr() if self.n_ret else None,
+                                       self.k_sr.data_ptr() if self.n_str else None,
+                                       self.v_sr.data_ptr() if self.n_str else None,
+                                       self.pos.data_ptr(), 0)
+        self.reset()
+
+    @property
+    def n(self) -> int:
+        return int(self.cache.n)
+
+    def reset(self, stream=None) -> None:
+        duo_cache_reset(self.handle, self.cache, stream)
+
+    def append(self, k_new, v_new, stream=None) -> None:
+        T = k_new.shape[1]
+        _lib._bf16(k_new, (self.B, T, self.Hkv, self.D), "k_new")
+        _lib._bf16(v_new, (self.B, T, self.Hkv, self.D), "v_new")
+        duo_kv_append(self.handle, self.cache, k_new, v_new, T, stream)
+
+    def prefill(self, q, k, v, out=None, kind_mask=3, stream=None):
+        import torch
+        T = q.shape[1]
+        _lib._bf16(q, (self.B, T, self.Hq, self.D), "q")
+        _lib._bf16(k, (self.B, T, self.Hkv, self.D), "k")
+        _lib._bf16(v, (self.B, T, self.Hkv, self.D), "v")
+        if out is None:
+            out = torch.empty_like(q)
+        _lib._bf16(out, (self.B, T, self.Hq, self.D), "o")
+        duo_attn_prefill_select(self.handle, self.cache, q, k, v, T, out, kind_mask, stream)
+        return out
+
+    def decode(self, q, out=None, stream=None):
+        import torch
+        _lib._bf16(q, (self.B, self.Hq, self.D), "q")
+        if out is None:
+            out = torch.empty_like(q)
+        _lib._bf16(out, (self.B, self.Hq, self.D), "o")
+        duo_attn_decode(self.handle, self.cache, q, out, self.workspace, stream)
+        return out
+
+    def close(self) -> None:
+        if getattr(self, "handle", None) is not None:
+            duo_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

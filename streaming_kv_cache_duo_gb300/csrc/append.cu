@@ -1,0 +1,88 @@
+// duo_kv_append: write new tokens into the retrieval caches and into the sink +
+// ring caches of the streaming heads.
+//
+// Slot rule (vLLM issue "Could you support Attention Sink?", block tables and
+// option 3): token t goes to slot t while t < S and to S + ((t - S) mod R) after
+// that; sink slots never move. Of the T tokens of one call only those still held
+// when the call ends are written (t < S, or t >= n + T - R), so the result equals
+// T single appends and no two threads write the same slot.
+//
+// HBM-bound copy: one thread moves one 16-byte vector of K and one of V, with
+// read-only 128-bit loads from the token-major input and 128-bit stores into the
+// head-major caches. Bytes moved: 2 * 2 * D * (T * n_ret + survivors * n_str) per
+// sequence, plus 4 bytes of pos per surviving token.
+#include "duo_internal.h"
+
+namespace duo {
+namespace {
+
+__global__ void __launch_bounds__(256) append_kernel(const AppendParams p) {
+  const int D = p.sh.D;
+  const int Hkv = p.sh.Hkv;
+  const int vpr = D / 8;  // 16-byte vectors per row
+  const int n_ret = p.sh.n_ret;
+  const int n_str = p.sh.n_str;
+  const int SR = p.sh.S + p.sh.R;
+  const int64_t T = p.T;
+  const int64_t ret_vecs = (int64_t)p.sh.B * T * n_ret * vpr;
+  const int64_t surv = p.sink_cnt + p.ring_cnt;
+  const int64_t str_vecs = (int64_t)p.sh.B * surv * n_str * vpr;
+  const int64_t total = ret_vecs + str_vecs;
+  const uint4* kin = reinterpret_cast<const uint4*>(p.k_new);
+  const uint4* vin = reinterpret_cast<const uint4*>(p.v_new);
+
+  for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    if (idx < ret_vecs) {
+      int64_t r = idx;
+      const int v = (int)(r % vpr);
+      r /= vpr;
+      const int ri = (int)(r % n_ret);
+      r /= n_ret;
+      const int64_t t = r % T;
+      const int64_t b = r / T;
+      const int h = p.heads.ret_head[ri];
+      const int64_t src = ((b * T + t) * Hkv + h) * vpr + v;
+      const int64_t dst = ((b * n_ret + ri) * p.sh.cap + p.n + t) * vpr + v;
+      const uint4 kv = __ldg(kin + src);
+      const uint4 vv = __ldg(vin + src);
+      reinterpret_cast<uint4*>(p.k_full)[dst] = kv;
+      reinterpret_cast<uint4*>(p.v_full)[dst] = vv;
+    } else {
+      int64_t r = idx - ret_vecs;
+      const int v = (int)(r % vpr);
+      r /= vpr;
+      const int si = (int)(r % n_str);
+      r /= n_str;
+      const int64_t k = r % surv;
+      const int64_t b = r / surv;
+      const int64_t t_abs = k < p.sink_cnt ? p.sink_lo + k : p.ring_lo + (k - p.sink_cnt);
+      const int64_t t = t_abs - p.n;
+      const int64_t slot = t_abs < p.sh.S ? t_abs : p.sh.S + (t_abs - p.sh.S) % p.sh.R;
+      const int h = p.heads.str_head[si];
+      const int64_t src = ((b * T + t) * Hkv + h) * vpr + v;
+      const int64_t dst = ((b * n_str + si) * SR + slot) * vpr + v;
+      const uint4 kv = __ldg(kin + src);
+      const uint4 vv = __ldg(vin + src);
+      reinterpret_cast<uint4*>(p.k_sr)[dst] = kv;
+      reinterpret_cast<uint4*>(p.v_sr)[dst] = vv;
+      if (si == 0 && v == 0) p.pos[b * SR + slot] = (int32_t)t_abs;
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_append(const AppendParams& p, int num_sms, cudaStream_t stream) {
+  const int vpr = p.sh.D / 8;
+  const int64_t total = (int64_t)p.sh.B * p.T * p.sh.n_ret * vpr +
+                        (int64_t)p.sh.B * (p.sink_cnt + p.ring_cnt) * p.sh.n_str * vpr;
+  if (total == 0) return cudaSuccess;
+  int64_t blocks = (total + 255) / 256;
+  const int64_t cap = (int64_t)num_sms * 8;
+  if (blocks > cap) blocks = cap;
+  append_kernel<<<(unsigned)blocks, 256, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace duo

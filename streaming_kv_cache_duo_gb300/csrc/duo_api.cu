@@ -1,0 +1,424 @@
+// Host side of the C ABI declared in include/duo_attn.h: argument checks, the
+// per-head retrieval/streaming map, TMA tensor-map encoding, work sizing and
+// kernel dispatch. No device memory is allocated here.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <string>
+
+#include "../../include/duo_attn.h"
+#include "duo_internal.h"
+
+using namespace duo;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+// Bumped whenever duo_device_error() finds that a kernel gave up a wait: decode
+// counters may then be left nonzero, so every handle clears them again.
+std::atomic<unsigned> g_error_epoch{0};
+
+duo_status fail(duo_status st, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+duo_status fail(duo_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+
+duo_status ok() {
+  g_last_error.clear();
+  return DUO_OK;
+}
+
+duo_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(DUO_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+}  // namespace
+
+struct duo_handle {
+  duo_config cfg;
+  Shape sh;
+  HeadTable heads;
+  int device;
+  int num_sms;
+  EncodeTiledFn encode;
+  const void* last_workspace;  // counters known to be zero for this address
+  bool workspace_dirty;
+  unsigned epoch;
+};
+
+namespace {
+
+// 4-D map over a token-major bf16 tensor [B, T, H, D]; box 64 x 1 x 128 x 1.
+duo_status encode_tokens(const duo_handle* h, CUtensorMap* map, const void* base, int B, int T, int H, int D) {
+  const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)T, (cuuint64_t)B};
+  const cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2, (cuuint64_t)T * H * D * 2};
+  const cuuint32_t box[4] = {64, 1, (cuuint32_t)kPrefillBM, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = h->encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(DUO_ERR_CUDA, "cuTensorMapEncodeTiled (token-major) failed: %d", (int)r);
+  return DUO_OK;
+}
+
+// 3-D map over a head-major cache [planes, rows_alloc, D] that exposes only the
+// first `rows` rows of each plane (later rows read as zero).
+duo_status encode_cache(const duo_handle* h, CUtensorMap* map, const void* base, int64_t planes, int64_t rows_alloc,
+                        int64_t rows, int D) {
+  const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)rows, (cuuint64_t)planes};
+  const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)rows_alloc * D * 2};
+  const cuuint32_t box[3] = {64, (cuuint32_t)kPrefillBN, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = h->encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(DUO_ERR_CUDA, "cuTensorMapEncodeTiled (cache) failed: %d", (int)r);
+  return DUO_OK;
+}
+
+duo_status check_handle(const duo_handle* h) {
+  if (!h) return fail(DUO_ERR_INVALID_ARG, "handle is NULL");
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev != h->device)
+    return fail(DUO_ERR_INVALID_ARG, "current device %d differs from the handle's device %d", dev, h->device);
+  return DUO_OK;
+}
+
+duo_status check_cache(const duo_handle* h, const duo_kv_cache* c, bool need_full, bool need_ring) {
+  if (!c) return fail(DUO_ERR_INVALID_ARG, "cache is NULL");
+  if (c->n < 0) return fail(DUO_ERR_INVALID_ARG, "cache->n = %lld < 0", (long long)c->n);
+  if (need_full && h->sh.n_ret > 0) {
+    if (!c->k_full || !c->v_full) return fail(DUO_ERR_INVALID_ARG, "k_full / v_full is NULL");
+    if (!aligned16(c->k_full) || !aligned16(c->v_full))
+      return fail(DUO_ERR_INVALID_ARG, "k_full / v_full not 16-byte aligned");
+  }
+  if (need_ring && h->sh.n_str > 0) {
+    if (!c->k_sr || !c->v_sr || !c->pos) return fail(DUO_ERR_INVALID_ARG, "k_sr / v_sr / pos is NULL");
+    if (!aligned16(c->k_sr) || !aligned16(c->v_sr) || !aligned16(c->pos))
+      return fail(DUO_ERR_INVALID_ARG, "k_sr / v_sr / pos not 16-byte aligned");
+  }
+  return DUO_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* duo_last_error(void) { return g_last_error.c_str(); }
+
+const char* duo_status_string(duo_status s) {
+  switch (s) {
+    case DUO_OK: return "DUO_OK";
+    case DUO_ERR_INVALID_ARG: return "DUO_ERR_INVALID_ARG";
+    case DUO_ERR_UNSUPPORTED: return "DUO_ERR_UNSUPPORTED";
+    case DUO_ERR_CAPACITY: return "DUO_ERR_CAPACITY";
+    case DUO_ERR_CUDA: return "DUO_ERR_CUDA";
+    case DUO_ERR_DEVICE_TIMEOUT: return "DUO_ERR_DEVICE_TIMEOUT";
+    case DUO_ERR_WORKSPACE: return "DUO_ERR_WORKSPACE";
+  }
+  return "DUO_ERR_UNKNOWN";
+}
+
+duo_status duo_classify_heads(const uint8_t* is_retrieval, int32_t num_kv_heads, int32_t* kind_index,
+                              int32_t* n_retrieval) {
+  if (!is_retrieval || !kind_index || !n_retrieval) return fail(DUO_ERR_INVALID_ARG, "NULL argument");
+  if (num_kv_heads < 1 || num_kv_heads > kMaxHeads)
+    return fail(DUO_ERR_INVALID_ARG, "num_kv_heads = %d outside [1, %d]", num_kv_heads, kMaxHeads);
+  int32_t nr = 0, ns = 0;
+  for (int32_t h = 0; h < num_kv_heads; ++h) kind_index[h] = is_retrieval[h] ? nr++ : ns++;
+  *n_retrieval = nr;
+  return ok();
+}
+
+duo_status duo_create(const duo_config* cfg, const uint8_t* is_retrieval, duo_handle** out) {
+  if (!cfg || !is_retrieval || !out) return fail(DUO_ERR_INVALID_ARG, "NULL argument");
+  *out = nullptr;
+  const duo_config& c = *cfg;
+  if (c.batch < 1 || c.batch > 65535) return fail(DUO_ERR_INVALID_ARG, "batch = %d outside [1, 65535]", c.batch);
+  if (c.num_kv_heads < 1 || c.num_kv_heads > kMaxHeads)
+    return fail(DUO_ERR_INVALID_ARG, "num_kv_heads = %d outside [1, %d]", c.num_kv_heads, kMaxHeads);
+  if (c.num_q_heads < 1 || c.num_q_heads % c.num_kv_heads != 0)
+    return fail(DUO_ERR_INVALID_ARG, "num_q_heads = %d is not a multiple of num_kv_heads = %d", c.num_q_heads,
+                c.num_kv_heads);
+  const int g = c.num_q_heads / c.num_kv_heads;
+  if (g != 1 && g != 2 && g != 4 && g != 8)
+    return fail(DUO_ERR_UNSUPPORTED, "num_q_heads / num_kv_heads = %d not in {1, 2, 4, 8}", g);
+  if (c.head_dim != 64 && c.head_dim != 128)
+    return fail(DUO_ERR_UNSUPPORTED, "head_dim = %d not in {64, 128}", c.head_dim);
+  if (c.sink_size < 0) return fail(DUO_ERR_INVALID_ARG, "sink_size = %d < 0", c.sink_size);
+  if (c.recent_size < 1) return fail(DUO_ERR_INVALID_ARG, "recent_size = %d < 1", c.recent_size);
+  if ((int64_t)c.sink_size + c.recent_size > (1 << 20))
+    return fail(DUO_ERR_UNSUPPORTED, "sink_size + recent_size > 2^20");
+  if (c.max_seq_len < 1 || c.max_seq_len > 0x7fffffffLL)
+    return fail(DUO_ERR_INVALID_ARG, "max_seq_len = %lld outside [1, 2^31)", (long long)c.max_seq_len);
+
+  duo_handle* h = new (std::nothrow) duo_handle();
+  if (!h) return fail(DUO_ERR_INVALID_ARG, "out of host memory");
+  h->cfg = c;
+  int nr = 0, ns = 0;
+  for (int k = 0; k < c.num_kv_heads; ++k) {
+    if (is_retrieval[k]) {
+      h->heads.ret_head[nr] = (uint8_t)k;
+      h->heads.kind[k] = DUO_RETRIEVAL;
+      h->heads.kidx[k] = (uint8_t)nr++;
+    } else {
+      h->heads.str_head[ns] = (uint8_t)k;
+      h->heads.kind[k] = DUO_STREAMING;
+      h->heads.kidx[k] = (uint8_t)ns++;
+    }
+  }
+  h->sh = Shape{c.batch, c.num_q_heads, c.num_kv_heads, c.head_dim, c.sink_size, c.recent_size, g, nr, ns,
+                c.max_seq_len};
+  h->last_workspace = nullptr;
+  h->workspace_dirty = true;
+  h->epoch = g_error_epoch.load();
+
+  cudaError_t e = cudaGetDevice(&h->device);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device);
+  int major = 0, minor = 0;
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, h->device);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, h->device);
+  if (e != cudaSuccess) {
+    delete h;
+    return cuda_fail(e, "device query");
+  }
+  if (major != 10 || minor != 3) {
+    delete h;
+    return fail(DUO_ERR_UNSUPPORTED, "device compute capability %d.%d: this library is built for sm_103a only", major,
+                minor);
+  }
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+  if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) {
+    delete h;
+    return fail(DUO_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
+  }
+  h->encode = reinterpret_cast<EncodeTiledFn>(fn);
+  *out = h;
+  return ok();
+}
+
+void duo_destroy(duo_handle* h) { delete h; }
+
+duo_status duo_cache_reset(duo_handle* h, duo_kv_cache* c, void* stream) {
+  duo_status st = check_handle(h);
+  if (st != DUO_OK) return st;
+  if (!c) return fail(DUO_ERR_INVALID_ARG, "cache is NULL");
+  if (h->sh.n_str > 0) {
+    if (!c->pos) return fail(DUO_ERR_INVALID_ARG, "pos is NULL");
+    cudaError_t e = cudaMemsetAsync(c->pos, 0xFF, (size_t)h->sh.B * (h->sh.S + h->sh.R) * sizeof(int32_t),
+                                    (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(pos)");
+  }
+  c->n = 0;
+  return ok();
+}
+
+duo_status duo_kv_append(duo_handle* h, duo_kv_cache* c, const void* k_new, const void* v_new, int32_t T,
+                         void* stream) {
+  duo_status st = check_handle(h);
+  if (st != DUO_OK) return st;
+  if ((st = check_cache(h, c, true, true)) != DUO_OK) return st;
+  if (T < 1) return fail(DUO_ERR_INVALID_ARG, "T = %d < 1", T);
+  if (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new))
+    return fail(DUO_ERR_INVALID_ARG, "k_new / v_new NULL or not 16-byte aligned");
+  const Shape& sh = h->sh;
+  if (c->n + T > 0x7fffffffLL) return fail(DUO_ERR_CAPACITY, "positions would reach 2^31");
+  if (sh.n_ret > 0 && c->n + T > sh.cap)
+    return fail(DUO_ERR_CAPACITY, "n + T = %lld exceeds max_seq_len = %lld", (long long)(c->n + T),
+                (long long)sh.cap);
+  AppendParams p;
+  p.k_new = static_cast<const uint16_t*>(k_new);
+  p.v_new = static_cast<const uint16_t*>(v_new);
+  p.k_full = static_cast<uint16_t*>(c->k_full);
+  p.v_full = static_cast<uint16_t*>(c->v_full);
+  p.k_sr = static_cast<uint16_t*>(c->k_sr);
+  p.v_sr = static_cast<uint16_t*>(c->v_sr);
+  p.pos = c->pos;
+  p.n = c->n;
+  p.T = T;
+  const int64_t n = c->n, e = c->n + T, S = sh.S, R = sh.R;
+  // survivors of the call: t < S, or t >= n + T - R
+  p.sink_lo = n;
+  p.sink_cnt = n < S ? ((e < S ? e : S) - n) : 0;
+  int64_t r0 = n;
+  if (r0 < S) r0 = S;
+  if (r0 < e - R) r0 = e - R;
+  p.ring_lo = r0;
+  p.ring_cnt = e > r0 ? e - r0 : 0;
+  p.sh = sh;
+  p.heads = h->heads;
+  cudaError_t ce = launch_append(p, h->num_sms, (cudaStream_t)stream);
+  if (ce != cudaSuccess) return cuda_fail(ce, "append launch");
+  c->n += T;
+  return ok();
+}
+
+static duo_status prefill_impl(duo_handle* h, const duo_kv_cache* c, const void* q, const void* k, const void* v,
+                               int32_t T, void* o, int32_t kind_mask, void* stream) {
+  duo_status st = check_handle(h);
+  if (st != DUO_OK) return st;
+  if (!c) return fail(DUO_ERR_INVALID_ARG, "cache is NULL");
+  const Shape& sh = h->sh;
+  const bool use_cache = c->n > 0;
+  if ((st = check_cache(h, c, use_cache, use_cache)) != DUO_OK) return st;
+  if (T < 1) return fail(DUO_ERR_INVALID_ARG, "T = %d < 1", T);
+  if (!q || !k || !v || !o) return fail(DUO_ERR_INVALID_ARG, "q / k / v / o is NULL");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o))
+    return fail(DUO_ERR_INVALID_ARG, "q / k / v / o not 16-byte aligned");
+  if (c->n + T > 0x7fffffffLL) return fail(DUO_ERR_INVALID_ARG, "positions would reach 2^31");
+  if (kind_mask < 0 || kind_mask > 3) return fail(DUO_ERR_INVALID_ARG, "kind_mask = %d outside [0, 3]", kind_mask);
+
+  PrefillParams p;
+  memset(&p, 0, sizeof(p));
+  if ((st = encode_tokens(h, &p.tm_q, q, sh.B, T, sh.Hq, sh.D)) != DUO_OK) return st;
+  if ((st = encode_tokens(h, &p.tm_k, k, sh.B, T, sh.Hkv, sh.D)) != DUO_OK) return st;
+  if ((st = encode_tokens(h, &p.tm_v, v, sh.B, T, sh.Hkv, sh.D)) != DUO_OK) return st;
+  const int64_t SR = (int64_t)sh.S + sh.R;
+  const int nvalid = (int)(c->n < SR ? c->n : SR);
+  if (use_cache && sh.n_ret > 0) {
+    if (c->n > sh.cap) return fail(DUO_ERR_INVALID_ARG, "cache->n exceeds max_seq_len");
+    if ((st = encode_cache(h, &p.tm_kfull, c->k_full, (int64_t)sh.B * sh.n_ret, sh.cap, c->n, sh.D)) != DUO_OK)
+      return st;
+    if ((st = encode_cache(h, &p.tm_vfull, c->v_full, (int64_t)sh.B * sh.n_ret, sh.cap, c->n, sh.D)) != DUO_OK)
+      return st;
+  }
+  if (use_cache && sh.n_str > 0) {
+    if ((st = encode_cache(h, &p.tm_ksr, c->k_sr, (int64_t)sh.B * sh.n_str, SR, nvalid, sh.D)) != DUO_OK) return st;
+    if ((st = encode_cache(h, &p.tm_vsr, c->v_sr, (int64_t)sh.B * sh.n_str, SR, nvalid, sh.D)) != DUO_OK) return st;
+  }
+  p.o = static_cast<uint16_t*>(o);
+  p.pos = c->pos;
+  p.n = c->n;
+  p.T = T;
+  p.nvalid = nvalid;
+  p.num_qt = (T + kPrefillBM - 1) / kPrefillBM;
+  const int64_t per_kind = (int64_t)sh.B * sh.g * p.num_qt;
+  const int64_t ir = (kind_mask & 2) ? per_kind * sh.n_ret : 0;
+  const int64_t is = (kind_mask & 1) ? per_kind * sh.n_str : 0;
+  if (ir + is > 0x7fffffffLL) return fail(DUO_ERR_UNSUPPORTED, "too many query tiles for one launch");
+  p.items_r = (int)ir;
+  p.items_s = (int)is;
+  p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)sh.D));
+  p.sh = sh;
+  p.heads = h->heads;
+  cudaError_t ce = launch_prefill(p, (cudaStream_t)stream);
+  if (ce != cudaSuccess) return cuda_fail(ce, "prefill launch");
+  return ok();
+}
+
+duo_status duo_attn_prefill(duo_handle* h, const duo_kv_cache* c, const void* q, const void* k, const void* v,
+                            int32_t T, void* o, void* stream) {
+  return prefill_impl(h, c, q, k, v, T, o, 3, stream);
+}
+
+duo_status duo_attn_prefill_select(duo_handle* h, const duo_kv_cache* c, const void* q, const void* k,
+                                   const void* v, int32_t T, void* o, int32_t kind_mask, void* stream) {
+  return prefill_impl(h, c, q, k, v, T, o, kind_mask, stream);
+}
+
+static void decode_plan(const duo_handle* h, int64_t n, DecodeParams* p) {
+  const Shape& sh = h->sh;
+  const int64_t SR = (int64_t)sh.S + sh.R;
+  p->n = n;
+  p->nvalid = (int)(n < SR ? n : SR);
+  p->U_r = sh.B * sh.n_ret;
+  p->U_s = sh.B * sh.n_str;
+  p->tiles_r = (n + kDecodeTK - 1) / kDecodeTK;
+  p->tiles_s = (p->nvalid + kDecodeTK - 1) / kDecodeTK;
+  p->W = (int64_t)p->U_r * p->tiles_r + (int64_t)p->U_s * p->tiles_s;
+  p->C = (int)(p->W < h->num_sms ? p->W : h->num_sms);
+}
+
+size_t duo_decode_workspace_size(const duo_handle* h, int64_t n) {
+  if (!h) return 0;
+  DecodeParams p;
+  decode_plan(h, n < 1 ? 1 : n, &p);
+  (void)p;
+  // sized for the largest grid so that one workspace serves every n
+  return decode_workspace_bytes(h->sh, h->num_sms);
+}
+
+duo_status duo_attn_decode(duo_handle* h, const duo_kv_cache* c, const void* q, void* o, void* workspace,
+                           size_t ws_bytes, void* stream) {
+  duo_status st = check_handle(h);
+  if (st != DUO_OK) return st;
+  if ((st = check_cache(h, c, true, true)) != DUO_OK) return st;
+  if (c->n < 1) return fail(DUO_ERR_INVALID_ARG, "decode needs the query token appended first (cache->n >= 1)");
+  if (h->sh.n_ret > 0 && c->n > h->sh.cap) return fail(DUO_ERR_INVALID_ARG, "cache->n exceeds max_seq_len");
+  if (!q || !o || !aligned16(q) || !aligned16(o))
+    return fail(DUO_ERR_INVALID_ARG, "q / o NULL or not 16-byte aligned");
+  const size_t need = decode_workspace_bytes(h->sh, h->num_sms);
+  if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return fail(DUO_ERR_INVALID_ARG, "workspace not 256-byte aligned");
+  if (!workspace || ws_bytes < need)
+    return fail(DUO_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need, workspace ? ws_bytes : 0);
+  const Shape& sh = h->sh;
+  DecodeParams p;
+  decode_plan(h, c->n, &p);
+  const int64_t U = (int64_t)sh.B * sh.Hkv;
+  const size_t counter_bytes = ((size_t)U * 4 + 255) / 256 * 256;
+  const unsigned epoch = g_error_epoch.load();
+  if (workspace != h->last_workspace || h->workspace_dirty || epoch != h->epoch) {
+    cudaError_t e = cudaMemsetAsync(workspace, 0, counter_bytes, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(workspace counters)");
+    h->last_workspace = workspace;
+    h->workspace_dirty = false;
+    h->epoch = epoch;
+  }
+  p.q = static_cast<const uint16_t*>(q);
+  p.o = static_cast<uint16_t*>(o);
+  p.k_full = static_cast<const uint16_t*>(c->k_full);
+  p.v_full = static_cast<const uint16_t*>(c->v_full);
+  p.k_sr = static_cast<const uint16_t*>(c->k_sr);
+  p.v_sr = static_cast<const uint16_t*>(c->v_sr);
+  p.pos = c->pos;
+  p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)sh.D));
+  p.counters = static_cast<uint32_t*>(workspace);
+  p.partials = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + counter_bytes);
+  p.sh = sh;
+  p.heads = h->heads;
+  cudaError_t ce = launch_decode(p, (cudaStream_t)stream);
+  if (ce != cudaSuccess) {
+    h->workspace_dirty = true;
+    return cuda_fail(ce, "decode launch");
+  }
+  return ok();
+}
+
+duo_status duo_device_error(uint32_t* code) {
+  if (!code) return fail(DUO_ERR_INVALID_ARG, "code is NULL");
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+  uint32_t a = 0, b = 0;
+  if ((e = prefill_read_clear_error(&a)) != cudaSuccess) return cuda_fail(e, "read prefill error word");
+  if ((e = decode_read_clear_error(&b)) != cudaSuccess) return cuda_fail(e, "read decode error word");
+  *code = a | b;
+  if (*code) g_error_epoch.fetch_add(1);
+  if (*code) return fail(DUO_ERR_DEVICE_TIMEOUT, "a kernel gave up a bounded wait (code 0x%x)", *code);
+  return ok();
+}
+
+}  // extern "C"

@@ -1,0 +1,116 @@
+// Internal types shared by the host API (duo_api.cu) and the kernel translation
+// units. Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace duo {
+
+// Upper bound of any single wait inside a kernel (an mbarrier phase). Normal
+// waits last microseconds; running out means a bug, never a slow GPU.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+constexpr int kMaxHeads = 128;
+
+// Error codes kernels OR into their error word.
+enum : uint32_t {
+  kErrPrefillProducer = 1u << 0,
+  kErrPrefillMma = 1u << 1,
+  kErrPrefillSoftmax = 1u << 2,
+  kErrDecodeProducer = 1u << 8,
+  kErrDecodeConsumer = 1u << 9,
+};
+
+struct Shape {
+  int B, Hq, Hkv, D, S, R, g, n_ret, n_str;
+  int64_t cap;  // retrieval cache capacity (tokens)
+};
+
+// Compact head lists: KV head of the r-th retrieval / s-th streaming head, and
+// for every KV head its kind and index within its kind.
+struct HeadTable {
+  uint8_t ret_head[kMaxHeads];
+  uint8_t str_head[kMaxHeads];
+  uint8_t kind[kMaxHeads];
+  uint8_t kidx[kMaxHeads];
+};
+
+// ------------------------------------------------------------------ append
+struct AppendParams {
+  const uint16_t* k_new;  // bf16 [B, T, Hkv, D]
+  const uint16_t* v_new;
+  uint16_t* k_full;  // bf16 [B, n_ret, cap, D]
+  uint16_t* v_full;
+  uint16_t* k_sr;  // bf16 [B, n_str, S+R, D]
+  uint16_t* v_sr;
+  int32_t* pos;  // int32 [B, S+R]
+  int64_t n;     // tokens before this call
+  int T;
+  // tokens of this call still held by a streaming head when it ends:
+  // positions [sink_lo, sink_lo + sink_cnt) and [ring_lo, ring_lo + ring_cnt)
+  int64_t sink_lo, sink_cnt, ring_lo, ring_cnt;
+  Shape sh;
+  HeadTable heads;
+};
+cudaError_t launch_append(const AppendParams& p, int num_sms, cudaStream_t stream);
+
+// ------------------------------------------------------------------ decode
+constexpr int kDecodeTK = 64;  // keys per decode tile
+
+struct DecodeParams {
+  const uint16_t* q;  // bf16 [B, Hq, D]
+  uint16_t* o;        // bf16 [B, Hq, D]
+  const uint16_t* k_full;
+  const uint16_t* v_full;
+  const uint16_t* k_sr;
+  const uint16_t* v_sr;
+  const int32_t* pos;
+  int64_t n;       // keys held by a retrieval head; the query is at position n - 1
+  int nvalid;      // valid ring slots, min(n, S + R)
+  int U_r, U_s;    // units (one per (sequence, KV head)) of each kind
+  int64_t tiles_r; // key tiles per retrieval unit
+  int64_t tiles_s; // key tiles per streaming unit
+  int64_t W;       // all tiles: U_r * tiles_r + U_s * tiles_s
+  int C;           // CTAs; CTA c takes tiles [c W / C, (c+1) W / C)
+  float scale_log2;    // log2(e) / sqrt(D)
+  uint32_t* counters;  // [U_r + U_s] arrival tickets, left at zero
+  float* partials;     // [C + U_r + U_s][g][D + 2] (o, max, sum) per segment
+  Shape sh;
+  HeadTable heads;
+};
+size_t decode_workspace_bytes(const Shape& sh, int num_ctas);
+cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream);
+
+// ------------------------------------------------------------------ prefill
+constexpr int kPrefillBM = 128;  // query rows per CTA tile
+constexpr int kPrefillBN = 128;  // keys per KV tile
+
+struct PrefillParams {
+  CUtensorMap tm_q;      // 4-D over q [B, T, Hq, D], box 64 x 1 x 128 x 1, 128B swizzle
+  CUtensorMap tm_k;      // 4-D over k [B, T, Hkv, D]
+  CUtensorMap tm_v;      // 4-D over v [B, T, Hkv, D]
+  CUtensorMap tm_kfull;  // 3-D over k_full [B * n_ret, n (extent), D]
+  CUtensorMap tm_vfull;
+  CUtensorMap tm_ksr;    // 3-D over k_sr [B * n_str, nvalid (extent), D]
+  CUtensorMap tm_vsr;
+  uint16_t* o;           // bf16 [B, T, Hq, D]
+  const int32_t* pos;    // int32 [B, S+R]
+  int64_t n;             // cache length before the chunk (absolute position of row 0)
+  int T;
+  int nvalid;            // valid ring slots before the chunk
+  int num_qt;            // query tiles per head: ceil(T / 128)
+  int items_r;           // work items of retrieval heads: B * n_ret * g * num_qt
+  int items_s;           // work items of streaming heads
+  float scale_log2;
+  Shape sh;
+  HeadTable heads;
+};
+cudaError_t launch_prefill(const PrefillParams& p, cudaStream_t stream);
+
+// Error words of the kernel translation units (synchronous read-and-clear).
+cudaError_t prefill_read_clear_error(uint32_t* code);
+cudaError_t decode_read_clear_error(uint32_t* code);
+
+}  // namespace duo
