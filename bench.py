@@ -29,7 +29,6 @@ import argparse
 import json
 import math
 import os
-import subprocess
 import sys
 import threading
 import time
@@ -53,61 +52,92 @@ def load_peaks():
 
 # ----------------------------------------------------------------------------- clocks
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+    """SM clock and throttle reasons sampled every 10 ms (NVML through ctypes) while the
+    timed region runs; falls back to `nvidia-smi -lms 200`."""
 
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
 
-    def __init__(self, gpu_index: int):
-        self.gpu = gpu_index
-        self.proc = None
-        self.lines = []
+    def __init__(self, cuda_index: int):
+        self.cuda_index = cuda_index
+        self.samples = []
+        self.max_mhz = None
+        self.stop_flag = threading.Event()
         self.thread = None
+        self.nvml = None
+        self.handle = None
+        self.how = None
+
+    def _open_nvml(self):
+        import ctypes
+        nv = ctypes.CDLL("libnvidia-ml.so.1")
+        if nv.nvmlInit_v2() != 0:
+            return False
+        h = ctypes.c_void_p()
+        bus = _pci_bus_id(self.cuda_index)
+        if bus is not None and nv.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(h)) == 0:
+            self.how = "nvml by PCI bus id"
+        else:
+            vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+            ids = [x for x in vis.split(",") if x.strip().isdigit()]
+            idx = int(ids[self.cuda_index]) if self.cuda_index < len(ids) else self.cuda_index
+            if nv.nvmlDeviceGetHandleByIndex_v2(idx, ctypes.byref(h)) != 0:
+                return False
+            self.how = f"nvml index {idx}"
+        self.nvml, self.handle = nv, h
+        mx = ctypes.c_uint()
+        if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+            self.max_mhz = float(mx.value)
+        return True
+
+    def _loop(self):
+        import ctypes
+        nv, h = self.nvml, self.handle
+        clk = ctypes.c_uint()
+        rs = ctypes.c_ulonglong()
+        get_r = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(nv, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        while not self.stop_flag.is_set():
+            if nv.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0 and get_r(h, ctypes.byref(rs)) == 0:
+                self.samples.append((float(clk.value), int(rs.value)))
+            time.sleep(0.01)
 
     def start(self):
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-        except (OSError, ValueError):
-            self.proc = None
+            ok = self._open_nvml()
+        except OSError:
+            ok = False
+        if not ok:
+            self.how = None
             return
-        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread = threading.Thread(target=self._loop, daemon=True)
         self.thread.start()
 
-    def _read(self):
-        for line in self.proc.stdout:
-            self.lines.append(line.strip())
-
     def stop(self):
-        if self.proc is None:
+        if self.thread is None:
             return None
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
-        if self.thread:
-            self.thread.join(timeout=2)
-        sm, mx, reasons = [], None, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
-            parts = [p.strip() for p in ln.split(",")]
-            if len(parts) < 8:
-                continue
-            try:
-                sm.append(float(parts[0]))
-                mx = float(parts[1])
-            except ValueError:
-                continue
-            for nm, val in zip(names, parts[4:8]):
-                if val.lower() == "active":
-                    reasons.add(nm)
-        if not sm:
+        self.stop_flag.set()
+        self.thread.join(timeout=2)
+        if not self.samples:
             return None
-        sm.sort()
-        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+        sm = sorted(c for c, _ in self.samples)
+        reasons = set()
+        for _, r in self.samples:
+            for bit, name in self.REASONS.items():
+                if r & bit:
+                    reasons.add(name)
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": self.max_mhz, "reasons": sorted(reasons),
+                "samples": len(sm), "source": self.how}
+
+
+def _pci_bus_id(cuda_index):
+    """NVML-style PCI bus id ("0000:XX:00.0") of a CUDA device, from torch's properties."""
+    try:
+        import torch
+        p = torch.cuda.get_device_properties(cuda_index)
+        return f"{p.pci_domain_id:08x}:{p.pci_bus_id:02x}:{p.pci_device_id:02x}.0"
+    except Exception:
+        return None
 
 
 # ----------------------------------------------------------------------------- helpers
@@ -175,9 +205,9 @@ def bench_prefill(w, steps, warmup, world, peaks, want_e2e):
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
            torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     clocks = ClockSampler(dev.index)
+    clocks.start()
     barrier(world)
     torch.cuda.synchronize()
-    clocks.start()
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
@@ -199,7 +229,8 @@ def bench_prefill(w, steps, warmup, world, peaks, want_e2e):
     ms_step = total_ms / steps
     value = flops * world / (ms_step * 1e-3) / 1e12
 
-    # retrieval heads alone (the tensor-core figure of merit)
+    # retrieval heads alone (the tensor-core figure of merit), one-shot: empty cache
+    layer.reset()
     sel = []
     for _ in range(max(3, warmup)):
         duo_attn_prefill_select(layer.handle, layer.cache, q, k, v, L, o, 2, stream)
@@ -404,7 +435,7 @@ def run_reference(args, w, world, rank):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="duo", choices=["duo", "reference"])
     ap.add_argument("--workload", default="llama3_8b_prefill32k")
