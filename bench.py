@@ -41,6 +41,27 @@ METRIC = "prefill attn TFLOP/s & decode KV-read GB/s, as % of GB300 roofline"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
+# DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from the ncu
+# captures summarised in profiles/, valid only for the kernel sources they were taken on.
+MEASURED_TRAFFIC = {
+    "prefill": {"src": ("prefill.cu", "duo_device.cuh", "duo_internal.h"), "sha1": "d90ca10f412132fa",
+                "bytes": 644.579840e6 + 232.985856e6},
+    "decode": {"src": ("decode.cu", "duo_device.cuh", "duo_internal.h"), "sha1": "17580c34e41f39c8",
+               "bytes": 1.074826e9 + 4.792832e6},
+}
+
+
+def measured_traffic(kernel):
+    """Traffic of the last ncu capture of `kernel`, or None if its sources changed since."""
+    import hashlib
+    rec = MEASURED_TRAFFIC[kernel]
+    m = hashlib.sha1()
+    for f in rec["src"]:
+        with open(os.path.join(ROOT, "streaming_kv_cache_duo_gb300", "csrc", f), "rb") as fh:
+            m.update(fh.read())
+    return rec["bytes"] if m.hexdigest()[:16] == rec["sha1"] else None
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -252,7 +273,7 @@ def bench_prefill(w, steps, warmup, world, peaks, want_e2e):
         "value": value, "ms_per_step": ms_step, "flops": flops,
         "prefill_ms": avg_prefill, "append_ms": sum(append_ms) / steps,
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
-                     "frac": round(achieved / peak, 4), "traffic": None,
+                     "frac": round(achieved / peak, 4), "traffic": measured_traffic("prefill"),
                      "kernel": "prefill_kernel<128>", "flops_per_launch": flops},
         "prefill_retrieval_only": {"tflops": round(fr / (sel_ms * 1e-3) / 1e12, 2), "ms": round(sel_ms, 4),
                                    "flops": fr, "frac_of_bf16_peak": round(fr / (sel_ms * 1e-3) / 1e12 / peak, 4)},
@@ -355,7 +376,8 @@ def bench_decode(w, steps_cap, peaks):
             "step_ms_with_append": round(step_ms, 4), "bytes_per_step": int(sum(nbytes) / len(nbytes)),
             "steps_timed": len(times),
             "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
-                         "frac": round(gbs / peak, 4), "traffic": None, "kernel": "decode_kernel<128,4>"}}
+                         "frac": round(gbs / peak, 4), "traffic": measured_traffic("decode"),
+                         "kernel": "decode_kernel<128,4>"}}
 
 
 # ----------------------------------------------------------------------------- oracle arm
