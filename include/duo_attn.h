@@ -155,6 +155,23 @@ size_t duo_decode_workspace_size(const duo_handle* handle, int64_t n);
 duo_status duo_attn_decode(duo_handle* handle, const duo_kv_cache* cache, const void* q, void* o, void* workspace,
                            size_t workspace_bytes, void* stream);
 
+/* duo_attn_decode without a workspace argument, for callers that cannot allocate
+ * device memory for scratch (an engine that has handed all device memory to its own
+ * pool, a loop that must not call cudaMalloc/cudaFree because they may synchronise,
+ * a runtime whose allocator owns every allocation). The pages have no counterpart:
+ * it is an interface variant of the decode step above and computes the same result.
+ * Scratch lives in a 2 MiB array inside the library (every GPU that loads the library
+ * holds it until the process exits); shapes whose scratch
+ * (duo_decode_workspace_size) exceeds 2 MiB get DUO_ERR_WORKSPACE. Nothing is
+ * allocated: no cudaMalloc, cudaFree or allocating library call. The first call on
+ * each device looks up the array's device address (cudaGetSymbolAddress); make that
+ * first call before any stream capture. Each call clears the array's counters with
+ * cudaMemsetAsync on `stream`. All calls on a device share the one array, so calls
+ * that overlap on the GPU (different streams, or several host threads) race: order
+ * them on one stream. */
+duo_status duo_attn_decode_static(duo_handle* handle, const duo_kv_cache* cache, const void* q, void* o,
+                                  void* stream);
+
 /* Synchronises the device, then returns (and clears) the OR of the error codes that
  * kernels of this library recorded when a bounded wait ran out; 0 = none. Sets
  * *code and returns DUO_ERR_DEVICE_TIMEOUT if it is nonzero. */

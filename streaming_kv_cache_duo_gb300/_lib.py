@@ -30,7 +30,7 @@ DUO_RETRIEVAL = 1
 EXPORTS = (
     "duo_classify_heads", "duo_create", "duo_destroy", "duo_cache_reset", "duo_kv_append",
     "duo_attn_prefill", "duo_attn_prefill_select", "duo_decode_workspace_size", "duo_attn_decode",
-    "duo_device_error", "duo_last_error", "duo_status_string",
+    "duo_attn_decode_static", "duo_device_error", "duo_last_error", "duo_status_string",
 )
 
 
@@ -76,6 +76,7 @@ def library() -> ctypes.CDLL:
         "duo_decode_workspace_size": (c_size_t, [c_void_p, c_int64]),
         "duo_attn_decode": (c_int32, [c_void_p, POINTER(duo_kv_cache), c_void_p, c_void_p, c_void_p, c_size_t,
                                       c_void_p]),
+        "duo_attn_decode_static": (c_int32, [c_void_p, POINTER(duo_kv_cache), c_void_p, c_void_p, c_void_p]),
         "duo_device_error": (c_int32, [POINTER(c_uint32)]),
         "duo_last_error": (c_char_p, []),
         "duo_status_string": (c_char_p, [c_int32]),
@@ -168,6 +169,12 @@ def duo_attn_decode(handle, cache: "duo_kv_cache", q, o, workspace, stream=None)
     nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(library().duo_attn_decode(handle, ctypes.byref(cache), _ptr(q), _ptr(o), _ptr(workspace), nbytes,
                                      _stream_ptr(stream)))
+
+
+def duo_attn_decode_static(handle, cache: "duo_kv_cache", q, o, stream=None) -> None:
+    """Decode with the library's built-in scratch array instead of a caller workspace,
+    for callers that cannot allocate device memory (see include/duo_attn.h)."""
+    _check(library().duo_attn_decode_static(handle, ctypes.byref(cache), _ptr(q), _ptr(o), _stream_ptr(stream)))
 
 
 def duo_device_error() -> int:

@@ -9,6 +9,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <new>
 #include <string>
 
@@ -422,3 +423,84 @@ duo_status duo_device_error(uint32_t* code) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Decode without a caller-provided workspace.
+//
+// Some callers cannot hand this library device memory for scratch: a serving
+// engine that reserved all device memory up front for its own pool, code that
+// must not call cudaMalloc/cudaFree because those calls can synchronise the
+// device or fragment memory in the middle of a latency-critical loop, or a host
+// runtime whose allocator owns every device allocation. For them,
+// duo_attn_decode_static() runs the same decode kernel with its scratch (the
+// per-unit arrival counters and the partial softmax results) in the array below,
+// which belongs to this library's module: every GPU that loads the library keeps
+// kStaticScratchBytes of device memory for it until the process exits.
+namespace {
+
+constexpr size_t kStaticScratchBytes = (size_t)2 << 20;  // 2 MiB
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_static_scratch_mu;
+void* g_static_scratch_addr[kMaxDevices];  // device address of the array, per device
+
+// Looks up the array's device address once per device. The name of a __device__
+// variable is only a host-side stand-in; kernels must be given this address.
+duo_status static_scratch_address(int device, void** out) {
+  if (device < 0 || device >= kMaxDevices) return fail(DUO_ERR_UNSUPPORTED, "device index %d >= %d", device, kMaxDevices);
+  std::lock_guard<std::mutex> lock(g_static_scratch_mu);
+  if (!g_static_scratch_addr[device]) {
+    void* ptr = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&ptr, g_static_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static decode scratch)");
+    if (!ptr) return fail(DUO_ERR_CUDA, "cudaGetSymbolAddress returned NULL for the static decode scratch");
+    g_static_scratch_addr[device] = ptr;
+  }
+  *out = g_static_scratch_addr[device];
+  return DUO_OK;
+}
+
+}  // namespace
+
+extern "C" duo_status duo_attn_decode_static(duo_handle* h, const duo_kv_cache* c, const void* q, void* o,
+                                             void* stream) {
+  duo_status st = check_handle(h);
+  if (st != DUO_OK) return st;
+  if ((st = check_cache(h, c, true, true)) != DUO_OK) return st;
+  if (c->n < 1) return fail(DUO_ERR_INVALID_ARG, "decode needs the query token appended first (cache->n >= 1)");
+  if (h->sh.n_ret > 0 && c->n > h->sh.cap) return fail(DUO_ERR_INVALID_ARG, "cache->n exceeds max_seq_len");
+  if (!q || !o || !aligned16(q) || !aligned16(o))
+    return fail(DUO_ERR_INVALID_ARG, "q / o NULL or not 16-byte aligned");
+  const size_t need = decode_workspace_bytes(h->sh, h->num_sms);
+  if (need > kStaticScratchBytes)
+    return fail(DUO_ERR_WORKSPACE,
+                "this shape needs %zu bytes of decode scratch, more than the %zu-byte built-in array; "
+                "use duo_attn_decode with a caller workspace",
+                need, kStaticScratchBytes);
+  void* scratch = nullptr;
+  if ((st = static_scratch_address(h->device, &scratch)) != DUO_OK) return st;
+  const Shape& sh = h->sh;
+  DecodeParams p;
+  decode_plan(h, c->n, &p);
+  const int64_t U = (int64_t)sh.B * sh.Hkv;
+  const size_t counter_bytes = ((size_t)U * 4 + 255) / 256 * 256;
+  // The counters must start at zero; the array keeps whatever the last call left.
+  cudaError_t e = cudaMemsetAsync(scratch, 0, counter_bytes, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(static decode scratch counters)");
+  p.q = static_cast<const uint16_t*>(q);
+  p.o = static_cast<uint16_t*>(o);
+  p.k_full = static_cast<const uint16_t*>(c->k_full);
+  p.v_full = static_cast<const uint16_t*>(c->v_full);
+  p.k_sr = static_cast<const uint16_t*>(c->k_sr);
+  p.v_sr = static_cast<const uint16_t*>(c->v_sr);
+  p.pos = c->pos;
+  p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)sh.D));
+  p.counters = static_cast<uint32_t*>(scratch);
+  p.partials = reinterpret_cast<float*>(static_cast<uint8_t*>(scratch) + counter_bytes);
+  p.sh = sh;
+  p.heads = h->heads;
+  cudaError_t ce = launch_decode(p, (cudaStream_t)stream);
+  if (ce != cudaSuccess) return cuda_fail(ce, "decode launch (static scratch)");
+  return ok();
+}
