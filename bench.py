@@ -171,7 +171,7 @@ def dist_setup():
         import torch.distributed as dist
         os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
         dist.init_process_group("gloo", rank=rank, world_size=world)
-    if torch.cuda.is_available():
+    if torch.cuda.is_available() and local < torch.cuda.device_count():
         torch.cuda.set_device(local)
     return rank, world, local
 
