@@ -177,6 +177,13 @@ duo_status duo_attn_decode_static(duo_handle* handle, const duo_kv_cache* cache,
  * *code and returns DUO_ERR_DEVICE_TIMEOUT if it is nonzero. */
 duo_status duo_device_error(uint32_t* code);
 
+/* Self-test of failure detection (the pages have no counterpart): launches one
+ * CTA that waits on an mbarrier nothing completes, with the same bounded wait
+ * the attention kernels use but a limit of limit_us microseconds (1 ... 10^6).
+ * The wait gives up and records an error code; a following duo_device_error()
+ * returns DUO_ERR_DEVICE_TIMEOUT, and the CUDA context stays usable. */
+duo_status duo_selftest_bounded_wait(uint32_t limit_us, void* stream);
+
 /* Message describing the last error of the calling host thread ("" if none). */
 const char* duo_last_error(void);
 

@@ -30,7 +30,8 @@ DUO_RETRIEVAL = 1
 EXPORTS = (
     "duo_classify_heads", "duo_create", "duo_destroy", "duo_cache_reset", "duo_kv_append",
     "duo_attn_prefill", "duo_attn_prefill_select", "duo_decode_workspace_size", "duo_attn_decode",
-    "duo_attn_decode_static", "duo_device_error", "duo_last_error", "duo_status_string",
+    "duo_attn_decode_static", "duo_device_error", "duo_selftest_bounded_wait", "duo_last_error",
+    "duo_status_string",
 )
 
 
@@ -78,6 +79,7 @@ def library() -> ctypes.CDLL:
                                       c_void_p]),
         "duo_attn_decode_static": (c_int32, [c_void_p, POINTER(duo_kv_cache), c_void_p, c_void_p, c_void_p]),
         "duo_device_error": (c_int32, [POINTER(c_uint32)]),
+        "duo_selftest_bounded_wait": (c_int32, [c_uint32, c_void_p]),
         "duo_last_error": (c_char_p, []),
         "duo_status_string": (c_char_p, [c_int32]),
     }
@@ -184,6 +186,11 @@ def duo_device_error() -> int:
     if st not in (DUO_OK, DUO_ERR_DEVICE_TIMEOUT):
         _check(st)
     return code.value
+
+
+def duo_selftest_bounded_wait(limit_us: int, stream=None) -> None:
+    """Launch a kernel whose bounded wait must run out (failure-detection self-test)."""
+    _check(library().duo_selftest_bounded_wait(limit_us, _stream_ptr(stream)))
 
 
 def duo_last_error() -> str:

@@ -25,7 +25,7 @@ FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", 
 
 LIBS = {
     os.path.join(PKG, "libduo_attn.so"): [os.path.join(CSRC, f) for f in
-                                          ("duo_api.cu", "append.cu", "decode.cu", "prefill.cu")],
+                                          ("duo_api.cu", "append.cu", "decode.cu", "prefill.cu", "selftest.cu")],
     os.path.join(ROOT, "duo_synth", "libduo_synth.so"): [os.path.join(ROOT, "duo_synth", "csrc", "synth.cu")],
 }
 

@@ -4,19 +4,28 @@
 // Work list. A "unit" is one (sequence, KV head): a retrieval unit holds n keys
 // (rows [0, n) of its full cache), a streaming unit min(n, S + R) ring slots.
 // Units are cut into tiles of kTK keys and all tiles are laid end to end; CTA c
-// takes tiles [c W / C, (c + 1) W / C), so every SM gets the same number of key
-// bytes whatever the mix of long retrieval and short streaming units (the
+// takes tiles [c W / C, (c + 1) W / C), so every SM streams the same number of
+// key bytes whatever the mix of long retrieval and short streaming units (the
 // transformers "Dynamic length in static cache" rule: only the n written
 // positions are read, never the capacity).
 //
-// Per CTA: one producer warp streams the K and V rows of each tile into a
-// 4-stage shared-memory ring with 1-D bulk copies (cp.async.bulk, completion on
-// an mbarrier); eight consumer warps read each K and V byte once for all g query
-// heads of the KV head. Each consumer lane owns 16 (or 8) dims of a key row:
-// 128-bit shared loads, fp32 dot products for the g heads, a warp-shuffle
-// reduction across the lanes of a key, an online softmax with lazy rescaling
-// (the running max moves only when a score exceeds it by 2^8), and fp32
-// accumulation of p * v.
+// Per CTA: eight warps; warp w owns keys [w kKPW, (w + 1) kKPW) of every tile and
+// streams its own rows of K and V into a private 3-stage shared-memory ring with
+// 1-D bulk copies (cp.async.bulk, completion on the warp's mbarrier). A warp
+// refills a stage as soon as it has finished with it, so no producer warp and no
+// cross-warp hand-off is needed, and each thread keeps up to 255 registers.
+//
+// Inside a warp, LPK lanes share a key row and each owns 16 (or 8) of its dims:
+// 128-bit shared loads, fp32 q pre-scaled by log2(e)/sqrt(D), packed fp32x2 FMAs
+// for q.k of all g query heads of the KV head (every K and V byte is read once
+// for all of them). The partial dot products are reduced across the lanes of a
+// key by a reduce-scatter: at each of the first log2(g) shuffle steps a lane
+// keeps half of its heads and sends the other half, so after log2(LPK) steps each
+// lane holds the full score of one head (lane-dependent head order makes every
+// step a plain add). The softmax then runs once per (key, head), the online
+// state (running max with lazy rescaling: it moves only when a score exceeds it
+// by 2^8, and running sum) is per lane for its head, and p of the other heads is
+// fetched by shuffles for the packed p.v FMAs.
 //
 // Merge. The part of a unit a CTA covers ("segment") ends with a cross-warp merge
 // in shared memory. A unit covered by one CTA is written out directly; otherwise
@@ -32,31 +41,38 @@ namespace {
 
 __device__ unsigned int g_decode_err;
 
-constexpr int kTK = kDecodeTK;
-constexpr int kStages = 4;
-constexpr int kCW = 8;  // consumer warps
-constexpr int kThreads = (kCW + 1) * 32;
+constexpr int kTK = kDecodeTK;  // keys per tile
+constexpr int kWarps = 8;
+constexpr int kThreads = kWarps * 32;
+constexpr int kKPW = kTK / kWarps;  // keys of a tile per warp
+constexpr int kNSW = 3;             // pipeline stages per warp
+
+constexpr int ilog2(int v) { return v <= 1 ? 0 : 1 + ilog2(v / 2); }
 
 template <int D, int G>
 struct Cfg {
   static constexpr int DPL = (G * 16 <= 64) ? 16 : 8;  // dims per lane
   static constexpr int LPK = D / DPL;                  // lanes per key
+  static constexpr int LB = ilog2(LPK);                // lane bits within a key group
+  static constexpr int GB = ilog2(G);                  // head bits
   static constexpr int KPI = 32 / LPK;                 // keys per warp iteration
-  static constexpr int KPW = kTK / kCW;                // keys per warp per tile
-  static constexpr int IT = KPW / KPI;                 // iterations per tile
+  static constexpr int IT = kKPW / KPI;                // iterations per tile
   static constexpr int CH = DPL / 8;                   // 16-byte chunks per lane
   static constexpr int ROW = D * 2;                    // bytes per key row
-  static constexpr int TILE = kTK * ROW;
-  static constexpr int STAGE = 2 * TILE;  // K tile, then V tile
-  static constexpr int RED = kCW * G * (D + 2);
-  static constexpr size_t SMEM = (size_t)kStages * STAGE + (size_t)RED * 4 + 256;
-  static_assert(IT >= 1 && KPW % KPI == 0, "tile split");
+  static constexpr int SLICE = kKPW * ROW;             // one warp's K (or V) rows of a tile
+  static constexpr int WSTAGE = 2 * SLICE;             // K slice then V slice
+  static constexpr int RING = kWarps * kNSW * WSTAGE;
+  static constexpr int RED = kWarps * G * (D + 2);
+  static constexpr size_t SMEM = (size_t)RING + (size_t)RED * 4 + 512;
+  static_assert(IT >= 1 && kKPW % KPI == 0, "tile split");
+  static_assert(G <= LPK, "every head needs a lane of each key group");
 };
 
 struct Unit {
   int b, kvh;
   bool streaming;
   int64_t keys;
+  int64_t ntiles;
   const uint16_t* kb;
   const uint16_t* vb;
 };
@@ -84,6 +100,7 @@ __device__ __forceinline__ Unit unit_info(const DecodeParams& p, int u) {
     x.kvh = p.heads.ret_head[ri];
     x.streaming = false;
     x.keys = p.n;
+    x.ntiles = p.tiles_r;
     const int64_t off = ((int64_t)x.b * p.sh.n_ret + ri) * p.sh.cap * D;
     x.kb = p.k_full + off;
     x.vb = p.v_full + off;
@@ -94,6 +111,7 @@ __device__ __forceinline__ Unit unit_info(const DecodeParams& p, int u) {
     x.kvh = p.heads.str_head[si];
     x.streaming = true;
     x.keys = p.nvalid;
+    x.ntiles = p.tiles_s;
     const int64_t off = ((int64_t)x.b * p.sh.n_str + si) * (int64_t)(p.sh.S + p.sh.R) * D;
     x.kb = p.k_sr + off;
     x.vb = p.v_sr + off;
@@ -101,8 +119,45 @@ __device__ __forceinline__ Unit unit_info(const DecodeParams& p, int u) {
   return x;
 }
 
-// Synchronisation of the consumer warps through an mbarrier (bounded wait).
-struct ConsumerSync {
+// Rows of local tile `lt` of a unit with `keys` keys that belong to warp w.
+__device__ __forceinline__ int warp_rows(int64_t keys, int64_t lt, int w) {
+  const int64_t r = keys - lt * kTK - (int64_t)w * kKPW;
+  return r <= 0 ? 0 : (r >= kKPW ? kKPW : (int)r);
+}
+
+// The tile this warp refills next, walked forward one tile at a time (no division).
+struct Cursor {
+  int64_t t;   // global tile index
+  int64_t lt;  // tile index within its unit
+  int u;
+  Unit x;
+  __device__ __forceinline__ void advance(const DecodeParams& p) {
+    ++t;
+    if (++lt == x.ntiles) {
+      lt = 0;
+      ++u;
+      if (u < p.U_r + p.U_s) x = unit_info(p, u);
+    }
+  }
+};
+
+template <int D, int G>
+__device__ __forceinline__ void issue_slice(const Cursor& cur, int w, uint8_t* stage, uint64_t* bar) {
+  using C = Cfg<D, G>;
+  const int rows = warp_rows(cur.x.keys, cur.lt, w);
+  const int64_t row0 = cur.lt * kTK + (int64_t)w * kKPW;
+  const uint32_t bytes = (uint32_t)rows * C::ROW;
+  mbar_arrive_expect_tx(bar, 2 * bytes);
+  if (rows > 0) {
+    bulk_g2s(stage, cur.x.kb + row0 * D, bytes, bar);
+    bulk_g2s(stage + C::SLICE, cur.x.vb + row0 * D, bytes, bar);
+  }
+}
+
+__device__ __forceinline__ float2 unpack2(uint32_t w) { return make_float2(bf16lo(w), bf16hi(w)); }
+
+// Synchronisation of the eight warps through an mbarrier (bounded wait).
+struct WarpSync {
   uint64_t* bar;
   uint32_t phase;
   __device__ __forceinline__ bool sync(DevError err) {
@@ -119,11 +174,9 @@ template <int D, int G>
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams p) {
   using C = Cfg<D, G>;
   extern __shared__ __align__(1024) uint8_t smem[];
-  uint8_t* stages = smem;
-  float* red = reinterpret_cast<float*>(smem + (size_t)kStages * C::STAGE);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)kStages * C::STAGE + (size_t)C::RED * 4);
-  uint64_t* empty = full + kStages;
-  uint64_t* segbar = empty + kStages;
+  float* red = reinterpret_cast<float*>(smem + C::RING);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::RING + (size_t)C::RED * 4);  // [kWarps][kNSW]
+  uint64_t* segbar = full + kWarps * kNSW;
   int* flag = reinterpret_cast<int*>(segbar + 1);
 
   const DevError err{&g_decode_err};
@@ -133,284 +186,298 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
   const int64_t t0 = (int64_t)c * p.W / p.C;
   // After any CTA of this kernel gave up a wait, later CTAs do no work.
   const int64_t t1 = (*(volatile unsigned int*)err.word != 0u) ? t0 : (int64_t)(c + 1) * p.W / p.C;
+  uint8_t* ring = smem + (size_t)warp * kNSW * C::WSTAGE;
+  uint64_t* wfull = full + warp * kNSW;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kCW);
-    }
-    mbar_init(segbar, kCW);
+    for (int s = 0; s < kWarps * kNSW; ++s) mbar_init(&full[s], 1);
+    mbar_init(segbar, kWarps);
     fence_mbarrier_init();
   }
   __syncthreads();
 
-  if (warp == kCW) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      int64_t j = 0;
-      bool ok = true;
-      for (int64_t t = t0; t < t1 && ok; ++t, ++j) {
-        const int u = unit_of(p, t);
-        const Unit x = unit_info(p, u);
-        const int64_t lt = t - unit_start(p, u);
-        const int64_t rem = x.keys - lt * kTK;
-        const int rows = rem < kTK ? (int)rem : kTK;
-        const int s = (int)(j % kStages);
-        const uint32_t ph = (uint32_t)((j / kStages) & 1);
-        if (!mbar_wait(&empty[s], ph ^ 1u, err, kErrDecodeProducer)) {
-          ok = false;
-          break;
+  // refill cursor (warp-uniform); the prologue issues the first kNSW - 1 slices
+  Cursor cur;
+  cur.t = t0;
+  cur.u = t0 < t1 ? unit_of(p, t0) : 0;
+  cur.lt = 0;
+  if (t0 < t1) {
+    cur.x = unit_info(p, cur.u);
+    cur.lt = t0 - unit_start(p, cur.u);
+  }
+  int64_t issued = 0;
+  for (int s = 0; s < kNSW - 1 && cur.t < t1; ++s) {
+    if (lane == 0) issue_slice<D, G>(cur, warp, ring + s * C::WSTAGE, &wfull[s]);
+    cur.advance(p);
+    ++issued;
+  }
+
+  const int kg = lane / C::LPK;           // key within the warp iteration
+  const int cl = lane % C::LPK;           // dims slot of this lane within its key group
+  const int hme = cl >> (C::LB - C::GB);  // the head this lane ends up owning
+  const int SR = p.sh.S + p.sh.R;
+  const int64_t pq = p.n - 1;  // query position
+  WarpSync ws{segbar, 0};
+  int64_t j = 0;  // tiles consumed
+  bool ok = true;
+  for (int64_t t = t0; t < t1 && ok;) {
+    const int u = unit_of(p, t);
+    const int64_t us = unit_start(p, u);
+    const Unit x = unit_info(p, u);
+    const int64_t ue = us + x.ntiles;
+    const int64_t te = ue < t1 ? ue : t1;
+
+    // q of head (hme ^ l) in slot l, this lane's dims, pre-scaled, as fp32 pairs
+    float2 q2[G][C::DPL / 2];
+#pragma unroll
+    for (int l = 0; l < G; ++l) {
+      const uint16_t* qh = p.q + ((int64_t)x.b * p.sh.Hq + (int64_t)x.kvh * G + (hme ^ l)) * D;
+#pragma unroll
+      for (int ch = 0; ch < C::CH; ++ch) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(qh + (cl + ch * C::LPK) * 8));
+        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = unpack2(w4[e]);
+          q2[l][ch * 4 + e] = make_float2(f.x * p.scale_log2, f.y * p.scale_log2);
         }
-        const uint32_t bytes = (uint32_t)rows * C::ROW;
-        mbar_arrive_expect_tx(&full[s], 2 * bytes);
-        uint8_t* sk = stages + (size_t)s * C::STAGE;
-        bulk_g2s(sk, x.kb + lt * kTK * D, bytes, &full[s]);
-        bulk_g2s(sk + C::TILE, x.vb + lt * kTK * D, bytes, &full[s]);
       }
-      // Copies still in flight (only after an early exit) land before the CTA ends.
-      const int64_t last = j;
-      for (int64_t jj = (last > kStages ? last - kStages : 0); jj < last; ++jj)
-        mbar_wait(&full[jj % kStages], (uint32_t)((jj / kStages) & 1), err, kErrDecodeProducer);
     }
-  } else {
-    // ------------------------------------------------------------ consumers
-    const int kg = lane / C::LPK;  // key within the warp iteration
-    const int cl = lane % C::LPK;  // chunk slot of this lane
-    const int SR = p.sh.S + p.sh.R;
-    const int64_t pq = p.n - 1;  // query position
-    ConsumerSync cs{segbar, 0};
-    int64_t j = 0;
-    bool ok = true;
-    for (int64_t t = t0; t < t1 && ok;) {
-      const int u = unit_of(p, t);
-      const int64_t us = unit_start(p, u);
-      const int64_t ue = unit_start(p, u + 1);
-      const int64_t te = ue < t1 ? ue : t1;
-      const Unit x = unit_info(p, u);
+    float2 o2[G][C::DPL / 2];
+#pragma unroll
+    for (int l = 0; l < G; ++l)
+#pragma unroll
+      for (int e = 0; e < C::DPL / 2; ++e) o2[l][e] = make_float2(0.f, 0.f);
+    float l_run = 0.f, m_run = -INFINITY;  // of head hme
 
-      // q of the g heads, this lane's dims, pre-scaled by log2(e) / sqrt(D) in fp32.
-      float qr[G][C::DPL];
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        const uint16_t* qh = p.q + ((int64_t)x.b * p.sh.Hq + (int64_t)x.kvh * G + h) * D;
-#pragma unroll
-        for (int ch = 0; ch < C::CH; ++ch) {
-          const uint4 v = __ldg(reinterpret_cast<const uint4*>(qh + (cl + ch * C::LPK) * 8));
-          const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            qr[h][ch * 8 + 2 * e] = bf16lo(w4[e]) * p.scale_log2;
-            qr[h][ch * 8 + 2 * e + 1] = bf16hi(w4[e]) * p.scale_log2;
-          }
-        }
+    for (; t < te; ++t, ++j) {
+      const int s = (int)(j % kNSW);
+      // refill: the stage used by tile j - 1 is free now (this warp finished it)
+      if (cur.t < t1) {
+        const int sn = (int)((j + kNSW - 1) % kNSW);
+        if (lane == 0) issue_slice<D, G>(cur, warp, ring + sn * C::WSTAGE, &wfull[sn]);
+        cur.advance(p);
+        ++issued;
       }
-      float acc_o[G][C::DPL];
-      float l[G], m[G];
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        l[h] = 0.f;
-        m[h] = -INFINITY;
-#pragma unroll
-        for (int e = 0; e < C::DPL; ++e) acc_o[h][e] = 0.f;
+      if (!mbar_wait(&wfull[s], (uint32_t)((j / kNSW) & 1), err, kErrDecodeConsumer)) {
+        ok = false;
+        break;
       }
+      const int64_t lt = t - us;
+      const int rows = warp_rows(x.keys, lt, warp);
+      const uint8_t* sk = ring + s * C::WSTAGE;
+      const uint8_t* sv = sk + C::SLICE;
+      const bool full_tile = rows == kKPW && !x.streaming;
 
-      for (; t < te; ++t, ++j) {
-        const int s = (int)(j % kStages);
-        if (!mbar_wait(&full[s], (uint32_t)((j / kStages) & 1), err, kErrDecodeConsumer)) {
-          ok = false;
-          break;
-        }
-        const int64_t lt = t - us;
-        const int64_t rem = x.keys - lt * kTK;
-        const int rows = rem < kTK ? (int)rem : kTK;
-        const uint8_t* sk = stages + (size_t)s * C::STAGE;
-        const uint8_t* sv = sk + C::TILE;
-
-        float sc[C::IT][G];
-        bool vis[C::IT];
+      float sc[C::IT];
+      bool vis[C::IT];
 #pragma unroll
-        for (int it = 0; it < C::IT; ++it) {
-          const int key = warp * C::KPW + it * C::KPI + kg;
-          bool valid = key < rows;
+      for (int it = 0; it < C::IT; ++it) {
+        const int key = it * C::KPI + kg;  // row within this warp's slice
+        bool valid = true;
+        if (!full_tile) {
+          valid = key < rows;
           if (x.streaming && valid) {
-            const int jp = __ldg(p.pos + (int64_t)x.b * SR + lt * kTK + key);
+            const int64_t slot = lt * kTK + (int64_t)warp * kKPW + key;
+            const int jp = __ldg(p.pos + (int64_t)x.b * SR + slot);
             valid = jp >= 0 && jp <= pq && (jp < p.sh.S || pq - jp < p.sh.R);
           }
-          vis[it] = valid;
-          float dot[G];
+        }
+        vis[it] = valid;
+        float2 acc[G];
 #pragma unroll
-          for (int h = 0; h < G; ++h) dot[h] = 0.f;
+        for (int l = 0; l < G; ++l) acc[l] = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int ch = 0; ch < C::CH; ++ch) {
+          const uint4 kv = *reinterpret_cast<const uint4*>(sk + key * C::ROW + (cl + ch * C::LPK) * 16);
+          const uint32_t w4[4] = {kv.x, kv.y, kv.z, kv.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 k2 = unpack2(w4[e]);
+#pragma unroll
+            for (int l = 0; l < G; ++l) acc[l] = __ffma2_rn(q2[l][ch * 4 + e], k2, acc[l]);
+          }
+        }
+        float dot[G];
+#pragma unroll
+        for (int l = 0; l < G; ++l) dot[l] = acc[l].x + acc[l].y;
+        // reduce-scatter over the high lane bits: keep the low half of the slots
+#pragma unroll
+        for (int k = 1; k <= C::GB; ++k) {
+          const int half = G >> k;
+          const int bit = 1 << (C::LB - k);
+#pragma unroll
+          for (int l = 0; l < half; ++l) dot[l] += __shfl_xor_sync(0xffffffffu, dot[l + half], bit);
+        }
+        // butterfly over the remaining lane bits
+#pragma unroll
+        for (int b = C::LB - C::GB - 1; b >= 0; --b) dot[0] += __shfl_xor_sync(0xffffffffu, dot[0], 1 << b);
+        sc[it] = valid ? dot[0] : -INFINITY;
+      }
+
+      // tile max of this lane's head over the warp, lazy rescale
+      float mx = sc[0];
+#pragma unroll
+      for (int it = 1; it < C::IT; ++it) mx = fmaxf(mx, sc[it]);
+#pragma unroll
+      for (int off = C::LPK; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+      const bool grow = mx > m_run + 8.f;
+      if (__any_sync(0xffffffffu, grow)) {
+        const float f = grow ? ex2_approx(m_run - mx) : 1.f;  // 0 when m was -inf
+        if (grow) {
+          l_run *= f;
+          m_run = mx;
+        }
+#pragma unroll
+        for (int l = 0; l < G; ++l) {
+          const float fl = __shfl_xor_sync(0xffffffffu, f, l << (C::LB - C::GB));
+          const float2 f2 = make_float2(fl, fl);
+#pragma unroll
+          for (int e = 0; e < C::DPL / 2; ++e) o2[l][e] = __fmul2_rn(o2[l][e], f2);
+        }
+      }
+#pragma unroll
+      for (int it = 0; it < C::IT; ++it) {
+        const float pv = vis[it] ? ex2_approx(sc[it] - m_run) : 0.f;
+        sc[it] = pv;
+        l_run += pv;
+      }
+#pragma unroll
+      for (int it = 0; it < C::IT; ++it) {
+        float pl[G];
+        pl[0] = sc[it];
+#pragma unroll
+        for (int l = 1; l < G; ++l) pl[l] = __shfl_xor_sync(0xffffffffu, sc[it], l << (C::LB - C::GB));
+        if (full_tile || vis[it]) {
+          const int key = it * C::KPI + kg;
 #pragma unroll
           for (int ch = 0; ch < C::CH; ++ch) {
-            const uint4 kv = *reinterpret_cast<const uint4*>(sk + key * C::ROW + (cl + ch * C::LPK) * 16);
-            const uint32_t w4[4] = {kv.x, kv.y, kv.z, kv.w};
+            const uint4 vv = *reinterpret_cast<const uint4*>(sv + key * C::ROW + (cl + ch * C::LPK) * 16);
+            const uint32_t w4[4] = {vv.x, vv.y, vv.z, vv.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const float k0 = bf16lo(w4[e]);
-              const float k1 = bf16hi(w4[e]);
+              const float2 v2 = unpack2(w4[e]);
 #pragma unroll
-              for (int h = 0; h < G; ++h) {
-                dot[h] = fmaf(qr[h][ch * 8 + 2 * e], k0, dot[h]);
-                dot[h] = fmaf(qr[h][ch * 8 + 2 * e + 1], k1, dot[h]);
-              }
+              for (int l = 0; l < G; ++l)
+                o2[l][ch * 4 + e] = __ffma2_rn(make_float2(pl[l], pl[l]), v2, o2[l][ch * 4 + e]);
             }
           }
-#pragma unroll
-          for (int off = 1; off < C::LPK; off <<= 1) {
-#pragma unroll
-            for (int h = 0; h < G; ++h) dot[h] += __shfl_xor_sync(0xffffffffu, dot[h], off);
-          }
-#pragma unroll
-          for (int h = 0; h < G; ++h) sc[it][h] = valid ? dot[h] : -INFINITY;
         }
+      }
+      __syncwarp();
+    }
+    if (!ok) break;
 
-        // tile max per head over the warp, lazy rescale of the running state
+    // ---------------------------------------------------- segment merge
+    // sum over the key groups of the warp (each holds other keys)
 #pragma unroll
-        for (int h = 0; h < G; ++h) {
-          float mx = sc[0][h];
+    for (int off = C::LPK; off < 32; off <<= 1) {
+      l_run += __shfl_xor_sync(0xffffffffu, l_run, off);
 #pragma unroll
-          for (int it = 1; it < C::IT; ++it) mx = fmaxf(mx, sc[it][h]);
+      for (int l = 0; l < G; ++l)
 #pragma unroll
-          for (int off = C::LPK; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-          if (mx > m[h] + 8.f) {
-            const float f = ex2_approx(m[h] - mx);  // 0 when m was -inf
-            l[h] *= f;
+        for (int e = 0; e < C::DPL / 2; ++e) {
+          const float2 o = make_float2(__shfl_xor_sync(0xffffffffu, o2[l][e].x, off),
+                                       __shfl_xor_sync(0xffffffffu, o2[l][e].y, off));
+          o2[l][e] = __fadd2_rn(o2[l][e], o);
+        }
+    }
+    if (kg == 0) {
 #pragma unroll
-            for (int e = 0; e < C::DPL; ++e) acc_o[h][e] *= f;
-            m[h] = mx;
+      for (int l = 0; l < G; ++l) {
+        float* r = red + (warp * G + (hme ^ l)) * (D + 2);
+#pragma unroll
+        for (int ch = 0; ch < C::CH; ++ch)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            r[(cl + ch * C::LPK) * 8 + 2 * e] = o2[l][ch * 4 + e].x;
+            r[(cl + ch * C::LPK) * 8 + 2 * e + 1] = o2[l][ch * 4 + e].y;
           }
-        }
-#pragma unroll
-        for (int it = 0; it < C::IT; ++it) {
-#pragma unroll
-          for (int h = 0; h < G; ++h) {
-            const float pv = vis[it] ? ex2_approx(sc[it][h] - m[h]) : 0.f;
-            sc[it][h] = pv;
-            l[h] += pv;
-          }
-        }
-#pragma unroll
-        for (int it = 0; it < C::IT; ++it) {
-          if (vis[it]) {
-            const int key = warp * C::KPW + it * C::KPI + kg;
-#pragma unroll
-            for (int ch = 0; ch < C::CH; ++ch) {
-              const uint4 vv = *reinterpret_cast<const uint4*>(sv + key * C::ROW + (cl + ch * C::LPK) * 16);
-              const uint32_t w4[4] = {vv.x, vv.y, vv.z, vv.w};
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const float v0 = bf16lo(w4[e]);
-                const float v1 = bf16hi(w4[e]);
-#pragma unroll
-                for (int h = 0; h < G; ++h) {
-                  acc_o[h][ch * 8 + 2 * e] = fmaf(sc[it][h], v0, acc_o[h][ch * 8 + 2 * e]);
-                  acc_o[h][ch * 8 + 2 * e + 1] = fmaf(sc[it][h], v1, acc_o[h][ch * 8 + 2 * e + 1]);
-                }
-              }
-            }
-          }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);
       }
-      if (!ok) break;
-
-      // ---------------------------------------------------- segment merge
-#pragma unroll
-      for (int off = C::LPK; off < 32; off <<= 1) {
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-          l[h] += __shfl_xor_sync(0xffffffffu, l[h], off);
-#pragma unroll
-          for (int e = 0; e < C::DPL; ++e) acc_o[h][e] += __shfl_xor_sync(0xffffffffu, acc_o[h][e], off);
-        }
-      }
-      if (kg == 0) {
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-          float* r = red + (warp * G + h) * (D + 2);
-#pragma unroll
-          for (int ch = 0; ch < C::CH; ++ch)
-#pragma unroll
-            for (int e = 0; e < 8; ++e) r[(cl + ch * C::LPK) * 8 + e] = acc_o[h][ch * 8 + e];
-          if (cl == 0) {
-            r[D] = m[h];
-            r[D + 1] = l[h];
-          }
-        }
-      }
-      if (!cs.sync(err)) {
-        ok = false;
-        break;
-      }
-      const int tid = threadIdx.x;  // 0 ... 255
-      const int c_first = cta_of(p, us);
-      const int n_parts = cta_of(p, ue - 1) - c_first + 1;
-      float* part = p.partials + (int64_t)(c + u) * G * (D + 2);
-      for (int e = tid; e < G * D; e += kCW * 32) {
-        const int h = e / D;
-        const int d = e % D;
-        float M = -INFINITY;
-        for (int w = 0; w < kCW; ++w) M = fmaxf(M, red[(w * G + h) * (D + 2) + D]);
-        float num = 0.f, den = 0.f;
-        for (int w = 0; w < kCW; ++w) {
-          const float* r = red + (w * G + h) * (D + 2);
-          const float f = r[D] == -INFINITY ? 0.f : ex2_approx(r[D] - M);
-          num = fmaf(f, r[d], num);
-          den = fmaf(f, r[D + 1], den);
-        }
-        if (n_parts == 1) {
-          p.o[((int64_t)x.b * p.sh.Hq + (int64_t)x.kvh * G + h) * D + d] = __bfloat16_as_ushort(__float2bfloat16_rn(num / den));
-        } else {
-          part[h * (D + 2) + d] = num;
-          if (d == 0) {
-            part[h * (D + 2) + D] = M;
-            part[h * (D + 2) + D + 1] = den;
-          }
-        }
-      }
-      if (n_parts > 1) {
-        __threadfence();
-        if (!cs.sync(err)) {
-          ok = false;
-          break;
-        }
-        if (tid == 0) {
-          const unsigned int old = atomicAdd(p.counters + u, 1u);
-          const int last = (old == (unsigned int)(n_parts - 1));
-          if (last) p.counters[u] = 0u;  // leave the counter at zero for the next call
-          *flag = last;
-        }
-        if (!cs.sync(err)) {
-          ok = false;
-          break;
-        }
-        if (*flag) {
-          __threadfence();
-          for (int e = tid; e < G * D; e += kCW * 32) {
-            const int h = e / D;
-            const int d = e % D;
-            float M = -INFINITY;
-            for (int cc = c_first; cc < c_first + n_parts; ++cc)
-              M = fmaxf(M, __ldcg(p.partials + ((int64_t)(cc + u) * G + h) * (D + 2) + D));
-            float num = 0.f, den = 0.f;
-            for (int cc = c_first; cc < c_first + n_parts; ++cc) {
-              const float* r = p.partials + ((int64_t)(cc + u) * G + h) * (D + 2);
-              const float mm = __ldcg(r + D);
-              const float f = mm == -INFINITY ? 0.f : ex2_approx(mm - M);
-              num = fmaf(f, __ldcg(r + d), num);
-              den = fmaf(f, __ldcg(r + D + 1), den);
-            }
-            p.o[((int64_t)x.b * p.sh.Hq + (int64_t)x.kvh * G + h) * D + d] = __bfloat16_as_ushort(__float2bfloat16_rn(num / den));
-          }
-        }
-      }
-      // the reduction buffer is reused by the next segment
-      if (!cs.sync(err)) {
-        ok = false;
-        break;
+      if ((cl & ((1 << (C::LB - C::GB)) - 1)) == 0) {  // one lane per head
+        float* r = red + (warp * G + hme) * (D + 2);
+        r[D] = m_run;
+        r[D + 1] = l_run;
       }
     }
+    if (!ws.sync(err)) {
+      ok = false;
+      break;
+    }
+    const int tid = threadIdx.x;
+    const int c_first = cta_of(p, us);
+    const int n_parts = cta_of(p, ue - 1) - c_first + 1;
+    float* part = p.partials + (int64_t)(c + u) * G * (D + 2);
+    for (int e = tid; e < G * D; e += kThreads) {
+      const int h = e / D;
+      const int d = e % D;
+      float M = -INFINITY;
+      for (int w = 0; w < kWarps; ++w) M = fmaxf(M, red[(w * G + h) * (D + 2) + D]);
+      float num = 0.f, den = 0.f;
+      for (int w = 0; w < kWarps; ++w) {
+        const float* r = red + (w * G + h) * (D + 2);
+        const float f = r[D] == -INFINITY ? 0.f : ex2_approx(r[D] - M);
+        num = fmaf(f, r[d], num);
+        den = fmaf(f, r[D + 1], den);
+      }
+      if (n_parts == 1) {
+        p.o[((int64_t)x.b * p.sh.Hq + (int64_t)x.kvh * G + h) * D + d] =
+            __bfloat16_as_ushort(__float2bfloat16_rn(num / den));
+      } else {
+        part[h * (D + 2) + d] = num;
+        if (d == 0) {
+          part[h * (D + 2) + D] = M;
+          part[h * (D + 2) + D + 1] = den;
+        }
+      }
+    }
+    if (n_parts > 1) {
+      __threadfence();
+      if (!ws.sync(err)) {
+        ok = false;
+        break;
+      }
+      if (tid == 0) {
+        const unsigned int old = atomicAdd(p.counters + u, 1u);
+        const int last = (old == (unsigned int)(n_parts - 1));
+        if (last) p.counters[u] = 0u;  // leave the counter at zero for the next call
+        *flag = last;
+      }
+      if (!ws.sync(err)) {
+        ok = false;
+        break;
+      }
+      if (*flag) {
+        __threadfence();
+        for (int e = tid; e < G * D; e += kThreads) {
+          const int h = e / D;
+          const int d = e % D;
+          float M = -INFINITY;
+          for (int cc = c_first; cc < c_first + n_parts; ++cc)
+            M = fmaxf(M, __ldcg(p.partials + ((int64_t)(cc + u) * G + h) * (D + 2) + D));
+          float num = 0.f, den = 0.f;
+          for (int cc = c_first; cc < c_first + n_parts; ++cc) {
+            const float* r = p.partials + ((int64_t)(cc + u) * G + h) * (D + 2);
+            const float mm = __ldcg(r + D);
+            const float f = mm == -INFINITY ? 0.f : ex2_approx(mm - M);
+            num = fmaf(f, __ldcg(r + d), num);
+            den = fmaf(f, __ldcg(r + D + 1), den);
+          }
+          p.o[((int64_t)x.b * p.sh.Hq + (int64_t)x.kvh * G + h) * D + d] =
+              __bfloat16_as_ushort(__float2bfloat16_rn(num / den));
+        }
+      }
+    }
+    // the reduction buffer is reused by the next segment
+    if (!ws.sync(err)) {
+      ok = false;
+      break;
+    }
+  }
+  // Copies still in flight (only after an early exit) land before the CTA ends.
+  if (lane == 0) {
+    for (int64_t jj = j; jj < issued; ++jj)
+      mbar_wait(&wfull[jj % kNSW], (uint32_t)((jj / kNSW) & 1), err, kErrDecodeConsumer);
   }
   __syncthreads();
 }

@@ -315,7 +315,7 @@ static duo_status prefill_impl(duo_handle* h, const duo_kv_cache* c, const void*
   p.n = c->n;
   p.T = T;
   p.nvalid = nvalid;
-  p.num_qt = (T + kPrefillBM - 1) / kPrefillBM;
+  p.num_qt = (T + kPrefillRowsPerCta - 1) / kPrefillRowsPerCta;
   const int64_t per_kind = (int64_t)sh.B * sh.g * p.num_qt;
   const int64_t ir = (kind_mask & 2) ? per_kind * sh.n_ret : 0;
   const int64_t is = (kind_mask & 1) ? per_kind * sh.n_str : 0;
@@ -413,12 +413,20 @@ duo_status duo_device_error(uint32_t* code) {
   if (!code) return fail(DUO_ERR_INVALID_ARG, "code is NULL");
   cudaError_t e = cudaDeviceSynchronize();
   if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
-  uint32_t a = 0, b = 0;
+  uint32_t a = 0, b = 0, t = 0;
   if ((e = prefill_read_clear_error(&a)) != cudaSuccess) return cuda_fail(e, "read prefill error word");
   if ((e = decode_read_clear_error(&b)) != cudaSuccess) return cuda_fail(e, "read decode error word");
-  *code = a | b;
+  if ((e = selftest_read_clear_error(&t)) != cudaSuccess) return cuda_fail(e, "read self-test error word");
+  *code = a | b | t;
   if (*code) g_error_epoch.fetch_add(1);
   if (*code) return fail(DUO_ERR_DEVICE_TIMEOUT, "a kernel gave up a bounded wait (code 0x%x)", *code);
+  return ok();
+}
+
+duo_status duo_selftest_bounded_wait(uint32_t limit_us, void* stream) {
+  if (limit_us < 1 || limit_us > 1000000) return fail(DUO_ERR_INVALID_ARG, "limit_us = %u outside [1, 10^6]", limit_us);
+  cudaError_t e = launch_selftest_wait((uint64_t)limit_us * 1000u, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "self-test launch");
   return ok();
 }
 

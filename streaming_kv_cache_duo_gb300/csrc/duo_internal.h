@@ -21,6 +21,7 @@ enum : uint32_t {
   kErrPrefillSoftmax = 1u << 2,
   kErrDecodeProducer = 1u << 8,
   kErrDecodeConsumer = 1u << 9,
+  kErrSelftest = 1u << 16,
 };
 
 struct Shape {
@@ -57,7 +58,7 @@ struct AppendParams {
 cudaError_t launch_append(const AppendParams& p, int num_sms, cudaStream_t stream);
 
 // ------------------------------------------------------------------ decode
-constexpr int kDecodeTK = 64;  // keys per decode tile
+constexpr int kDecodeTK = 128;  // keys per decode tile
 
 struct DecodeParams {
   const uint16_t* q;  // bf16 [B, Hq, D]
@@ -84,8 +85,9 @@ size_t decode_workspace_bytes(const Shape& sh, int num_ctas);
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream);
 
 // ------------------------------------------------------------------ prefill
-constexpr int kPrefillBM = 128;  // query rows per CTA tile
-constexpr int kPrefillBN = 128;  // keys per KV tile
+constexpr int kPrefillBM = 128;        // query rows per query tile
+constexpr int kPrefillBN = 128;        // keys per KV tile
+constexpr int kPrefillRowsPerCta = 256;  // two query tiles per CTA
 
 struct PrefillParams {
   CUtensorMap tm_q;      // 4-D over q [B, T, Hq, D], box 64 x 1 x 128 x 1, 128B swizzle
@@ -100,7 +102,7 @@ struct PrefillParams {
   int64_t n;             // cache length before the chunk (absolute position of row 0)
   int T;
   int nvalid;            // valid ring slots before the chunk
-  int num_qt;            // query tiles per head: ceil(T / 128)
+  int num_qt;            // 256-row query blocks per head: ceil(T / 256)
   int items_r;           // work items of retrieval heads: B * n_ret * g * num_qt
   int items_s;           // work items of streaming heads
   float scale_log2;
@@ -112,5 +114,7 @@ cudaError_t launch_prefill(const PrefillParams& p, cudaStream_t stream);
 // Error words of the kernel translation units (synchronous read-and-clear).
 cudaError_t prefill_read_clear_error(uint32_t* code);
 cudaError_t decode_read_clear_error(uint32_t* code);
+cudaError_t selftest_read_clear_error(uint32_t* code);
+cudaError_t launch_selftest_wait(uint64_t limit_ns, cudaStream_t stream);
 
 }  // namespace duo

@@ -9,23 +9,31 @@
 // one-shot prefill (n = 0) and each chunk of a chunked prefill against the
 // growing cache are the same kernel.
 //
-// One CTA computes one 128-row query tile of one query head:
-//   warp 4      TMA producer: Q once, then K and V tiles (128 keys x D, 128-byte
-//               swizzle) into a 2-stage ring, completion on mbarriers;
-//   warp 5      allocates 512 TMEM columns; one thread issues tcgen05.mma:
-//               S = Q K^T (A and B from shared memory) into one of two S
-//               buffers, and O += P V with P read from TMEM (bf16) and V from
-//               shared memory; tcgen05.commit signals each result;
-//   warps 0-3   softmax: thread r owns query row r (TMEM lane r): loads its S
-//               row with tcgen05.ld, masks it where the tile needs a mask,
-//               keeps the running max and sum in fp32 (exp2 with the scale
-//               log2(e)/sqrt(D) applied to the fp32 product), rescales O in TMEM
-//               only when the max grows by more than 2^8, writes P (bf16) to
-//               TMEM; at the end normalises O and stores it.
-// S_{j+1} is computed while the softmax works on S_j. Tiles that no row of the
-// query tile can see are never visited: a streaming head's query tile visits
-// the sink tile(s) and the <= 4 tiles of its window instead of all earlier tiles
-// (the block skipping of the block-sparse streaming attention the README uses).
+// One CTA computes two 128-row query tiles (256 consecutive query rows) of one
+// query head, sharing every K and V tile between them (12 warps; setmaxnreg
+// moves registers from the TMA/MMA warpgroup to the two softmax warpgroups):
+//   warp 8      TMA producer: both Q tiles once, then K and V tiles (128 keys x D,
+//               128-byte swizzle) into a 2-stage ring, completion on mbarriers;
+//   warp 9      allocates all 512 TMEM columns (per query tile: S, 128 columns,
+//               and O, D columns); one thread issues tcgen05.mma in the order
+//               S0(j), S1(j), PV0(j), S0(j+1), PV1(j), S1(j+1), ... so the tensor
+//               core always has the other tile's work while one softmax runs;
+//               P (bf16) overwrites the first 64 columns of its S buffer and is
+//               the TMEM A operand of O += P V (V MN-major in shared memory);
+//   warps 0-3   softmax of query tile 0, warps 4-7 softmax of query tile 1:
+//               thread r owns query row r (TMEM lane r): its whole S row in one
+//               TMEM round trip, row max with three-input max, fp32 running max
+//               and sum with exp2 and the
+//               scale log2(e)/sqrt(D) applied to the fp32 product, O rescaled in
+//               TMEM only when the max grows by more than 2^8, P packed to bf16;
+//               at the end O / sum is stored as bf16.
+// A commit after S_x(j) also covers PV_x(j-1) issued before it, so when the
+// softmax sees S_x(j) it may overwrite P_x(j-1) and rescale O_x without waiting
+// for anything else.
+// KV tiles that no row of the CTA can see are never visited: a streaming head's
+// CTA visits the sink tile(s), the ring tiles that can still be visible and the
+// <= 5 window tiles instead of all earlier tiles (the block skipping of the
+// block-sparse streaming attention the README uses).
 #include "duo_device.cuh"
 
 namespace duo {
@@ -33,23 +41,35 @@ namespace {
 
 __device__ unsigned int g_prefill_err;
 
-constexpr int BM = kPrefillBM;
-constexpr int BN = kPrefillBN;
+constexpr int BM = kPrefillBM;  // rows per query tile
+constexpr int BN = kPrefillBN;  // keys per KV tile
+constexpr int kQT = 2;          // query tiles per CTA
+constexpr int kRows = BM * kQT;
 constexpr int kNS = 2;  // K/V pipeline stages
-constexpr int kWarpTma = 4;
-constexpr int kWarpMma = 5;
-constexpr int kThreads = 192;
+constexpr int kWarpTma = 8;
+constexpr int kWarpMma = 9;
+constexpr int kThreads = 384;  // warpgroups: softmax 0, softmax 1, (TMA, MMA, 2 idle)
+// Register split: the block is launched with kLaunchRegs per thread (384 x 168 =
+// 64512); the third warpgroup drops to kRegsCtl, the softmax warpgroups rise to
+// kRegsSoftmax: 2 x 128 x 200 + 128 x 104 = 64512, exactly the launch total. The
+// host refuses to launch unless the compiled kernel uses kLaunchRegs.
+constexpr int kLaunchRegs = 168;
+constexpr int kRegsSoftmax = 200;
+constexpr int kRegsCtl = 104;
+static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsCtl <= kThreads * kLaunchRegs, "register split");
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256, kColP0 = 384, kColP1 = 448;
 constexpr int kBox = 128 * 128;  // bytes of a 128-row x 64-column bf16 box
+
+__host__ __device__ constexpr uint32_t col_s(int x) { return (uint32_t)x * 256u; }
+__host__ __device__ constexpr uint32_t col_o(int x) { return (uint32_t)x * 256u + 128u; }
 
 template <int D>
 struct PCfg {
   static constexpr int NBOX = D / 64;
-  static constexpr int Q_BYTES = BM * D * 2;
+  static constexpr int Q_BYTES = BM * D * 2;  // one query tile
   static constexpr int KV_BYTES = BN * D * 2;
   static constexpr int OFF_Q = 0;
-  static constexpr int OFF_K = OFF_Q + Q_BYTES;
+  static constexpr int OFF_K = OFF_Q + kQT * Q_BYTES;
   static constexpr int OFF_V = OFF_K + kNS * KV_BYTES;
   static constexpr int OFF_BAR = OFF_V + kNS * KV_BYTES;
   static constexpr size_t SMEM = (size_t)OFF_BAR + 256 + 1024;  // + alignment slack
@@ -59,14 +79,14 @@ struct Bars {
   uint64_t q_full;
   uint64_t k_full[kNS], k_empty[kNS];
   uint64_t v_full[kNS], v_empty[kNS];
-  uint64_t s_full[2], p_full[2], pv_done[2];
+  uint64_t s_full[kQT], p_full[kQT], o_final[kQT];
   uint64_t drain;
   uint32_t tmem_base;
 };
 
 struct Item {
   bool streaming;
-  int b, hq, kvh, cidx, qt;
+  int b, hq, kvh, cidx, qp;  // qp: index of the 256-row block of query rows
 };
 
 __device__ __forceinline__ Item item_of(const PrefillParams& p, int idx) {
@@ -81,10 +101,10 @@ __device__ __forceinline__ Item item_of(const PrefillParams& p, int idx) {
     it.streaming = true;
     nk = p.sh.n_str;
   }
-  const int per_qt = p.sh.B * nk * g;
-  const int qt_rev = idx / per_qt;  // longest query tiles first
-  int r = idx % per_qt;
-  it.qt = p.num_qt - 1 - qt_rev;
+  const int per_qp = p.sh.B * nk * g;
+  const int qp_rev = idx / per_qp;  // longest query blocks first
+  int r = idx % per_qp;
+  it.qp = p.num_qt - 1 - qp_rev;
   it.b = r / (nk * g);
   r %= nk * g;
   it.cidx = r / g;
@@ -93,30 +113,33 @@ __device__ __forceinline__ Item item_of(const PrefillParams& p, int idx) {
   return it;
 }
 
-// The KV tiles an item visits: first tiles of the cache (phase 0), then tiles of
-// the new tokens (phase 1).
+// The KV tiles a CTA visits: first tiles of the cache (phase 0), then tiles of
+// the new tokens (phase 1): [0, sink_eff) for sinks, then [w_lo, k_hi].
 struct TilePlan {
-  int n_cache;   // cache tiles visited
-  int sink_eff;  // new-token tiles [0, sink_eff) for sinks
-  int w_lo;      // then new-token tiles [w_lo, qt]
+  int n_cache;
+  int sink_eff;
+  int w_lo;
+  int k_hi;
   int total;
 };
 
 struct Tile {
   int phase;  // 0 = cache, 1 = new tokens
   int k;      // tile index within its source
-  bool masked;
 };
 
 __device__ __forceinline__ TilePlan plan_of(const PrefillParams& p, const Item& it) {
   TilePlan t;
+  const int q0 = it.qp * kRows;  // first query row (chunk-local) of the CTA
+  const int last_row = min(p.T, q0 + kRows) - 1;
+  t.k_hi = last_row / BN;
   if (!it.streaming) {
     t.n_cache = (int)((p.n + BN - 1) / BN);
     t.sink_eff = 0;
     t.w_lo = 0;
   } else {
     const int ring_tiles = (p.nvalid + BN - 1) / BN;
-    if ((int64_t)it.qt * BM + 1 < p.sh.R) {
+    if (q0 + 1 < p.sh.R) {
       t.n_cache = ring_tiles;  // the first rows still see ring entries
     } else {
       const int sinks = p.sh.S < p.nvalid ? p.sh.S : p.nvalid;
@@ -124,27 +147,70 @@ __device__ __forceinline__ TilePlan plan_of(const PrefillParams& p, const Item& 
     }
     const int64_t sink_cols = (int64_t)p.sh.S - p.n;  // new tokens that are sinks
     const int sink_tiles = sink_cols > 0 ? (int)((sink_cols + BN - 1) / BN) : 0;
-    const int64_t c_lo = (int64_t)it.qt * BM - p.sh.R + 1;
-    t.w_lo = c_lo > 0 ? (int)(c_lo / BN) : 0;
+    const int c_lo = q0 - p.sh.R + 1;
+    t.w_lo = c_lo > 0 ? c_lo / BN : 0;
     t.sink_eff = sink_tiles < t.w_lo ? sink_tiles : t.w_lo;
   }
-  t.total = t.n_cache + t.sink_eff + (it.qt - t.w_lo + 1);
+  t.total = t.n_cache + t.sink_eff + (t.k_hi - t.w_lo + 1);
   return t;
 }
 
-__device__ __forceinline__ Tile tile_at(const PrefillParams& p, const Item& it, const TilePlan& pl, int j) {
+__device__ __forceinline__ Tile tile_at(const TilePlan& pl, int j) {
   Tile t;
   if (j < pl.n_cache) {
     t.phase = 0;
     t.k = j;
-    t.masked = it.streaming || (int64_t)(j + 1) * BN > p.n;
   } else {
     j -= pl.n_cache;
     t.phase = 1;
     t.k = j < pl.sink_eff ? j : pl.w_lo + (j - pl.sink_eff);
-    t.masked = it.streaming || t.k == it.qt;
   }
   return t;
+}
+
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// Sets masked scores of one 32-column chunk to -inf (columns c0 ... c0+31 of tile t).
+__device__ __forceinline__ void mask_chunk(float* v, const PrefillParams& p, const Item& it, const Tile& t, int c0,
+                                           int i_abs) {
+  const int S = p.sh.S, R = p.sh.R;
+  if (t.phase == 1) {
+    const int j0 = (int)p.n + t.k * BN + c0;
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+      const int jp = j0 + e;
+      const int d = i_abs - jp;
+      const bool vis = d >= 0 && (!it.streaming || jp < S || d < R);
+      if (!vis) v[e] = -INFINITY;
+    }
+  } else if (!it.streaming) {
+    const int lim = (int)p.n - t.k * BN - c0;  // rows >= n hold no token
+#pragma unroll
+    for (int e = 0; e < 32; ++e)
+      if (e >= lim) v[e] = -INFINITY;
+  } else {
+    const int32_t* prow = p.pos + (int64_t)it.b * (S + R);
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+      const int slot = t.k * BN + c0 + e;
+      const int jp = slot < p.nvalid ? __ldg(prow + slot) : -1;
+      const bool vis = jp >= 0 && jp <= i_abs && (jp < S || i_abs - jp < R);
+      if (!vis) v[e] = -INFINITY;
+    }
+  }
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
 }
 
 template <int D>
@@ -174,10 +240,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       mbar_init(&bars->v_full[s], 1);
       mbar_init(&bars->v_empty[s], 1);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&bars->s_full[s], 1);
-      mbar_init(&bars->p_full[s], 4);
-      mbar_init(&bars->pv_done[s], 1);
+    for (int x = 0; x < kQT; ++x) {
+      mbar_init(&bars->s_full[x], 1);
+      mbar_init(&bars->p_full[x], 4);
+      mbar_init(&bars->o_final[x], 1);
     }
     mbar_init(&bars->drain, 1);
     fence_mbarrier_init();
@@ -190,177 +256,179 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
-
-  if (warp == kWarpTma) {
-    // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      prefetch_tmap(&p.tm_q);
-      mbar_arrive_expect_tx(&bars->q_full, C::Q_BYTES);
-#pragma unroll
-      for (int bx = 0; bx < C::NBOX; ++bx)
-        tma_load_4d(sQ + bx * kBox, &p.tm_q, bx * 64, it.hq, it.qt * BM, it.b, &bars->q_full);
-      bool ok = true;
-      int j = 0;
-      for (; j < ntiles && ok; ++j) {
-        const Tile t = tile_at(p, it, pl, j);
-        const int s = j % kNS;
-        const uint32_t ph = (uint32_t)((j / kNS) & 1);
-        // K
-        if (!mbar_wait(&bars->k_empty[s], ph ^ 1u, err, kErrPrefillProducer)) {
-          ok = false;
-          break;
+  if (warp >= 8) {
+    // ================================================ warpgroup 2: TMA, MMA, idle
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsCtl));
+    if (warp == kWarpTma) {
+      // ------------------------------------------------------------ TMA producer
+      if (lane == 0) {
+        prefetch_tmap(&p.tm_q);
+        mbar_arrive_expect_tx(&bars->q_full, kQT * C::Q_BYTES);
+  #pragma unroll
+        for (int x = 0; x < kQT; ++x)
+  #pragma unroll
+          for (int bx = 0; bx < C::NBOX; ++bx)
+            tma_load_4d(sQ + x * C::Q_BYTES + bx * kBox, &p.tm_q, bx * 64, it.hq, it.qp * kRows + x * BM, it.b,
+                        &bars->q_full);
+        bool ok = true;
+        int j = 0;
+        for (; j < ntiles && ok; ++j) {
+          const Tile t = tile_at(pl, j);
+          const int s = j % kNS;
+          const uint32_t ph = (uint32_t)((j / kNS) & 1);
+          if (!mbar_wait(&bars->k_empty[s], ph ^ 1u, err, kErrPrefillProducer)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&bars->k_full[s], C::KV_BYTES);
+          uint8_t* dk = sK + s * C::KV_BYTES;
+  #pragma unroll
+          for (int bx = 0; bx < C::NBOX; ++bx) {
+            if (t.phase == 1)
+              tma_load_4d(dk + bx * kBox, &p.tm_k, bx * 64, it.kvh, t.k * BN, it.b, &bars->k_full[s]);
+            else if (!it.streaming)
+              tma_load_3d(dk + bx * kBox, &p.tm_kfull, bx * 64, t.k * BN, it.b * p.sh.n_ret + it.cidx, &bars->k_full[s]);
+            else
+              tma_load_3d(dk + bx * kBox, &p.tm_ksr, bx * 64, t.k * BN, it.b * p.sh.n_str + it.cidx, &bars->k_full[s]);
+          }
+          if (!mbar_wait(&bars->v_empty[s], ph ^ 1u, err, kErrPrefillProducer)) {
+            ok = false;
+            ++j;  // the K copy of this tile is in flight
+            break;
+          }
+          mbar_arrive_expect_tx(&bars->v_full[s], C::KV_BYTES);
+          uint8_t* dv = sV + s * C::KV_BYTES;
+  #pragma unroll
+          for (int bx = 0; bx < C::NBOX; ++bx) {
+            if (t.phase == 1)
+              tma_load_4d(dv + bx * kBox, &p.tm_v, bx * 64, it.kvh, t.k * BN, it.b, &bars->v_full[s]);
+            else if (!it.streaming)
+              tma_load_3d(dv + bx * kBox, &p.tm_vfull, bx * 64, t.k * BN, it.b * p.sh.n_ret + it.cidx, &bars->v_full[s]);
+            else
+              tma_load_3d(dv + bx * kBox, &p.tm_vsr, bx * 64, t.k * BN, it.b * p.sh.n_str + it.cidx, &bars->v_full[s]);
+          }
         }
-        mbar_arrive_expect_tx(&bars->k_full[s], C::KV_BYTES);
-        uint8_t* dk = sK + s * C::KV_BYTES;
-#pragma unroll
-        for (int bx = 0; bx < C::NBOX; ++bx) {
-          if (t.phase == 1)
-            tma_load_4d(dk + bx * kBox, &p.tm_k, bx * 64, it.kvh, t.k * BN, it.b, &bars->k_full[s]);
-          else if (!it.streaming)
-            tma_load_3d(dk + bx * kBox, &p.tm_kfull, bx * 64, t.k * BN, it.b * p.sh.n_ret + it.cidx, &bars->k_full[s]);
-          else
-            tma_load_3d(dk + bx * kBox, &p.tm_ksr, bx * 64, t.k * BN, it.b * p.sh.n_str + it.cidx, &bars->k_full[s]);
-        }
-        // V
-        if (!mbar_wait(&bars->v_empty[s], ph ^ 1u, err, kErrPrefillProducer)) {
-          ok = false;
-          ++j;  // the K copy of this tile is in flight
-          break;
-        }
-        mbar_arrive_expect_tx(&bars->v_full[s], C::KV_BYTES);
-        uint8_t* dv = sV + s * C::KV_BYTES;
-#pragma unroll
-        for (int bx = 0; bx < C::NBOX; ++bx) {
-          if (t.phase == 1)
-            tma_load_4d(dv + bx * kBox, &p.tm_v, bx * 64, it.kvh, t.k * BN, it.b, &bars->v_full[s]);
-          else if (!it.streaming)
-            tma_load_3d(dv + bx * kBox, &p.tm_vfull, bx * 64, t.k * BN, it.b * p.sh.n_ret + it.cidx, &bars->v_full[s]);
-          else
-            tma_load_3d(dv + bx * kBox, &p.tm_vsr, bx * 64, t.k * BN, it.b * p.sh.n_str + it.cidx, &bars->v_full[s]);
+        if (!ok) {
+          // after an early exit, let the copies already issued land before the CTA ends
+          mbar_wait(&bars->q_full, 0, err, kErrPrefillProducer);
+          for (int jj = (j > kNS ? j - kNS : 0); jj < j; ++jj) {
+            mbar_wait(&bars->k_full[jj % kNS], (uint32_t)((jj / kNS) & 1), err, kErrPrefillProducer);
+            mbar_wait(&bars->v_full[jj % kNS], (uint32_t)((jj / kNS) & 1), err, kErrPrefillProducer);
+          }
         }
       }
-      if (!ok) {
-        // after an early exit, let the copies already issued land before the CTA ends
-        mbar_wait(&bars->q_full, 0, err, kErrPrefillProducer);
-        for (int jj = (j > kNS ? j - kNS : 0); jj < j; ++jj) {
-          mbar_wait(&bars->k_full[jj % kNS], (uint32_t)((jj / kNS) & 1), err, kErrPrefillProducer);
-          mbar_wait(&bars->v_full[jj % kNS], (uint32_t)((jj / kNS) & 1), err, kErrPrefillProducer);
-        }
-      }
-    }
-  } else if (warp == kWarpMma) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_bf16_f32(BM, BN, 0, 0);
-      constexpr uint32_t idesc_pv = idesc_bf16_f32(BM, D, 0, 1);
-      const uint32_t sQa = smem_u32(sQ);
-      bool ok = mbar_wait(&bars->q_full, 0, err, kErrPrefillMma);
-      auto issue_s = [&](int jj) -> bool {
-        const int s = jj % kNS;
-        if (!mbar_wait(&bars->k_full[s], (uint32_t)((jj / kNS) & 1), err, kErrPrefillMma)) return false;
-        tc_fence_after();
-        const uint32_t sKa = smem_u32(sK + s * C::KV_BYTES);
-        const uint32_t dS = tmem + ((jj & 1) ? kColS1 : kColS0);
+    } else if (warp == kWarpMma) {
+      // ------------------------------------------------------------ MMA issuer
+      if (lane == 0) {
+        constexpr uint32_t idesc_s = idesc_bf16_f32(BM, BN, 0, 0);
+        constexpr uint32_t idesc_pv = idesc_bf16_f32(BM, D, 0, 1);
+        bool ok = mbar_wait(&bars->q_full, 0, err, kErrPrefillMma);
+        // Descriptors are built once; a k-step only moves the start address, which
+      // lives in the low bits (address >> 4 < 2^14, so the add never carries out).
+      const uint64_t dq0 = smem_desc_sw128(smem_u32(sQ), 16, 1024);
+      const uint64_t dk0 = smem_desc_sw128(smem_u32(sK), 16, 1024);
+      const uint64_t dv0 = smem_desc_sw128(smem_u32(sV), kBox, 1024);
+      // S_x(jj) = Q_x K(jj)^T
+      auto issue_s = [&](int x, int jj) {
+        const uint64_t dq = dq0 + (uint64_t)((x * C::Q_BYTES) >> 4);
+        const uint64_t dk = dk0 + (uint64_t)(((jj % kNS) * C::KV_BYTES) >> 4);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t koff = (kk >> 2) * kBox + (kk & 3) * 32;
-          mma_ss(dS, smem_desc_sw128(sQa + koff, 16, 1024), smem_desc_sw128(sKa + koff, 16, 1024), idesc_s,
-                 kk > 0 ? 1u : 0u);
+          const uint32_t koff = ((kk >> 2) * kBox + (kk & 3) * 32) >> 4;
+          mma_ss(tmem + col_s(x), dq + koff, dk + koff, idesc_s, kk > 0 ? 1u : 0u);
         }
-        tc_commit(&bars->s_full[jj & 1]);
-        tc_commit(&bars->k_empty[s]);
-        return true;
+        tc_commit(&bars->s_full[x]);
       };
-      if (ok && ntiles > 0) ok = issue_s(0);
-      if (ok && ntiles > 1) ok = issue_s(1);
-      for (int j = 0; j < ntiles && ok; ++j) {
-        const int s = j % kNS;
-        if (!mbar_wait(&bars->p_full[j & 1], (uint32_t)((j >> 1) & 1), err, kErrPrefillMma)) {
-          ok = false;
-          break;
-        }
-        if (!mbar_wait(&bars->v_full[s], (uint32_t)((j / kNS) & 1), err, kErrPrefillMma)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t sVa = smem_u32(sV + s * C::KV_BYTES);
-        const uint32_t aP = tmem + ((j & 1) ? kColP1 : kColP0);
+      // O_x += P_x(jj) V(jj)
+      auto issue_pv = [&](int x, int jj) {
+        const uint64_t dv = dv0 + (uint64_t)(((jj % kNS) * C::KV_BYTES) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk) {
-          mma_ts(tmem + kColO, aP + kk * 8, smem_desc_sw128(sVa + kk * 2048, kBox, 1024), idesc_pv,
-                 (j > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < BN / 16; ++kk)
+          mma_ts(tmem + col_o(x), tmem + col_s(x) + kk * 8, dv + (uint64_t)((kk * 2048) >> 4), idesc_pv,
+                 (jj > 0 || kk > 0) ? 1u : 0u);
+      };
+      if (ok && ntiles > 0) {
+          ok = mbar_wait(&bars->k_full[0], 0, err, kErrPrefillMma);
+          if (ok) {
+            tc_fence_after();
+            issue_s(0, 0);
+            issue_s(1, 0);
+            tc_commit(&bars->k_empty[0]);
+          }
         }
-        tc_commit(&bars->pv_done[j & 1]);
-        tc_commit(&bars->v_empty[s]);
-        if (j + 2 < ntiles) ok = issue_s(j + 2);
+        for (int j = 0; j < ntiles && ok; ++j) {
+          const int s = j % kNS;
+          const bool more = j + 1 < ntiles;
+          if (!mbar_wait(&bars->v_full[s], (uint32_t)((j / kNS) & 1), err, kErrPrefillMma)) {
+            ok = false;
+            break;
+          }
+          if (more && !mbar_wait(&bars->k_full[(j + 1) % kNS], (uint32_t)(((j + 1) / kNS) & 1), err, kErrPrefillMma)) {
+            ok = false;
+            break;
+          }
+          for (int x = 0; x < kQT && ok; ++x) {
+            if (!mbar_wait(&bars->p_full[x], (uint32_t)(j & 1), err, kErrPrefillMma)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_pv(x, j);
+            if (!more) tc_commit(&bars->o_final[x]);
+            if (more) issue_s(x, j + 1);
+          }
+          if (!ok) break;
+          tc_commit(&bars->v_empty[s]);
+          if (more) tc_commit(&bars->k_empty[(j + 1) % kNS]);
+        }
+        // every MMA this thread issued has finished before TMEM is released
+        tc_commit(&bars->drain);
+        mbar_wait(&bars->drain, 0, err, kErrPrefillMma);
       }
-      // every MMA this thread issued has finished before TMEM is released
-      tc_commit(&bars->drain);
-      mbar_wait(&bars->drain, 0, err, kErrPrefillMma);
     }
   } else {
-    // ------------------------------------------------------------ softmax (warps 0-3)
-    const int r = warp * 32 + lane;  // query row within the tile == TMEM lane
-    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
-    const int i_abs = (int)p.n + it.qt * BM + r;  // absolute query position (< 2^31, checked on the host)
-    const int S = p.sh.S, R = p.sh.R;
+    // ================================================ warpgroups 0, 1: softmax
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
+    const int x = warp >> 2;                     // query tile of this warpgroup
+    const int r = (warp & 3) * 32 + lane;        // row within the tile == TMEM lane
+    const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    const uint32_t sbase = lane_base + col_s(x);
+    const uint32_t obase = lane_base + col_o(x);
+    const int row_local = it.qp * kRows + x * BM + r;  // chunk-local query row
+    const int i_abs = (int)p.n + row_local;            // absolute position (< 2^31, checked on the host)
     const float sl2 = p.scale_log2;
-    const int SR = S + R;
+    const int q_last = x == 0 ? it.qp * kQT : it.qp * kQT + 1;  // diagonal tile of this query tile
     float m_run = -INFINITY;  // running max of scaled scores (log2 units)
     float l_run = 0.f;
     bool ok = true;
     for (int j = 0; j < ntiles && ok; ++j) {
-      const Tile t = tile_at(p, it, pl, j);
-      if (!mbar_wait(&bars->s_full[j & 1], (uint32_t)((j >> 1) & 1), err, kErrPrefillSoftmax)) {
+      const Tile t = tile_at(pl, j);
+      const bool masked = it.streaming || (t.phase == 0 ? (int64_t)(t.k + 1) * BN > p.n : t.k >= q_last);
+      if (!mbar_wait(&bars->s_full[x], (uint32_t)(j & 1), err, kErrPrefillSoftmax)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      float sc[BN];
+      // the whole S row of this thread in one TMEM round trip
+      float v[BN];
       {
-        const uint32_t sbase = lane_base + ((j & 1) ? kColS1 : kColS0);
+        uint32_t raw[BN];
+        tmem_ld128_sync(sbase, raw);
 #pragma unroll
-        for (int q4 = 0; q4 < BN / 32; ++q4) {
-          uint32_t raw[32];
-          tmem_ld32_sync(sbase + q4 * 32, raw);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) sc[q4 * 32 + e] = __uint_as_float(raw[e]);
-        }
+        for (int e = 0; e < BN; ++e) v[e] = __uint_as_float(raw[e]);
       }
-      if (t.masked) {
-        if (t.phase == 1) {
-          // new tokens: key position n + k*BN + c; d = i - j
-          const int d0 = i_abs - (p.n + t.k * BN);
+      if (masked) {
 #pragma unroll
-          for (int c = 0; c < BN; ++c) {
-            const int d = d0 - c;
-            const int jp = p.n + t.k * BN + c;
-            const bool vis = d >= 0 && (!it.streaming || jp < S || d < R);
-            if (!vis) sc[c] = -INFINITY;
-          }
-        } else if (!it.streaming) {
-          // retrieval cache: rows >= n hold no token
-          const int lim = p.n - t.k * BN;
-#pragma unroll
-          for (int c = 0; c < BN; ++c)
-            if (c >= lim) sc[c] = -INFINITY;
-        } else {
-          // sink + ring cache: the position of each slot comes from pos[]
-          const int32_t* prow = p.pos + (int64_t)it.b * SR;
-#pragma unroll
-          for (int c = 0; c < BN; ++c) {
-            const int slot = t.k * BN + c;
-            const int jp = slot < p.nvalid ? __ldg(prow + slot) : -1;
-            const bool vis = jp >= 0 && jp <= i_abs && (jp < S || i_abs - jp < R);
-            if (!vis) sc[c] = -INFINITY;
-          }
-        }
+        for (int q4 = 0; q4 < BN / 32; ++q4) mask_chunk(v + q4 * 32, p, it, t, q4 * 32, i_abs);
       }
-      float mx4[4] = {sc[0], sc[1], sc[2], sc[3]};
+      float mxa = v[0], mxb = v[1];
 #pragma unroll
-      for (int c = 4; c < BN; ++c) mx4[c & 3] = fmaxf(mx4[c & 3], sc[c]);
-      const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+      for (int e = 2; e < BN; e += 4) {
+        mxa = max3(mxa, v[e], v[e + 1]);
+        if (e + 3 < BN) mxb = max3(mxb, v[e + 2], v[e + 3]);
+        else mxb = fmaxf(mxb, v[e + 2]);
+      }
+      const float mx = fmaxf(mxa, mxb);
       const float mx_s = mx * sl2;
       float f = 1.f;
       if (mx_s > m_run + 8.f) {
@@ -368,61 +436,48 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         l_run *= f;
         m_run = mx_s;
       }
-      // P of tile j overwrites P of tile j - 2: PV(j - 2) must be done
-      if (j >= 2 && !mbar_wait(&bars->pv_done[j & 1], (uint32_t)(((j - 2) >> 1) & 1), err, kErrPrefillSoftmax)) {
-        ok = false;
-        break;
-      }
-      // O rescale (rare): needs PV(j - 1) done
+      // O rescale (rare); PV_x(j-1) is complete since S_x(j) is
       if (__any_sync(0xffffffffu, f != 1.f && j > 0)) {
-        if (!mbar_wait(&bars->pv_done[(j - 1) & 1], (uint32_t)(((j - 1) >> 1) & 1), err, kErrPrefillSoftmax)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
 #pragma unroll 1
         for (int q4 = 0; q4 < D / 32; ++q4) {
           uint32_t ov[32];
-          tmem_ld32_sync(lane_base + kColO + q4 * 32, ov);
+          tmem_ld32_sync(obase + q4 * 32, ov);
 #pragma unroll
           for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * f);
-          tmem_st32(lane_base + kColO + q4 * 32, ov);
+          tmem_st32(obase + q4 * 32, ov);
         }
-        tmem_wait_st();
       }
+      // P = exp2(s * scale - m), written over the first 64 columns of S
       const float m_use = m_run == -INFINITY ? 0.f : m_run;
-      float ls[4] = {0.f, 0.f, 0.f, 0.f};
-      const uint32_t pbase = lane_base + ((j & 1) ? kColP1 : kColP0);
+      float2 ls = make_float2(0.f, 0.f);
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t pk[32];
+      for (int q4 = 0; q4 < BN / 32; ++q4) {
+        uint32_t pk[16];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const float p0 = ex2_approx(fmaf(sc[h * 64 + 2 * e], sl2, -m_use));
-          const float p1 = ex2_approx(fmaf(sc[h * 64 + 2 * e + 1], sl2, -m_use));
-          ls[e & 3] += p0 + p1;
+        for (int e = 0; e < 16; ++e) {
+          const float p0 = ex2_approx(fmaf(v[q4 * 32 + 2 * e], sl2, -m_use));
+          const float p1 = ex2_approx(fmaf(v[q4 * 32 + 2 * e + 1], sl2, -m_use));
+          ls = __fadd2_rn(ls, make_float2(p0, p1));
           pk[e] = pack_bf16x2(p0, p1);
         }
-        tmem_st32(pbase + h * 32, pk);
+        tmem_st16(sbase + q4 * 16, pk);
       }
-      l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+      l_run += ls.x + ls.y;
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->p_full[j & 1]);
+      if (lane == 0) mbar_arrive(&bars->p_full[x]);
     }
     // ---------------------------------------------------------------- epilogue
-    if (ok && ntiles > 0 &&
-        mbar_wait(&bars->pv_done[(ntiles - 1) & 1], (uint32_t)(((ntiles - 1) >> 1) & 1), err, kErrPrefillSoftmax)) {
+    if (ok && ntiles > 0 && mbar_wait(&bars->o_final[x], 0, err, kErrPrefillSoftmax)) {
       tc_fence_after();
-      const int64_t t_row = (int64_t)it.qt * BM + r;
-      const bool store = t_row < p.T;
+      const bool store = row_local < p.T;
       const float inv = 1.f / l_run;
-      uint16_t* orow = p.o + (((int64_t)it.b * p.T + t_row) * p.sh.Hq + it.hq) * D;
+      uint16_t* orow = p.o + (((int64_t)it.b * p.T + row_local) * p.sh.Hq + it.hq) * D;
 #pragma unroll 1
       for (int q4 = 0; q4 < D / 32; ++q4) {
         uint32_t ov[32];
-        tmem_ld32_sync(lane_base + kColO + q4 * 32, ov);
+        tmem_ld32_sync(obase + q4 * 32, ov);
         if (store) {
           uint32_t pk[16];
 #pragma unroll
@@ -453,6 +508,15 @@ cudaError_t launch_t(const PrefillParams& p, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
+  static int regs = -1;
+  if (regs < 0) {
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, prefill_kernel<D>);
+    if (e != cudaSuccess) return e;
+    regs = fa.numRegs;
+  }
+  // the setmaxnreg split is sized for exactly this launch allocation
+  if (regs != kLaunchRegs) return cudaErrorInvalidConfiguration;
   const int grid = p.items_r + p.items_s;
   if (grid == 0) return cudaSuccess;
   prefill_kernel<D><<<grid, kThreads, C::SMEM, stream>>>(p);
