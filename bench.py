@@ -44,10 +44,10 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from the ncu
 # captures summarised in profiles/, valid only for the kernel sources they were taken on.
 MEASURED_TRAFFIC = {
-    "prefill": {"src": ("prefill.cu", "duo_device.cuh", "duo_internal.h"), "sha1": "d90ca10f412132fa",
-                "bytes": 644.579840e6 + 232.985856e6},
-    "decode": {"src": ("decode.cu", "duo_device.cuh", "duo_internal.h"), "sha1": "17580c34e41f39c8",
-               "bytes": 1.074826e9 + 4.792832e6},
+    "prefill": {"src": ("prefill.cu", "duo_device.cuh", "duo_internal.h"), "sha1": "baefd6a3b400300a",
+                "bytes": 570.968576e6 + 232.430336e6},
+    "decode": {"src": ("decode.cu", "duo_device.cuh", "duo_internal.h"), "sha1": "6e56680095835d47",
+               "bytes": 1.074851e9 + 3.965440e6},
 }
 
 

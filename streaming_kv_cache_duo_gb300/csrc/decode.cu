@@ -63,6 +63,7 @@ struct Cfg {
   static constexpr int WSTAGE = 2 * SLICE;             // K slice then V slice
   static constexpr int RING = kWarps * kNSW * WSTAGE;
   static constexpr int RED = kWarps * G * (D + 2);
+  static constexpr int PS = D + 4;  // floats per head of a partial in the workspace (16-byte multiple)
   static constexpr size_t SMEM = (size_t)RING + (size_t)RED * 4 + 512;
   static_assert(IT >= 1 && kKPW % KPI == 0, "tile split");
   static_assert(G <= LPK, "every head needs a lane of each key group");
@@ -407,7 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
     const int tid = threadIdx.x;
     const int c_first = cta_of(p, us);
     const int n_parts = cta_of(p, ue - 1) - c_first + 1;
-    float* part = p.partials + (int64_t)(c + u) * G * (D + 2);
+    float* part = p.partials + (int64_t)(c + u) * G * C::PS;
     for (int e = tid; e < G * D; e += kThreads) {
       const int h = e / D;
       const int d = e % D;
@@ -424,10 +425,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
         p.o[((int64_t)x.b * p.sh.Hq + (int64_t)x.kvh * G + h) * D + d] =
             __bfloat16_as_ushort(__float2bfloat16_rn(num / den));
       } else {
-        part[h * (D + 2) + d] = num;
+        part[h * C::PS + d] = num;
         if (d == 0) {
-          part[h * (D + 2) + D] = M;
-          part[h * (D + 2) + D + 1] = den;
+          part[h * C::PS + D] = M;
+          part[h * C::PS + D + 1] = den;
         }
       }
     }
@@ -448,23 +449,77 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
         break;
       }
       if (*flag) {
+        // Last CTA of the unit: merge its n_parts partials. Warps 0 .. g-1 find
+        // each head's max; then warp w takes partials w, w + 8, ..., each lane
+        // 16 (or more) consecutive outputs of one head with 128-bit loads, so the
+        // loads of all partials are in flight together; a shared-memory sum over
+        // the warps finishes it.
         __threadfence();
+        float* Mh = reinterpret_cast<float*>(flag + 4);  // [G]
+        if (warp < G) {
+          float mm = -INFINITY;
+          for (int cc = c_first + lane; cc < c_first + n_parts; cc += 32)
+            mm = fmaxf(mm, __ldcg(p.partials + ((int64_t)(cc + u) * G + warp) * C::PS + D));
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) mm = fmaxf(mm, __shfl_xor_sync(0xffffffffu, mm, off));
+          if (lane == 0) Mh[warp] = mm;
+        }
+        if (!ws.sync(err)) {
+          ok = false;
+          break;
+        }
+        constexpr int EPL = G * D / 32;  // outputs per lane (2 ... 32), all of one head
+        static_assert(EPL % 2 == 0 && D % EPL == 0, "merge split");
+        const int e0 = lane * EPL;
+        const int hl = e0 / D;
+        const int d0 = e0 % D;
+        const float Mhl = Mh[hl];
+        float acc[EPL];
+#pragma unroll
+        for (int k = 0; k < EPL; ++k) acc[k] = 0.f;
+        float den = 0.f;
+        for (int cc = c_first + warp; cc < c_first + n_parts; cc += kWarps) {
+          const float* r = p.partials + ((int64_t)(cc + u) * G + hl) * C::PS;
+          const float mm = __ldcg(r + D);
+          const float f = mm == -INFINITY ? 0.f : ex2_approx(mm - Mhl);
+          den = fmaf(f, __ldcg(r + D + 1), den);
+          if constexpr (EPL % 4 == 0) {
+#pragma unroll
+            for (int k = 0; k < EPL; k += 4) {
+              const float4 o4 = __ldcg(reinterpret_cast<const float4*>(r + d0 + k));
+              acc[k] = fmaf(f, o4.x, acc[k]);
+              acc[k + 1] = fmaf(f, o4.y, acc[k + 1]);
+              acc[k + 2] = fmaf(f, o4.z, acc[k + 2]);
+              acc[k + 3] = fmaf(f, o4.w, acc[k + 3]);
+            }
+          } else {
+#pragma unroll
+            for (int k = 0; k < EPL; k += 2) {
+              const float2 o2v = __ldcg(reinterpret_cast<const float2*>(r + d0 + k));
+              acc[k] = fmaf(f, o2v.x, acc[k]);
+              acc[k + 1] = fmaf(f, o2v.y, acc[k + 1]);
+            }
+          }
+        }
+        float* rw = red + (warp * G + hl) * (D + 2);
+#pragma unroll
+        for (int k = 0; k < EPL; ++k) rw[d0 + k] = acc[k];
+        if (d0 == 0) rw[D + 1] = den;
+        if (!ws.sync(err)) {
+          ok = false;
+          break;
+        }
         for (int e = tid; e < G * D; e += kThreads) {
           const int h = e / D;
           const int d = e % D;
-          float M = -INFINITY;
-          for (int cc = c_first; cc < c_first + n_parts; ++cc)
-            M = fmaxf(M, __ldcg(p.partials + ((int64_t)(cc + u) * G + h) * (D + 2) + D));
-          float num = 0.f, den = 0.f;
-          for (int cc = c_first; cc < c_first + n_parts; ++cc) {
-            const float* r = p.partials + ((int64_t)(cc + u) * G + h) * (D + 2);
-            const float mm = __ldcg(r + D);
-            const float f = mm == -INFINITY ? 0.f : ex2_approx(mm - M);
-            num = fmaf(f, __ldcg(r + d), num);
-            den = fmaf(f, __ldcg(r + D + 1), den);
+          float num = 0.f, dsum = 0.f;
+#pragma unroll
+          for (int w = 0; w < kWarps; ++w) {
+            num += red[(w * G + h) * (D + 2) + d];
+            dsum += red[(w * G + h) * (D + 2) + D + 1];
           }
           p.o[((int64_t)x.b * p.sh.Hq + (int64_t)x.kvh * G + h) * D + d] =
-              __bfloat16_as_ushort(__float2bfloat16_rn(num / den));
+              __bfloat16_as_ushort(__float2bfloat16_rn(num / dsum));
         }
       }
     }
@@ -500,7 +555,7 @@ cudaError_t launch_t(const DecodeParams& p, cudaStream_t stream) {
 size_t decode_workspace_bytes(const Shape& sh, int num_ctas) {
   const int64_t U = (int64_t)sh.B * sh.Hkv;
   const size_t counters = ((size_t)U * 4 + 255) / 256 * 256;
-  const size_t parts = (size_t)(num_ctas + U) * sh.g * (sh.D + 2) * 4;
+  const size_t parts = (size_t)(num_ctas + U) * sh.g * (sh.D + 4) * 4;  // Cfg::PS floats per head
   return counters + parts;
 }
 

@@ -77,7 +77,7 @@ struct DecodeParams {
   int C;           // CTAs; CTA c takes tiles [c W / C, (c+1) W / C)
   float scale_log2;    // log2(e) / sqrt(D)
   uint32_t* counters;  // [U_r + U_s] arrival tickets, left at zero
-  float* partials;     // [C + U_r + U_s][g][D + 2] (o, max, sum) per segment
+  float* partials;     // [C + U_r + U_s][g][D + 4] (o, max, sum, 2 pad) per segment
   Shape sh;
   HeadTable heads;
 };
