@@ -380,6 +380,69 @@ def bench_decode(w, steps_cap, peaks):
                          "kernel": "decode_kernel<128,4>"}}
 
 
+def bench_decode_graph(w, peaks):
+    """Batched decode with per-sequence lengths held on the device: one step (append one
+    token to every sequence, then decode) is captured once in a CUDA graph and replayed
+    for every decode step of the workload."""
+    import torch
+
+    import duo_synth as ds
+    from streaming_kv_cache_duo_gb300 import DuoLayer, duo_device_error, workload as wl
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+    kinds = w.is_retrieval
+    max_len = w.context + w.decode_steps
+    layer = DuoLayer(w.B, w.Hq, w.Hkv, w.D, w.S, w.R, max_len, kinds, device=dev)
+    chunk = 65536
+    for c0 in range(0, w.context, chunk):
+        T = min(chunk, w.context - c0)
+        kk = ds.stream_torch(w.seed, ds.STREAM_K, w.B, c0, T, w.Hkv, w.D, device=dev)
+        vv = ds.stream_torch(w.seed, ds.STREAM_V, w.B, c0, T, w.Hkv, w.D, device=dev)
+        layer.append(kk, vv)
+        del kk, vv
+    q = ds.stream_torch(w.seed, ds.STREAM_Q, w.B, w.context, w.decode_steps, w.Hq, w.D, device=dev)
+    kn = ds.stream_torch(w.seed, ds.STREAM_K, w.B, w.context, w.decode_steps, w.Hkv, w.D, device=dev)
+    vn = ds.stream_torch(w.seed, ds.STREAM_V, w.B, w.context, w.decode_steps, w.Hkv, w.D, device=dev)
+    seq_lens = torch.full((w.B,), w.context, dtype=torch.int32, device=dev)
+    sq = torch.empty((w.B, w.Hq, w.D), dtype=torch.bfloat16, device=dev)
+    sk = torch.empty((w.B, 1, w.Hkv, w.D), dtype=torch.bfloat16, device=dev)
+    sv = torch.empty_like(sk)
+    so = torch.empty_like(sq)
+    sq.copy_(q[:, 0])
+    sk.copy_(kn[:, 0:1])
+    sv.copy_(vn[:, 0:1])
+    layer.append_varlen(sk, sv, seq_lens)  # eager step 0 (clears the workspace counters)
+    layer.decode_varlen(sq, seq_lens, max_len, out=so)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        layer.append_varlen(sk, sv, seq_lens)
+        layer.decode_varlen(sq, seq_lens, max_len, out=so)
+    stream = torch.cuda.current_stream()
+    steps = w.decode_steps - 1
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for s_ in range(1, w.decode_steps):
+        sq.copy_(q[:, s_])
+        sk.copy_(kn[:, s_:s_ + 1])
+        sv.copy_(vn[:, s_:s_ + 1])
+        graph.replay()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if duo_device_error():
+        raise RuntimeError("a kernel reported an error")
+    ms = t0.elapsed_time(t1) / steps
+    nbytes = sum(sum(wl.decode_bytes(w.B, w.Hq, w.Hkv, w.D, w.S, w.R, kinds, w.context + s_ + 1))
+                 for s_ in range(1, w.decode_steps)) / steps
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    layer.close()
+    return {"workload": w.name, "value": round(gbs, 1), "unit": "GB/s", "step_ms": round(ms, 4),
+            "bytes_per_step": int(nbytes), "steps_timed": steps,
+            "how": "device-held sequence lengths; (append + decode) captured once in a CUDA graph and "
+                   "replayed; step time includes the three 1-token input copies",
+            "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 4)}
+
+
 # ----------------------------------------------------------------------------- oracle arm
 def oracle_prefill_sample(w, budget_s):
     """Time the CPU oracle on sampled rows of the prefill (rows of every head kind)."""
@@ -482,9 +545,10 @@ def main():
     __graft_entry__.build()
     peaks, peak_src = load_peaks()
     res = bench_prefill(w, args.steps, args.warmup, world, peaks, not args.no_e2e)
-    dec = None
+    dec = dec_graph = None
     if not args.no_decode:
         dec = bench_decode(ds.WORKLOADS["decode_ctx1m"], 64, peaks)
+        dec_graph = bench_decode_graph(ds.WORKLOADS["batched_decode_ctx128k"], peaks)
     if rank != 0:
         return
     cpu = None
@@ -505,6 +569,7 @@ def main():
         "roofline": res["roofline"],
         "prefill_retrieval_only": res["prefill_retrieval_only"],
         "decode": dec,
+        "decode_batched_graph": dec_graph,
         "cpu_baseline": cpu,
         "e2e": res.get("e2e"),
         "clocks": res["clocks"],

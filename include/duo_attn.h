@@ -172,9 +172,33 @@ duo_status duo_attn_decode(duo_handle* handle, const duo_kv_cache* cache, const 
 duo_status duo_attn_decode_static(duo_handle* handle, const duo_kv_cache* cache, const void* q, void* o,
                                   void* stream);
 
+/* Per-sequence lengths on the device: serving batches
+ * hold sequences of different lengths, and a decode step whose lengths live in device
+ * memory can be captured once in a CUDA graph and replayed step after step. The
+ * transformers pull request "[WIP] Dynamic length in static cache" debates exactly
+ * this: a length the compiled step reads at run time instead of a host integer.
+ *
+ * duo_kv_append_varlen: appends ONE token to every sequence b at position
+ * seq_lens[b] (int32 [B], device memory, read and then advanced by one on the device).
+ * k_new, v_new: bf16 [B, 1, Hkv, D]. Same slot rule as duo_kv_append. A sequence whose
+ * retrieval cache is full is left unchanged and duo_device_error() reports
+ * DUO_ERR_CAPACITY. cache->n is not used or changed. */
+duo_status duo_kv_append_varlen(duo_handle* handle, duo_kv_cache* cache, int32_t* seq_lens, const void* k_new,
+                                const void* v_new, void* stream);
+
+/* duo_attn_decode with per-sequence lengths: sequence b holds seq_lens[b] tokens
+ * (device int32 [B], values clamped to [0, max_len]) and its query is at position
+ * seq_lens[b] - 1. The work split is planned for max_len (host, 1 ... max_seq_len),
+ * so the launch shape does not depend on the device values; a sequence of length 0
+ * gets a zero output. cache->n is not used. Workspace as for duo_attn_decode. */
+duo_status duo_attn_decode_varlen(duo_handle* handle, const duo_kv_cache* cache, const int32_t* seq_lens,
+                                  int64_t max_len, const void* q, void* o, void* workspace, size_t workspace_bytes,
+                                  void* stream);
+
 /* Synchronises the device, then returns (and clears) the OR of the error codes that
- * kernels of this library recorded when a bounded wait ran out; 0 = none. Sets
- * *code and returns DUO_ERR_DEVICE_TIMEOUT if it is nonzero. */
+ * kernels of this library recorded when a bounded wait ran out, or when a device-side
+ * append met a full cache; 0 = none. Sets *code and returns DUO_ERR_DEVICE_TIMEOUT if
+ * a wait ran out, DUO_ERR_CAPACITY if the only error is a full cache. */
 duo_status duo_device_error(uint32_t* code);
 
 /* Self-test of failure detection (the pages have no counterpart): launches one

@@ -10,9 +10,10 @@ work counters used to report throughput (``workload``).
 from __future__ import annotations
 
 from . import _lib
-from ._lib import (DUO_RETRIEVAL, DUO_STREAMING, DuoError, duo_attn_decode, duo_attn_prefill,  # noqa: F401
-                   duo_attn_prefill_select, duo_cache_reset, duo_classify_heads, duo_create,
-                   duo_decode_workspace_size, duo_destroy, duo_device_error, duo_kv_append, duo_last_error)
+from ._lib import (DUO_RETRIEVAL, DUO_STREAMING, DuoError, duo_attn_decode, duo_attn_decode_varlen,  # noqa: F401
+                   duo_attn_prefill, duo_attn_prefill_select, duo_cache_reset, duo_classify_heads, duo_create,
+                   duo_decode_workspace_size, duo_destroy, duo_device_error, duo_kv_append, duo_kv_append_varlen,
+                   duo_last_error)
 
 
 class DuoLayer:
@@ -84,6 +85,24 @@ class DuoLayer:
         duo_attn_decode(self.handle, self.cache, q, out, self.workspace, stream)
         return out
 
+    def append_varlen(self, k_new, v_new, seq_lens, stream=None) -> None:
+        """One token per sequence at positions seq_lens (device int32 [B]), which advance by one."""
+        _lib._bf16(k_new, (self.B, 1, self.Hkv, self.D), "k_new")
+        _lib._bf16(v_new, (self.B, 1, self.Hkv, self.D), "v_new")
+        _check_lens(seq_lens, self.B)
+        duo_kv_append_varlen(self.handle, self.cache, seq_lens, k_new, v_new, stream)
+
+    def decode_varlen(self, q, seq_lens, max_len, out=None, stream=None):
+        """Decode where sequence b holds seq_lens[b] tokens (device int32 [B], <= max_len)."""
+        import torch
+        _lib._bf16(q, (self.B, self.Hq, self.D), "q")
+        _check_lens(seq_lens, self.B)
+        if out is None:
+            out = torch.empty_like(q)
+        _lib._bf16(out, (self.B, self.Hq, self.D), "o")
+        duo_attn_decode_varlen(self.handle, self.cache, seq_lens, max_len, q, out, self.workspace, stream)
+        return out
+
     def close(self) -> None:
         if getattr(self, "handle", None) is not None:
             duo_destroy(self.handle)
@@ -94,3 +113,9 @@ class DuoLayer:
             self.close()
         except Exception:
             pass
+
+
+def _check_lens(seq_lens, B):
+    import torch
+    if seq_lens.dtype != torch.int32 or not seq_lens.is_cuda or not seq_lens.is_contiguous() or seq_lens.numel() != B:
+        raise ValueError(f"seq_lens: need a contiguous CUDA int32 tensor of {B} elements")

@@ -30,8 +30,8 @@ DUO_RETRIEVAL = 1
 EXPORTS = (
     "duo_classify_heads", "duo_create", "duo_destroy", "duo_cache_reset", "duo_kv_append",
     "duo_attn_prefill", "duo_attn_prefill_select", "duo_decode_workspace_size", "duo_attn_decode",
-    "duo_attn_decode_static", "duo_device_error", "duo_selftest_bounded_wait", "duo_last_error",
-    "duo_status_string",
+    "duo_attn_decode_static", "duo_kv_append_varlen", "duo_attn_decode_varlen", "duo_device_error",
+    "duo_selftest_bounded_wait", "duo_last_error", "duo_status_string",
 )
 
 
@@ -78,6 +78,10 @@ def library() -> ctypes.CDLL:
         "duo_attn_decode": (c_int32, [c_void_p, POINTER(duo_kv_cache), c_void_p, c_void_p, c_void_p, c_size_t,
                                       c_void_p]),
         "duo_attn_decode_static": (c_int32, [c_void_p, POINTER(duo_kv_cache), c_void_p, c_void_p, c_void_p]),
+        "duo_kv_append_varlen": (c_int32, [c_void_p, POINTER(duo_kv_cache), c_void_p, c_void_p, c_void_p,
+                                           c_void_p]),
+        "duo_attn_decode_varlen": (c_int32, [c_void_p, POINTER(duo_kv_cache), c_void_p, c_int64, c_void_p, c_void_p,
+                                             c_void_p, c_size_t, c_void_p]),
         "duo_device_error": (c_int32, [POINTER(c_uint32)]),
         "duo_selftest_bounded_wait": (c_int32, [c_uint32, c_void_p]),
         "duo_last_error": (c_char_p, []),
@@ -179,11 +183,25 @@ def duo_attn_decode_static(handle, cache: "duo_kv_cache", q, o, stream=None) -> 
     _check(library().duo_attn_decode_static(handle, ctypes.byref(cache), _ptr(q), _ptr(o), _stream_ptr(stream)))
 
 
+def duo_kv_append_varlen(handle, cache: "duo_kv_cache", seq_lens, k_new, v_new, stream=None) -> None:
+    """One token per sequence at the device-held positions seq_lens (int32 [B]), then seq_lens += 1."""
+    _check(library().duo_kv_append_varlen(handle, ctypes.byref(cache), _ptr(seq_lens), _ptr(k_new), _ptr(v_new),
+                                          _stream_ptr(stream)))
+
+
+def duo_attn_decode_varlen(handle, cache: "duo_kv_cache", seq_lens, max_len: int, q, o, workspace,
+                           stream=None) -> None:
+    """Decode with per-sequence lengths read on the device (launch shape planned for max_len)."""
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(library().duo_attn_decode_varlen(handle, ctypes.byref(cache), _ptr(seq_lens), max_len, _ptr(q), _ptr(o),
+                                            _ptr(workspace), nbytes, _stream_ptr(stream)))
+
+
 def duo_device_error() -> int:
-    """Synchronise; return the kernels' bounded-wait error code (0 = none)."""
+    """Synchronise; return the kernels' recorded error code (0 = none)."""
     code = c_uint32()
     st = library().duo_device_error(ctypes.byref(code))
-    if st not in (DUO_OK, DUO_ERR_DEVICE_TIMEOUT):
+    if st not in (DUO_OK, DUO_ERR_DEVICE_TIMEOUT, DUO_ERR_CAPACITY):
         _check(st)
     return code.value
 

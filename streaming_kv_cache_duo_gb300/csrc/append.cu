@@ -71,7 +71,72 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendParams p) {
   }
 }
 
+__device__ unsigned int g_append_err;
+
+// One CTA per sequence: append its one new token at position n_b = seq_lens[b],
+// then advance seq_lens[b]. Every thread reads n_b before the barrier and only
+// thread 0 writes it after, and no other CTA touches sequence b, so the update
+// is race-free. A sequence whose retrieval cache is full is left unchanged and
+// the capacity error is recorded.
+__global__ void __launch_bounds__(256) append_varlen_kernel(const AppendParams p, int32_t* seq_lens) {
+  const int b = blockIdx.x;
+  const int D = p.sh.D;
+  const int Hkv = p.sh.Hkv;
+  const int vpr = D / 8;
+  const int SR = p.sh.S + p.sh.R;
+  const int64_t n = seq_lens[b];
+  const bool fits = n >= 0 && (p.sh.n_ret == 0 || n < p.sh.cap) && n < 0x7fffffff;
+  __syncthreads();
+  if (fits) {
+    const uint4* kin = reinterpret_cast<const uint4*>(p.k_new);
+    const uint4* vin = reinterpret_cast<const uint4*>(p.v_new);
+    const int64_t slot = n < p.sh.S ? n : p.sh.S + (n - p.sh.S) % p.sh.R;
+    for (int idx = threadIdx.x; idx < Hkv * vpr; idx += blockDim.x) {
+      const int h = idx / vpr;
+      const int v = idx % vpr;
+      const int64_t src = ((int64_t)b * Hkv + h) * vpr + v;
+      const uint4 kv = __ldg(kin + src);
+      const uint4 vv = __ldg(vin + src);
+      const int ki = p.heads.kidx[h];
+      if (p.heads.kind[h]) {
+        const int64_t dst = (((int64_t)b * p.sh.n_ret + ki) * p.sh.cap + n) * vpr + v;
+        reinterpret_cast<uint4*>(p.k_full)[dst] = kv;
+        reinterpret_cast<uint4*>(p.v_full)[dst] = vv;
+      } else {
+        const int64_t dst = (((int64_t)b * p.sh.n_str + ki) * SR + slot) * vpr + v;
+        reinterpret_cast<uint4*>(p.k_sr)[dst] = kv;
+        reinterpret_cast<uint4*>(p.v_sr)[dst] = vv;
+      }
+    }
+    if (threadIdx.x == 0 && p.sh.n_str > 0) p.pos[(int64_t)b * SR + slot] = (int32_t)n;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    if (fits) seq_lens[b] = (int32_t)(n + 1);
+    else atomicOr(&g_append_err, kErrAppendCapacity);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_append_varlen(const AppendParams& p, int32_t* seq_lens, cudaStream_t stream) {
+  const int work = p.sh.Hkv * (p.sh.D / 8);
+  const int threads = work < 256 ? ((work + 31) / 32) * 32 : 256;
+  append_varlen_kernel<<<p.sh.B, threads, 0, stream>>>(p, seq_lens);
+  return cudaGetLastError();
+}
+
+cudaError_t append_read_clear_error(uint32_t* code) {
+  unsigned int v = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_append_err, sizeof(v));
+  if (e != cudaSuccess) return e;
+  *code = v;
+  if (v) {
+    v = 0;
+    e = cudaMemcpyToSymbol(g_append_err, &v, sizeof(v));
+  }
+  return e;
+}
 
 cudaError_t launch_append(const AppendParams& p, int num_sms, cudaStream_t stream) {
   const int vpr = p.sh.D / 8;

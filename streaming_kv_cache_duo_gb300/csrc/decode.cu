@@ -3,11 +3,12 @@
 //
 // Work list. A "unit" is one (sequence, KV head): a retrieval unit holds n keys
 // (rows [0, n) of its full cache), a streaming unit min(n, S + R) ring slots.
-// Units are cut into tiles of kTK keys and all tiles are laid end to end; CTA c
-// takes tiles [c W / C, (c + 1) W / C), so every SM streams the same number of
-// key bytes whatever the mix of long retrieval and short streaming units (the
-// transformers "Dynamic length in static cache" rule: only the n written
-// positions are read, never the capacity).
+// Retrieval units are cut into tiles of kTK keys laid end to end; CTA c takes
+// tiles [c W / C, (c + 1) W / C), so every SM streams the same number of key
+// bytes however long the contexts are. Streaming units (at most S + R keys) are
+// dealt whole, round-robin: CTA c also takes units c, c + C, ... Only the n
+// written positions are ever read, never the capacity (the transformers
+// "Dynamic length in static cache" rule).
 //
 // Per CTA: eight warps; warp w owns keys [w kKPW, (w + 1) kKPW) of every tile and
 // streams its own rows of K and V into a private 3-stage shared-memory ring with
@@ -72,24 +73,24 @@ struct Cfg {
 struct Unit {
   int b, kvh;
   bool streaming;
-  int64_t keys;
+  int64_t keys;  // keys this unit holds
+  int64_t pq;    // position of the query
   int64_t ntiles;
   const uint16_t* kb;
   const uint16_t* vb;
 };
 
-__device__ __forceinline__ int64_t unit_start(const DecodeParams& p, int u) {
-  return u <= p.U_r ? (int64_t)u * p.tiles_r : (int64_t)p.U_r * p.tiles_r + (int64_t)(u - p.U_r) * p.tiles_s;
-}
-
-__device__ __forceinline__ int unit_of(const DecodeParams& p, int64_t t) {
-  const int64_t rt = (int64_t)p.U_r * p.tiles_r;
-  return t < rt ? (int)(t / p.tiles_r) : p.U_r + (int)((t - rt) / p.tiles_s);
-}
-
-// CTA whose tile range contains tile t (ranges are [c W / C, (c + 1) W / C)).
+// CTA whose share of the retrieval tiles contains tile t (shares are [c W / C, (c + 1) W / C)).
 __device__ __forceinline__ int cta_of(const DecodeParams& p, int64_t t) {
   return (int)(((t + 1) * p.C - 1) / p.W);
+}
+
+// Tokens held by sequence b: the uniform n, or its entry of the device length
+// array clamped to the planned maximum n (so no tile beyond the plan is read).
+__device__ __forceinline__ int64_t seq_len(const DecodeParams& p, int b) {
+  if (!p.seq_lens) return p.n;
+  const int64_t v = __ldg(p.seq_lens + b);
+  return v < 0 ? 0 : (v > p.n ? p.n : v);
 }
 
 __device__ __forceinline__ Unit unit_info(const DecodeParams& p, int u) {
@@ -100,7 +101,8 @@ __device__ __forceinline__ Unit unit_info(const DecodeParams& p, int u) {
     x.b = u / p.sh.n_ret;
     x.kvh = p.heads.ret_head[ri];
     x.streaming = false;
-    x.keys = p.n;
+    x.pq = seq_len(p, x.b) - 1;
+    x.keys = x.pq + 1;
     x.ntiles = p.tiles_r;
     const int64_t off = ((int64_t)x.b * p.sh.n_ret + ri) * p.sh.cap * D;
     x.kb = p.k_full + off;
@@ -111,7 +113,8 @@ __device__ __forceinline__ Unit unit_info(const DecodeParams& p, int u) {
     x.b = us / p.sh.n_str;
     x.kvh = p.heads.str_head[si];
     x.streaming = true;
-    x.keys = p.nvalid;
+    x.pq = seq_len(p, x.b) - 1;
+    x.keys = x.pq + 1 < (int64_t)(p.sh.S + p.sh.R) ? x.pq + 1 : (int64_t)(p.sh.S + p.sh.R);
     x.ntiles = p.tiles_s;
     const int64_t off = ((int64_t)x.b * p.sh.n_str + si) * (int64_t)(p.sh.S + p.sh.R) * D;
     x.kb = p.k_sr + off;
@@ -126,18 +129,54 @@ __device__ __forceinline__ int warp_rows(int64_t keys, int64_t lt, int w) {
   return r <= 0 ? 0 : (r >= kKPW ? kKPW : (int)r);
 }
 
-// The tile this warp refills next, walked forward one tile at a time (no division).
+// The work of CTA c, in order: its share [t0, t1) of the retrieval tiles (cut into
+// segments at unit boundaries), then streaming units c, c + C, c + 2C, ... whole.
+// Dealing the short streaming units round-robin keeps their fixed per-segment
+// cost (q load, merges) from piling up on the last CTAs.
+struct SegState {
+  int64_t rt;  // next retrieval tile
+  int k;       // next streaming unit ordinal of this CTA
+};
+
+__device__ __forceinline__ bool next_segment(const DecodeParams& p, int c, int64_t t1, bool streaming_too,
+                                             SegState& st, int& u, int64_t& lt0, int64_t& lt1) {
+  if (st.rt < t1) {
+    u = (int)(st.rt / p.tiles_r);  // once per segment
+    const int64_t us = (int64_t)u * p.tiles_r;
+    const int64_t te = us + p.tiles_r < t1 ? us + p.tiles_r : t1;
+    lt0 = st.rt - us;
+    lt1 = te - us;
+    st.rt = te;
+    return true;
+  }
+  const int64_t sidx = c + (int64_t)st.k * p.C;
+  if (streaming_too && sidx < p.U_s) {
+    u = p.U_r + (int)sidx;
+    lt0 = 0;
+    lt1 = p.tiles_s;
+    ++st.k;
+    return true;
+  }
+  return false;
+}
+
+// The tile this warp refills next, walked forward one tile at a time.
 struct Cursor {
-  int64_t t;   // global tile index
-  int64_t lt;  // tile index within its unit
+  SegState st;
   int u;
+  int64_t lt, lt1;
   Unit x;
-  __device__ __forceinline__ void advance(const DecodeParams& p) {
-    ++t;
-    if (++lt == x.ntiles) {
-      lt = 0;
-      ++u;
-      if (u < p.U_r + p.U_s) x = unit_info(p, u);
+  bool live;
+  __device__ __forceinline__ void init(const DecodeParams& p, int c, int64_t t0, int64_t t1, bool streaming_too) {
+    st.rt = t0;
+    st.k = 0;
+    live = next_segment(p, c, t1, streaming_too, st, u, lt, lt1);
+    if (live) x = unit_info(p, u);
+  }
+  __device__ __forceinline__ void advance(const DecodeParams& p, int c, int64_t t1, bool streaming_too) {
+    if (++lt == lt1) {
+      live = next_segment(p, c, t1, streaming_too, st, u, lt, lt1);
+      if (live) x = unit_info(p, u);
     }
   }
 };
@@ -186,7 +225,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
   const int c = blockIdx.x;
   const int64_t t0 = (int64_t)c * p.W / p.C;
   // After any CTA of this kernel gave up a wait, later CTAs do no work.
-  const int64_t t1 = (*(volatile unsigned int*)err.word != 0u) ? t0 : (int64_t)(c + 1) * p.W / p.C;
+  const bool live = *(volatile unsigned int*)err.word == 0u;
+  const int64_t t1 = live ? (int64_t)(c + 1) * p.W / p.C : t0;
   uint8_t* ring = smem + (size_t)warp * kNSW * C::WSTAGE;
   uint64_t* wfull = full + warp * kNSW;
 
@@ -199,17 +239,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
 
   // refill cursor (warp-uniform); the prologue issues the first kNSW - 1 slices
   Cursor cur;
-  cur.t = t0;
-  cur.u = t0 < t1 ? unit_of(p, t0) : 0;
-  cur.lt = 0;
-  if (t0 < t1) {
-    cur.x = unit_info(p, cur.u);
-    cur.lt = t0 - unit_start(p, cur.u);
-  }
+  cur.init(p, c, t0, t1, live);
   int64_t issued = 0;
-  for (int s = 0; s < kNSW - 1 && cur.t < t1; ++s) {
+  for (int s = 0; s < kNSW - 1 && cur.live; ++s) {
     if (lane == 0) issue_slice<D, G>(cur, warp, ring + s * C::WSTAGE, &wfull[s]);
-    cur.advance(p);
+    cur.advance(p, c, t1, live);
     ++issued;
   }
 
@@ -217,16 +251,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
   const int cl = lane % C::LPK;           // dims slot of this lane within its key group
   const int hme = cl >> (C::LB - C::GB);  // the head this lane ends up owning
   const int SR = p.sh.S + p.sh.R;
-  const int64_t pq = p.n - 1;  // query position
   WarpSync ws{segbar, 0};
   int64_t j = 0;  // tiles consumed
   bool ok = true;
-  for (int64_t t = t0; t < t1 && ok;) {
-    const int u = unit_of(p, t);
-    const int64_t us = unit_start(p, u);
+  SegState seg{t0, 0};
+  int u;
+  int64_t lt_begin, lt_end;
+  while (ok && next_segment(p, c, t1, live, seg, u, lt_begin, lt_end)) {
     const Unit x = unit_info(p, u);
-    const int64_t ue = us + x.ntiles;
-    const int64_t te = ue < t1 ? ue : t1;
 
     // q of head (hme ^ l) in slot l, this lane's dims, pre-scaled, as fp32 pairs
     float2 q2[G][C::DPL / 2];
@@ -251,20 +283,19 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
       for (int e = 0; e < C::DPL / 2; ++e) o2[l][e] = make_float2(0.f, 0.f);
     float l_run = 0.f, m_run = -INFINITY;  // of head hme
 
-    for (; t < te; ++t, ++j) {
+    for (int64_t lt = lt_begin; lt < lt_end; ++lt, ++j) {
       const int s = (int)(j % kNSW);
       // refill: the stage used by tile j - 1 is free now (this warp finished it)
-      if (cur.t < t1) {
+      if (cur.live) {
         const int sn = (int)((j + kNSW - 1) % kNSW);
         if (lane == 0) issue_slice<D, G>(cur, warp, ring + sn * C::WSTAGE, &wfull[sn]);
-        cur.advance(p);
+        cur.advance(p, c, t1, live);
         ++issued;
       }
       if (!mbar_wait(&wfull[s], (uint32_t)((j / kNSW) & 1), err, kErrDecodeConsumer)) {
         ok = false;
         break;
       }
-      const int64_t lt = t - us;
       const int rows = warp_rows(x.keys, lt, warp);
       const uint8_t* sk = ring + s * C::WSTAGE;
       const uint8_t* sv = sk + C::SLICE;
@@ -281,7 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
           if (x.streaming && valid) {
             const int64_t slot = lt * kTK + (int64_t)warp * kKPW + key;
             const int jp = __ldg(p.pos + (int64_t)x.b * SR + slot);
-            valid = jp >= 0 && jp <= pq && (jp < p.sh.S || pq - jp < p.sh.R);
+            valid = jp >= 0 && jp <= x.pq && (jp < p.sh.S || x.pq - jp < p.sh.R);
           }
         }
         vis[it] = valid;
@@ -406,8 +437,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
       break;
     }
     const int tid = threadIdx.x;
-    const int c_first = cta_of(p, us);
-    const int n_parts = cta_of(p, ue - 1) - c_first + 1;
+    // streaming units are whole in one CTA; a retrieval unit spans CTAs c_first ...
+    const int64_t us = (int64_t)u * p.tiles_r;
+    const int c_first = x.streaming ? c : cta_of(p, us);
+    const int n_parts = x.streaming ? 1 : cta_of(p, us + p.tiles_r - 1) - c_first + 1;
     float* part = p.partials + (int64_t)(c + u) * G * C::PS;
     for (int e = tid; e < G * D; e += kThreads) {
       const int h = e / D;
@@ -423,7 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
       }
       if (n_parts == 1) {
         p.o[((int64_t)x.b * p.sh.Hq + (int64_t)x.kvh * G + h) * D + d] =
-            __bfloat16_as_ushort(__float2bfloat16_rn(num / den));
+            __bfloat16_as_ushort(__float2bfloat16_rn(den > 0.f ? num / den : 0.f));
       } else {
         part[h * C::PS + d] = num;
         if (d == 0) {
@@ -519,7 +552,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
             dsum += red[(w * G + h) * (D + 2) + D + 1];
           }
           p.o[((int64_t)x.b * p.sh.Hq + (int64_t)x.kvh * G + h) * D + d] =
-              __bfloat16_as_ushort(__float2bfloat16_rn(num / dsum));
+              __bfloat16_as_ushort(__float2bfloat16_rn(dsum > 0.f ? num / dsum : 0.f));
         }
       }
     }

@@ -342,6 +342,7 @@ duo_status duo_attn_prefill_select(duo_handle* h, const duo_kv_cache* c, const v
 
 static void decode_plan(const duo_handle* h, int64_t n, DecodeParams* p) {
   const Shape& sh = h->sh;
+  p->seq_lens = nullptr;  // uniform length n unless a caller sets device lengths
   const int64_t SR = (int64_t)sh.S + sh.R;
   p->n = n;
   p->nvalid = (int)(n < SR ? n : SR);
@@ -349,8 +350,9 @@ static void decode_plan(const duo_handle* h, int64_t n, DecodeParams* p) {
   p->U_s = sh.B * sh.n_str;
   p->tiles_r = (n + kDecodeTK - 1) / kDecodeTK;
   p->tiles_s = (p->nvalid + kDecodeTK - 1) / kDecodeTK;
-  p->W = (int64_t)p->U_r * p->tiles_r + (int64_t)p->U_s * p->tiles_s;
-  p->C = (int)(p->W < h->num_sms ? p->W : h->num_sms);
+  p->W = (int64_t)p->U_r * p->tiles_r;  // retrieval tiles; streaming units are dealt whole
+  const int64_t work = p->W + p->U_s;
+  p->C = (int)(work < h->num_sms ? work : h->num_sms);
 }
 
 size_t duo_decode_workspace_size(const duo_handle* h, int64_t n) {
@@ -409,16 +411,93 @@ duo_status duo_attn_decode(duo_handle* h, const duo_kv_cache* c, const void* q, 
   return ok();
 }
 
+duo_status duo_kv_append_varlen(duo_handle* h, duo_kv_cache* c, int32_t* seq_lens, const void* k_new,
+                                const void* v_new, void* stream) {
+  duo_status st = check_handle(h);
+  if (st != DUO_OK) return st;
+  if ((st = check_cache(h, c, true, true)) != DUO_OK) return st;
+  if (!seq_lens) return fail(DUO_ERR_INVALID_ARG, "seq_lens is NULL");
+  if (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new))
+    return fail(DUO_ERR_INVALID_ARG, "k_new / v_new NULL or not 16-byte aligned");
+  AppendParams p;
+  memset(&p, 0, sizeof(p));
+  p.k_new = static_cast<const uint16_t*>(k_new);
+  p.v_new = static_cast<const uint16_t*>(v_new);
+  p.k_full = static_cast<uint16_t*>(c->k_full);
+  p.v_full = static_cast<uint16_t*>(c->v_full);
+  p.k_sr = static_cast<uint16_t*>(c->k_sr);
+  p.v_sr = static_cast<uint16_t*>(c->v_sr);
+  p.pos = c->pos;
+  p.T = 1;
+  p.sh = h->sh;
+  p.heads = h->heads;
+  cudaError_t ce = launch_append_varlen(p, seq_lens, (cudaStream_t)stream);
+  if (ce != cudaSuccess) return cuda_fail(ce, "append (device lengths) launch");
+  return ok();
+}
+
+duo_status duo_attn_decode_varlen(duo_handle* h, const duo_kv_cache* c, const int32_t* seq_lens, int64_t max_len,
+                                  const void* q, void* o, void* workspace, size_t ws_bytes, void* stream) {
+  duo_status st = check_handle(h);
+  if (st != DUO_OK) return st;
+  if ((st = check_cache(h, c, true, true)) != DUO_OK) return st;
+  if (!seq_lens) return fail(DUO_ERR_INVALID_ARG, "seq_lens is NULL");
+  if (max_len < 1) return fail(DUO_ERR_INVALID_ARG, "max_len = %lld < 1", (long long)max_len);
+  if (h->sh.n_ret > 0 && max_len > h->sh.cap) return fail(DUO_ERR_INVALID_ARG, "max_len exceeds max_seq_len");
+  if (!q || !o || !aligned16(q) || !aligned16(o))
+    return fail(DUO_ERR_INVALID_ARG, "q / o NULL or not 16-byte aligned");
+  const size_t need = decode_workspace_bytes(h->sh, h->num_sms);
+  if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return fail(DUO_ERR_INVALID_ARG, "workspace not 256-byte aligned");
+  if (!workspace || ws_bytes < need)
+    return fail(DUO_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need, workspace ? ws_bytes : 0);
+  const Shape& sh = h->sh;
+  DecodeParams p;
+  decode_plan(h, max_len, &p);
+  const int64_t U = (int64_t)sh.B * sh.Hkv;
+  const size_t counter_bytes = ((size_t)U * 4 + 255) / 256 * 256;
+  const unsigned epoch = g_error_epoch.load();
+  if (workspace != h->last_workspace || h->workspace_dirty || epoch != h->epoch) {
+    cudaError_t e = cudaMemsetAsync(workspace, 0, counter_bytes, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(workspace counters)");
+    h->last_workspace = workspace;
+    h->workspace_dirty = false;
+    h->epoch = epoch;
+  }
+  p.seq_lens = seq_lens;
+  p.q = static_cast<const uint16_t*>(q);
+  p.o = static_cast<uint16_t*>(o);
+  p.k_full = static_cast<const uint16_t*>(c->k_full);
+  p.v_full = static_cast<const uint16_t*>(c->v_full);
+  p.k_sr = static_cast<const uint16_t*>(c->k_sr);
+  p.v_sr = static_cast<const uint16_t*>(c->v_sr);
+  p.pos = c->pos;
+  p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)sh.D));
+  p.counters = static_cast<uint32_t*>(workspace);
+  p.partials = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + counter_bytes);
+  p.sh = sh;
+  p.heads = h->heads;
+  cudaError_t ce = launch_decode(p, (cudaStream_t)stream);
+  if (ce != cudaSuccess) {
+    h->workspace_dirty = true;
+    return cuda_fail(ce, "decode launch (device lengths)");
+  }
+  return ok();
+}
+
 duo_status duo_device_error(uint32_t* code) {
   if (!code) return fail(DUO_ERR_INVALID_ARG, "code is NULL");
   cudaError_t e = cudaDeviceSynchronize();
   if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
-  uint32_t a = 0, b = 0, t = 0;
+  uint32_t a = 0, b = 0, t = 0, ap = 0;
   if ((e = prefill_read_clear_error(&a)) != cudaSuccess) return cuda_fail(e, "read prefill error word");
   if ((e = decode_read_clear_error(&b)) != cudaSuccess) return cuda_fail(e, "read decode error word");
   if ((e = selftest_read_clear_error(&t)) != cudaSuccess) return cuda_fail(e, "read self-test error word");
-  *code = a | b | t;
-  if (*code) g_error_epoch.fetch_add(1);
+  if ((e = append_read_clear_error(&ap)) != cudaSuccess) return cuda_fail(e, "read append error word");
+  *code = a | b | t | ap;
+  if (a | b | t) g_error_epoch.fetch_add(1);
+  if (ap && !(a | b | t))
+    return fail(DUO_ERR_CAPACITY, "a device-side append found a full retrieval cache (code 0x%x)", *code);
   if (*code) return fail(DUO_ERR_DEVICE_TIMEOUT, "a kernel gave up a bounded wait (code 0x%x)", *code);
   return ok();
 }

@@ -22,6 +22,7 @@ enum : uint32_t {
   kErrDecodeProducer = 1u << 8,
   kErrDecodeConsumer = 1u << 9,
   kErrSelftest = 1u << 16,
+  kErrAppendCapacity = 1u << 20,
 };
 
 struct Shape {
@@ -56,6 +57,10 @@ struct AppendParams {
   HeadTable heads;
 };
 cudaError_t launch_append(const AppendParams& p, int num_sms, cudaStream_t stream);
+// One token per sequence at the position held in seq_lens[b] (device), which is
+// then advanced; T is 1 and n is unused.
+cudaError_t launch_append_varlen(const AppendParams& p, int32_t* seq_lens, cudaStream_t stream);
+cudaError_t append_read_clear_error(uint32_t* code);
 
 // ------------------------------------------------------------------ decode
 constexpr int kDecodeTK = 128;  // keys per decode tile
@@ -69,12 +74,14 @@ struct DecodeParams {
   const uint16_t* v_sr;
   const int32_t* pos;
   int64_t n;       // keys held by a retrieval head; the query is at position n - 1
+  const int32_t* seq_lens;  // optional [B] device lengths (then n = the planned maximum)
   int nvalid;      // valid ring slots, min(n, S + R)
   int U_r, U_s;    // units (one per (sequence, KV head)) of each kind
   int64_t tiles_r; // key tiles per retrieval unit
   int64_t tiles_s; // key tiles per streaming unit
-  int64_t W;       // all tiles: U_r * tiles_r + U_s * tiles_s
-  int C;           // CTAs; CTA c takes tiles [c W / C, (c+1) W / C)
+  int64_t W;       // retrieval tiles: U_r * tiles_r
+  int C;           // CTAs; CTA c takes retrieval tiles [c W / C, (c+1) W / C) and
+                   // streaming units c, c + C, ...
   float scale_log2;    // log2(e) / sqrt(D)
   uint32_t* counters;  // [U_r + U_s] arrival tickets, left at zero
   float* partials;     // [C + U_r + U_s][g][D + 4] (o, max, sum, 2 pad) per segment
