@@ -172,6 +172,31 @@ duo_status duo_attn_decode(duo_handle* handle, const duo_kv_cache* cache, const 
 duo_status duo_attn_decode_static(duo_handle* handle, const duo_kv_cache* cache, const void* q, void* o,
                                   void* stream);
 
+/* Paged retrieval caches, as a block allocator hands out memory in a serving engine
+ * (vLLM issue "Could you support Attention Sink?" discusses the cache as fixed-size
+ * token blocks chained by a block table). With a duo_paged descriptor, cache->k_full
+ * and cache->v_full are pools of blocks, bf16 [num_blocks, block_size, D], shared by
+ * every sequence and retrieval head; row t of retrieval head r of sequence b is row
+ * t % block_size of block block_table[(b * n_ret + r) * max_blocks + t / block_size].
+ * Streaming heads keep their sink + ring cache unchanged (a block-granular eviction
+ * would change which keys a query sees). The capacity of a retrieval head is
+ * block_size * max_blocks tokens (max_seq_len is not used). A block id outside
+ * [0, num_blocks) is never dereferenced: its rows are skipped and duo_device_error()
+ * reports DUO_ERR_INVALID_ARG. Results equal the contiguous layout's, bit for bit. */
+typedef struct {
+  const int32_t* block_table; /* int32 [B, n_ret, max_blocks], device memory */
+  int32_t block_size;         /* rows per block, a positive multiple of 128 */
+  int32_t max_blocks;         /* table entries per (sequence, retrieval head) */
+  int64_t num_blocks;         /* blocks in each pool */
+} duo_paged;
+
+duo_status duo_kv_append_paged(duo_handle* handle, duo_kv_cache* cache, const duo_paged* paged, const void* k_new,
+                               const void* v_new, int32_t T, void* stream);
+duo_status duo_attn_prefill_paged(duo_handle* handle, const duo_kv_cache* cache, const duo_paged* paged,
+                                  const void* q, const void* k, const void* v, int32_t T, void* o, void* stream);
+duo_status duo_attn_decode_paged(duo_handle* handle, const duo_kv_cache* cache, const duo_paged* paged,
+                                 const void* q, void* o, void* workspace, size_t workspace_bytes, void* stream);
+
 /* Per-sequence lengths on the device: serving batches
  * hold sequences of different lengths, and a decode step whose lengths live in device
  * memory can be captured once in a CUDA graph and replayed step after step. The

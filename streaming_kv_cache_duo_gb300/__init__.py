@@ -115,6 +115,51 @@ class DuoLayer:
             pass
 
 
+class DuoPagedLayer(DuoLayer):
+    """A layer whose retrieval caches live in a shared pool of blocks addressed through
+    a block table (int32 [B, n_ret, max_blocks] on the device); streaming heads keep the
+    sink + ring cache."""
+
+    def __init__(self, batch, num_q_heads, num_kv_heads, head_dim, sink_size, recent_size, block_size,
+                 max_blocks, num_blocks, block_table, is_retrieval, device="cuda"):
+        import torch
+        super().__init__(batch, num_q_heads, num_kv_heads, head_dim, sink_size, recent_size, 1, is_retrieval,
+                         device=device)
+        bf = dict(dtype=torch.bfloat16, device=self.device)
+        self.k_full = torch.empty((num_blocks, block_size, head_dim), **bf)
+        self.v_full = torch.empty_like(self.k_full)
+        self.cache.k_full = self.k_full.data_ptr()
+        self.cache.v_full = self.v_full.data_ptr()
+        assert block_table.dtype == torch.int32 and block_table.is_cuda and block_table.is_contiguous()
+        assert tuple(block_table.shape) == (batch, self.n_ret, max_blocks)
+        self.block_table = block_table
+        self.paged = _lib.duo_paged(block_table.data_ptr(), block_size, max_blocks, num_blocks)
+
+    def append(self, k_new, v_new, stream=None) -> None:
+        T = k_new.shape[1]
+        _lib._bf16(k_new, (self.B, T, self.Hkv, self.D), "k_new")
+        _lib._bf16(v_new, (self.B, T, self.Hkv, self.D), "v_new")
+        _lib.duo_kv_append_paged(self.handle, self.cache, self.paged, k_new, v_new, T, stream)
+
+    def prefill(self, q, k, v, out=None, kind_mask=3, stream=None):
+        import torch
+        assert kind_mask == 3
+        T = q.shape[1]
+        _lib._bf16(q, (self.B, T, self.Hq, self.D), "q")
+        if out is None:
+            out = torch.empty_like(q)
+        _lib.duo_attn_prefill_paged(self.handle, self.cache, self.paged, q, k, v, T, out, stream)
+        return out
+
+    def decode(self, q, out=None, stream=None):
+        import torch
+        _lib._bf16(q, (self.B, self.Hq, self.D), "q")
+        if out is None:
+            out = torch.empty_like(q)
+        _lib.duo_attn_decode_paged(self.handle, self.cache, self.paged, q, out, self.workspace, stream)
+        return out
+
+
 def _check_lens(seq_lens, B):
     import torch
     if seq_lens.dtype != torch.int32 or not seq_lens.is_cuda or not seq_lens.is_contiguous() or seq_lens.numel() != B:

@@ -30,8 +30,9 @@ DUO_RETRIEVAL = 1
 EXPORTS = (
     "duo_classify_heads", "duo_create", "duo_destroy", "duo_cache_reset", "duo_kv_append",
     "duo_attn_prefill", "duo_attn_prefill_select", "duo_decode_workspace_size", "duo_attn_decode",
-    "duo_attn_decode_static", "duo_kv_append_varlen", "duo_attn_decode_varlen", "duo_device_error",
-    "duo_selftest_bounded_wait", "duo_last_error", "duo_status_string",
+    "duo_attn_decode_static", "duo_kv_append_paged", "duo_attn_prefill_paged", "duo_attn_decode_paged",
+    "duo_kv_append_varlen", "duo_attn_decode_varlen", "duo_device_error", "duo_selftest_bounded_wait",
+    "duo_last_error", "duo_status_string",
 )
 
 
@@ -45,6 +46,11 @@ class duo_config(ctypes.Structure):
     _fields_ = [("batch", c_int32), ("num_q_heads", c_int32), ("num_kv_heads", c_int32),
                 ("head_dim", c_int32), ("sink_size", c_int32), ("recent_size", c_int32),
                 ("max_seq_len", c_int64)]
+
+
+class duo_paged(ctypes.Structure):
+    _fields_ = [("block_table", c_void_p), ("block_size", c_int32), ("max_blocks", c_int32),
+                ("num_blocks", c_int64)]
 
 
 class duo_kv_cache(ctypes.Structure):
@@ -78,6 +84,12 @@ def library() -> ctypes.CDLL:
         "duo_attn_decode": (c_int32, [c_void_p, POINTER(duo_kv_cache), c_void_p, c_void_p, c_void_p, c_size_t,
                                       c_void_p]),
         "duo_attn_decode_static": (c_int32, [c_void_p, POINTER(duo_kv_cache), c_void_p, c_void_p, c_void_p]),
+        "duo_kv_append_paged": (c_int32, [c_void_p, POINTER(duo_kv_cache), POINTER(duo_paged), c_void_p, c_void_p,
+                                          c_int32, c_void_p]),
+        "duo_attn_prefill_paged": (c_int32, [c_void_p, POINTER(duo_kv_cache), POINTER(duo_paged), c_void_p,
+                                             c_void_p, c_void_p, c_int32, c_void_p, c_void_p]),
+        "duo_attn_decode_paged": (c_int32, [c_void_p, POINTER(duo_kv_cache), POINTER(duo_paged), c_void_p,
+                                            c_void_p, c_void_p, c_size_t, c_void_p]),
         "duo_kv_append_varlen": (c_int32, [c_void_p, POINTER(duo_kv_cache), c_void_p, c_void_p, c_void_p,
                                            c_void_p]),
         "duo_attn_decode_varlen": (c_int32, [c_void_p, POINTER(duo_kv_cache), c_void_p, c_int64, c_void_p, c_void_p,
@@ -183,6 +195,24 @@ def duo_attn_decode_static(handle, cache: "duo_kv_cache", q, o, stream=None) -> 
     _check(library().duo_attn_decode_static(handle, ctypes.byref(cache), _ptr(q), _ptr(o), _stream_ptr(stream)))
 
 
+def duo_kv_append_paged(handle, cache: "duo_kv_cache", paged: "duo_paged", k_new, v_new, T: int,
+                        stream=None) -> None:
+    _check(library().duo_kv_append_paged(handle, ctypes.byref(cache), ctypes.byref(paged), _ptr(k_new), _ptr(v_new),
+                                         T, _stream_ptr(stream)))
+
+
+def duo_attn_prefill_paged(handle, cache: "duo_kv_cache", paged: "duo_paged", q, k, v, T: int, o,
+                           stream=None) -> None:
+    _check(library().duo_attn_prefill_paged(handle, ctypes.byref(cache), ctypes.byref(paged), _ptr(q), _ptr(k),
+                                            _ptr(v), T, _ptr(o), _stream_ptr(stream)))
+
+
+def duo_attn_decode_paged(handle, cache: "duo_kv_cache", paged: "duo_paged", q, o, workspace, stream=None) -> None:
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(library().duo_attn_decode_paged(handle, ctypes.byref(cache), ctypes.byref(paged), _ptr(q), _ptr(o),
+                                           _ptr(workspace), nbytes, _stream_ptr(stream)))
+
+
 def duo_kv_append_varlen(handle, cache: "duo_kv_cache", seq_lens, k_new, v_new, stream=None) -> None:
     """One token per sequence at the device-held positions seq_lens (int32 [B]), then seq_lens += 1."""
     _check(library().duo_kv_append_varlen(handle, ctypes.byref(cache), _ptr(seq_lens), _ptr(k_new), _ptr(v_new),
@@ -201,7 +231,7 @@ def duo_device_error() -> int:
     """Synchronise; return the kernels' recorded error code (0 = none)."""
     code = c_uint32()
     st = library().duo_device_error(ctypes.byref(code))
-    if st not in (DUO_OK, DUO_ERR_DEVICE_TIMEOUT, DUO_ERR_CAPACITY):
+    if code.value == 0:
         _check(st)
     return code.value
 

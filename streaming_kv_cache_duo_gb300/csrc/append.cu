@@ -16,6 +16,8 @@
 namespace duo {
 namespace {
 
+__device__ unsigned int g_append_err;
+
 __global__ void __launch_bounds__(256) append_kernel(const AppendParams p) {
   const int D = p.sh.D;
   const int Hkv = p.sh.Hkv;
@@ -43,7 +45,12 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendParams p) {
       const int64_t b = r / T;
       const int h = p.heads.ret_head[ri];
       const int64_t src = ((b * T + t) * Hkv + h) * vpr + v;
-      const int64_t dst = ((b * n_ret + ri) * p.sh.cap + p.n + t) * vpr + v;
+      const int64_t off = retrieval_row(p.pg, p.sh.cap, D, b * n_ret + ri, p.n + t);
+      if (off < 0) {  // paged: block id out of range
+        if (v == 0) atomicOr(&g_append_err, kErrBadBlock);
+        continue;
+      }
+      const int64_t dst = off / 8 + v;
       const uint4 kv = __ldg(kin + src);
       const uint4 vv = __ldg(vin + src);
       reinterpret_cast<uint4*>(p.k_full)[dst] = kv;
@@ -71,8 +78,6 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendParams p) {
   }
 }
 
-__device__ unsigned int g_append_err;
-
 // One CTA per sequence: append its one new token at position n_b = seq_lens[b],
 // then advance seq_lens[b]. Every thread reads n_b before the barrier and only
 // thread 0 writes it after, and no other CTA touches sequence b, so the update
@@ -85,7 +90,8 @@ __global__ void __launch_bounds__(256) append_varlen_kernel(const AppendParams p
   const int vpr = D / 8;
   const int SR = p.sh.S + p.sh.R;
   const int64_t n = seq_lens[b];
-  const bool fits = n >= 0 && (p.sh.n_ret == 0 || n < p.sh.cap) && n < 0x7fffffff;
+  const int64_t cap = p.pg.table ? (int64_t)p.pg.block_size * p.pg.max_blocks : p.sh.cap;
+  const bool fits = n >= 0 && (p.sh.n_ret == 0 || n < cap) && n < 0x7fffffff;
   __syncthreads();
   if (fits) {
     const uint4* kin = reinterpret_cast<const uint4*>(p.k_new);
@@ -99,7 +105,12 @@ __global__ void __launch_bounds__(256) append_varlen_kernel(const AppendParams p
       const uint4 vv = __ldg(vin + src);
       const int ki = p.heads.kidx[h];
       if (p.heads.kind[h]) {
-        const int64_t dst = (((int64_t)b * p.sh.n_ret + ki) * p.sh.cap + n) * vpr + v;
+        const int64_t off = retrieval_row(p.pg, p.sh.cap, D, (int64_t)b * p.sh.n_ret + ki, n);
+        if (off < 0) {
+          if (v == 0) atomicOr(&g_append_err, kErrBadBlock);
+          continue;
+        }
+        const int64_t dst = off / 8 + v;
         reinterpret_cast<uint4*>(p.k_full)[dst] = kv;
         reinterpret_cast<uint4*>(p.v_full)[dst] = vv;
       } else {

@@ -72,6 +72,7 @@ struct Cfg {
 
 struct Unit {
   int b, kvh;
+  int64_t plane;  // retrieval: b * n_ret + ri (its row map in the cache)
   bool streaming;
   int64_t keys;  // keys this unit holds
   int64_t pq;    // position of the query
@@ -99,6 +100,7 @@ __device__ __forceinline__ Unit unit_info(const DecodeParams& p, int u) {
   if (u < p.U_r) {
     const int ri = u % p.sh.n_ret;
     x.b = u / p.sh.n_ret;
+    x.plane = u;
     x.kvh = p.heads.ret_head[ri];
     x.streaming = false;
     x.pq = seq_len(p, x.b) - 1;
@@ -111,6 +113,7 @@ __device__ __forceinline__ Unit unit_info(const DecodeParams& p, int u) {
     const int us = u - p.U_r;
     const int si = us % p.sh.n_str;
     x.b = us / p.sh.n_str;
+    x.plane = -1;
     x.kvh = p.heads.str_head[si];
     x.streaming = true;
     x.pq = seq_len(p, x.b) - 1;
@@ -181,16 +184,41 @@ struct Cursor {
   }
 };
 
+// Rows of tile `lt` this warp reads: its 16-row slice, or none if the tile lies in a
+// paged block whose id is out of range (recorded as an error).
+__device__ __forceinline__ int slice_rows(const DecodeParams& p, const Unit& x, int64_t lt, int w,
+                                          const uint16_t** kp, const uint16_t** vp) {
+  const int rows = warp_rows(x.keys, lt, w);
+  const int64_t row0 = lt * kTK + (int64_t)w * kKPW;
+  if (x.streaming || !p.pg.table) {
+    *kp = x.kb + row0 * p.sh.D;
+    *vp = x.vb + row0 * p.sh.D;
+    return rows;
+  }
+  if (rows == 0) return 0;
+  const int64_t off = retrieval_row(p.pg, p.sh.cap, p.sh.D, x.plane, row0);  // a slice never crosses a block
+  if (off < 0) return -1;
+  *kp = p.k_full + off;
+  *vp = p.v_full + off;
+  return rows;
+}
+
 template <int D, int G>
-__device__ __forceinline__ void issue_slice(const Cursor& cur, int w, uint8_t* stage, uint64_t* bar) {
+__device__ __forceinline__ void issue_slice(const DecodeParams& p, const Cursor& cur, int w, uint8_t* stage,
+                                            uint64_t* bar) {
   using C = Cfg<D, G>;
-  const int rows = warp_rows(cur.x.keys, cur.lt, w);
-  const int64_t row0 = cur.lt * kTK + (int64_t)w * kKPW;
+  const uint16_t* kp = nullptr;
+  const uint16_t* vp = nullptr;
+  int rows = slice_rows(p, cur.x, cur.lt, w, &kp, &vp);
+  if (rows < 0) {
+    atomicOr(&g_decode_err, kErrBadBlock);
+    rows = 0;
+  }
   const uint32_t bytes = (uint32_t)rows * C::ROW;
   mbar_arrive_expect_tx(bar, 2 * bytes);
   if (rows > 0) {
-    bulk_g2s(stage, cur.x.kb + row0 * D, bytes, bar);
-    bulk_g2s(stage + C::SLICE, cur.x.vb + row0 * D, bytes, bar);
+    bulk_g2s(stage, kp, bytes, bar);
+    bulk_g2s(stage + C::SLICE, vp, bytes, bar);
   }
 }
 
@@ -242,7 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
   cur.init(p, c, t0, t1, live);
   int64_t issued = 0;
   for (int s = 0; s < kNSW - 1 && cur.live; ++s) {
-    if (lane == 0) issue_slice<D, G>(cur, warp, ring + s * C::WSTAGE, &wfull[s]);
+    if (lane == 0) issue_slice<D, G>(p, cur, warp, ring + s * C::WSTAGE, &wfull[s]);
     cur.advance(p, c, t1, live);
     ++issued;
   }
@@ -288,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
       // refill: the stage used by tile j - 1 is free now (this warp finished it)
       if (cur.live) {
         const int sn = (int)((j + kNSW - 1) % kNSW);
-        if (lane == 0) issue_slice<D, G>(cur, warp, ring + sn * C::WSTAGE, &wfull[sn]);
+        if (lane == 0) issue_slice<D, G>(p, cur, warp, ring + sn * C::WSTAGE, &wfull[sn]);
         cur.advance(p, c, t1, live);
         ++issued;
       }
@@ -296,7 +324,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
         ok = false;
         break;
       }
-      const int rows = warp_rows(x.keys, lt, warp);
+      const uint16_t* kp_unused;
+      const uint16_t* vp_unused;
+      const int rows_raw = slice_rows(p, x, lt, warp, &kp_unused, &vp_unused);
+      const int rows = rows_raw < 0 ? 0 : rows_raw;
       const uint8_t* sk = ring + s * C::WSTAGE;
       const uint8_t* sv = sk + C::SLICE;
       const bool full_tile = rows == kKPW && !x.streaming;

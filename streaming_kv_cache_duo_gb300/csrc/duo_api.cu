@@ -122,6 +122,26 @@ duo_status check_cache(const duo_handle* h, const duo_kv_cache* c, bool need_ful
   return DUO_OK;
 }
 
+duo_status check_paged(const duo_handle* h, const duo_paged* pg, PagedLayout* out) {
+  *out = PagedLayout{nullptr, 0, 0, 0};
+  if (!pg) return DUO_OK;
+  if (!pg->block_table || (reinterpret_cast<uintptr_t>(pg->block_table) & 3u))
+    return fail(DUO_ERR_INVALID_ARG, "block_table NULL or not 4-byte aligned");
+  if (pg->block_size < 128 || pg->block_size % 128 != 0)
+    return fail(DUO_ERR_UNSUPPORTED, "block_size = %d is not a positive multiple of 128", pg->block_size);
+  if (pg->max_blocks < 1 || pg->num_blocks < 1 || pg->num_blocks > 0x7fffffffLL)
+    return fail(DUO_ERR_INVALID_ARG, "max_blocks / num_blocks out of range");
+  if ((int64_t)pg->block_size * pg->max_blocks > 0x7fffffffLL)
+    return fail(DUO_ERR_INVALID_ARG, "block_size x max_blocks >= 2^31");
+  *out = PagedLayout{pg->block_table, pg->block_size, pg->max_blocks, pg->num_blocks};
+  (void)h;
+  return DUO_OK;
+}
+
+int64_t retrieval_capacity(const duo_handle* h, const PagedLayout& pg) {
+  return pg.table ? (int64_t)pg.block_size * pg.max_blocks : h->sh.cap;
+}
+
 }  // namespace
 
 extern "C" {
@@ -237,20 +257,25 @@ duo_status duo_cache_reset(duo_handle* h, duo_kv_cache* c, void* stream) {
   return ok();
 }
 
-duo_status duo_kv_append(duo_handle* h, duo_kv_cache* c, const void* k_new, const void* v_new, int32_t T,
-                         void* stream) {
+static duo_status append_impl(duo_handle* h, duo_kv_cache* c, const duo_paged* pgd, const void* k_new,
+                              const void* v_new, int32_t T, void* stream) {
   duo_status st = check_handle(h);
   if (st != DUO_OK) return st;
   if ((st = check_cache(h, c, true, true)) != DUO_OK) return st;
+  PagedLayout pg;
+  if ((st = check_paged(h, pgd, &pg)) != DUO_OK) return st;
   if (T < 1) return fail(DUO_ERR_INVALID_ARG, "T = %d < 1", T);
   if (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new))
     return fail(DUO_ERR_INVALID_ARG, "k_new / v_new NULL or not 16-byte aligned");
   const Shape& sh = h->sh;
   if (c->n + T > 0x7fffffffLL) return fail(DUO_ERR_CAPACITY, "positions would reach 2^31");
-  if (sh.n_ret > 0 && c->n + T > sh.cap)
-    return fail(DUO_ERR_CAPACITY, "n + T = %lld exceeds max_seq_len = %lld", (long long)(c->n + T),
-                (long long)sh.cap);
+  const int64_t cap = retrieval_capacity(h, pg);
+  if (sh.n_ret > 0 && c->n + T > cap)
+    return fail(DUO_ERR_CAPACITY, "n + T = %lld exceeds the retrieval capacity %lld", (long long)(c->n + T),
+                (long long)cap);
   AppendParams p;
+  memset(&p, 0, sizeof(p));
+  p.pg = pg;
   p.k_new = static_cast<const uint16_t*>(k_new);
   p.v_new = static_cast<const uint16_t*>(v_new);
   p.k_full = static_cast<uint16_t*>(c->k_full);
@@ -277,14 +302,27 @@ duo_status duo_kv_append(duo_handle* h, duo_kv_cache* c, const void* k_new, cons
   return ok();
 }
 
-static duo_status prefill_impl(duo_handle* h, const duo_kv_cache* c, const void* q, const void* k, const void* v,
-                               int32_t T, void* o, int32_t kind_mask, void* stream) {
+duo_status duo_kv_append(duo_handle* h, duo_kv_cache* c, const void* k_new, const void* v_new, int32_t T,
+                         void* stream) {
+  return append_impl(h, c, nullptr, k_new, v_new, T, stream);
+}
+
+duo_status duo_kv_append_paged(duo_handle* h, duo_kv_cache* c, const duo_paged* paged, const void* k_new,
+                               const void* v_new, int32_t T, void* stream) {
+  if (!paged) return fail(DUO_ERR_INVALID_ARG, "paged is NULL");
+  return append_impl(h, c, paged, k_new, v_new, T, stream);
+}
+
+static duo_status prefill_impl(duo_handle* h, const duo_kv_cache* c, const duo_paged* pgd, const void* q,
+                               const void* k, const void* v, int32_t T, void* o, int32_t kind_mask, void* stream) {
   duo_status st = check_handle(h);
   if (st != DUO_OK) return st;
   if (!c) return fail(DUO_ERR_INVALID_ARG, "cache is NULL");
   const Shape& sh = h->sh;
   const bool use_cache = c->n > 0;
   if ((st = check_cache(h, c, use_cache, use_cache)) != DUO_OK) return st;
+  PagedLayout pg;
+  if ((st = check_paged(h, pgd, &pg)) != DUO_OK) return st;
   if (T < 1) return fail(DUO_ERR_INVALID_ARG, "T = %d < 1", T);
   if (!q || !k || !v || !o) return fail(DUO_ERR_INVALID_ARG, "q / k / v / o is NULL");
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o))
@@ -300,12 +338,24 @@ static duo_status prefill_impl(duo_handle* h, const duo_kv_cache* c, const void*
   const int64_t SR = (int64_t)sh.S + sh.R;
   const int nvalid = (int)(c->n < SR ? c->n : SR);
   if (use_cache && sh.n_ret > 0) {
-    if (c->n > sh.cap) return fail(DUO_ERR_INVALID_ARG, "cache->n exceeds max_seq_len");
-    if ((st = encode_cache(h, &p.tm_kfull, c->k_full, (int64_t)sh.B * sh.n_ret, sh.cap, c->n, sh.D)) != DUO_OK)
-      return st;
-    if ((st = encode_cache(h, &p.tm_vfull, c->v_full, (int64_t)sh.B * sh.n_ret, sh.cap, c->n, sh.D)) != DUO_OK)
-      return st;
+    if (c->n > retrieval_capacity(h, pg)) return fail(DUO_ERR_INVALID_ARG, "cache->n exceeds the retrieval capacity");
+    if (!pg.table) {
+      if ((st = encode_cache(h, &p.tm_kfull, c->k_full, (int64_t)sh.B * sh.n_ret, sh.cap, c->n, sh.D)) != DUO_OK)
+        return st;
+      if ((st = encode_cache(h, &p.tm_vfull, c->v_full, (int64_t)sh.B * sh.n_ret, sh.cap, c->n, sh.D)) != DUO_OK)
+        return st;
+    } else {
+      // the pool as [num_blocks, block_size, D]; a second view stops at the written rows of the last block
+      const int64_t bs = pg.block_size;
+      if ((st = encode_cache(h, &p.tm_kfull, c->k_full, pg.num_blocks, bs, bs, sh.D)) != DUO_OK) return st;
+      if ((st = encode_cache(h, &p.tm_vfull, c->v_full, pg.num_blocks, bs, bs, sh.D)) != DUO_OK) return st;
+      if (c->n % bs) {
+        if ((st = encode_cache(h, &p.tm_klast, c->k_full, pg.num_blocks, bs, c->n % bs, sh.D)) != DUO_OK) return st;
+        if ((st = encode_cache(h, &p.tm_vlast, c->v_full, pg.num_blocks, bs, c->n % bs, sh.D)) != DUO_OK) return st;
+      }
+    }
   }
+  p.pg = pg;
   if (use_cache && sh.n_str > 0) {
     if ((st = encode_cache(h, &p.tm_ksr, c->k_sr, (int64_t)sh.B * sh.n_str, SR, nvalid, sh.D)) != DUO_OK) return st;
     if ((st = encode_cache(h, &p.tm_vsr, c->v_sr, (int64_t)sh.B * sh.n_str, SR, nvalid, sh.D)) != DUO_OK) return st;
@@ -332,17 +382,24 @@ static duo_status prefill_impl(duo_handle* h, const duo_kv_cache* c, const void*
 
 duo_status duo_attn_prefill(duo_handle* h, const duo_kv_cache* c, const void* q, const void* k, const void* v,
                             int32_t T, void* o, void* stream) {
-  return prefill_impl(h, c, q, k, v, T, o, 3, stream);
+  return prefill_impl(h, c, nullptr, q, k, v, T, o, 3, stream);
 }
 
 duo_status duo_attn_prefill_select(duo_handle* h, const duo_kv_cache* c, const void* q, const void* k,
                                    const void* v, int32_t T, void* o, int32_t kind_mask, void* stream) {
-  return prefill_impl(h, c, q, k, v, T, o, kind_mask, stream);
+  return prefill_impl(h, c, nullptr, q, k, v, T, o, kind_mask, stream);
+}
+
+duo_status duo_attn_prefill_paged(duo_handle* h, const duo_kv_cache* c, const duo_paged* paged, const void* q,
+                                  const void* k, const void* v, int32_t T, void* o, void* stream) {
+  if (!paged) return fail(DUO_ERR_INVALID_ARG, "paged is NULL");
+  return prefill_impl(h, c, paged, q, k, v, T, o, 3, stream);
 }
 
 static void decode_plan(const duo_handle* h, int64_t n, DecodeParams* p) {
   const Shape& sh = h->sh;
   p->seq_lens = nullptr;  // uniform length n unless a caller sets device lengths
+  p->pg = PagedLayout{nullptr, 0, 0, 0};  // contiguous retrieval caches unless paged
   const int64_t SR = (int64_t)sh.S + sh.R;
   p->n = n;
   p->nvalid = (int)(n < SR ? n : SR);
@@ -364,13 +421,16 @@ size_t duo_decode_workspace_size(const duo_handle* h, int64_t n) {
   return decode_workspace_bytes(h->sh, h->num_sms);
 }
 
-duo_status duo_attn_decode(duo_handle* h, const duo_kv_cache* c, const void* q, void* o, void* workspace,
-                           size_t ws_bytes, void* stream) {
+static duo_status decode_impl(duo_handle* h, const duo_kv_cache* c, const duo_paged* pgd, const void* q, void* o,
+                              void* workspace, size_t ws_bytes, void* stream) {
   duo_status st = check_handle(h);
   if (st != DUO_OK) return st;
   if ((st = check_cache(h, c, true, true)) != DUO_OK) return st;
+  PagedLayout pg;
+  if ((st = check_paged(h, pgd, &pg)) != DUO_OK) return st;
   if (c->n < 1) return fail(DUO_ERR_INVALID_ARG, "decode needs the query token appended first (cache->n >= 1)");
-  if (h->sh.n_ret > 0 && c->n > h->sh.cap) return fail(DUO_ERR_INVALID_ARG, "cache->n exceeds max_seq_len");
+  if (h->sh.n_ret > 0 && c->n > retrieval_capacity(h, pg))
+    return fail(DUO_ERR_INVALID_ARG, "cache->n exceeds the retrieval capacity");
   if (!q || !o || !aligned16(q) || !aligned16(o))
     return fail(DUO_ERR_INVALID_ARG, "q / o NULL or not 16-byte aligned");
   const size_t need = decode_workspace_bytes(h->sh, h->num_sms);
@@ -403,12 +463,24 @@ duo_status duo_attn_decode(duo_handle* h, const duo_kv_cache* c, const void* q, 
   p.partials = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + counter_bytes);
   p.sh = sh;
   p.heads = h->heads;
+  p.pg = pg;
   cudaError_t ce = launch_decode(p, (cudaStream_t)stream);
   if (ce != cudaSuccess) {
     h->workspace_dirty = true;
     return cuda_fail(ce, "decode launch");
   }
   return ok();
+}
+
+duo_status duo_attn_decode(duo_handle* h, const duo_kv_cache* c, const void* q, void* o, void* workspace,
+                           size_t ws_bytes, void* stream) {
+  return decode_impl(h, c, nullptr, q, o, workspace, ws_bytes, stream);
+}
+
+duo_status duo_attn_decode_paged(duo_handle* h, const duo_kv_cache* c, const duo_paged* paged, const void* q,
+                                 void* o, void* workspace, size_t ws_bytes, void* stream) {
+  if (!paged) return fail(DUO_ERR_INVALID_ARG, "paged is NULL");
+  return decode_impl(h, c, paged, q, o, workspace, ws_bytes, stream);
 }
 
 duo_status duo_kv_append_varlen(duo_handle* h, duo_kv_cache* c, int32_t* seq_lens, const void* k_new,
@@ -495,7 +567,9 @@ duo_status duo_device_error(uint32_t* code) {
   if ((e = selftest_read_clear_error(&t)) != cudaSuccess) return cuda_fail(e, "read self-test error word");
   if ((e = append_read_clear_error(&ap)) != cudaSuccess) return cuda_fail(e, "read append error word");
   *code = a | b | t | ap;
-  if (a | b | t) g_error_epoch.fetch_add(1);
+  if ((a | b | t) & ~kErrBadBlock) g_error_epoch.fetch_add(1);
+  if ((*code & kErrBadBlock) && !(*code & ~(kErrBadBlock | kErrAppendCapacity)))
+    return fail(DUO_ERR_INVALID_ARG, "a block table held an id outside [0, num_blocks) (code 0x%x)", *code);
   if (ap && !(a | b | t))
     return fail(DUO_ERR_CAPACITY, "a device-side append found a full retrieval cache (code 0x%x)", *code);
   if (*code) return fail(DUO_ERR_DEVICE_TIMEOUT, "a kernel gave up a bounded wait (code 0x%x)", *code);

@@ -23,6 +23,7 @@ enum : uint32_t {
   kErrDecodeConsumer = 1u << 9,
   kErrSelftest = 1u << 16,
   kErrAppendCapacity = 1u << 20,
+  kErrBadBlock = 1u << 21,
 };
 
 struct Shape {
@@ -38,6 +39,25 @@ struct HeadTable {
   uint8_t kind[kMaxHeads];
   uint8_t kidx[kMaxHeads];
 };
+
+// Optional paged layout of the retrieval caches: k_full / v_full are pools of
+// blocks [num_blocks, block_size, D]; row r of plane (b, ri) is row r % block_size
+// of block table[(b * n_ret + ri) * max_blocks + r / block_size].
+struct PagedLayout {
+  const int32_t* table;  // nullptr = contiguous [B, n_ret, cap, D]
+  int32_t block_size;    // a multiple of 128
+  int32_t max_blocks;
+  int64_t num_blocks;
+};
+
+// Element offset of row r of retrieval plane `plane`; -1 if its block id is out of range.
+__host__ __device__ __forceinline__ int64_t retrieval_row(const PagedLayout& pg, int64_t cap, int D, int64_t plane,
+                                                          int64_t r) {
+  if (!pg.table) return (plane * cap + r) * D;
+  const int64_t blk = pg.table[plane * pg.max_blocks + r / pg.block_size];
+  if (blk < 0 || blk >= pg.num_blocks) return -1;
+  return (blk * pg.block_size + r % pg.block_size) * D;
+}
 
 // ------------------------------------------------------------------ append
 struct AppendParams {
@@ -55,6 +75,7 @@ struct AppendParams {
   int64_t sink_lo, sink_cnt, ring_lo, ring_cnt;
   Shape sh;
   HeadTable heads;
+  PagedLayout pg;
 };
 cudaError_t launch_append(const AppendParams& p, int num_sms, cudaStream_t stream);
 // One token per sequence at the position held in seq_lens[b] (device), which is
@@ -87,6 +108,7 @@ struct DecodeParams {
   float* partials;     // [C + U_r + U_s][g][D + 4] (o, max, sum, 2 pad) per segment
   Shape sh;
   HeadTable heads;
+  PagedLayout pg;
 };
 size_t decode_workspace_bytes(const Shape& sh, int num_ctas);
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream);
@@ -100,8 +122,10 @@ struct PrefillParams {
   CUtensorMap tm_q;      // 4-D over q [B, T, Hq, D], box 64 x 1 x 128 x 1, 128B swizzle
   CUtensorMap tm_k;      // 4-D over k [B, T, Hkv, D]
   CUtensorMap tm_v;      // 4-D over v [B, T, Hkv, D]
-  CUtensorMap tm_kfull;  // 3-D over k_full [B * n_ret, n (extent), D]
-  CUtensorMap tm_vfull;
+  CUtensorMap tm_kfull;  // 3-D over k_full [B * n_ret, n (extent), D]; paged: over the pool
+  CUtensorMap tm_vfull;  //   [num_blocks, block_size, D]
+  CUtensorMap tm_klast;  // paged only: the pool with row extent n % block_size (last block)
+  CUtensorMap tm_vlast;
   CUtensorMap tm_ksr;    // 3-D over k_sr [B * n_str, nvalid (extent), D]
   CUtensorMap tm_vsr;
   uint16_t* o;           // bf16 [B, T, Hq, D]
@@ -115,6 +139,7 @@ struct PrefillParams {
   float scale_log2;
   Shape sh;
   HeadTable heads;
+  PagedLayout pg;
 };
 cudaError_t launch_prefill(const PrefillParams& p, cudaStream_t stream);
 

@@ -128,6 +128,14 @@ struct Tile {
   int k;      // tile index within its source
 };
 
+// Where cache tile k of a retrieval item lies in a paged pool (map_k null: contiguous).
+struct PagedTile {
+  const CUtensorMap* map_k = nullptr;
+  const CUtensorMap* map_v = nullptr;
+  int row = 0;  // first row within the block
+  int blk = 0;  // block id
+};
+
 __device__ __forceinline__ TilePlan plan_of(const PrefillParams& p, const Item& it) {
   TilePlan t;
   const int q0 = it.qp * kRows;  // first query row (chunk-local) of the CTA
@@ -166,6 +174,25 @@ __device__ __forceinline__ Tile tile_at(const TilePlan& pl, int j) {
     t.k = j < pl.sink_eff ? j : pl.w_lo + (j - pl.sink_eff);
   }
   return t;
+}
+
+__device__ __forceinline__ PagedTile paged_tile(const PrefillParams& p, const Item& it, int k) {
+  PagedTile pt;
+  if (!p.pg.table) return pt;
+  const int64_t r0 = (int64_t)k * BN;  // a 128-row tile never crosses a block
+  const int64_t plane = (int64_t)it.b * p.sh.n_ret + it.cidx;
+  int64_t blk = p.pg.table[plane * p.pg.max_blocks + r0 / p.pg.block_size];
+  if (blk < 0 || blk >= p.pg.num_blocks) {
+    atomicOr(&g_prefill_err, kErrBadBlock);
+    blk = p.pg.num_blocks;  // out of range: TMA reads zeros
+  }
+  // the last block, when partly written, goes through the map whose row extent stops at n
+  const bool last = (r0 / p.pg.block_size == (p.n - 1) / p.pg.block_size) && (p.n % p.pg.block_size != 0);
+  pt.map_k = last ? &p.tm_klast : &p.tm_kfull;
+  pt.map_v = last ? &p.tm_vlast : &p.tm_vfull;
+  pt.row = (int)(r0 % p.pg.block_size);
+  pt.blk = (int)blk;
+  return pt;
 }
 
 __device__ __forceinline__ float max3(float a, float b, float c) {
@@ -276,6 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
           const Tile t = tile_at(pl, j);
           const int s = j % kNS;
           const uint32_t ph = (uint32_t)((j / kNS) & 1);
+          const PagedTile pt = (t.phase == 0 && !it.streaming) ? paged_tile(p, it, t.k) : PagedTile{};
           if (!mbar_wait(&bars->k_empty[s], ph ^ 1u, err, kErrPrefillProducer)) {
             ok = false;
             break;
@@ -286,6 +314,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
           for (int bx = 0; bx < C::NBOX; ++bx) {
             if (t.phase == 1)
               tma_load_4d(dk + bx * kBox, &p.tm_k, bx * 64, it.kvh, t.k * BN, it.b, &bars->k_full[s]);
+            else if (!it.streaming && pt.map_k)
+              tma_load_3d(dk + bx * kBox, pt.map_k, bx * 64, pt.row, pt.blk, &bars->k_full[s]);
             else if (!it.streaming)
               tma_load_3d(dk + bx * kBox, &p.tm_kfull, bx * 64, t.k * BN, it.b * p.sh.n_ret + it.cidx, &bars->k_full[s]);
             else
@@ -302,6 +332,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
           for (int bx = 0; bx < C::NBOX; ++bx) {
             if (t.phase == 1)
               tma_load_4d(dv + bx * kBox, &p.tm_v, bx * 64, it.kvh, t.k * BN, it.b, &bars->v_full[s]);
+            else if (!it.streaming && pt.map_v)
+              tma_load_3d(dv + bx * kBox, pt.map_v, bx * 64, pt.row, pt.blk, &bars->v_full[s]);
             else if (!it.streaming)
               tma_load_3d(dv + bx * kBox, &p.tm_vfull, bx * 64, t.k * BN, it.b * p.sh.n_ret + it.cidx, &bars->v_full[s]);
             else
