@@ -325,7 +325,26 @@ def e2e_prefill(w, layer, q, k, v, o, flops, steps, warmup, world):
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": ho.numel() * 2}
 
 
-def bench_decode(w, steps_cap, peaks):
+def make_layer(w, cap, dev, paged_block):
+    """A DuoLayer, or with paged_block > 0 a DuoPagedLayer whose retrieval blocks are
+    scattered over the pool in a seeded random order."""
+    import numpy as np
+    import torch
+
+    from streaming_kv_cache_duo_gb300 import DuoLayer, DuoPagedLayer
+    kinds = w.is_retrieval
+    if paged_block <= 0:
+        return DuoLayer(w.B, w.Hq, w.Hkv, w.D, w.S, w.R, cap, kinds, device=dev)
+    n_ret = sum(kinds)
+    max_blocks = -(-cap // paged_block)
+    num_blocks = w.B * n_ret * max_blocks
+    ids = np.random.default_rng(w.seed).permutation(num_blocks).reshape(w.B, n_ret, max_blocks)
+    table = torch.tensor(ids, dtype=torch.int32, device=dev)
+    return DuoPagedLayer(w.B, w.Hq, w.Hkv, w.D, w.S, w.R, paged_block, max_blocks, num_blocks, table, kinds,
+                         device=dev)
+
+
+def bench_decode(w, steps_cap, peaks, paged_block=0):
     """Million-token decode: build the cache by appends, then time (append 1 token + decode)."""
     import torch
 
@@ -335,7 +354,7 @@ def bench_decode(w, steps_cap, peaks):
     dev = torch.device("cuda", torch.cuda.current_device())
     kinds = w.is_retrieval
     steps = min(w.decode_steps, steps_cap)
-    layer = DuoLayer(w.B, w.Hq, w.Hkv, w.D, w.S, w.R, w.context + w.decode_steps, kinds, device=dev)
+    layer = make_layer(w, w.context + w.decode_steps, dev, paged_block)
     chunk = 65536
     for c0 in range(0, w.context, chunk):
         kk = ds.stream_torch(w.seed, ds.STREAM_K, w.B, c0, chunk, w.Hkv, w.D, device=dev)
@@ -358,7 +377,7 @@ def bench_decode(w, steps_cap, peaks):
         layer.append(ks[s], vs[s])
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        duo_attn_decode(layer.handle, layer.cache, qs[s], o, layer.workspace, stream)
+        layer.decode(qs[s], out=o, stream=stream)
         b.record(stream)
         ev.append((a, b, layer.n))
     t1.record(stream)
@@ -445,7 +464,7 @@ def bench_decode_graph(w, peaks):
             "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 4)}
 
 
-def bench_chunked(w, steps, warmup, peaks):
+def bench_chunked(w, steps, warmup, peaks, paged_block=0):
     """Chunked prefill against the growing cache: one step = for each chunk, prefill of
     the chunk (keys: cache before it + the chunk) then its append."""
     import torch
@@ -456,7 +475,7 @@ def bench_chunked(w, steps, warmup, peaks):
     dev = torch.device("cuda", torch.cuda.current_device())
     L, C = w.prefill_len, w.chunk
     kinds = w.is_retrieval
-    layer = DuoLayer(w.B, w.Hq, w.Hkv, w.D, w.S, w.R, L, kinds, device=dev)
+    layer = make_layer(w, L, dev, paged_block)
     q = ds.stream_torch(w.seed, ds.STREAM_Q, w.B, 0, L, w.Hq, w.D, device=dev)
     k = ds.stream_torch(w.seed, ds.STREAM_K, w.B, 0, L, w.Hkv, w.D, device=dev)
     v = ds.stream_torch(w.seed, ds.STREAM_V, w.B, 0, L, w.Hkv, w.D, device=dev)
@@ -477,7 +496,7 @@ def bench_chunked(w, steps, warmup, peaks):
             b = torch.cuda.Event(enable_timing=True) if record else None
             if record:
                 a.record(stream)
-            duo_attn_prefill_select(layer.handle, layer.cache, qs[i], ks[i], vs[i], T, os_[i], 3, stream)
+            layer.prefill(qs[i], ks[i], vs[i], out=os_[i], stream=stream)
             if record:
                 b.record(stream)
                 pre.append((a, b))
@@ -588,15 +607,20 @@ def other_workload(args, w, world, rank, peaks):
             "config": {"workload": w.name, "batch": w.B, "q_heads": w.Hq, "kv_heads": w.Hkv, "head_dim": w.D,
                        "retrieval_kv_heads": sum(w.is_retrieval), "sink": w.S, "recent": w.R,
                        "parallelism": f"replicas{world}"}}
+    if args.paged:
+        base["config"]["paged_block"] = args.paged
     if w.chunk:
-        r = bench_chunked(w, args.steps, args.warmup, peaks)
+        r = bench_chunked(w, args.steps, args.warmup, peaks, args.paged)
         base["config"].update(seq_len=w.prefill_len, chunk=w.chunk,
                               step="8 x (prefill of a 4096-token chunk against the cache, append)")
         line = dict(base, value=round(r["value"] * world, 2), unit="TFLOP/s", ms_per_step=round(r["ms_per_step"], 4),
                     roofline=r["roofline"], gpu_launches=r["launches"],
                     breakdown_ms={"prefill": round(r["prefill_ms"], 4)})
     else:
-        r = bench_decode_graph(w, peaks) if w.B > 1 else bench_decode(w, w.decode_steps, peaks)
+        if args.paged or w.B == 1:
+            r = bench_decode(w, w.decode_steps, peaks, args.paged)
+        else:
+            r = bench_decode_graph(w, peaks)
         base["config"].update(context=w.context, decode_steps=w.decode_steps)
         line = dict(base, value=round(r["value"] * world, 1), unit="GB/s", ms_per_step=r.get("step_ms",
                     r.get("step_ms_with_append")), decode=r, gpu_launches=2 * r["steps_timed"])
@@ -615,6 +639,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--paged", type=int, default=0,
+                    help="decode / chunked workloads: retrieval caches in blocks of this many tokens, scattered")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")

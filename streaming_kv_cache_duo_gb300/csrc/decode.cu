@@ -163,56 +163,82 @@ __device__ __forceinline__ bool next_segment(const DecodeParams& p, int c, int64
   return false;
 }
 
-// The tile this warp refills next, walked forward one tile at a time.
+// The tile this warp refills next, walked forward one tile at a time. With a paged
+// pool (kPaged) the cursor also tracks the pool block of its tile: the eight warp
+// slices of a tile lie in one block (block sizes are multiples of kTK), so the
+// block table is read only when the cursor enters a new block, one tile before the
+// copy is issued, and a division is needed only where a segment starts.
+template <bool kPaged>
 struct Cursor {
   SegState st;
   int u;
   int64_t lt, lt1;
   Unit x;
   bool live;
+  int tpb;  // kPaged: tiles per block
+  int bi;   // kPaged: index of the block holding tile lt in the unit's table row
+  int bt;   // kPaged: tile lt's index within that block
+  int blk;  // kPaged: the block id there (as stored, unchecked)
+  __device__ __forceinline__ void fetch_block(const DecodeParams& p) {
+    // tiles past the keys are never read (their table entry may not exist)
+    if (lt * kTK < x.keys) blk = p.pg.table[x.plane * p.pg.max_blocks + bi];
+  }
+  __device__ __forceinline__ void enter_segment(const DecodeParams& p) {
+    if (live && !x.streaming) {
+      // rows stay below block_size x max_blocks < 2^31 (checked on the host)
+      bi = (int)((uint32_t)lt / (uint32_t)tpb);
+      bt = (int)lt - bi * tpb;
+      fetch_block(p);
+    }
+  }
   __device__ __forceinline__ void init(const DecodeParams& p, int c, int64_t t0, int64_t t1, bool streaming_too) {
     st.rt = t0;
     st.k = 0;
     live = next_segment(p, c, t1, streaming_too, st, u, lt, lt1);
     if (live) x = unit_info(p, u);
+    if (kPaged) {
+      tpb = p.pg.block_size / kTK;
+      bi = bt = blk = 0;
+      enter_segment(p);
+    }
   }
   __device__ __forceinline__ void advance(const DecodeParams& p, int c, int64_t t1, bool streaming_too) {
     if (++lt == lt1) {
       live = next_segment(p, c, t1, streaming_too, st, u, lt, lt1);
       if (live) x = unit_info(p, u);
+      if (kPaged) enter_segment(p);
+    } else if (kPaged && !x.streaming && ++bt == tpb) {
+      bt = 0;
+      ++bi;
+      fetch_block(p);
     }
   }
 };
 
-// Rows of tile `lt` this warp reads: its 16-row slice, or none if the tile lies in a
-// paged block whose id is out of range (recorded as an error).
-__device__ __forceinline__ int slice_rows(const DecodeParams& p, const Unit& x, int64_t lt, int w,
-                                          const uint16_t** kp, const uint16_t** vp) {
-  const int rows = warp_rows(x.keys, lt, w);
-  const int64_t row0 = lt * kTK + (int64_t)w * kKPW;
-  if (x.streaming || !p.pg.table) {
-    *kp = x.kb + row0 * p.sh.D;
-    *vp = x.vb + row0 * p.sh.D;
-    return rows;
-  }
-  if (rows == 0) return 0;
-  const int64_t off = retrieval_row(p.pg, p.sh.cap, p.sh.D, x.plane, row0);  // a slice never crosses a block
-  if (off < 0) return -1;
-  *kp = p.k_full + off;
-  *vp = p.v_full + off;
-  return rows;
-}
-
-template <int D, int G>
-__device__ __forceinline__ void issue_slice(const DecodeParams& p, const Cursor& cur, int w, uint8_t* stage,
-                                            uint64_t* bar) {
+// Copies this warp's slice of the cursor's tile into a stage. Returns true when the
+// slice lies in a paged block whose id is out of range: then nothing is copied, the
+// error is recorded and the consumer skips the slice's rows.
+template <int D, int G, bool kPaged>
+__device__ __forceinline__ bool issue_slice(const DecodeParams& p, const Cursor<kPaged>& cur, int w,
+                                            uint8_t* stage, uint64_t* bar) {
   using C = Cfg<D, G>;
-  const uint16_t* kp = nullptr;
-  const uint16_t* vp = nullptr;
-  int rows = slice_rows(p, cur.x, cur.lt, w, &kp, &vp);
-  if (rows < 0) {
-    atomicOr(&g_decode_err, kErrBadBlock);
-    rows = 0;
+  int rows = warp_rows(cur.x.keys, cur.lt, w);
+  const uint16_t* kp;
+  const uint16_t* vp;
+  bool bad = false;
+  if (kPaged && !cur.x.streaming) {
+    if (rows > 0 && (cur.blk < 0 || cur.blk >= p.pg.num_blocks)) {
+      atomicOr(&g_decode_err, kErrBadBlock);
+      rows = 0;
+      bad = true;
+    }
+    const int64_t off = ((int64_t)cur.blk * p.pg.block_size + cur.bt * kTK + w * kKPW) * D;
+    kp = p.k_full + off;
+    vp = p.v_full + off;
+  } else {
+    const int64_t row0 = cur.lt * kTK + (int64_t)w * kKPW;
+    kp = cur.x.kb + row0 * D;
+    vp = cur.x.vb + row0 * D;
   }
   const uint32_t bytes = (uint32_t)rows * C::ROW;
   mbar_arrive_expect_tx(bar, 2 * bytes);
@@ -220,6 +246,7 @@ __device__ __forceinline__ void issue_slice(const DecodeParams& p, const Cursor&
     bulk_g2s(stage, kp, bytes, bar);
     bulk_g2s(stage + C::SLICE, vp, bytes, bar);
   }
+  return bad;
 }
 
 __device__ __forceinline__ float2 unpack2(uint32_t w) { return make_float2(bf16lo(w), bf16hi(w)); }
@@ -238,7 +265,7 @@ struct WarpSync {
   }
 };
 
-template <int D, int G>
+template <int D, int G, bool kPaged>
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams p) {
   using C = Cfg<D, G>;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -266,11 +293,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
   __syncthreads();
 
   // refill cursor (warp-uniform); the prologue issues the first kNSW - 1 slices
-  Cursor cur;
+  Cursor<kPaged> cur;
   cur.init(p, c, t0, t1, live);
   int64_t issued = 0;
+  uint32_t badmask = 0;  // lane 0: bit s set when stage s holds a skipped (bad-block) slice
   for (int s = 0; s < kNSW - 1 && cur.live; ++s) {
-    if (lane == 0) issue_slice<D, G>(p, cur, warp, ring + s * C::WSTAGE, &wfull[s]);
+    if (lane == 0) {
+      const bool bad = issue_slice<D, G, kPaged>(p, cur, warp, ring + s * C::WSTAGE, &wfull[s]);
+      if (kPaged) badmask = bad ? (badmask | (1u << s)) : (badmask & ~(1u << s));
+    }
     cur.advance(p, c, t1, live);
     ++issued;
   }
@@ -316,7 +347,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
       // refill: the stage used by tile j - 1 is free now (this warp finished it)
       if (cur.live) {
         const int sn = (int)((j + kNSW - 1) % kNSW);
-        if (lane == 0) issue_slice<D, G>(p, cur, warp, ring + sn * C::WSTAGE, &wfull[sn]);
+        if (lane == 0) {
+          const bool bad = issue_slice<D, G, kPaged>(p, cur, warp, ring + sn * C::WSTAGE, &wfull[sn]);
+          if (kPaged) badmask = bad ? (badmask | (1u << sn)) : (badmask & ~(1u << sn));
+        }
         cur.advance(p, c, t1, live);
         ++issued;
       }
@@ -324,10 +358,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
         ok = false;
         break;
       }
-      const uint16_t* kp_unused;
-      const uint16_t* vp_unused;
-      const int rows_raw = slice_rows(p, x, lt, warp, &kp_unused, &vp_unused);
-      const int rows = rows_raw < 0 ? 0 : rows_raw;
+      int rows = warp_rows(x.keys, lt, warp);
+      if (kPaged && ((__shfl_sync(0xffffffffu, badmask, 0) >> s) & 1u)) rows = 0;
       const uint8_t* sk = ring + s * C::WSTAGE;
       const uint8_t* sv = sk + C::SLICE;
       const bool full_tile = rows == kKPW && !x.streaming;
@@ -601,17 +633,25 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
   __syncthreads();
 }
 
-template <int D, int G>
-cudaError_t launch_t(const DecodeParams& p, cudaStream_t stream) {
+template <int D, int G, bool kPaged>
+cudaError_t launch_v(const DecodeParams& p, cudaStream_t stream) {
   using C = Cfg<D, G>;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
+    cudaError_t e =
+        cudaFuncSetAttribute(decode_kernel<D, G, kPaged>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  decode_kernel<D, G><<<p.C, kThreads, C::SMEM, stream>>>(p);
+  decode_kernel<D, G, kPaged><<<p.C, kThreads, C::SMEM, stream>>>(p);
   return cudaGetLastError();
+}
+
+// contiguous and paged retrieval caches are separate kernels, so the paged block
+// bookkeeping costs the contiguous kernel nothing
+template <int D, int G>
+cudaError_t launch_t(const DecodeParams& p, cudaStream_t stream) {
+  return p.pg.table ? launch_v<D, G, true>(p, stream) : launch_v<D, G, false>(p, stream);
 }
 
 }  // namespace

@@ -58,6 +58,10 @@ constexpr int kRegsSoftmax = 200;
 constexpr int kRegsCtl = 104;
 static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsCtl <= kThreads * kLaunchRegs, "register split");
 constexpr uint32_t kTmemCols = 512;
+// Kernel variants, compiled separately so that the paged producer path leaves the
+// register allocation of the contiguous kernel untouched.
+constexpr int kModePlain = 0;  // contiguous retrieval caches
+constexpr int kModePaged = 1;  // retrieval caches in a paged pool (block table)
 constexpr int kBox = 128 * 128;  // bytes of a 128-row x 64-column bf16 box
 
 __host__ __device__ constexpr uint32_t col_s(int x) { return (uint32_t)x * 256u; }
@@ -128,13 +132,6 @@ struct Tile {
   int k;      // tile index within its source
 };
 
-// Where cache tile k of a retrieval item lies in a paged pool (map_k null: contiguous).
-struct PagedTile {
-  const CUtensorMap* map_k = nullptr;
-  const CUtensorMap* map_v = nullptr;
-  int row = 0;  // first row within the block
-  int blk = 0;  // block id
-};
 
 __device__ __forceinline__ TilePlan plan_of(const PrefillParams& p, const Item& it) {
   TilePlan t;
@@ -176,24 +173,21 @@ __device__ __forceinline__ Tile tile_at(const TilePlan& pl, int j) {
   return t;
 }
 
-__device__ __forceinline__ PagedTile paged_tile(const PrefillParams& p, const Item& it, int k) {
-  PagedTile pt;
-  if (!p.pg.table) return pt;
-  const int64_t r0 = (int64_t)k * BN;  // a 128-row tile never crosses a block
-  const int64_t plane = (int64_t)it.b * p.sh.n_ret + it.cidx;
-  int64_t blk = p.pg.table[plane * p.pg.max_blocks + r0 / p.pg.block_size];
-  if (blk < 0 || blk >= p.pg.num_blocks) {
-    atomicOr(&g_prefill_err, kErrBadBlock);
-    blk = p.pg.num_blocks;  // out of range: TMA reads zeros
+// Where the cache tiles of one retrieval item lie in a paged pool. Block sizes are
+// multiples of 128, so a 128-row tile never crosses a block; everything that does not
+// change from tile to tile is worked out once per CTA, leaving one 32-bit division
+// per tile on the producer thread.
+struct PagedWalk {
+  const int32_t* row;  // this item's row of the block table
+  int tpb;             // tiles per block
+  int last_blk;        // block holding row n - 1 when that block is partly written, else -1
+  __device__ __forceinline__ void init(const PrefillParams& p, const Item& it) {
+    row = p.pg.table + ((int64_t)it.b * p.sh.n_ret + it.cidx) * p.pg.max_blocks;
+    tpb = p.pg.block_size / BN;
+    last_blk = (p.n % p.pg.block_size != 0) ? (int)((p.n - 1) / p.pg.block_size) : -1;
   }
-  // the last block, when partly written, goes through the map whose row extent stops at n
-  const bool last = (r0 / p.pg.block_size == (p.n - 1) / p.pg.block_size) && (p.n % p.pg.block_size != 0);
-  pt.map_k = last ? &p.tm_klast : &p.tm_kfull;
-  pt.map_v = last ? &p.tm_vlast : &p.tm_vfull;
-  pt.row = (int)(r0 % p.pg.block_size);
-  pt.blk = (int)blk;
-  return pt;
-}
+  __device__ __forceinline__ int block_index(int k) const { return (int)((unsigned)k / (unsigned)tpb); }
+};
 
 __device__ __forceinline__ float max3(float a, float b, float c) {
   float r;
@@ -240,7 +234,7 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
       : "memory");
 }
 
-template <int D>
+template <int D, int kMode>
 __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ PrefillParams p) {
   using C = PCfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -298,12 +292,38 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             tma_load_4d(sQ + x * C::Q_BYTES + bx * kBox, &p.tm_q, bx * 64, it.hq, it.qp * kRows + x * BM, it.b,
                         &bars->q_full);
         bool ok = true;
+        // paged: the block id of the next cache tile is read one tile ahead, so its
+        // latency overlaps the wait for a free stage
+        const bool paged = kMode == kModePaged && !it.streaming;
+        PagedWalk pw;
+        int blk_next = 0;
+        if (paged) {
+          pw.init(p, it);
+          if (ntiles > 0 && pl.n_cache > 0) blk_next = __ldg(pw.row);  // cache tile 0 is in block 0
+        }
         int j = 0;
         for (; j < ntiles && ok; ++j) {
           const Tile t = tile_at(pl, j);
+          // paged cache tile: pool block, first row within it, and the maps to read through
+          int blk = 0, prow = 0;
+          const CUtensorMap* map_k = &p.tm_kfull;
+          const CUtensorMap* map_v = &p.tm_vfull;
+          if (paged && t.phase == 0) {
+            blk = blk_next;
+            const int bi = pw.block_index(t.k);
+            prow = (t.k - bi * pw.tpb) * BN;
+            if (bi == pw.last_blk) {
+              map_k = &p.tm_klast;
+              map_v = &p.tm_vlast;
+            }
+            if (j + 1 < pl.n_cache && j + 1 < ntiles) blk_next = __ldg(pw.row + pw.block_index(t.k + 1));
+            if (blk < 0 || blk >= p.pg.num_blocks) {
+              atomicOr(&g_prefill_err, kErrBadBlock);
+              blk = p.pg.num_blocks;  // out of range: TMA reads zeros
+            }
+          }
           const int s = j % kNS;
           const uint32_t ph = (uint32_t)((j / kNS) & 1);
-          const PagedTile pt = (t.phase == 0 && !it.streaming) ? paged_tile(p, it, t.k) : PagedTile{};
           if (!mbar_wait(&bars->k_empty[s], ph ^ 1u, err, kErrPrefillProducer)) {
             ok = false;
             break;
@@ -314,8 +334,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
           for (int bx = 0; bx < C::NBOX; ++bx) {
             if (t.phase == 1)
               tma_load_4d(dk + bx * kBox, &p.tm_k, bx * 64, it.kvh, t.k * BN, it.b, &bars->k_full[s]);
-            else if (!it.streaming && pt.map_k)
-              tma_load_3d(dk + bx * kBox, pt.map_k, bx * 64, pt.row, pt.blk, &bars->k_full[s]);
+            else if (paged)
+              tma_load_3d(dk + bx * kBox, map_k, bx * 64, prow, blk, &bars->k_full[s]);
             else if (!it.streaming)
               tma_load_3d(dk + bx * kBox, &p.tm_kfull, bx * 64, t.k * BN, it.b * p.sh.n_ret + it.cidx, &bars->k_full[s]);
             else
@@ -332,8 +352,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
           for (int bx = 0; bx < C::NBOX; ++bx) {
             if (t.phase == 1)
               tma_load_4d(dv + bx * kBox, &p.tm_v, bx * 64, it.kvh, t.k * BN, it.b, &bars->v_full[s]);
-            else if (!it.streaming && pt.map_v)
-              tma_load_3d(dv + bx * kBox, pt.map_v, bx * 64, pt.row, pt.blk, &bars->v_full[s]);
+            else if (paged)
+              tma_load_3d(dv + bx * kBox, map_v, bx * 64, prow, blk, &bars->v_full[s]);
             else if (!it.streaming)
               tma_load_3d(dv + bx * kBox, &p.tm_vfull, bx * 64, t.k * BN, it.b * p.sh.n_ret + it.cidx, &bars->v_full[s]);
             else
@@ -530,20 +550,20 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   }
 }
 
-template <int D>
+template <int D, int kMode>
 cudaError_t launch_t(const PrefillParams& p, cudaStream_t stream) {
   using C = PCfg<D>;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e =
-        cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
+        cudaFuncSetAttribute(prefill_kernel<D, kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
   static int regs = -1;
   if (regs < 0) {
     cudaFuncAttributes fa;
-    cudaError_t e = cudaFuncGetAttributes(&fa, prefill_kernel<D>);
+    cudaError_t e = cudaFuncGetAttributes(&fa, prefill_kernel<D, kMode>);
     if (e != cudaSuccess) return e;
     regs = fa.numRegs;
   }
@@ -551,16 +571,21 @@ cudaError_t launch_t(const PrefillParams& p, cudaStream_t stream) {
   if (regs != kLaunchRegs) return cudaErrorInvalidConfiguration;
   const int grid = p.items_r + p.items_s;
   if (grid == 0) return cudaSuccess;
-  prefill_kernel<D><<<grid, kThreads, C::SMEM, stream>>>(p);
+  prefill_kernel<D, kMode><<<grid, kThreads, C::SMEM, stream>>>(p);
   return cudaGetLastError();
+}
+
+template <int kMode>
+cudaError_t launch_mode(const PrefillParams& p, cudaStream_t stream) {
+  if (p.sh.D == 128) return launch_t<128, kMode>(p, stream);
+  if (p.sh.D == 64) return launch_t<64, kMode>(p, stream);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace
 
 cudaError_t launch_prefill(const PrefillParams& p, cudaStream_t stream) {
-  if (p.sh.D == 128) return launch_t<128>(p, stream);
-  if (p.sh.D == 64) return launch_t<64>(p, stream);
-  return cudaErrorInvalidValue;
+  return p.pg.table ? launch_mode<kModePaged>(p, stream) : launch_mode<kModePlain>(p, stream);
 }
 
 cudaError_t prefill_read_clear_error(uint32_t* code) {
