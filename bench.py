@@ -339,9 +339,11 @@ def e2e_prefill(w, layer, q, k, v, o, flops, steps, warmup, world):
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": ho.numel() * 2}
 
 
-def make_layer(w, cap, dev, paged_block):
+def make_layer(w, cap, dev, paged_block, pool=False):
     """A DuoLayer, or with paged_block > 0 a DuoPagedLayer whose retrieval blocks are
-    scattered over the pool in a seeded random order."""
+    scattered over the pool in a seeded random order; with `pool` the streaming heads
+    live in the same pool too (every block of their table allocated: the ones that
+    fall out of the window are simply never touched again)."""
     import numpy as np
     import torch
 
@@ -350,15 +352,18 @@ def make_layer(w, cap, dev, paged_block):
     if paged_block <= 0:
         return DuoLayer(w.B, w.Hq, w.Hkv, w.D, w.S, w.R, cap, kinds, device=dev)
     n_ret = sum(kinds)
+    n_str = len(kinds) - n_ret
     max_blocks = -(-cap // paged_block)
-    num_blocks = w.B * n_ret * max_blocks
-    ids = np.random.default_rng(w.seed).permutation(num_blocks).reshape(w.B, n_ret, max_blocks)
-    table = torch.tensor(ids, dtype=torch.int32, device=dev)
+    planes = n_ret + (n_str if pool else 0)
+    num_blocks = w.B * planes * max_blocks
+    ids = np.random.default_rng(w.seed).permutation(num_blocks).reshape(w.B, planes, max_blocks)
+    table = torch.tensor(ids[:, :n_ret], dtype=torch.int32, device=dev) if n_ret else None
+    stream = torch.tensor(ids[:, n_ret:], dtype=torch.int32, device=dev) if pool else None
     return DuoPagedLayer(w.B, w.Hq, w.Hkv, w.D, w.S, w.R, paged_block, max_blocks, num_blocks, table, kinds,
-                         device=dev)
+                         device=dev, stream_table=stream)
 
 
-def bench_decode(w, steps_cap, peaks, paged_block=0):
+def bench_decode(w, steps_cap, peaks, paged_block=0, pool=False):
     """Million-token decode: build the cache by appends, then time (append 1 token + decode)."""
     import torch
 
@@ -368,7 +373,7 @@ def bench_decode(w, steps_cap, peaks, paged_block=0):
     dev = torch.device("cuda", torch.cuda.current_device())
     kinds = w.is_retrieval
     steps = min(w.decode_steps, steps_cap)
-    layer = make_layer(w, w.context + w.decode_steps, dev, paged_block)
+    layer = make_layer(w, w.context + w.decode_steps, dev, paged_block, pool)
     chunk = 65536
     for c0 in range(0, w.context, chunk):
         kk = ds.stream_torch(w.seed, ds.STREAM_K, w.B, c0, chunk, w.Hkv, w.D, device=dev)
@@ -478,7 +483,7 @@ def bench_decode_graph(w, peaks):
             "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 4)}
 
 
-def bench_chunked(w, steps, warmup, peaks, paged_block=0):
+def bench_chunked(w, steps, warmup, peaks, paged_block=0, pool=False):
     """Chunked prefill against the growing cache: one step = for each chunk, prefill of
     the chunk (keys: cache before it + the chunk) then its append."""
     import torch
@@ -489,7 +494,7 @@ def bench_chunked(w, steps, warmup, peaks, paged_block=0):
     dev = torch.device("cuda", torch.cuda.current_device())
     L, C = w.prefill_len, w.chunk
     kinds = w.is_retrieval
-    layer = make_layer(w, L, dev, paged_block)
+    layer = make_layer(w, L, dev, paged_block, pool)
     q = ds.stream_torch(w.seed, ds.STREAM_Q, w.B, 0, L, w.Hq, w.D, device=dev)
     k = ds.stream_torch(w.seed, ds.STREAM_K, w.B, 0, L, w.Hkv, w.D, device=dev)
     v = ds.stream_torch(w.seed, ds.STREAM_V, w.B, 0, L, w.Hkv, w.D, device=dev)
@@ -623,8 +628,9 @@ def other_workload(args, w, world, rank, peaks):
                        "parallelism": f"replicas{world}"}}
     if args.paged:
         base["config"]["paged_block"] = args.paged
+        base["config"]["streaming_heads"] = "paged pool" if args.pool else "sink + ring cache"
     if w.chunk:
-        r = bench_chunked(w, args.steps, args.warmup, peaks, args.paged)
+        r = bench_chunked(w, args.steps, args.warmup, peaks, args.paged, args.pool)
         base["config"].update(seq_len=w.prefill_len, chunk=w.chunk,
                               step="8 x (prefill of a 4096-token chunk against the cache, append)")
         line = dict(base, value=round(r["value"] * world, 2), unit="TFLOP/s", ms_per_step=round(r["ms_per_step"], 4),
@@ -632,7 +638,7 @@ def other_workload(args, w, world, rank, peaks):
                     breakdown_ms={"prefill": round(r["prefill_ms"], 4)})
     else:
         if args.paged or w.B == 1:
-            r = bench_decode(w, w.decode_steps, peaks, args.paged)
+            r = bench_decode(w, w.decode_steps, peaks, args.paged, args.pool)
         else:
             r = bench_decode_graph(w, peaks)
         base["config"].update(context=w.context, decode_steps=w.decode_steps)
@@ -653,6 +659,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--pool", action="store_true",
+                    help="with --paged: streaming heads in the paged pool too (block-granular eviction)")
     ap.add_argument("--paged", type=int, default=0,
                     help="decode / chunked workloads: retrieval caches in blocks of this many tokens, scattered")
     args = ap.parse_args()

@@ -172,23 +172,45 @@ duo_status duo_attn_decode(duo_handle* handle, const duo_kv_cache* cache, const 
 duo_status duo_attn_decode_static(duo_handle* handle, const duo_kv_cache* cache, const void* q, void* o,
                                   void* stream);
 
-/* Paged retrieval caches, as a block allocator hands out memory in a serving engine
- * (vLLM issue "Could you support Attention Sink?" discusses the cache as fixed-size
- * token blocks chained by a block table). With a duo_paged descriptor, cache->k_full
- * and cache->v_full are pools of blocks, bf16 [num_blocks, block_size, D], shared by
- * every sequence and retrieval head; row t of retrieval head r of sequence b is row
- * t % block_size of block block_table[(b * n_ret + r) * max_blocks + t / block_size].
- * Streaming heads keep their sink + ring cache unchanged (a block-granular eviction
- * would change which keys a query sees). The capacity of a retrieval head is
- * block_size * max_blocks tokens (max_seq_len is not used). A block id outside
- * [0, num_blocks) is never dereferenced: its rows are skipped and duo_device_error()
- * reports DUO_ERR_INVALID_ARG. Results equal the contiguous layout's, bit for bit. */
+/* Paged caches, as a block allocator hands out memory in a serving engine (vLLM issue
+ * "Could you support Attention Sink?" discusses the cache as fixed-size token blocks
+ * chained by a block table, and keeping the first block as the sinks while dropping
+ * the middle blocks and keeping the recent ones). With a duo_paged descriptor,
+ * cache->k_full and cache->v_full are pools of blocks, bf16 [num_blocks, block_size,
+ * D], shared by every sequence and head; row t of retrieval head r of sequence b is
+ * row t % block_size of block block_table[(b * n_ret + r) * max_blocks + t / block_size].
+ *
+ * stream_table == NULL: streaming heads keep their sink + ring cache (cache->k_sr,
+ * v_sr, pos). stream_table != NULL: streaming heads live in the same pools too, token
+ * t of streaming head s of sequence b at row t % block_size of block
+ * stream_table[(b * n_str + s) * max_blocks + t / block_size]; cache->k_sr, v_sr and pos
+ * are then not used (may be NULL). Block granularity is only a storage choice: a query
+ * still sees exactly the sinks and its recent window, token by token, so results match
+ * the ring cache up to fp32 summation order. Once the cache holds n tokens, the blocks
+ * duo_paged_stream_dead_blocks names hold no token any later query can see: the caller
+ * may free them (their table entries are never read again). An append writes a
+ * streaming token only if its block is still live when the call ends, so only live
+ * blocks need to exist: the sink blocks and those reaching back R tokens from the end.
+ *
+ * The capacity of a head is block_size * max_blocks tokens (max_seq_len is not used).
+ * A block id outside [0, num_blocks) that would be read or written is never
+ * dereferenced: its rows are skipped and duo_device_error() reports
+ * DUO_ERR_INVALID_ARG. Retrieval results equal the contiguous layout's, bit for bit. */
 typedef struct {
-  const int32_t* block_table; /* int32 [B, n_ret, max_blocks], device memory */
-  int32_t block_size;         /* rows per block, a positive multiple of 128 */
-  int32_t max_blocks;         /* table entries per (sequence, retrieval head) */
-  int64_t num_blocks;         /* blocks in each pool */
+  const int32_t* block_table;  /* int32 [B, n_ret, max_blocks], device memory (NULL if n_ret = 0) */
+  int32_t block_size;          /* rows per block, a positive multiple of 128 */
+  int32_t max_blocks;          /* table entries per (sequence, head) */
+  int64_t num_blocks;          /* blocks in each pool */
+  const int32_t* stream_table; /* int32 [B, n_str, max_blocks], device memory, or NULL */
 } duo_paged;
+
+/* Logical blocks [*lo, *hi) of a paged streaming head that no query at a position
+ * >= n - 1 can see once the cache holds n tokens: blocks past the sink blocks
+ * (lo = ceil(S / block_size)) that end at or before the recent window of the last
+ * token (hi = max(lo, floor(max(0, n - R) / block_size))). The range only grows with
+ * n, so after each call the caller may free [previous hi, hi). Host only. */
+duo_status duo_paged_stream_dead_blocks(int32_t sink_size, int32_t recent_size, int32_t block_size, int64_t n,
+                                        int64_t* lo, int64_t* hi);
 
 duo_status duo_kv_append_paged(duo_handle* handle, duo_kv_cache* cache, const duo_paged* paged, const void* k_new,
                                const void* v_new, int32_t T, void* stream);

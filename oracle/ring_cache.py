@@ -84,3 +84,20 @@ def append_survivors(n: int, T: int, S: int, R: int) -> list:
     for t in range(n, n + T):
         last_writer[ring_slot(t, S, R)] = t
     return sorted(last_writer.values())
+
+
+def paged_stream_dead_blocks(n: int, S: int, R: int, block_size: int) -> list:
+    """Streaming head kept in a pool of token blocks (token t at row t): the logical
+    blocks, among those holding rows [0, n), that a caller may free once n tokens are
+    held.
+
+    Source: the same vLLM issue, whose later comment proposes keeping the first block
+    as the sink, dropping the blocks in the middle and keeping the recent ones. Read
+    here as storage only: a query still sees exactly the tokens the sink + ring cache
+    would hold, and those are what ``ring_positions_after`` simulates -- for the query
+    at position n - 1 and, as the window only moves forward, for every later one. A
+    block can go when it holds none of them; found by checking every block against
+    every held position (no closed form)."""
+    held = [p for p in ring_positions_after(n, S, R) if p != EMPTY]
+    blocks = (n + block_size - 1) // block_size
+    return [k for k in range(blocks) if not any(k * block_size <= p < (k + 1) * block_size for p in held)]

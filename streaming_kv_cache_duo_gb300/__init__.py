@@ -13,7 +13,7 @@ from . import _lib
 from ._lib import (DUO_RETRIEVAL, DUO_STREAMING, DuoError, duo_attn_decode, duo_attn_decode_varlen,  # noqa: F401
                    duo_attn_prefill, duo_attn_prefill_select, duo_cache_reset, duo_classify_heads, duo_create,
                    duo_decode_workspace_size, duo_destroy, duo_device_error, duo_kv_append, duo_kv_append_varlen,
-                   duo_last_error)
+                   duo_last_error, duo_paged_stream_dead_blocks)
 
 
 class DuoLayer:
@@ -116,24 +116,36 @@ class DuoLayer:
 
 
 class DuoPagedLayer(DuoLayer):
-    """A layer whose retrieval caches live in a shared pool of blocks addressed through
-    a block table (int32 [B, n_ret, max_blocks] on the device); streaming heads keep the
-    sink + ring cache."""
+    """A layer whose caches live in a shared pool of blocks addressed through block
+    tables (device int32): retrieval heads through ``block_table`` [B, n_ret,
+    max_blocks]; streaming heads through ``stream_table`` [B, n_str, max_blocks] when
+    given (block-granular eviction: ``dead_blocks()`` names the blocks the caller may
+    free), else they keep the sink + ring cache."""
 
     def __init__(self, batch, num_q_heads, num_kv_heads, head_dim, sink_size, recent_size, block_size,
-                 max_blocks, num_blocks, block_table, is_retrieval, device="cuda"):
+                 max_blocks, num_blocks, block_table, is_retrieval, device="cuda", stream_table=None):
         import torch
         super().__init__(batch, num_q_heads, num_kv_heads, head_dim, sink_size, recent_size, 1, is_retrieval,
                          device=device)
         bf = dict(dtype=torch.bfloat16, device=self.device)
+        self.block_size = block_size
         self.k_full = torch.empty((num_blocks, block_size, head_dim), **bf)
         self.v_full = torch.empty_like(self.k_full)
         self.cache.k_full = self.k_full.data_ptr()
         self.cache.v_full = self.v_full.data_ptr()
-        assert block_table.dtype == torch.int32 and block_table.is_cuda and block_table.is_contiguous()
-        assert tuple(block_table.shape) == (batch, self.n_ret, max_blocks)
+        for name, t, rows in (("block_table", block_table, self.n_ret), ("stream_table", stream_table, self.n_str)):
+            if t is not None:
+                assert t.dtype == torch.int32 and t.is_cuda and t.is_contiguous(), name
+                assert tuple(t.shape) == (batch, rows, max_blocks), name
         self.block_table = block_table
-        self.paged = _lib.duo_paged(block_table.data_ptr(), block_size, max_blocks, num_blocks)
+        self.stream_table = stream_table
+        self.paged = _lib.duo_paged(block_table.data_ptr() if block_table is not None else None, block_size,
+                                    max_blocks, num_blocks,
+                                    stream_table.data_ptr() if stream_table is not None else None)
+
+    def dead_blocks(self, n=None) -> tuple:
+        """Logical blocks [lo, hi) of every streaming head that no query can see any more."""
+        return _lib.duo_paged_stream_dead_blocks(self.S, self.R, self.block_size, self.n if n is None else n)
 
     def append(self, k_new, v_new, stream=None) -> None:
         T = k_new.shape[1]

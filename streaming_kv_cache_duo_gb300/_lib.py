@@ -31,6 +31,7 @@ EXPORTS = (
     "duo_classify_heads", "duo_create", "duo_destroy", "duo_cache_reset", "duo_kv_append",
     "duo_attn_prefill", "duo_attn_prefill_select", "duo_decode_workspace_size", "duo_attn_decode",
     "duo_attn_decode_static", "duo_kv_append_paged", "duo_attn_prefill_paged", "duo_attn_decode_paged",
+    "duo_paged_stream_dead_blocks",
     "duo_kv_append_varlen", "duo_attn_decode_varlen", "duo_device_error", "duo_selftest_bounded_wait",
     "duo_last_error", "duo_status_string",
 )
@@ -50,7 +51,7 @@ class duo_config(ctypes.Structure):
 
 class duo_paged(ctypes.Structure):
     _fields_ = [("block_table", c_void_p), ("block_size", c_int32), ("max_blocks", c_int32),
-                ("num_blocks", c_int64)]
+                ("num_blocks", c_int64), ("stream_table", c_void_p)]
 
 
 class duo_kv_cache(ctypes.Structure):
@@ -90,6 +91,8 @@ def library() -> ctypes.CDLL:
                                              c_void_p, c_void_p, c_int32, c_void_p, c_void_p]),
         "duo_attn_decode_paged": (c_int32, [c_void_p, POINTER(duo_kv_cache), POINTER(duo_paged), c_void_p,
                                             c_void_p, c_void_p, c_size_t, c_void_p]),
+        "duo_paged_stream_dead_blocks": (c_int32, [c_int32, c_int32, c_int32, c_int64, POINTER(c_int64),
+                                                   POINTER(c_int64)]),
         "duo_kv_append_varlen": (c_int32, [c_void_p, POINTER(duo_kv_cache), c_void_p, c_void_p, c_void_p,
                                            c_void_p]),
         "duo_attn_decode_varlen": (c_int32, [c_void_p, POINTER(duo_kv_cache), c_void_p, c_int64, c_void_p, c_void_p,
@@ -211,6 +214,14 @@ def duo_attn_decode_paged(handle, cache: "duo_kv_cache", paged: "duo_paged", q, 
     nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(library().duo_attn_decode_paged(handle, ctypes.byref(cache), ctypes.byref(paged), _ptr(q), _ptr(o),
                                            _ptr(workspace), nbytes, _stream_ptr(stream)))
+
+
+def duo_paged_stream_dead_blocks(sink_size: int, recent_size: int, block_size: int, n: int) -> tuple:
+    """(lo, hi): logical blocks of a paged streaming head no later query can see."""
+    lo, hi = c_int64(0), c_int64(0)
+    _check(library().duo_paged_stream_dead_blocks(sink_size, recent_size, block_size, n, ctypes.byref(lo),
+                                                  ctypes.byref(hi)))
+    return int(lo.value), int(hi.value)
 
 
 def duo_kv_append_varlen(handle, cache: "duo_kv_cache", seq_lens, k_new, v_new, stream=None) -> None:

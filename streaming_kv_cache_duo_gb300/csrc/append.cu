@@ -7,6 +7,10 @@
 // when the call ends are written (t < S, or t >= n + T - R), so the result equals
 // T single appends and no two threads write the same slot.
 //
+// Streaming heads kept in a paged pool (block-granular eviction) take every token
+// whose block is still live when the call ends instead, at row = position; the host
+// passes those tokens as the same two intervals.
+//
 // HBM-bound copy: one thread moves one 16-byte vector of K and one of V, with
 // read-only 128-bit loads from the token-major input and 128-bit stores into the
 // head-major caches. Bytes moved: 2 * 2 * D * (T * n_ret + survivors * n_str) per
@@ -65,12 +69,22 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendParams p) {
       const int64_t b = r / surv;
       const int64_t t_abs = k < p.sink_cnt ? p.sink_lo + k : p.ring_lo + (k - p.sink_cnt);
       const int64_t t = t_abs - p.n;
-      const int64_t slot = t_abs < p.sh.S ? t_abs : p.sh.S + (t_abs - p.sh.S) % p.sh.R;
       const int h = p.heads.str_head[si];
       const int64_t src = ((b * T + t) * Hkv + h) * vpr + v;
-      const int64_t dst = ((b * n_str + si) * SR + slot) * vpr + v;
       const uint4 kv = __ldg(kin + src);
       const uint4 vv = __ldg(vin + src);
+      if (p.pg.stream_table) {  // in the pool, at row = position
+        const int64_t off = pool_row(p.pg, p.pg.stream_table, D, b * n_str + si, t_abs);
+        if (off < 0) {
+          if (v == 0) atomicOr(&g_append_err, kErrBadBlock);
+          continue;
+        }
+        reinterpret_cast<uint4*>(p.k_full)[off / 8 + v] = kv;
+        reinterpret_cast<uint4*>(p.v_full)[off / 8 + v] = vv;
+        continue;
+      }
+      const int64_t slot = t_abs < p.sh.S ? t_abs : p.sh.S + (t_abs - p.sh.S) % p.sh.R;
+      const int64_t dst = ((b * n_str + si) * SR + slot) * vpr + v;
       reinterpret_cast<uint4*>(p.k_sr)[dst] = kv;
       reinterpret_cast<uint4*>(p.v_sr)[dst] = vv;
       if (si == 0 && v == 0) p.pos[b * SR + slot] = (int32_t)t_abs;

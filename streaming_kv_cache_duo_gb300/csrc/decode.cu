@@ -3,9 +3,11 @@
 //
 // Work list. A "unit" is one (sequence, KV head): a retrieval unit holds n keys
 // (rows [0, n) of its full cache), a streaming unit min(n, S + R) ring slots.
-// Retrieval units are cut into tiles of kTK keys laid end to end; CTA c takes
-// tiles [c W / C, (c + 1) W / C), so every SM streams the same number of key
-// bytes however long the contexts are. Streaming units (at most S + R keys) are
+// Retrieval units are cut into tiles of kTK keys laid end to end; CTA c < Cr takes
+// tiles [c W / Cr, (c + 1) W / Cr) with Cr = min(C, W), so no share is empty and
+// every SM streams the same number of key bytes however long the contexts are
+// (an empty share inside a unit's span would be counted as a part of the unit that
+// never arrives). Streaming units (at most S + R keys) are
 // dealt whole, round-robin: CTA c also takes units c, c + C, ... Only the n
 // written positions are ever read, never the capacity (the transformers
 // "Dynamic length in static cache" rule).
@@ -50,6 +52,12 @@ constexpr int kNSW = 3;             // pipeline stages per warp
 
 constexpr int ilog2(int v) { return v <= 1 ? 0 : 1 + ilog2(v / 2); }
 
+// Kernel variants, compiled separately so that the paged paths leave the register
+// allocation of the kernels that do not use them untouched.
+constexpr int kModePlain = 0;  // contiguous retrieval caches, ring caches for streaming heads
+constexpr int kModePaged = 1;  // retrieval caches in a paged pool (block table), ring caches
+constexpr int kModePool = 2;   // both head kinds in the paged pool
+
 template <int D, int G>
 struct Cfg {
   static constexpr int DPL = (G * 16 <= 64) ? 16 : 8;  // dims per lane
@@ -81,9 +89,9 @@ struct Unit {
   const uint16_t* vb;
 };
 
-// CTA whose share of the retrieval tiles contains tile t (shares are [c W / C, (c + 1) W / C)).
+// CTA whose share of the retrieval tiles contains tile t (shares are [c W / Cr, (c + 1) W / Cr)).
 __device__ __forceinline__ int cta_of(const DecodeParams& p, int64_t t) {
-  return (int)(((t + 1) * p.C - 1) / p.W);
+  return (int)(((t + 1) * p.Cr - 1) / p.W);
 }
 
 // Tokens held by sequence b: the uniform n, or its entry of the device length
@@ -94,6 +102,8 @@ __device__ __forceinline__ int64_t seq_len(const DecodeParams& p, int b) {
   return v < 0 ? 0 : (v > p.n ? p.n : v);
 }
 
+// kModePool: streaming heads live in the pool, rows = positions.
+template <int kMode>
 __device__ __forceinline__ Unit unit_info(const DecodeParams& p, int u) {
   Unit x;
   const int D = p.sh.D;
@@ -118,6 +128,10 @@ __device__ __forceinline__ Unit unit_info(const DecodeParams& p, int u) {
     x.streaming = true;
     x.pq = seq_len(p, x.b) - 1;
     x.keys = x.pq + 1 < (int64_t)(p.sh.S + p.sh.R) ? x.pq + 1 : (int64_t)(p.sh.S + p.sh.R);
+    if (kMode == kModePool) {  // rows [0, n) of its pool blocks, of which only some tiles are read
+      x.plane = us;
+      x.keys = x.pq + 1;
+    }
     x.ntiles = p.tiles_s;
     const int64_t off = ((int64_t)x.b * p.sh.n_str + si) * (int64_t)(p.sh.S + p.sh.R) * D;
     x.kb = p.k_sr + off;
@@ -163,31 +177,44 @@ __device__ __forceinline__ bool next_segment(const DecodeParams& p, int c, int64
   return false;
 }
 
+// Row tile read at local tile lt of a streaming unit kept in the pool: its sink
+// tiles, then the window tiles that are not among them.
+__device__ __forceinline__ int64_t stream_tile(const DecodeParams& p, int64_t lt) {
+  return lt < p.s_sink_tiles ? lt : p.s_win_lo + (lt - p.s_sink_tiles);
+}
+
 // The tile this warp refills next, walked forward one tile at a time. With a paged
-// pool (kPaged) the cursor also tracks the pool block of its tile: the eight warp
-// slices of a tile lie in one block (block sizes are multiples of kTK), so the
-// block table is read only when the cursor enters a new block, one tile before the
-// copy is issued, and a division is needed only where a segment starts.
-template <bool kPaged>
+// pool (kMode != kModePlain) the cursor also tracks the pool block of its tile: the eight warp
+// slices of a tile lie in one block (block sizes are multiples of kTK), so for a
+// retrieval unit the block table is read only when the cursor enters a new block, one
+// tile before the copy is issued, and a division is needed only where a segment
+// starts. The few tiles of a streaming unit in the pool are located one by one.
+template <int kMode>
 struct Cursor {
+  static constexpr bool kPaged = kMode != kModePlain;
   SegState st;
   int u;
   int64_t lt, lt1;
   Unit x;
   bool live;
-  int tpb;  // kPaged: tiles per block
-  int bi;   // kPaged: index of the block holding tile lt in the unit's table row
-  int bt;   // kPaged: tile lt's index within that block
-  int blk;  // kPaged: the block id there (as stored, unchecked)
+  int tpb;  // paged: tiles per block
+  int bi;   // paged: index of the block holding the tile in the unit's table row
+  int bt;   // paged: the tile's index within that block
+  int blk;  // paged: the block id there (as stored, unchecked)
+  __device__ __forceinline__ bool in_pool() const { return !x.streaming || kMode == kModePool; }
+  // row tile of the current position (= lt except for a streaming unit in the pool)
+  __device__ __forceinline__ int64_t row_tile() const { return (int64_t)bi * tpb + bt; }
   __device__ __forceinline__ void fetch_block(const DecodeParams& p) {
     // tiles past the keys are never read (their table entry may not exist)
-    if (lt * kTK < x.keys) blk = p.pg.table[x.plane * p.pg.max_blocks + bi];
+    if ((kMode == kModePool ? row_tile() : lt) * kTK < x.keys)
+      blk = ((kMode == kModePool && x.streaming) ? p.pg.stream_table : p.pg.table)[x.plane * p.pg.max_blocks + bi];
   }
-  __device__ __forceinline__ void enter_segment(const DecodeParams& p) {
-    if (live && !x.streaming) {
+  __device__ __forceinline__ void locate(const DecodeParams& p) {
+    if (live && in_pool()) {
       // rows stay below block_size x max_blocks < 2^31 (checked on the host)
-      bi = (int)((uint32_t)lt / (uint32_t)tpb);
-      bt = (int)lt - bi * tpb;
+      const int64_t k = (kMode == kModePool && x.streaming) ? stream_tile(p, lt) : lt;
+      bi = (int)((uint32_t)k / (uint32_t)tpb);
+      bt = (int)k - bi * tpb;
       fetch_block(p);
     }
   }
@@ -195,22 +222,26 @@ struct Cursor {
     st.rt = t0;
     st.k = 0;
     live = next_segment(p, c, t1, streaming_too, st, u, lt, lt1);
-    if (live) x = unit_info(p, u);
+    if (live) x = unit_info<kMode>(p, u);
     if (kPaged) {
       tpb = p.pg.block_size / kTK;
       bi = bt = blk = 0;
-      enter_segment(p);
+      locate(p);
     }
   }
   __device__ __forceinline__ void advance(const DecodeParams& p, int c, int64_t t1, bool streaming_too) {
     if (++lt == lt1) {
       live = next_segment(p, c, t1, streaming_too, st, u, lt, lt1);
-      if (live) x = unit_info(p, u);
-      if (kPaged) enter_segment(p);
-    } else if (kPaged && !x.streaming && ++bt == tpb) {
-      bt = 0;
-      ++bi;
-      fetch_block(p);
+      if (live) x = unit_info<kMode>(p, u);
+      if (kPaged) locate(p);
+    } else if (kPaged && !x.streaming) {
+      if (++bt == tpb) {
+        bt = 0;
+        ++bi;
+        fetch_block(p);
+      }
+    } else if (kMode == kModePool) {
+      locate(p);
     }
   }
 };
@@ -218,15 +249,16 @@ struct Cursor {
 // Copies this warp's slice of the cursor's tile into a stage. Returns true when the
 // slice lies in a paged block whose id is out of range: then nothing is copied, the
 // error is recorded and the consumer skips the slice's rows.
-template <int D, int G, bool kPaged>
-__device__ __forceinline__ bool issue_slice(const DecodeParams& p, const Cursor<kPaged>& cur, int w,
+template <int D, int G, int kMode>
+__device__ __forceinline__ bool issue_slice(const DecodeParams& p, const Cursor<kMode>& cur, int w,
                                             uint8_t* stage, uint64_t* bar) {
   using C = Cfg<D, G>;
-  int rows = warp_rows(cur.x.keys, cur.lt, w);
+  const bool pool = kMode != kModePlain && cur.in_pool();
+  int rows = warp_rows(cur.x.keys, kMode == kModePool ? cur.row_tile() : cur.lt, w);
   const uint16_t* kp;
   const uint16_t* vp;
   bool bad = false;
-  if (kPaged && !cur.x.streaming) {
+  if (pool) {
     if (rows > 0 && (cur.blk < 0 || cur.blk >= p.pg.num_blocks)) {
       atomicOr(&g_decode_err, kErrBadBlock);
       rows = 0;
@@ -265,7 +297,7 @@ struct WarpSync {
   }
 };
 
-template <int D, int G, bool kPaged>
+template <int D, int G, int kMode>
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams p) {
   using C = Cfg<D, G>;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -278,10 +310,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int c = blockIdx.x;
-  const int64_t t0 = (int64_t)c * p.W / p.C;
+  const int64_t t0 = c < p.Cr ? (int64_t)c * p.W / p.Cr : p.W;
   // After any CTA of this kernel gave up a wait, later CTAs do no work.
   const bool live = *(volatile unsigned int*)err.word == 0u;
-  const int64_t t1 = live ? (int64_t)(c + 1) * p.W / p.C : t0;
+  const int64_t t1 = live && c < p.Cr ? (int64_t)(c + 1) * p.W / p.Cr : t0;
   uint8_t* ring = smem + (size_t)warp * kNSW * C::WSTAGE;
   uint64_t* wfull = full + warp * kNSW;
 
@@ -293,13 +325,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
   __syncthreads();
 
   // refill cursor (warp-uniform); the prologue issues the first kNSW - 1 slices
-  Cursor<kPaged> cur;
+  constexpr bool kPaged = kMode != kModePlain;
+  Cursor<kMode> cur;
   cur.init(p, c, t0, t1, live);
   int64_t issued = 0;
   uint32_t badmask = 0;  // lane 0: bit s set when stage s holds a skipped (bad-block) slice
   for (int s = 0; s < kNSW - 1 && cur.live; ++s) {
     if (lane == 0) {
-      const bool bad = issue_slice<D, G, kPaged>(p, cur, warp, ring + s * C::WSTAGE, &wfull[s]);
+      const bool bad = issue_slice<D, G, kMode>(p, cur, warp, ring + s * C::WSTAGE, &wfull[s]);
       if (kPaged) badmask = bad ? (badmask | (1u << s)) : (badmask & ~(1u << s));
     }
     cur.advance(p, c, t1, live);
@@ -317,7 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
   int u;
   int64_t lt_begin, lt_end;
   while (ok && next_segment(p, c, t1, live, seg, u, lt_begin, lt_end)) {
-    const Unit x = unit_info(p, u);
+    const Unit x = unit_info<kMode>(p, u);
 
     // q of head (hme ^ l) in slot l, this lane's dims, pre-scaled, as fp32 pairs
     float2 q2[G][C::DPL / 2];
@@ -348,7 +381,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
       if (cur.live) {
         const int sn = (int)((j + kNSW - 1) % kNSW);
         if (lane == 0) {
-          const bool bad = issue_slice<D, G, kPaged>(p, cur, warp, ring + sn * C::WSTAGE, &wfull[sn]);
+          const bool bad = issue_slice<D, G, kMode>(p, cur, warp, ring + sn * C::WSTAGE, &wfull[sn]);
           if (kPaged) badmask = bad ? (badmask | (1u << sn)) : (badmask & ~(1u << sn));
         }
         cur.advance(p, c, t1, live);
@@ -358,7 +391,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
         ok = false;
         break;
       }
-      int rows = warp_rows(x.keys, lt, warp);
+      // streaming unit in the pool: keys are rows (= positions) of row tile kt
+      const bool str_pool = kMode == kModePool && x.streaming;
+      const int64_t kt = str_pool ? stream_tile(p, lt) : lt;
+      int rows = warp_rows(x.keys, kt, warp);
       if (kPaged && ((__shfl_sync(0xffffffffu, badmask, 0) >> s) & 1u)) rows = 0;
       const uint8_t* sk = ring + s * C::WSTAGE;
       const uint8_t* sv = sk + C::SLICE;
@@ -373,8 +409,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
         if (!full_tile) {
           valid = key < rows;
           if (x.streaming && valid) {
-            const int64_t slot = lt * kTK + (int64_t)warp * kKPW + key;
-            const int jp = __ldg(p.pos + (int64_t)x.b * SR + slot);
+            const int64_t slot = kt * kTK + (int64_t)warp * kKPW + key;
+            const int jp = str_pool ? (int)slot : __ldg(p.pos + (int64_t)x.b * SR + slot);
             valid = jp >= 0 && jp <= x.pq && (jp < p.sh.S || x.pq - jp < p.sh.R);
           }
         }
@@ -633,17 +669,17 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
   __syncthreads();
 }
 
-template <int D, int G, bool kPaged>
+template <int D, int G, int kMode>
 cudaError_t launch_v(const DecodeParams& p, cudaStream_t stream) {
   using C = Cfg<D, G>;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e =
-        cudaFuncSetAttribute(decode_kernel<D, G, kPaged>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
+        cudaFuncSetAttribute(decode_kernel<D, G, kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  decode_kernel<D, G, kPaged><<<p.C, kThreads, C::SMEM, stream>>>(p);
+  decode_kernel<D, G, kMode><<<p.C, kThreads, C::SMEM, stream>>>(p);
   return cudaGetLastError();
 }
 
@@ -651,7 +687,8 @@ cudaError_t launch_v(const DecodeParams& p, cudaStream_t stream) {
 // bookkeeping costs the contiguous kernel nothing
 template <int D, int G>
 cudaError_t launch_t(const DecodeParams& p, cudaStream_t stream) {
-  return p.pg.table ? launch_v<D, G, true>(p, stream) : launch_v<D, G, false>(p, stream);
+  if (p.pg.stream_table) return launch_v<D, G, kModePool>(p, stream);
+  return p.pg.table ? launch_v<D, G, kModePaged>(p, stream) : launch_v<D, G, kModePlain>(p, stream);
 }
 
 }  // namespace

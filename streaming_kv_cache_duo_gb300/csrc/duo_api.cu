@@ -123,23 +123,47 @@ duo_status check_cache(const duo_handle* h, const duo_kv_cache* c, bool need_ful
 }
 
 duo_status check_paged(const duo_handle* h, const duo_paged* pg, PagedLayout* out) {
-  *out = PagedLayout{nullptr, 0, 0, 0};
+  *out = PagedLayout{nullptr, 0, 0, 0, nullptr};
   if (!pg) return DUO_OK;
-  if (!pg->block_table || (reinterpret_cast<uintptr_t>(pg->block_table) & 3u))
+  if (h->sh.n_ret > 0 && (!pg->block_table || (reinterpret_cast<uintptr_t>(pg->block_table) & 3u)))
     return fail(DUO_ERR_INVALID_ARG, "block_table NULL or not 4-byte aligned");
+  if (reinterpret_cast<uintptr_t>(pg->stream_table) & 3u)
+    return fail(DUO_ERR_INVALID_ARG, "stream_table not 4-byte aligned");
+  if (h->sh.n_ret == 0 && !(h->sh.n_str > 0 && pg->stream_table))
+    return fail(DUO_ERR_INVALID_ARG, "paged layout with no head in the pool");
   if (pg->block_size < 128 || pg->block_size % 128 != 0)
     return fail(DUO_ERR_UNSUPPORTED, "block_size = %d is not a positive multiple of 128", pg->block_size);
   if (pg->max_blocks < 1 || pg->num_blocks < 1 || pg->num_blocks > 0x7fffffffLL)
     return fail(DUO_ERR_INVALID_ARG, "max_blocks / num_blocks out of range");
   if ((int64_t)pg->block_size * pg->max_blocks > 0x7fffffffLL)
     return fail(DUO_ERR_INVALID_ARG, "block_size x max_blocks >= 2^31");
-  *out = PagedLayout{pg->block_table, pg->block_size, pg->max_blocks, pg->num_blocks};
-  (void)h;
+  *out = PagedLayout{h->sh.n_ret > 0 ? pg->block_table : nullptr, pg->block_size, pg->max_blocks, pg->num_blocks,
+                     h->sh.n_str > 0 ? pg->stream_table : nullptr};
   return DUO_OK;
 }
 
+bool is_paged(const PagedLayout& pg) { return pg.table || pg.stream_table; }
+
 int64_t retrieval_capacity(const duo_handle* h, const PagedLayout& pg) {
-  return pg.table ? (int64_t)pg.block_size * pg.max_blocks : h->sh.cap;
+  return is_paged(pg) ? (int64_t)pg.block_size * pg.max_blocks : h->sh.cap;
+}
+
+// Tokens a cache can hold: every head kind kept in the pool, or with full rows,
+// stops at its capacity; ring caches have none.
+duo_status check_capacity(const duo_handle* h, const PagedLayout& pg, int64_t n, duo_status code) {
+  const int64_t cap = retrieval_capacity(h, pg);
+  const bool bounded = h->sh.n_ret > 0 || pg.stream_table;
+  if (bounded && n > cap)
+    return fail(code, "%lld tokens exceed the cache capacity %lld", (long long)n, (long long)cap);
+  return DUO_OK;
+}
+
+// Streaming heads in the pool: logical blocks [lo, hi) hold no token a query at a
+// position >= n - 1 can see (past the sink blocks, ending at or before n - R).
+void stream_dead_blocks(int64_t S, int64_t R, int64_t bs, int64_t n, int64_t* lo, int64_t* hi) {
+  *lo = (S + bs - 1) / bs;
+  const int64_t w = n > R ? n - R : 0;
+  *hi = w / bs > *lo ? w / bs : *lo;
 }
 
 }  // namespace
@@ -261,18 +285,15 @@ static duo_status append_impl(duo_handle* h, duo_kv_cache* c, const duo_paged* p
                               const void* v_new, int32_t T, void* stream) {
   duo_status st = check_handle(h);
   if (st != DUO_OK) return st;
-  if ((st = check_cache(h, c, true, true)) != DUO_OK) return st;
   PagedLayout pg;
   if ((st = check_paged(h, pgd, &pg)) != DUO_OK) return st;
+  if ((st = check_cache(h, c, true, !pg.stream_table)) != DUO_OK) return st;
   if (T < 1) return fail(DUO_ERR_INVALID_ARG, "T = %d < 1", T);
   if (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new))
     return fail(DUO_ERR_INVALID_ARG, "k_new / v_new NULL or not 16-byte aligned");
   const Shape& sh = h->sh;
   if (c->n + T > 0x7fffffffLL) return fail(DUO_ERR_CAPACITY, "positions would reach 2^31");
-  const int64_t cap = retrieval_capacity(h, pg);
-  if (sh.n_ret > 0 && c->n + T > cap)
-    return fail(DUO_ERR_CAPACITY, "n + T = %lld exceeds the retrieval capacity %lld", (long long)(c->n + T),
-                (long long)cap);
+  if ((st = check_capacity(h, pg, c->n + T, DUO_ERR_CAPACITY)) != DUO_OK) return st;
   AppendParams p;
   memset(&p, 0, sizeof(p));
   p.pg = pg;
@@ -286,12 +307,20 @@ static duo_status append_impl(duo_handle* h, duo_kv_cache* c, const duo_paged* p
   p.n = c->n;
   p.T = T;
   const int64_t n = c->n, e = c->n + T, S = sh.S, R = sh.R;
-  // survivors of the call: t < S, or t >= n + T - R
+  // survivors of the call: t < S, or t >= n + T - R (ring cache); in a pool, every
+  // token whose block is still live when the call ends: t < lo * bs or t >= hi * bs
+  int64_t sink_end = S, win_lo = e - R;
+  if (pg.stream_table) {
+    int64_t lo, hi;
+    stream_dead_blocks(S, R, pg.block_size, e, &lo, &hi);
+    sink_end = lo * pg.block_size;
+    win_lo = hi * pg.block_size;
+  }
   p.sink_lo = n;
-  p.sink_cnt = n < S ? ((e < S ? e : S) - n) : 0;
+  p.sink_cnt = n < sink_end ? ((e < sink_end ? e : sink_end) - n) : 0;
   int64_t r0 = n;
-  if (r0 < S) r0 = S;
-  if (r0 < e - R) r0 = e - R;
+  if (r0 < sink_end) r0 = sink_end;
+  if (r0 < win_lo) r0 = win_lo;
   p.ring_lo = r0;
   p.ring_cnt = e > r0 ? e - r0 : 0;
   p.sh = sh;
@@ -320,9 +349,9 @@ static duo_status prefill_impl(duo_handle* h, const duo_kv_cache* c, const duo_p
   if (!c) return fail(DUO_ERR_INVALID_ARG, "cache is NULL");
   const Shape& sh = h->sh;
   const bool use_cache = c->n > 0;
-  if ((st = check_cache(h, c, use_cache, use_cache)) != DUO_OK) return st;
   PagedLayout pg;
   if ((st = check_paged(h, pgd, &pg)) != DUO_OK) return st;
+  if ((st = check_cache(h, c, use_cache, use_cache && !pg.stream_table)) != DUO_OK) return st;
   if (T < 1) return fail(DUO_ERR_INVALID_ARG, "T = %d < 1", T);
   if (!q || !k || !v || !o) return fail(DUO_ERR_INVALID_ARG, "q / k / v / o is NULL");
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o))
@@ -337,9 +366,9 @@ static duo_status prefill_impl(duo_handle* h, const duo_kv_cache* c, const duo_p
   if ((st = encode_tokens(h, &p.tm_v, v, sh.B, T, sh.Hkv, sh.D)) != DUO_OK) return st;
   const int64_t SR = (int64_t)sh.S + sh.R;
   const int nvalid = (int)(c->n < SR ? c->n : SR);
-  if (use_cache && sh.n_ret > 0) {
-    if (c->n > retrieval_capacity(h, pg)) return fail(DUO_ERR_INVALID_ARG, "cache->n exceeds the retrieval capacity");
-    if (!pg.table) {
+  if (use_cache && (sh.n_ret > 0 || pg.stream_table)) {
+    if ((st = check_capacity(h, pg, c->n, DUO_ERR_INVALID_ARG)) != DUO_OK) return st;
+    if (!is_paged(pg)) {
       if ((st = encode_cache(h, &p.tm_kfull, c->k_full, (int64_t)sh.B * sh.n_ret, sh.cap, c->n, sh.D)) != DUO_OK)
         return st;
       if ((st = encode_cache(h, &p.tm_vfull, c->v_full, (int64_t)sh.B * sh.n_ret, sh.cap, c->n, sh.D)) != DUO_OK)
@@ -356,7 +385,7 @@ static duo_status prefill_impl(duo_handle* h, const duo_kv_cache* c, const duo_p
     }
   }
   p.pg = pg;
-  if (use_cache && sh.n_str > 0) {
+  if (use_cache && sh.n_str > 0 && !pg.stream_table) {
     if ((st = encode_cache(h, &p.tm_ksr, c->k_sr, (int64_t)sh.B * sh.n_str, SR, nvalid, sh.D)) != DUO_OK) return st;
     if ((st = encode_cache(h, &p.tm_vsr, c->v_sr, (int64_t)sh.B * sh.n_str, SR, nvalid, sh.D)) != DUO_OK) return st;
   }
@@ -399,7 +428,8 @@ duo_status duo_attn_prefill_paged(duo_handle* h, const duo_kv_cache* c, const du
 static void decode_plan(const duo_handle* h, int64_t n, DecodeParams* p) {
   const Shape& sh = h->sh;
   p->seq_lens = nullptr;  // uniform length n unless a caller sets device lengths
-  p->pg = PagedLayout{nullptr, 0, 0, 0};  // contiguous retrieval caches unless paged
+  p->pg = PagedLayout{nullptr, 0, 0, 0, nullptr};  // contiguous retrieval caches unless paged
+  p->s_sink_tiles = p->s_win_lo = 0;
   const int64_t SR = (int64_t)sh.S + sh.R;
   p->n = n;
   p->nvalid = (int)(n < SR ? n : SR);
@@ -410,6 +440,7 @@ static void decode_plan(const duo_handle* h, int64_t n, DecodeParams* p) {
   p->W = (int64_t)p->U_r * p->tiles_r;  // retrieval tiles; streaming units are dealt whole
   const int64_t work = p->W + p->U_s;
   p->C = (int)(work < h->num_sms ? work : h->num_sms);
+  p->Cr = (int)(p->W < p->C ? p->W : p->C);
 }
 
 size_t duo_decode_workspace_size(const duo_handle* h, int64_t n) {
@@ -425,12 +456,11 @@ static duo_status decode_impl(duo_handle* h, const duo_kv_cache* c, const duo_pa
                               void* workspace, size_t ws_bytes, void* stream) {
   duo_status st = check_handle(h);
   if (st != DUO_OK) return st;
-  if ((st = check_cache(h, c, true, true)) != DUO_OK) return st;
   PagedLayout pg;
   if ((st = check_paged(h, pgd, &pg)) != DUO_OK) return st;
+  if ((st = check_cache(h, c, true, !pg.stream_table)) != DUO_OK) return st;
   if (c->n < 1) return fail(DUO_ERR_INVALID_ARG, "decode needs the query token appended first (cache->n >= 1)");
-  if (h->sh.n_ret > 0 && c->n > retrieval_capacity(h, pg))
-    return fail(DUO_ERR_INVALID_ARG, "cache->n exceeds the retrieval capacity");
+  if ((st = check_capacity(h, pg, c->n, DUO_ERR_INVALID_ARG)) != DUO_OK) return st;
   if (!q || !o || !aligned16(q) || !aligned16(o))
     return fail(DUO_ERR_INVALID_ARG, "q / o NULL or not 16-byte aligned");
   const size_t need = decode_workspace_bytes(h->sh, h->num_sms);
@@ -464,6 +494,19 @@ static duo_status decode_impl(duo_handle* h, const duo_kv_cache* c, const duo_pa
   p.sh = sh;
   p.heads = h->heads;
   p.pg = pg;
+  if (pg.stream_table) {
+    // streaming units read rows (= positions) of the pool: the sink tiles, then the
+    // tiles of the window [max(S, n - R), n) not already among them
+    const int64_t n = c->n;
+    const int64_t st_tiles = ((n < sh.S ? n : sh.S) + kDecodeTK - 1) / kDecodeTK;
+    const int64_t w0 = n - sh.R > sh.S ? n - sh.R : sh.S;
+    int64_t wl = w0 / kDecodeTK;
+    if (wl < st_tiles) wl = st_tiles;
+    const int64_t te = (n + kDecodeTK - 1) / kDecodeTK;
+    p.s_sink_tiles = (int)st_tiles;
+    p.s_win_lo = (int)wl;
+    p.tiles_s = (int)(st_tiles + (te > wl ? te - wl : 0));
+  }
   cudaError_t ce = launch_decode(p, (cudaStream_t)stream);
   if (ce != cudaSuccess) {
     h->workspace_dirty = true;
@@ -481,6 +524,17 @@ duo_status duo_attn_decode_paged(duo_handle* h, const duo_kv_cache* c, const duo
                                  void* o, void* workspace, size_t ws_bytes, void* stream) {
   if (!paged) return fail(DUO_ERR_INVALID_ARG, "paged is NULL");
   return decode_impl(h, c, paged, q, o, workspace, ws_bytes, stream);
+}
+
+duo_status duo_paged_stream_dead_blocks(int32_t sink_size, int32_t recent_size, int32_t block_size, int64_t n,
+                                        int64_t* lo, int64_t* hi) {
+  if (!lo || !hi) return fail(DUO_ERR_INVALID_ARG, "lo / hi is NULL");
+  if (sink_size < 0 || recent_size < 1 || n < 0)
+    return fail(DUO_ERR_INVALID_ARG, "sink_size < 0, recent_size < 1 or n < 0");
+  if (block_size < 128 || block_size % 128 != 0)
+    return fail(DUO_ERR_UNSUPPORTED, "block_size = %d is not a positive multiple of 128", block_size);
+  stream_dead_blocks(sink_size, recent_size, block_size, n, lo, hi);
+  return ok();
 }
 
 duo_status duo_kv_append_varlen(duo_handle* h, duo_kv_cache* c, int32_t* seq_lens, const void* k_new,

@@ -48,15 +48,23 @@ struct PagedLayout {
   int32_t block_size;    // a multiple of 128
   int32_t max_blocks;
   int64_t num_blocks;
+  const int32_t* stream_table;  // streaming heads in the pool too (row = position); nullptr = ring caches
 };
+
+// Element offset in the pool of row r of plane `plane` of a block table; -1 if its
+// block id is out of range.
+__host__ __device__ __forceinline__ int64_t pool_row(const PagedLayout& pg, const int32_t* table, int D,
+                                                     int64_t plane, int64_t r) {
+  const int64_t blk = table[plane * pg.max_blocks + r / pg.block_size];
+  if (blk < 0 || blk >= pg.num_blocks) return -1;
+  return (blk * pg.block_size + r % pg.block_size) * D;
+}
 
 // Element offset of row r of retrieval plane `plane`; -1 if its block id is out of range.
 __host__ __device__ __forceinline__ int64_t retrieval_row(const PagedLayout& pg, int64_t cap, int D, int64_t plane,
                                                           int64_t r) {
   if (!pg.table) return (plane * cap + r) * D;
-  const int64_t blk = pg.table[plane * pg.max_blocks + r / pg.block_size];
-  if (blk < 0 || blk >= pg.num_blocks) return -1;
-  return (blk * pg.block_size + r % pg.block_size) * D;
+  return pool_row(pg, pg.table, D, plane, r);
 }
 
 // ------------------------------------------------------------------ append
@@ -100,9 +108,13 @@ struct DecodeParams {
   int U_r, U_s;    // units (one per (sequence, KV head)) of each kind
   int64_t tiles_r; // key tiles per retrieval unit
   int64_t tiles_s; // key tiles per streaming unit
+  int s_sink_tiles, s_win_lo;  // streaming heads in the pool: local tile lt reads row tile lt
+                               // (lt < s_sink_tiles), else s_win_lo + lt - s_sink_tiles
   int64_t W;       // retrieval tiles: U_r * tiles_r
-  int C;           // CTAs; CTA c takes retrieval tiles [c W / C, (c+1) W / C) and
-                   // streaming units c, c + C, ...
+  int C;           // CTAs; CTA c < Cr takes retrieval tiles [c W / Cr, (c+1) W / Cr), and
+                   // every CTA c streaming units c, c + C, ...
+  int Cr;          // CTAs sharing the retrieval tiles: min(C, W), so none of them gets an
+                   // empty share inside a unit's span (its partial would never arrive)
   float scale_log2;    // log2(e) / sqrt(D)
   uint32_t* counters;  // [U_r + U_s] arrival tickets, left at zero
   float* partials;     // [C + U_r + U_s][g][D + 4] (o, max, sum, 2 pad) per segment

@@ -58,10 +58,11 @@ constexpr int kRegsSoftmax = 200;
 constexpr int kRegsCtl = 104;
 static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsCtl <= kThreads * kLaunchRegs, "register split");
 constexpr uint32_t kTmemCols = 512;
-// Kernel variants, compiled separately so that the paged producer path leaves the
-// register allocation of the contiguous kernel untouched.
-constexpr int kModePlain = 0;  // contiguous retrieval caches
-constexpr int kModePaged = 1;  // retrieval caches in a paged pool (block table)
+// Kernel variants, compiled separately so that the paged paths leave the register
+// allocation of the kernels that do not use them untouched.
+constexpr int kModePlain = 0;  // contiguous retrieval caches, ring caches for streaming heads
+constexpr int kModePaged = 1;  // retrieval caches in a paged pool (block table), ring caches
+constexpr int kModePool = 2;   // both head kinds in the paged pool
 constexpr int kBox = 128 * 128;  // bytes of a 128-row x 64-column bf16 box
 
 __host__ __device__ constexpr uint32_t col_s(int x) { return (uint32_t)x * 256u; }
@@ -118,9 +119,13 @@ __device__ __forceinline__ Item item_of(const PrefillParams& p, int idx) {
 }
 
 // The KV tiles a CTA visits: first tiles of the cache (phase 0), then tiles of
-// the new tokens (phase 1): [0, sink_eff) for sinks, then [w_lo, k_hi].
+// the new tokens (phase 1): [0, sink_eff) for sinks, then [w_lo, k_hi]. Cache tiles
+// are [0, n_cache), except for a streaming head kept in a paged pool (rows =
+// positions): [0, c_sink) then [c_wlo, c_wlo + n_cache - c_sink).
 struct TilePlan {
   int n_cache;
+  int c_sink;
+  int c_wlo;
   int sink_eff;
   int w_lo;
   int k_hi;
@@ -133,6 +138,7 @@ struct Tile {
 };
 
 
+template <int kMode>
 __device__ __forceinline__ TilePlan plan_of(const PrefillParams& p, const Item& it) {
   TilePlan t;
   const int q0 = it.qp * kRows;  // first query row (chunk-local) of the CTA
@@ -142,6 +148,25 @@ __device__ __forceinline__ TilePlan plan_of(const PrefillParams& p, const Item& 
     t.n_cache = (int)((p.n + BN - 1) / BN);
     t.sink_eff = 0;
     t.w_lo = 0;
+  } else if (kMode == kModePool) {
+    // sink rows [0, min(S, n)), then the rows the first query row can still see:
+    // [max(S, n + q0 - R + 1), n), skipping tiles already taken as sink tiles
+    const int64_t sinks = p.sh.S < p.n ? p.sh.S : p.n;
+    t.c_sink = (int)((sinks + BN - 1) / BN);
+    int64_t w0 = p.n + q0 - p.sh.R + 1;
+    if (w0 < p.sh.S) w0 = p.sh.S;
+    int wl = (int)(w0 / BN);
+    if (wl < t.c_sink) wl = t.c_sink;
+    const int te = (int)((p.n + BN - 1) / BN);
+    t.c_wlo = wl;
+    t.n_cache = t.c_sink + (w0 < p.n && te > wl ? te - wl : 0);
+    const int64_t sink_cols = (int64_t)p.sh.S - p.n;  // new tokens that are sinks
+    const int sink_tiles = sink_cols > 0 ? (int)((sink_cols + BN - 1) / BN) : 0;
+    const int c_lo = q0 - p.sh.R + 1;
+    t.w_lo = c_lo > 0 ? c_lo / BN : 0;
+    t.sink_eff = sink_tiles < t.w_lo ? sink_tiles : t.w_lo;
+    t.total = t.n_cache + t.sink_eff + (t.k_hi - t.w_lo + 1);
+    return t;
   } else {
     const int ring_tiles = (p.nvalid + BN - 1) / BN;
     if (q0 + 1 < p.sh.R) {
@@ -156,15 +181,18 @@ __device__ __forceinline__ TilePlan plan_of(const PrefillParams& p, const Item& 
     t.w_lo = c_lo > 0 ? c_lo / BN : 0;
     t.sink_eff = sink_tiles < t.w_lo ? sink_tiles : t.w_lo;
   }
+  t.c_sink = t.n_cache;
+  t.c_wlo = 0;
   t.total = t.n_cache + t.sink_eff + (t.k_hi - t.w_lo + 1);
   return t;
 }
 
+template <int kMode>
 __device__ __forceinline__ Tile tile_at(const TilePlan& pl, int j) {
   Tile t;
   if (j < pl.n_cache) {
     t.phase = 0;
-    t.k = j;
+    t.k = (kMode == kModePool && j >= pl.c_sink) ? pl.c_wlo + (j - pl.c_sink) : j;
   } else {
     j -= pl.n_cache;
     t.phase = 1;
@@ -181,8 +209,11 @@ struct PagedWalk {
   const int32_t* row;  // this item's row of the block table
   int tpb;             // tiles per block
   int last_blk;        // block holding row n - 1 when that block is partly written, else -1
+  template <int kMode>
   __device__ __forceinline__ void init(const PrefillParams& p, const Item& it) {
-    row = p.pg.table + ((int64_t)it.b * p.sh.n_ret + it.cidx) * p.pg.max_blocks;
+    row = (kMode == kModePool && it.streaming)
+              ? p.pg.stream_table + ((int64_t)it.b * p.sh.n_str + it.cidx) * p.pg.max_blocks
+              : p.pg.table + ((int64_t)it.b * p.sh.n_ret + it.cidx) * p.pg.max_blocks;
     tpb = p.pg.block_size / BN;
     last_blk = (p.n % p.pg.block_size != 0) ? (int)((p.n - 1) / p.pg.block_size) : -1;
   }
@@ -196,6 +227,7 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
 }
 
 // Sets masked scores of one 32-column chunk to -inf (columns c0 ... c0+31 of tile t).
+template <int kMode>
 __device__ __forceinline__ void mask_chunk(float* v, const PrefillParams& p, const Item& it, const Tile& t, int c0,
                                            int i_abs) {
   const int S = p.sh.S, R = p.sh.R;
@@ -213,6 +245,15 @@ __device__ __forceinline__ void mask_chunk(float* v, const PrefillParams& p, con
 #pragma unroll
     for (int e = 0; e < 32; ++e)
       if (e >= lim) v[e] = -INFINITY;
+  } else if (kMode == kModePool) {
+    // a streaming head in the pool: row = position; rows >= n hold no token
+    const int j0 = t.k * BN + c0;
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+      const int jp = j0 + e;
+      const bool vis = jp < p.n && jp <= i_abs && (jp < S || i_abs - jp < R);
+      if (!vis) v[e] = -INFINITY;
+    }
   } else {
     const int32_t* prow = p.pos + (int64_t)it.b * (S + R);
 #pragma unroll
@@ -248,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const Item it = item_of(p, blockIdx.x);
-  const TilePlan pl = plan_of(p, it);
+  const TilePlan pl = plan_of<kMode>(p, it);
   // After any CTA of this kernel gave up a wait, later CTAs do no work, so a
   // failure ends in about one wait limit instead of one per CTA.
   const int ntiles = (*(volatile unsigned int*)err.word != 0u) ? 0 : pl.total;
@@ -294,16 +335,17 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         bool ok = true;
         // paged: the block id of the next cache tile is read one tile ahead, so its
         // latency overlaps the wait for a free stage
-        const bool paged = kMode == kModePaged && !it.streaming;
+        const bool paged = (kMode == kModePaged && !it.streaming) || kMode == kModePool;
         PagedWalk pw;
         int blk_next = 0;
         if (paged) {
-          pw.init(p, it);
-          if (ntiles > 0 && pl.n_cache > 0) blk_next = __ldg(pw.row);  // cache tile 0 is in block 0
+          pw.init<kMode>(p, it);
+          if (ntiles > 0 && pl.n_cache > 0)  // (a retrieval item's cache tile 0 is in block 0)
+            blk_next = __ldg(pw.row + (kMode == kModePool ? pw.block_index(tile_at<kMode>(pl, 0).k) : 0));
         }
         int j = 0;
         for (; j < ntiles && ok; ++j) {
-          const Tile t = tile_at(pl, j);
+          const Tile t = tile_at<kMode>(pl, j);
           // paged cache tile: pool block, first row within it, and the maps to read through
           int blk = 0, prow = 0;
           const CUtensorMap* map_k = &p.tm_kfull;
@@ -316,7 +358,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
               map_k = &p.tm_klast;
               map_v = &p.tm_vlast;
             }
-            if (j + 1 < pl.n_cache && j + 1 < ntiles) blk_next = __ldg(pw.row + pw.block_index(t.k + 1));
+            if (j + 1 < pl.n_cache && j + 1 < ntiles)
+              blk_next = __ldg(pw.row + pw.block_index(kMode == kModePool ? tile_at<kMode>(pl, j + 1).k : t.k + 1));
             if (blk < 0 || blk >= p.pg.num_blocks) {
               atomicOr(&g_prefill_err, kErrBadBlock);
               blk = p.pg.num_blocks;  // out of range: TMA reads zeros
@@ -454,7 +497,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     float l_run = 0.f;
     bool ok = true;
     for (int j = 0; j < ntiles && ok; ++j) {
-      const Tile t = tile_at(pl, j);
+      const Tile t = tile_at<kMode>(pl, j);
       const bool masked = it.streaming || (t.phase == 0 ? (int64_t)(t.k + 1) * BN > p.n : t.k >= q_last);
       if (!mbar_wait(&bars->s_full[x], (uint32_t)(j & 1), err, kErrPrefillSoftmax)) {
         ok = false;
@@ -471,7 +514,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       }
       if (masked) {
 #pragma unroll
-        for (int q4 = 0; q4 < BN / 32; ++q4) mask_chunk(v + q4 * 32, p, it, t, q4 * 32, i_abs);
+        for (int q4 = 0; q4 < BN / 32; ++q4) mask_chunk<kMode>(v + q4 * 32, p, it, t, q4 * 32, i_abs);
       }
       float mxa = v[0], mxb = v[1];
 #pragma unroll
@@ -585,6 +628,7 @@ cudaError_t launch_mode(const PrefillParams& p, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_prefill(const PrefillParams& p, cudaStream_t stream) {
+  if (p.pg.stream_table) return launch_mode<kModePool>(p, stream);
   return p.pg.table ? launch_mode<kModePaged>(p, stream) : launch_mode<kModePlain>(p, stream);
 }
 

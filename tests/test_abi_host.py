@@ -71,3 +71,22 @@ def test_null_handle_is_rejected(lib):
 def test_status_strings(lib):
     assert lib.status_string(0) == "DUO_OK"
     assert lib.status_string(3) == "DUO_ERR_CAPACITY"
+
+
+def test_paged_stream_dead_blocks_match_the_oracle(lib):
+    from oracle.ring_cache import paged_stream_dead_blocks
+    for S, R, bs in ((0, 1, 128), (4, 64, 128), (64, 256, 128), (200, 100, 256), (1, 1000, 384)):
+        for n in list(range(0, 1200, 7)) + [4096, 65536 + 3]:
+            lo, hi = lib.duo_paged_stream_dead_blocks(S, R, bs, n)
+            if n < 5000:
+                assert list(range(lo, hi)) == paged_stream_dead_blocks(n, S, R, bs), (S, R, bs, n)
+            assert lo == -(-S // bs) and hi >= lo
+
+
+@pytest.mark.parametrize("args,status", [((4, 0, 128, 10), "DUO_ERR_INVALID_ARG"),
+                                         ((-1, 4, 128, 10), "DUO_ERR_INVALID_ARG"),
+                                         ((4, 4, 100, 10), "DUO_ERR_UNSUPPORTED"),
+                                         ((4, 4, 128, -1), "DUO_ERR_INVALID_ARG")])
+def test_paged_stream_dead_blocks_rejects_bad_arguments(lib, args, status):
+    with pytest.raises(lib.DuoError, match=status):
+        lib.duo_paged_stream_dead_blocks(*args)

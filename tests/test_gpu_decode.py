@@ -47,6 +47,11 @@ CASES = [
     (1, 4, 4, 128, 2, 9, [0, 0, 0, 0], 1, 20),       # all streaming, ring fills during decode
     (1, 8, 4, 64, 8, 40, [1, 0, 0, 1], 0, 30),       # decode from an empty cache
     (4, 8, 4, 128, 16, 100, [0, 1, 0, 0], 5000, 2),  # several tiles per unit
+    # fewer retrieval tiles than CTAs (streaming units add CTAs): a unit's tiles must
+    # not be cut over CTAs with empty shares, whose parts would never arrive
+    (1, 4, 4, 128, 4, 32, [0, 0, 1, 0], 641, 2),
+    (1, 8, 4, 64, 0, 1, [0, 0, 1, 0], 200, 2),
+    (2, 16, 8, 128, 4, 32, [0, 0, 1, 0, 0, 0, 0, 1], 1000, 2),
 ]
 
 

@@ -107,3 +107,54 @@ def test_invalid_parameters():
         RingCacheSim(2, 0)
     with pytest.raises(ValueError):
         ring_slot(-1, 2, 3)
+
+
+# --------------------------------------------------- block-granular eviction (paged pool)
+def _held(n, S, R):
+    return [p for p in rc.ring_positions_after(n, S, R) if p >= 0]
+
+
+@pytest.mark.parametrize("S,R,bs", [(0, 16, 4), (2, 14, 4), (4, 32, 8), (64, 256, 128), (5, 3, 4), (130, 1, 128)])
+def test_dead_blocks_closed_form(S, R, bs):
+    # past the sink blocks, and ending at or before the window of the last token
+    for n in range(0, 6 * (S + R + bs)):
+        lo = -(-S // bs)
+        hi = max(lo, max(0, n - R) // bs)
+        assert rc.paged_stream_dead_blocks(n, S, R, bs) == list(range(lo, hi)), n
+
+
+@pytest.mark.parametrize("S,R,bs", [(0, 16, 4), (2, 14, 4), (3, 5, 4), (64, 256, 128)])
+def test_dead_blocks_never_hold_a_visible_token_and_only_grow(S, R, bs):
+    prev = set()
+    for n in range(1, 4 * (S + R + bs)):
+        dead = set(rc.paged_stream_dead_blocks(n, S, R, bs))
+        # every key the query at n - 1 or a later query can see is in a kept block
+        q = n - 1
+        for j in range(n):
+            if j < S or q - j < R:
+                assert j // bs not in dead
+        # a block dropped once stays dropped; the kept blocks are exactly those of held tokens
+        assert prev <= dead
+        prev = dead
+        kept = set(range(-(-n // bs))) - dead
+        assert kept == {p // bs for p in _held(n, S, R)}
+
+
+def test_dead_blocks_special_cases():
+    # window covering everything: nothing to drop; R = 1, no sinks: all but the last token's block
+    assert rc.paged_stream_dead_blocks(100, 0, 1000, 16) == []
+    assert rc.paged_stream_dead_blocks(100, 0, 1, 16) == list(range(6))
+    # sinks only reach into block 0: the blocks between it and the window go
+    assert rc.paged_stream_dead_blocks(100, 4, 20, 16) == [1, 2, 3, 4]
+
+
+def test_planted_window_off_by_one_fails_the_pins(monkeypatch):
+    # a window one token too short (the query's own row dropped) frees a block the last query reads
+    real = rc.ring_positions_after
+
+    def short_window(n, S, R):
+        return real(n, S, max(R - 1, 1)) if R > 1 else real(n, S, R)
+
+    monkeypatch.setattr(rc, "ring_positions_after", short_window)
+    with pytest.raises(AssertionError):
+        test_dead_blocks_never_hold_a_visible_token_and_only_grow(2, 14, 4)
