@@ -15,6 +15,9 @@ Plain, slow, float64 restatements of what the pages define:
   keys), decode over a cache, chunked prefill against a growing cache, and the
   log-sum-exp merge of partial softmaxes used by the vLLM Dual Chunk Attention
   pull request.
+* ``dca``: Dual Chunk Attention from that pull request (three query vectors chosen
+  by the chunk of the key relative to the query's, a per-position fp32 scale),
+  written as the definition and as the pull request's brute-force schedule.
 
 Every function is pinned by tests in ``tests/test_oracle_*.py`` against the
 pages' worked tables (``tests/golden/``), closed forms, brute force and an
