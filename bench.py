@@ -617,6 +617,87 @@ def run_reference(args, w, world, rank):
 
 
 # ----------------------------------------------------------------------------- main
+def bench_dca(w, steps, warmup, peaks):
+    """Dual Chunk Attention: one-shot prefill of the prompt (all heads full attention,
+    query vector chosen by the key's chunk, per-position mscale), timed per launch;
+    then the prompt's keys are appended and decode steps timed. The plain causal
+    prefill of the same shape is timed beside it to show what the three query vectors
+    cost."""
+    import torch
+
+    import duo_synth as ds
+    from streaming_kv_cache_duo_gb300 import DuoLayer, duo_device_error, workload as wl
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+    L, CL = w.prefill_len, w.dca_chunk
+    kinds = [1] * w.Hkv
+    layer = DuoLayer(w.B, w.Hq, w.Hkv, w.D, w.S, w.R, L + w.decode_steps, kinds, device=dev)
+    gen = lambda s, pos0, T, H: ds.stream_torch(w.seed, s, w.B, pos0, T, H, w.D, device=dev)
+    q, qs, qi = gen(ds.STREAM_Q, 0, L, w.Hq), gen(ds.STREAM_Q_SUCC, 0, L, w.Hq), gen(ds.STREAM_Q_INTER, 0, L, w.Hq)
+    k, v = gen(ds.STREAM_K, 0, L, w.Hkv), gen(ds.STREAM_V, 0, L, w.Hkv)
+    ms_all = torch.from_numpy(ds.dca_mscale(w.B, L + w.decode_steps, CL)).to(dev)
+    ms = ms_all[:, :L].contiguous()
+    o = torch.empty_like(q)
+    stream = torch.cuda.current_stream()
+    fr, _ = wl.prefill_flops(w.B, w.Hq, w.Hkv, w.D, w.S, w.R, kinds, L)
+
+    def timed(fn, n):
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        for a, b in ev:
+            a.record(stream)
+            fn()
+            b.record(stream)
+        torch.cuda.synchronize()
+        return sum(a.elapsed_time(b) for a, b in ev) / n
+
+    n = max(3, min(steps, 10))
+    for _ in range(warmup):
+        layer.dca_prefill(q, qs, qi, k, v, CL, mscale=ms, out=o, stream=stream)
+    torch.cuda.synchronize()
+    dca_ms = timed(lambda: layer.dca_prefill(q, qs, qi, k, v, CL, mscale=ms, out=o, stream=stream), n)
+    plain_ms = timed(lambda: layer.prefill(q, k, v, out=o, stream=stream), n)
+    # decode: the prompt's keys into the cache, then one token per step
+    layer.reset()
+    layer.append(k, v)
+    del q, qs, qi, o
+    qd, qsd, qid = (gen(s, L, w.decode_steps, w.Hq) for s in (ds.STREAM_Q, ds.STREAM_Q_SUCC, ds.STREAM_Q_INTER))
+    kd, vd = gen(ds.STREAM_K, L, w.decode_steps, w.Hkv), gen(ds.STREAM_V, L, w.decode_steps, w.Hkv)
+    od = torch.empty_like(qd[:, 0])
+    dec, plain_dec = [], []
+    for s in range(w.decode_steps):
+        layer.append(kd[:, s:s + 1].contiguous(), vd[:, s:s + 1].contiguous(), stream=stream)
+        args = [x[:, s].contiguous() for x in (qd, qsd, qid)]
+        m1 = ms_all[:, L + s].contiguous()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        layer.dca_decode(*args, CL, mscale=m1, out=od, stream=stream)
+        b.record(stream)
+        dec.append((a, b, L + s + 1))
+        c, d = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        c.record(stream)
+        layer.decode(args[0], out=od, stream=stream)  # the plain decode of the same step, for comparison
+        d.record(stream)
+        plain_dec.append((c, d))
+    torch.cuda.synchronize()
+    if duo_device_error():
+        raise RuntimeError("a kernel gave up a bounded wait")
+    warm = min(3, len(dec) - 1)
+    dt = [a.elapsed_time(b) for a, b, _ in dec][warm:]
+    pdt = [c.elapsed_time(d) for c, d in plain_dec][warm:]
+    nb = [sum(wl.decode_bytes(w.B, w.Hq, w.Hkv, w.D, w.S, w.R, kinds, nn)) for _, _, nn in dec][warm:]
+    layer.close()
+    peak = peaks["bf16_tflops"]
+    ach = fr / (dca_ms * 1e-3) / 1e12
+    return {"value": ach, "ms": dca_ms, "plain_causal_ms": plain_ms, "flops": fr, "launches": n,
+            "roofline": {"bound": "tensor", "achieved": round(ach, 2), "peak": peak, "unit": "TFLOP/s",
+                         "frac": round(ach / peak, 4), "traffic": None, "kernel": f"prefill_kernel<{w.D},dca>"},
+            "decode": {"decode_ms": round(sum(dt) / len(dt), 4),
+                       "gbs": round(sum(nb) / (sum(dt) * 1e-3) / 1e9, 1),
+                       "frac_of_hbm": round(sum(nb) / (sum(dt) * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+                       "kernel": f"decode_kernel<{w.D},{w.Hq // w.Hkv},dca>", "steps_timed": len(dt),
+                       "plain_decode_ms": round(sum(pdt) / len(pdt), 4)}}
+
+
 def other_workload(args, w, world, rank, peaks):
     """JSON line for the workloads other than the one-shot prefill: decode (GB/s) or
     chunked prefill (TFLOP/s)."""
@@ -629,7 +710,14 @@ def other_workload(args, w, world, rank, peaks):
     if args.paged:
         base["config"]["paged_block"] = args.paged
         base["config"]["streaming_heads"] = "paged pool" if args.pool else "sink + ring cache"
-    if w.chunk:
+    if w.dca_chunk:
+        r = bench_dca(w, args.steps, args.warmup, peaks)
+        base["config"].update(seq_len=w.prefill_len, dca_chunk_len=w.dca_chunk, decode_steps=w.decode_steps,
+                              step="one Dual Chunk Attention prefill launch of the prompt (all heads)")
+        line = dict(base, value=round(r["value"] * world, 2), unit="TFLOP/s", ms_per_step=round(r["ms"], 4),
+                    roofline=r["roofline"], gpu_launches=r["launches"],
+                    plain_causal_prefill_ms=round(r["plain_causal_ms"], 4), decode=r["decode"])
+    elif w.chunk:
         r = bench_chunked(w, args.steps, args.warmup, peaks, args.paged, args.pool)
         base["config"].update(seq_len=w.prefill_len, chunk=w.chunk,
                               step="8 x (prefill of a 4096-token chunk against the cache, append)")
@@ -671,7 +759,7 @@ def main():
     w = ds.WORKLOADS[args.workload]
     rank, world, local = dist_setup()
     if args.impl == "reference":
-        if w.prefill_len == 0 or w.chunk:
+        if w.prefill_len == 0 or w.chunk or w.dca_chunk:
             if rank == 0:
                 print(json.dumps({"impl": "reference", "unavailable": "the oracle arm times the one-shot "
                                   "prefill workloads only"}))
@@ -682,7 +770,7 @@ def main():
     import __graft_entry__
     __graft_entry__.build()
     peaks, peak_src = load_peaks()
-    if w.prefill_len == 0 or w.chunk:
+    if w.prefill_len == 0 or w.chunk or w.dca_chunk:
         other_workload(args, w, world, rank, peaks)
         return
     res = bench_prefill(w, args.steps, args.warmup, world, peaks, not args.no_e2e)

@@ -38,6 +38,8 @@ import numpy as np
 STREAM_Q = 0
 STREAM_K = 1
 STREAM_V = 2
+STREAM_Q_SUCC = 3   # Dual Chunk Attention: query vectors for the previous chunk
+STREAM_Q_INTER = 4  # and for earlier chunks
 STREAM_HEADS = 15  # the seeded head permutation
 
 _GAMMA = np.uint64(0x9E3779B97F4A7C15)
@@ -215,6 +217,7 @@ class Workload:
     context: int = 0              # tokens appended without attention before decoding
     decode_steps: int = 0
     fixed_retrieval: tuple = field(default=None)
+    dca_chunk: int = 0            # Dual Chunk Attention chunk length (0 = not DCA)
 
     @property
     def is_retrieval(self) -> list:
@@ -236,4 +239,17 @@ WORKLOADS = {
                                              prefill_len=32768, chunk=4096),
     "decode_ctx1m": Workload("decode_ctx1m", 5, 1, 32, 8, 128, 64, 256, 2,
                              context=1 << 20, decode_steps=64),
+    # Dual Chunk Attention (Qwen2-72B-shaped layer: 64 query / 8 KV heads, all full
+    # attention), 131072-token prompt in chunks of 32768, then decode steps
+    "qwen2_72b_dca_prefill128k": Workload("qwen2_72b_dca_prefill128k", 6, 1, 64, 8, 128, 0, 1, 8,
+                                          prefill_len=131072, decode_steps=16, dca_chunk=32768),
 }
+
+
+def dca_mscale(B: int, T: int, chunk_len: int, pos0: int = 0) -> np.ndarray:
+    """A smooth per-position fp32 scale for Dual Chunk Attention inputs (an input of
+    the method, not part of it): 1 + 0.1 ln(1 + position / chunk_len), the same row
+    for every sequence, float32 [B, T]."""
+    pos = np.arange(pos0, pos0 + T, dtype=np.float64)
+    row = (1.0 + 0.1 * np.log1p(pos / chunk_len)).astype(np.float32)
+    return np.broadcast_to(row, (B, T)).copy()

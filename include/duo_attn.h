@@ -219,6 +219,35 @@ duo_status duo_attn_prefill_paged(duo_handle* handle, const duo_kv_cache* cache,
 duo_status duo_attn_decode_paged(duo_handle* handle, const duo_kv_cache* cache, const duo_paged* paged,
                                  const void* q, void* o, void* workspace, size_t workspace_bytes, void* stream);
 
+/* Dual Chunk Attention (vLLM pull request "[Model] Implement DualChunkAttention for
+ * Qwen2 Models"): the sequence is cut into chunks of chunk_len positions from the start
+ * (the last one may be shorter) and every position carries three query vectors made by
+ * the rotary layer. Query i attends causally to every key j <= i with
+ *     weight = (q_x(i) . k_j) * softmax_scale * mscale[i],   softmax_scale = 1/sqrt(D),
+ * where q_x is q when j lies in i's chunk, q_succ when j lies in the chunk just before,
+ * and q_inter for any earlier chunk; mscale is an fp32 per-position factor applied to
+ * the fp32 product (NULL: 1). The pull request asks for this as one fused kernel in
+ * place of three attention calls per chunk merged by log-sum-exp.
+ *
+ * Both entry points treat every head as full attention: the handle must have no
+ * streaming head (DUO_ERR_UNSUPPORTED otherwise). chunk_len must be a positive multiple
+ * of 256 (DUO_ERR_UNSUPPORTED otherwise) so that chunk boundaries fall on the
+ * kernels' 256-row query blocks and 128-key tiles.
+ *
+ * duo_dca_prefill: one-shot prefill of T tokens at positions 0 ... T-1 (no cache).
+ * q, q_succ, q_inter: bf16 [B, T, Hq, D]; k, v: bf16 [B, T, Hkv, D]; mscale: fp32
+ * [B, T] device memory or NULL; o: bf16 [B, T, Hq, D]; all device, 16-byte aligned.
+ * Append k and v with duo_kv_append to decode afterwards. */
+duo_status duo_dca_prefill(duo_handle* handle, const void* q, const void* q_succ, const void* q_inter, const void* k,
+                           const void* v, const float* mscale, int32_t T, int32_t chunk_len, void* o, void* stream);
+
+/* duo_dca_decode: one decode step at position cache->n - 1 (the token appended first)
+ * over the retrieval caches. q, q_succ, q_inter: bf16 [B, Hq, D]; mscale: fp32 [B] or
+ * NULL; o: bf16 [B, Hq, D]; workspace as for duo_attn_decode. */
+duo_status duo_dca_decode(duo_handle* handle, const duo_kv_cache* cache, const void* q, const void* q_succ,
+                          const void* q_inter, const float* mscale, int32_t chunk_len, void* o, void* workspace,
+                          size_t workspace_bytes, void* stream);
+
 /* Per-sequence lengths on the device: serving batches
  * hold sequences of different lengths, and a decode step whose lengths live in device
  * memory can be captured once in a CUDA graph and replayed step after step. The

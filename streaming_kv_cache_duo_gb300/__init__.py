@@ -85,6 +85,34 @@ class DuoLayer:
         duo_attn_decode(self.handle, self.cache, q, out, self.workspace, stream)
         return out
 
+    def dca_prefill(self, q, q_succ, q_inter, k, v, chunk_len, mscale=None, out=None, stream=None):
+        """Dual Chunk Attention prefill of T tokens at positions 0 ... T-1 (every head full
+        attention); mscale: fp32 [B, T] on the device or None."""
+        import torch
+        T = q.shape[1]
+        for name, t in (("q", q), ("q_succ", q_succ), ("q_inter", q_inter)):
+            _lib._bf16(t, (self.B, T, self.Hq, self.D), name)
+        _lib._bf16(k, (self.B, T, self.Hkv, self.D), "k")
+        _lib._bf16(v, (self.B, T, self.Hkv, self.D), "v")
+        _check_mscale(mscale, (self.B, T))
+        if out is None:
+            out = torch.empty_like(q)
+        _lib._bf16(out, (self.B, T, self.Hq, self.D), "o")
+        _lib.duo_dca_prefill(self.handle, q, q_succ, q_inter, k, v, mscale, T, chunk_len, out, stream)
+        return out
+
+    def dca_decode(self, q, q_succ, q_inter, chunk_len, mscale=None, out=None, stream=None):
+        """Dual Chunk Attention decode of the token at position n - 1; mscale fp32 [B] or None."""
+        import torch
+        for name, t in (("q", q), ("q_succ", q_succ), ("q_inter", q_inter)):
+            _lib._bf16(t, (self.B, self.Hq, self.D), name)
+        _check_mscale(mscale, (self.B,))
+        if out is None:
+            out = torch.empty_like(q)
+        _lib._bf16(out, (self.B, self.Hq, self.D), "o")
+        _lib.duo_dca_decode(self.handle, self.cache, q, q_succ, q_inter, mscale, chunk_len, out, self.workspace, stream)
+        return out
+
     def append_varlen(self, k_new, v_new, seq_lens, stream=None) -> None:
         """One token per sequence at positions seq_lens (device int32 [B]), which advance by one."""
         _lib._bf16(k_new, (self.B, 1, self.Hkv, self.D), "k_new")
@@ -170,6 +198,15 @@ class DuoPagedLayer(DuoLayer):
             out = torch.empty_like(q)
         _lib.duo_attn_decode_paged(self.handle, self.cache, self.paged, q, out, self.workspace, stream)
         return out
+
+
+def _check_mscale(mscale, shape):
+    import torch
+    if mscale is None:
+        return
+    if (mscale.dtype != torch.float32 or not mscale.is_cuda or not mscale.is_contiguous()
+            or tuple(mscale.shape) != tuple(shape)):
+        raise ValueError(f"mscale: need a contiguous CUDA float32 tensor of shape {tuple(shape)}")
 
 
 def _check_lens(seq_lens, B):

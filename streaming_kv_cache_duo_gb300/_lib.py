@@ -31,7 +31,7 @@ EXPORTS = (
     "duo_classify_heads", "duo_create", "duo_destroy", "duo_cache_reset", "duo_kv_append",
     "duo_attn_prefill", "duo_attn_prefill_select", "duo_decode_workspace_size", "duo_attn_decode",
     "duo_attn_decode_static", "duo_kv_append_paged", "duo_attn_prefill_paged", "duo_attn_decode_paged",
-    "duo_paged_stream_dead_blocks",
+    "duo_paged_stream_dead_blocks", "duo_dca_prefill", "duo_dca_decode",
     "duo_kv_append_varlen", "duo_attn_decode_varlen", "duo_device_error", "duo_selftest_bounded_wait",
     "duo_last_error", "duo_status_string",
 )
@@ -93,6 +93,10 @@ def library() -> ctypes.CDLL:
                                             c_void_p, c_void_p, c_size_t, c_void_p]),
         "duo_paged_stream_dead_blocks": (c_int32, [c_int32, c_int32, c_int32, c_int64, POINTER(c_int64),
                                                    POINTER(c_int64)]),
+        "duo_dca_prefill": (c_int32, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int32,
+                                      c_int32, c_void_p, c_void_p]),
+        "duo_dca_decode": (c_int32, [c_void_p, POINTER(duo_kv_cache), c_void_p, c_void_p, c_void_p, c_void_p,
+                                     c_int32, c_void_p, c_void_p, c_size_t, c_void_p]),
         "duo_kv_append_varlen": (c_int32, [c_void_p, POINTER(duo_kv_cache), c_void_p, c_void_p, c_void_p,
                                            c_void_p]),
         "duo_attn_decode_varlen": (c_int32, [c_void_p, POINTER(duo_kv_cache), c_void_p, c_int64, c_void_p, c_void_p,
@@ -214,6 +218,18 @@ def duo_attn_decode_paged(handle, cache: "duo_kv_cache", paged: "duo_paged", q, 
     nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(library().duo_attn_decode_paged(handle, ctypes.byref(cache), ctypes.byref(paged), _ptr(q), _ptr(o),
                                            _ptr(workspace), nbytes, _stream_ptr(stream)))
+
+
+def duo_dca_prefill(handle, q, q_succ, q_inter, k, v, mscale, T: int, chunk_len: int, o, stream=None) -> None:
+    _check(library().duo_dca_prefill(handle, _ptr(q), _ptr(q_succ), _ptr(q_inter), _ptr(k), _ptr(v), _ptr(mscale), T,
+                                     chunk_len, _ptr(o), _stream_ptr(stream)))
+
+
+def duo_dca_decode(handle, cache: "duo_kv_cache", q, q_succ, q_inter, mscale, chunk_len: int, o, workspace,
+                   stream=None) -> None:
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(library().duo_dca_decode(handle, ctypes.byref(cache), _ptr(q), _ptr(q_succ), _ptr(q_inter), _ptr(mscale),
+                                    chunk_len, _ptr(o), _ptr(workspace), nbytes, _stream_ptr(stream)))
 
 
 def duo_paged_stream_dead_blocks(sink_size: int, recent_size: int, block_size: int, n: int) -> tuple:

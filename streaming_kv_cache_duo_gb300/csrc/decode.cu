@@ -57,6 +57,10 @@ constexpr int ilog2(int v) { return v <= 1 ? 0 : 1 + ilog2(v / 2); }
 constexpr int kModePlain = 0;  // contiguous retrieval caches, ring caches for streaming heads
 constexpr int kModePaged = 1;  // retrieval caches in a paged pool (block table), ring caches
 constexpr int kModePool = 2;   // both head kinds in the paged pool
+constexpr int kModeDca = 3;    // Dual Chunk Attention: the query vector depends on the key's chunk
+
+// retrieval caches (and maybe streaming ones) in the paged pool
+__host__ __device__ constexpr bool is_paged_mode(int mode) { return mode == kModePaged || mode == kModePool; }
 
 template <int D, int G>
 struct Cfg {
@@ -184,14 +188,14 @@ __device__ __forceinline__ int64_t stream_tile(const DecodeParams& p, int64_t lt
 }
 
 // The tile this warp refills next, walked forward one tile at a time. With a paged
-// pool (kMode != kModePlain) the cursor also tracks the pool block of its tile: the eight warp
+// pool (kModePaged, kModePool) the cursor also tracks the pool block of its tile: the eight warp
 // slices of a tile lie in one block (block sizes are multiples of kTK), so for a
 // retrieval unit the block table is read only when the cursor enters a new block, one
 // tile before the copy is issued, and a division is needed only where a segment
 // starts. The few tiles of a streaming unit in the pool are located one by one.
 template <int kMode>
 struct Cursor {
-  static constexpr bool kPaged = kMode != kModePlain;
+  static constexpr bool kPaged = is_paged_mode(kMode);
   SegState st;
   int u;
   int64_t lt, lt1;
@@ -253,7 +257,7 @@ template <int D, int G, int kMode>
 __device__ __forceinline__ bool issue_slice(const DecodeParams& p, const Cursor<kMode>& cur, int w,
                                             uint8_t* stage, uint64_t* bar) {
   using C = Cfg<D, G>;
-  const bool pool = kMode != kModePlain && cur.in_pool();
+  const bool pool = is_paged_mode(kMode) && cur.in_pool();
   int rows = warp_rows(cur.x.keys, kMode == kModePool ? cur.row_tile() : cur.lt, w);
   const uint16_t* kp;
   const uint16_t* vp;
@@ -325,7 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
   __syncthreads();
 
   // refill cursor (warp-uniform); the prologue issues the first kNSW - 1 slices
-  constexpr bool kPaged = kMode != kModePlain;
+  constexpr bool kPaged = is_paged_mode(kMode);
   Cursor<kMode> cur;
   cur.init(p, c, t0, t1, live);
   int64_t issued = 0;
@@ -354,19 +358,41 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
 
     // q of head (hme ^ l) in slot l, this lane's dims, pre-scaled, as fp32 pairs
     float2 q2[G][C::DPL / 2];
+    auto load_q = [&](const uint16_t* qsrc, float factor) {
 #pragma unroll
-    for (int l = 0; l < G; ++l) {
-      const uint16_t* qh = p.q + ((int64_t)x.b * p.sh.Hq + (int64_t)x.kvh * G + (hme ^ l)) * D;
+      for (int l = 0; l < G; ++l) {
+        const uint16_t* qh = qsrc + ((int64_t)x.b * p.sh.Hq + (int64_t)x.kvh * G + (hme ^ l)) * D;
 #pragma unroll
-      for (int ch = 0; ch < C::CH; ++ch) {
-        const uint4 v = __ldg(reinterpret_cast<const uint4*>(qh + (cl + ch * C::LPK) * 8));
-        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+        for (int ch = 0; ch < C::CH; ++ch) {
+          const uint4 v = __ldg(reinterpret_cast<const uint4*>(qh + (cl + ch * C::LPK) * 8));
+          const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float2 f = unpack2(w4[e]);
-          q2[l][ch * 4 + e] = make_float2(f.x * p.scale_log2, f.y * p.scale_log2);
+          for (int e = 0; e < 4; ++e) {
+            const float2 f = unpack2(w4[e]);
+            q2[l][ch * 4 + e] = make_float2(f.x * factor, f.y * factor);
+          }
         }
       }
+    };
+    // DCA: which query vectors the keys of tile lt take (0 query, 1 query_succ for the
+    // chunk before the query's, 2 query_inter further back; chunk_len is a multiple of
+    // the tile), and the factor: softmax scale times the sequence's fp32 mscale, on fp32 q
+    float qfactor = p.scale_log2;
+    int qv = 0;
+    int64_t t_intra = 0, t_succ = 0;  // first tile of the query's chunk and of the one before
+    if (kMode == kModeDca) {
+      const int64_t tpc = p.chunk_len / kTK;
+      t_intra = (x.pq / p.chunk_len) * tpc;
+      t_succ = t_intra - tpc;
+    }
+    auto dca_var = [&](int64_t lt) { return lt >= t_intra ? 0 : (lt >= t_succ ? 1 : 2); };
+    auto dca_q = [&](int v) { return v == 0 ? p.q : (v == 1 ? p.q_succ : p.q_inter); };
+    if (kMode == kModeDca) {
+      if (p.mscale) qfactor *= __ldg(p.mscale + x.b);
+      qv = dca_var(lt_begin);
+      load_q(dca_q(qv), qfactor);
+    } else {
+      load_q(p.q, qfactor);
     }
     float2 o2[G][C::DPL / 2];
 #pragma unroll
@@ -377,6 +403,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
 
     for (int64_t lt = lt_begin; lt < lt_end; ++lt, ++j) {
       const int s = (int)(j % kNSW);
+      if (kMode == kModeDca) {
+        const int v = dca_var(lt);
+        if (v != qv) {  // at most twice per unit
+          qv = v;
+          load_q(dca_q(v), qfactor);
+        }
+      }
       // refill: the stage used by tile j - 1 is free now (this warp finished it)
       if (cur.live) {
         const int sn = (int)((j + kNSW - 1) % kNSW);
@@ -687,6 +720,7 @@ cudaError_t launch_v(const DecodeParams& p, cudaStream_t stream) {
 // bookkeeping costs the contiguous kernel nothing
 template <int D, int G>
 cudaError_t launch_t(const DecodeParams& p, cudaStream_t stream) {
+  if (p.chunk_len > 0) return launch_v<D, G, kModeDca>(p, stream);
   if (p.pg.stream_table) return launch_v<D, G, kModePool>(p, stream);
   return p.pg.table ? launch_v<D, G, kModePaged>(p, stream) : launch_v<D, G, kModePlain>(p, stream);
 }

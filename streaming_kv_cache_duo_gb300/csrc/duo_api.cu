@@ -430,6 +430,9 @@ static void decode_plan(const duo_handle* h, int64_t n, DecodeParams* p) {
   p->seq_lens = nullptr;  // uniform length n unless a caller sets device lengths
   p->pg = PagedLayout{nullptr, 0, 0, 0, nullptr};  // contiguous retrieval caches unless paged
   p->s_sink_tiles = p->s_win_lo = 0;
+  p->q_succ = p->q_inter = nullptr;  // not Dual Chunk Attention unless a caller sets chunk_len
+  p->mscale = nullptr;
+  p->chunk_len = 0;
   const int64_t SR = (int64_t)sh.S + sh.R;
   p->n = n;
   p->nvalid = (int)(n < SR ? n : SR);
@@ -452,10 +455,35 @@ size_t duo_decode_workspace_size(const duo_handle* h, int64_t n) {
   return decode_workspace_bytes(h->sh, h->num_sms);
 }
 
+// Dual Chunk Attention arguments of a decode step (nullptr: plain decode).
+struct DcaDecode {
+  const void* q_succ;
+  const void* q_inter;
+  const float* mscale;
+  int32_t chunk_len;
+};
+
+// DCA entry points treat every head as full attention, and need chunk boundaries that
+// fall on 256-row blocks / 128-key tiles.
+static duo_status check_dca(const duo_handle* h, int32_t chunk_len, const float* mscale) {
+  if (h->sh.n_str > 0)
+    return fail(DUO_ERR_UNSUPPORTED, "Dual Chunk Attention needs every head to be a retrieval (full) head");
+  if (chunk_len < kPrefillRowsPerCta || chunk_len % kPrefillRowsPerCta != 0)
+    return fail(DUO_ERR_UNSUPPORTED, "chunk_len = %d is not a positive multiple of %d", chunk_len,
+                kPrefillRowsPerCta);
+  if (reinterpret_cast<uintptr_t>(mscale) & 3u) return fail(DUO_ERR_INVALID_ARG, "mscale not 4-byte aligned");
+  return DUO_OK;
+}
+
 static duo_status decode_impl(duo_handle* h, const duo_kv_cache* c, const duo_paged* pgd, const void* q, void* o,
-                              void* workspace, size_t ws_bytes, void* stream) {
+                              void* workspace, size_t ws_bytes, void* stream, const DcaDecode* dca = nullptr) {
   duo_status st = check_handle(h);
   if (st != DUO_OK) return st;
+  if (dca) {
+    if ((st = check_dca(h, dca->chunk_len, dca->mscale)) != DUO_OK) return st;
+    if (!dca->q_succ || !dca->q_inter || !aligned16(dca->q_succ) || !aligned16(dca->q_inter))
+      return fail(DUO_ERR_INVALID_ARG, "q_succ / q_inter NULL or not 16-byte aligned");
+  }
   PagedLayout pg;
   if ((st = check_paged(h, pgd, &pg)) != DUO_OK) return st;
   if ((st = check_cache(h, c, true, !pg.stream_table)) != DUO_OK) return st;
@@ -494,6 +522,12 @@ static duo_status decode_impl(duo_handle* h, const duo_kv_cache* c, const duo_pa
   p.sh = sh;
   p.heads = h->heads;
   p.pg = pg;
+  if (dca) {
+    p.q_succ = static_cast<const uint16_t*>(dca->q_succ);
+    p.q_inter = static_cast<const uint16_t*>(dca->q_inter);
+    p.mscale = dca->mscale;
+    p.chunk_len = dca->chunk_len;
+  }
   if (pg.stream_table) {
     // streaming units read rows (= positions) of the pool: the sink tiles, then the
     // tiles of the window [max(S, n - R), n) not already among them
@@ -535,6 +569,48 @@ duo_status duo_paged_stream_dead_blocks(int32_t sink_size, int32_t recent_size, 
     return fail(DUO_ERR_UNSUPPORTED, "block_size = %d is not a positive multiple of 128", block_size);
   stream_dead_blocks(sink_size, recent_size, block_size, n, lo, hi);
   return ok();
+}
+
+duo_status duo_dca_prefill(duo_handle* h, const void* q, const void* q_succ, const void* q_inter, const void* k,
+                           const void* v, const float* mscale, int32_t T, int32_t chunk_len, void* o, void* stream) {
+  duo_status st = check_handle(h);
+  if (st != DUO_OK) return st;
+  if ((st = check_dca(h, chunk_len, mscale)) != DUO_OK) return st;
+  if (T < 1) return fail(DUO_ERR_INVALID_ARG, "T = %d < 1", T);
+  const void* ptrs[] = {q, q_succ, q_inter, k, v, o};
+  for (const void* ptr : ptrs)
+    if (!ptr || !aligned16(ptr)) return fail(DUO_ERR_INVALID_ARG, "q / q_succ / q_inter / k / v / o NULL or not 16-byte aligned");
+  const Shape& sh = h->sh;
+  PrefillParams p;
+  memset(&p, 0, sizeof(p));
+  if ((st = encode_tokens(h, &p.tm_q, q, sh.B, T, sh.Hq, sh.D)) != DUO_OK) return st;
+  if ((st = encode_tokens(h, &p.tm_qs, q_succ, sh.B, T, sh.Hq, sh.D)) != DUO_OK) return st;
+  if ((st = encode_tokens(h, &p.tm_qi, q_inter, sh.B, T, sh.Hq, sh.D)) != DUO_OK) return st;
+  if ((st = encode_tokens(h, &p.tm_k, k, sh.B, T, sh.Hkv, sh.D)) != DUO_OK) return st;
+  if ((st = encode_tokens(h, &p.tm_v, v, sh.B, T, sh.Hkv, sh.D)) != DUO_OK) return st;
+  p.o = static_cast<uint16_t*>(o);
+  p.n = 0;
+  p.T = T;
+  p.num_qt = (T + kPrefillRowsPerCta - 1) / kPrefillRowsPerCta;
+  const int64_t items = (int64_t)sh.B * sh.g * p.num_qt * sh.n_ret;
+  if (items > 0x7fffffffLL) return fail(DUO_ERR_UNSUPPORTED, "too many query tiles for one launch");
+  p.items_r = (int)items;
+  p.items_s = 0;
+  p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)sh.D));
+  p.sh = sh;
+  p.heads = h->heads;
+  p.mscale = mscale;
+  p.chunk_len = chunk_len;
+  cudaError_t ce = launch_prefill(p, (cudaStream_t)stream);
+  if (ce != cudaSuccess) return cuda_fail(ce, "DCA prefill launch");
+  return ok();
+}
+
+duo_status duo_dca_decode(duo_handle* h, const duo_kv_cache* c, const void* q, const void* q_succ,
+                          const void* q_inter, const float* mscale, int32_t chunk_len, void* o, void* workspace,
+                          size_t workspace_bytes, void* stream) {
+  const DcaDecode dca{q_succ, q_inter, mscale, chunk_len};
+  return decode_impl(h, c, nullptr, q, o, workspace, workspace_bytes, stream, &dca);
 }
 
 duo_status duo_kv_append_varlen(duo_handle* h, duo_kv_cache* c, int32_t* seq_lens, const void* k_new,

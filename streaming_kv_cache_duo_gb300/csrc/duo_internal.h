@@ -121,6 +121,12 @@ struct DecodeParams {
   Shape sh;
   HeadTable heads;
   PagedLayout pg;
+  // Dual Chunk Attention (chunk_len > 0; every head full attention): the query vectors
+  // for keys one chunk back and further back, and a per-sequence scale
+  const uint16_t* q_succ;  // bf16 [B, Hq, D]
+  const uint16_t* q_inter;
+  const float* mscale;     // fp32 [B] or nullptr (1)
+  int chunk_len;           // 0: not DCA; else a multiple of 256
 };
 size_t decode_workspace_bytes(const Shape& sh, int num_ctas);
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream);
@@ -152,6 +158,12 @@ struct PrefillParams {
   Shape sh;
   HeadTable heads;
   PagedLayout pg;
+  // Dual Chunk Attention (chunk_len > 0; every head full attention, no cache): the
+  // query vectors for keys one chunk back and further back, and a per-position scale
+  CUtensorMap tm_qs;     // 4-D over q_succ [B, T, Hq, D], as tm_q
+  CUtensorMap tm_qi;     // 4-D over q_inter [B, T, Hq, D]
+  const float* mscale;   // fp32 [B, T] or nullptr (1)
+  int chunk_len;         // 0: not DCA; else a multiple of 256
 };
 cudaError_t launch_prefill(const PrefillParams& p, cudaStream_t stream);
 

@@ -63,6 +63,7 @@ constexpr uint32_t kTmemCols = 512;
 constexpr int kModePlain = 0;  // contiguous retrieval caches, ring caches for streaming heads
 constexpr int kModePaged = 1;  // retrieval caches in a paged pool (block table), ring caches
 constexpr int kModePool = 2;   // both head kinds in the paged pool
+constexpr int kModeDca = 3;    // Dual Chunk Attention: one of three query vectors per key tile
 constexpr int kBox = 128 * 128;  // bytes of a 128-row x 64-column bf16 box
 
 __host__ __device__ constexpr uint32_t col_s(int x) { return (uint32_t)x * 256u; }
@@ -87,6 +88,7 @@ struct Bars {
   uint64_t s_full[kQT], p_full[kQT], o_final[kQT];
   uint64_t drain;
   uint32_t tmem_base;
+  uint64_t q_free;  // DCA: the MMAs reading the current query vectors have completed
 };
 
 struct Item {
@@ -220,6 +222,25 @@ struct PagedWalk {
   __device__ __forceinline__ int block_index(int k) const { return (int)((unsigned)k / (unsigned)tpb); }
 };
 
+// Dual Chunk Attention: which query vectors (0 query, 1 query_succ, 2 query_inter)
+// the 256 query rows of a block use against key tile kt. chunk_len is a multiple of
+// 256, so both lie in one chunk each; the block's chunk gives two tile thresholds,
+// worked out once per CTA.
+struct DcaTiles {
+  int t_intra;  // first key tile of the query block's chunk
+  int t_succ;   // first key tile of the chunk before it
+  __device__ __forceinline__ void init(const PrefillParams& p, int qp) {
+    const int tpc = p.chunk_len / BN;
+    t_intra = (qp * kRows / p.chunk_len) * tpc;
+    t_succ = t_intra - tpc;
+  }
+  __device__ __forceinline__ int var(int kt) const { return kt >= t_intra ? 0 : (kt >= t_succ ? 1 : 2); }
+};
+
+__device__ __forceinline__ const CUtensorMap* dca_map(const PrefillParams& p, int v) {
+  return v == 0 ? &p.tm_q : (v == 1 ? &p.tm_qs : &p.tm_qi);
+}
+
 __device__ __forceinline__ float max3(float a, float b, float c) {
   float r;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
@@ -308,6 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       mbar_init(&bars->o_final[x], 1);
     }
     mbar_init(&bars->drain, 1);
+    if (kMode == kModeDca) mbar_init(&bars->q_free, 1);
     fence_mbarrier_init();
   }
   if (warp == kWarpMma) {
@@ -324,13 +346,23 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     if (warp == kWarpTma) {
       // ------------------------------------------------------------ TMA producer
       if (lane == 0) {
-        prefetch_tmap(&p.tm_q);
+        // DCA: the query vectors of the first key tile; switched when a tile of
+        // another chunk relation comes (at most twice per CTA)
+        int qvar = 0, q_loads = 1;
+        const CUtensorMap* qmap = &p.tm_q;
+        DcaTiles dt;
+        if (kMode == kModeDca) {
+          dt.init(p, it.qp);
+          qvar = ntiles > 0 ? dt.var(tile_at<kMode>(pl, 0).k) : 0;
+          qmap = dca_map(p, qvar);
+        }
+        prefetch_tmap(qmap);
         mbar_arrive_expect_tx(&bars->q_full, kQT * C::Q_BYTES);
   #pragma unroll
         for (int x = 0; x < kQT; ++x)
   #pragma unroll
           for (int bx = 0; bx < C::NBOX; ++bx)
-            tma_load_4d(sQ + x * C::Q_BYTES + bx * kBox, &p.tm_q, bx * 64, it.hq, it.qp * kRows + x * BM, it.b,
+            tma_load_4d(sQ + x * C::Q_BYTES + bx * kBox, qmap, bx * 64, it.hq, it.qp * kRows + x * BM, it.b,
                         &bars->q_full);
         bool ok = true;
         // paged: the block id of the next cache tile is read one tile ahead, so its
@@ -346,6 +378,26 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         int j = 0;
         for (; j < ntiles && ok; ++j) {
           const Tile t = tile_at<kMode>(pl, j);
+          if (kMode == kModeDca) {
+            const int v = dt.var(t.k);
+            if (v != qvar) {
+              // the S MMAs that read the previous query vectors have completed
+              if (!mbar_wait(&bars->q_free, (uint32_t)((q_loads - 1) & 1), err, kErrPrefillProducer)) {
+                ok = false;
+                break;
+              }
+              qvar = v;
+              const CUtensorMap* m = dca_map(p, v);
+              mbar_arrive_expect_tx(&bars->q_full, kQT * C::Q_BYTES);
+  #pragma unroll
+              for (int x = 0; x < kQT; ++x)
+  #pragma unroll
+                for (int bx = 0; bx < C::NBOX; ++bx)
+                  tma_load_4d(sQ + x * C::Q_BYTES + bx * kBox, m, bx * 64, it.hq, it.qp * kRows + x * BM, it.b,
+                              &bars->q_full);
+              ++q_loads;
+            }
+          }
           // paged cache tile: pool block, first row within it, and the maps to read through
           int blk = 0, prow = 0;
           const CUtensorMap* map_k = &p.tm_kfull;
@@ -405,7 +457,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         }
         if (!ok) {
           // after an early exit, let the copies already issued land before the CTA ends
-          mbar_wait(&bars->q_full, 0, err, kErrPrefillProducer);
+          mbar_wait(&bars->q_full, kMode == kModeDca ? (uint32_t)((q_loads - 1) & 1) : 0u, err, kErrPrefillProducer);
           for (int jj = (j > kNS ? j - kNS : 0); jj < j; ++jj) {
             mbar_wait(&bars->k_full[jj % kNS], (uint32_t)((jj / kNS) & 1), err, kErrPrefillProducer);
             mbar_wait(&bars->v_full[jj % kNS], (uint32_t)((jj / kNS) & 1), err, kErrPrefillProducer);
@@ -451,9 +503,28 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             tc_commit(&bars->k_empty[0]);
           }
         }
+        // DCA: query vectors in shared memory, and the q_full phase of their last load
+        DcaTiles dt;
+        int qv = 0;
+        if (kMode == kModeDca) {
+          dt.init(p, it.qp);
+          qv = ntiles > 0 ? dt.var(tile_at<kMode>(pl, 0).k) : 0;
+        }
+        uint32_t qph = 0;
         for (int j = 0; j < ntiles && ok; ++j) {
           const int s = j % kNS;
           const bool more = j + 1 < ntiles;
+          bool qswitch = false;
+          if (kMode == kModeDca && more) {
+            const int v = dt.var(tile_at<kMode>(pl, j + 1).k);
+            if (v != qv) {
+              // S_0(j) and S_1(j), issued before this commit, were the last reads of
+              // the current vectors; the producer reloads the buffer once they finish
+              qv = v;
+              qswitch = true;
+              tc_commit(&bars->q_free);
+            }
+          }
           if (!mbar_wait(&bars->v_full[s], (uint32_t)((j / kNS) & 1), err, kErrPrefillMma)) {
             ok = false;
             break;
@@ -470,7 +541,17 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             tc_fence_after();
             issue_pv(x, j);
             if (!more) tc_commit(&bars->o_final[x]);
-            if (more) issue_s(x, j + 1);
+            if (more) {
+              if (kMode == kModeDca && qswitch && x == 0) {
+                qph ^= 1u;
+                if (!mbar_wait(&bars->q_full, qph, err, kErrPrefillMma)) {
+                  ok = false;
+                  break;
+                }
+                tc_fence_after();
+              }
+              issue_s(x, j + 1);
+            }
           }
           if (!ok) break;
           tc_commit(&bars->v_empty[s]);
@@ -491,7 +572,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     const uint32_t obase = lane_base + col_o(x);
     const int row_local = it.qp * kRows + x * BM + r;  // chunk-local query row
     const int i_abs = (int)p.n + row_local;            // absolute position (< 2^31, checked on the host)
-    const float sl2 = p.scale_log2;
+    // DCA: the fp32 per-position scale joins softmax_scale on the fp32 product
+    const float sl2 = (kMode == kModeDca && p.mscale && row_local < p.T)
+                          ? p.scale_log2 * __ldg(p.mscale + (int64_t)it.b * p.T + row_local)
+                          : p.scale_log2;
     const int q_last = x == 0 ? it.qp * kQT : it.qp * kQT + 1;  // diagonal tile of this query tile
     float m_run = -INFINITY;  // running max of scaled scores (log2 units)
     float l_run = 0.f;
@@ -628,6 +712,7 @@ cudaError_t launch_mode(const PrefillParams& p, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_prefill(const PrefillParams& p, cudaStream_t stream) {
+  if (p.chunk_len > 0) return launch_mode<kModeDca>(p, stream);
   if (p.pg.stream_table) return launch_mode<kModePool>(p, stream);
   return p.pg.table ? launch_mode<kModePaged>(p, stream) : launch_mode<kModePlain>(p, stream);
 }

@@ -1,0 +1,108 @@
+"""Dual Chunk Attention on the GPU (duo_dca_prefill, duo_dca_decode) against the float64
+oracle (oracle.dca, pinned against the pull request's brute-force schedule), on sampled
+query rows of every head: the first and last rows of each chunk, their neighbours, the
+ragged tail, and random rows. With q_succ = q_inter = q and no mscale the method is
+plain causal attention, and the DCA kernel must then give exactly the plain kernel's
+bits."""
+
+import numpy as np
+import pytest
+import torch
+
+import duo_synth as ds
+import oracle.dca as dca
+from gpu_util import assert_close, device_stream, host_stream, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+def _inputs(seed, B, Hq, Hkv, D, T, dev=True):
+    f = (lambda s, H: device_stream(seed, s, B, 0, T, H, D, "cuda")) if dev else \
+        (lambda s, H: host_stream(seed, s, B, 0, T, H, D))
+    return (f(ds.STREAM_Q, Hq), f(ds.STREAM_Q_SUCC, Hq), f(ds.STREAM_Q_INTER, Hq), f(ds.STREAM_K, Hkv),
+            f(ds.STREAM_V, Hkv))
+
+
+def _rows(T, chunk_len, seed):
+    rows = {0, 1, T - 1, T - 2}
+    for c0 in range(0, T, chunk_len):
+        rows |= {c0, c0 + 1, c0 - 1, c0 + chunk_len - 1, c0 + 255, c0 + 256}
+    rng = np.random.default_rng(seed)
+    rows |= set(rng.integers(0, T, 12).tolist())
+    return np.array(sorted(r for r in rows if 0 <= r < T))
+
+
+CASES = [
+    # B, Hq, Hkv, D, T, chunk_len
+    (1, 4, 2, 128, 1100, 256),   # five chunks, ragged last chunk and block
+    (2, 8, 8, 64, 700, 256),     # MHA, D 64
+    (1, 4, 4, 128, 300, 512),    # one chunk: query only
+    (1, 8, 2, 128, 1536, 512),   # three whole chunks, GQA 4
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=[f"case{i}" for i in range(len(CASES))])
+def test_dca_prefill_and_decode_match_oracle(case):
+    from streaming_kv_cache_duo_gb300 import DuoLayer, duo_device_error
+    B, Hq, Hkv, D, T, chunk_len = case
+    steps = 3
+    seed = 500 + T
+    total = T + steps
+    Q, QS, QI, K, V = _inputs(seed, B, Hq, Hkv, D, total)
+    Qh, QSh, QIh, Kh, Vh = _inputs(seed, B, Hq, Hkv, D, total, dev=False)
+    ms = ds.dca_mscale(B, total, chunk_len)
+    msd = torch.from_numpy(ms).cuda()
+    layer = DuoLayer(B, Hq, Hkv, D, 0, 1, total, [1] * Hkv)
+    sl = slice(0, T)
+    o = layer.dca_prefill(*(x[:, sl].contiguous() for x in (Q, QS, QI, K, V)), chunk_len,
+                          mscale=msd[:, sl].contiguous())
+    torch.cuda.synchronize()
+    assert duo_device_error() == 0
+    rows = _rows(T, chunk_len, seed)
+    got = to_np(o)
+    for b in range(B):
+        ref = dca.attention(Qh[b, :T], QSh[b, :T], QIh[b, :T], Kh[b, :T], Vh[b, :T], ms[b, :T], chunk_len, rows=rows)
+        assert_close(got[b, rows], ref, f"prefill b{b}")
+    # decode the next tokens over the cache the prefill's keys went into
+    layer.append(K[:, sl].contiguous(), V[:, sl].contiguous())
+    for s in range(steps):
+        p = T + s
+        layer.append(K[:, p:p + 1].contiguous(), V[:, p:p + 1].contiguous())
+        od = layer.dca_decode(Q[:, p].contiguous(), QS[:, p].contiguous(), QI[:, p].contiguous(), chunk_len,
+                              mscale=msd[:, p].contiguous())
+        torch.cuda.synchronize()
+        assert duo_device_error() == 0
+        g = Hq // Hkv
+        for b in range(B):
+            ref = np.stack([dca.decode(Qh[b, p, h], QSh[b, p, h], QIh[b, p, h], Kh[b, :p + 1, h // g],
+                                       Vh[b, :p + 1, h // g], ms[b, p], p, chunk_len) for h in range(Hq)])
+            assert_close(to_np(od[b]), ref, f"decode step {s} b{b}")
+
+
+def test_one_query_vector_is_the_plain_kernel_bit_for_bit():
+    from streaming_kv_cache_duo_gb300 import DuoLayer
+    B, Hq, Hkv, D, T = 1, 8, 2, 128, 1300
+    Q, _, _, K, V = _inputs(9, B, Hq, Hkv, D, T)
+    layer = DuoLayer(B, Hq, Hkv, D, 0, 1, T, [1, 1])
+    a = layer.dca_prefill(Q, Q, Q, K, V, 256)
+    b = layer.prefill(Q, K, V)
+    layer.append(K, V)
+    q1 = Q[:, T - 1].contiguous()
+    c = layer.dca_decode(q1, q1, q1, 256)
+    d = layer.decode(q1)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+    assert torch.equal(c, d)
+
+
+def test_dca_argument_checks():
+    from streaming_kv_cache_duo_gb300 import DuoError, DuoLayer
+    Q, QS, QI, K, V = _inputs(2, 1, 2, 2, 64, 300)
+    mixed = DuoLayer(1, 2, 2, 64, 4, 16, 300, [1, 0])
+    with pytest.raises(DuoError, match="DUO_ERR_UNSUPPORTED"):
+        mixed.dca_prefill(Q, QS, QI, K, V, 256)
+    full = DuoLayer(1, 2, 2, 64, 0, 1, 300, [1, 1])
+    with pytest.raises(DuoError, match="DUO_ERR_UNSUPPORTED"):
+        full.dca_prefill(Q, QS, QI, K, V, 384)
+    with pytest.raises(DuoError, match="DUO_ERR_UNSUPPORTED"):
+        full.dca_prefill(Q, QS, QI, K, V, 128)
