@@ -15,6 +15,9 @@ Plain, slow, float64 restatements of what the pages define:
   keys), decode over a cache, chunked prefill against a growing cache, and the
   log-sum-exp merge of partial softmaxes used by the vLLM Dual Chunk Attention
   pull request.
+* ``kv4``: the 4-bit KV cache row encoding (asymmetric codes with an fp16 scale and
+  zero per row; the README pairs DuoAttention with a 4-bit KV cache but gives no
+  format, so this is the plainest reading, stated in the module).
 * ``dca``: Dual Chunk Attention from that pull request (three query vectors chosen
   by the chunk of the key relative to the query's, a per-position fp32 scale),
   written as the definition and as the pull request's brute-force schedule.
