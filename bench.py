@@ -339,7 +339,7 @@ def e2e_prefill(w, layer, q, k, v, o, flops, steps, warmup, world):
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": ho.numel() * 2}
 
 
-def make_layer(w, cap, dev, paged_block, pool=False):
+def make_layer(w, cap, dev, paged_block, pool=False, kv4=False):
     """A DuoLayer, or with paged_block > 0 a DuoPagedLayer whose retrieval blocks are
     scattered over the pool in a seeded random order; with `pool` the streaming heads
     live in the same pool too (every block of their table allocated: the ones that
@@ -347,8 +347,10 @@ def make_layer(w, cap, dev, paged_block, pool=False):
     import numpy as np
     import torch
 
-    from streaming_kv_cache_duo_gb300 import DuoLayer, DuoPagedLayer
+    from streaming_kv_cache_duo_gb300 import DuoKv4Layer, DuoLayer, DuoPagedLayer
     kinds = w.is_retrieval
+    if kv4:
+        return DuoKv4Layer(w.B, w.Hq, w.Hkv, w.D, w.S, w.R, cap, kinds, device=dev)
     if paged_block <= 0:
         return DuoLayer(w.B, w.Hq, w.Hkv, w.D, w.S, w.R, cap, kinds, device=dev)
     n_ret = sum(kinds)
@@ -363,7 +365,7 @@ def make_layer(w, cap, dev, paged_block, pool=False):
                          device=dev, stream_table=stream)
 
 
-def bench_decode(w, steps_cap, peaks, paged_block=0, pool=False):
+def bench_decode(w, steps_cap, peaks, paged_block=0, pool=False, kv4=False):
     """Million-token decode: build the cache by appends, then time (append 1 token + decode)."""
     import torch
 
@@ -373,7 +375,7 @@ def bench_decode(w, steps_cap, peaks, paged_block=0, pool=False):
     dev = torch.device("cuda", torch.cuda.current_device())
     kinds = w.is_retrieval
     steps = min(w.decode_steps, steps_cap)
-    layer = make_layer(w, w.context + w.decode_steps, dev, paged_block, pool)
+    layer = make_layer(w, w.context + w.decode_steps, dev, paged_block, pool, kv4)
     chunk = 65536
     for c0 in range(0, w.context, chunk):
         kk = ds.stream_torch(w.seed, ds.STREAM_K, w.B, c0, chunk, w.Hkv, w.D, device=dev)
@@ -406,7 +408,8 @@ def bench_decode(w, steps_cap, peaks, paged_block=0, pool=False):
     # the first steps warm up; report the rest
     warm = min(3, steps - 1)
     times = [a.elapsed_time(b) for a, b, _ in ev][warm:]
-    nbytes = [sum(wl.decode_bytes(w.B, w.Hq, w.Hkv, w.D, w.S, w.R, kinds, n)) for _, _, n in ev][warm:]
+    count = wl.decode_bytes_kv4 if kv4 else wl.decode_bytes
+    nbytes = [sum(count(w.B, w.Hq, w.Hkv, w.D, w.S, w.R, kinds, n)) for _, _, n in ev][warm:]
     avg_ms = sum(times) / len(times)
     gbs = sum(nbytes) / (sum(times) * 1e-3) / 1e9
     step_ms = t0.elapsed_time(t1) / steps
@@ -416,8 +419,10 @@ def bench_decode(w, steps_cap, peaks, paged_block=0, pool=False):
             "step_ms_with_append": round(step_ms, 4), "bytes_per_step": int(sum(nbytes) / len(nbytes)),
             "steps_timed": len(times),
             "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
-                         "frac": round(gbs / peak, 4), "traffic": measured_traffic("decode"),
-                         "kernel": "decode_kernel<128,4>"}}
+                         "frac": round(gbs / peak, 4),
+                         "traffic": None if (kv4 or paged_block) else measured_traffic("decode"),
+                         "kernel": f"decode_kernel<{w.D},{w.Hq // w.Hkv},{'kv4' if kv4 else 'plain'}>"},
+            "tokens_per_s": round(1e3 / (sum(times) / len(times)), 1)}
 
 
 def bench_decode_graph(w, peaks):
@@ -707,6 +712,8 @@ def other_workload(args, w, world, rank, peaks):
             "config": {"workload": w.name, "batch": w.B, "q_heads": w.Hq, "kv_heads": w.Hkv, "head_dim": w.D,
                        "retrieval_kv_heads": sum(w.is_retrieval), "sink": w.S, "recent": w.R,
                        "parallelism": f"replicas{world}"}}
+    if args.kv4:
+        base["config"]["cache"] = "4-bit codes + fp16 (scale, zero) per row; bytes counted as stored"
     if args.paged:
         base["config"]["paged_block"] = args.paged
         base["config"]["streaming_heads"] = "paged pool" if args.pool else "sink + ring cache"
@@ -725,8 +732,8 @@ def other_workload(args, w, world, rank, peaks):
                     roofline=r["roofline"], gpu_launches=r["launches"],
                     breakdown_ms={"prefill": round(r["prefill_ms"], 4)})
     else:
-        if args.paged or w.B == 1:
-            r = bench_decode(w, w.decode_steps, peaks, args.paged, args.pool)
+        if args.paged or args.kv4 or w.B == 1:
+            r = bench_decode(w, w.decode_steps, peaks, args.paged, args.pool, args.kv4)
         else:
             r = bench_decode_graph(w, peaks)
         base["config"].update(context=w.context, decode_steps=w.decode_steps)
@@ -747,6 +754,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--kv4", action="store_true",
+                    help="decode workloads: caches stored as 4-bit codes with an fp16 (scale, zero) per row")
     ap.add_argument("--pool", action="store_true",
                     help="with --paged: streaming heads in the paged pool too (block-granular eviction)")
     ap.add_argument("--paged", type=int, default=0,

@@ -219,6 +219,42 @@ duo_status duo_attn_prefill_paged(duo_handle* handle, const duo_kv_cache* cache,
 duo_status duo_attn_decode_paged(duo_handle* handle, const duo_kv_cache* cache, const duo_paged* paged,
                                  const void* q, void* o, void* workspace, size_t workspace_bytes, void* stream);
 
+/* 4-bit KV caches. The DuoAttention README pairs the method with a 4-bit KV cache to
+ * decode millions of tokens on one GPU (quick-start demo, Efficiency section) but gives
+ * no format; this library uses the plainest asymmetric one. Each cached row (the D
+ * values of one token of one head) is stored as D 4-bit codes plus an fp16 scale and
+ * zero: scale = fp16((max - min) / 15), zero = fp16(min), code = clamp(rint((x - zero)
+ * / scale), 0, 15) with every step in fp32 round-to-nearest (all codes 0 when the
+ * scale is 0), value = code * scale + zero. Codes are packed two per byte, the even
+ * dim in the low nibble. Rows must stay within the fp16 range.
+ *
+ * Layout (all device memory, caller-owned, 16-byte aligned), with cap16 = max_seq_len
+ * and sr16 = S + R each rounded up to a multiple of 16 rows:
+ *   k_codes, v_codes    u8  [B, n_ret, cap16, D / 2]   retrieval heads, row t = token t
+ *   k_sz, v_sz          u32 [B, n_ret, cap16]          fp16 scale (low half), zero (high)
+ *   ks_codes, vs_codes  u8  [B, n_str, sr16, D / 2]    streaming heads, sink + ring slots
+ *   ks_sz, vs_sz        u32 [B, n_str, sr16]
+ * cache->n and cache->pos keep their meaning; cache->k_full, v_full, k_sr, v_sr are not
+ * used. duo_kv_append_kv4 quantizes and stores the new tokens (same slot rule as
+ * duo_kv_append); duo_attn_decode_kv4 is duo_attn_decode over these arrays, with the
+ * dequantization folded into the dot products (q . k = scale (q . codes) + zero sum(q)).
+ * Prefill never reads a cache in this form: chunked prefill needs the bf16 caches. */
+typedef struct {
+  void* k_codes;
+  void* v_codes;
+  void* k_sz;
+  void* v_sz;
+  void* ks_codes;
+  void* vs_codes;
+  void* ks_sz;
+  void* vs_sz;
+} duo_kv4_cache;
+
+duo_status duo_kv_append_kv4(duo_handle* handle, duo_kv_cache* cache, const duo_kv4_cache* kv4, const void* k_new,
+                             const void* v_new, int32_t T, void* stream);
+duo_status duo_attn_decode_kv4(duo_handle* handle, const duo_kv_cache* cache, const duo_kv4_cache* kv4,
+                               const void* q, void* o, void* workspace, size_t workspace_bytes, void* stream);
+
 /* Dual Chunk Attention (vLLM pull request "[Model] Implement DualChunkAttention for
  * Qwen2 Models"): the sequence is cut into chunks of chunk_len positions from the start
  * (the last one may be shorter) and every position carries three query vectors made by

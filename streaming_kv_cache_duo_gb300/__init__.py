@@ -200,6 +200,56 @@ class DuoPagedLayer(DuoLayer):
         return out
 
 
+class DuoKv4Layer(DuoLayer):
+    """A layer whose caches hold 4-bit codes with an fp16 (scale, zero) pair per row
+    (layout in include/duo_attn.h): codes u8 [B, planes, pitch, D/2] and pairs int32
+    [B, planes, pitch], pitch = capacity rounded up to 16 rows. Prefill attention is
+    computed from bf16 inputs as usual; appends quantize; decode reads the codes."""
+
+    def __init__(self, batch, num_q_heads, num_kv_heads, head_dim, sink_size, recent_size, max_seq_len,
+                 is_retrieval, device="cuda"):
+        import torch
+        super().__init__(batch, num_q_heads, num_kv_heads, head_dim, sink_size, recent_size, 1, is_retrieval,
+                         device=device)
+        self.cap = max_seq_len
+        cap16 = -(-max_seq_len // 16) * 16
+        sr16 = -(-(sink_size + recent_size) // 16) * 16
+        u8 = dict(dtype=torch.uint8, device=self.device)
+        i32 = dict(dtype=torch.int32, device=self.device)
+        self.k_codes = torch.zeros((batch, self.n_ret, cap16 if self.n_ret else 0, head_dim // 2), **u8)
+        self.v_codes = torch.zeros_like(self.k_codes)
+        self.k_sz = torch.zeros((batch, self.n_ret, cap16 if self.n_ret else 0), **i32)
+        self.v_sz = torch.zeros_like(self.k_sz)
+        self.ks_codes = torch.zeros((batch, self.n_str, sr16, head_dim // 2), **u8)
+        self.vs_codes = torch.zeros_like(self.ks_codes)
+        self.ks_sz = torch.zeros((batch, self.n_str, sr16), **i32)
+        self.vs_sz = torch.zeros_like(self.ks_sz)
+        # the handle's capacity is max_seq_len: recreate it with the real value
+        duo_destroy(self.handle)
+        with torch.cuda.device(self.device):
+            self.handle = duo_create(batch, num_q_heads, num_kv_heads, head_dim, sink_size, recent_size, max_seq_len,
+                                     self.is_retrieval)
+        ptr = lambda t: t.data_ptr() if t.numel() else None
+        self.kv4 = _lib.duo_kv4_cache(ptr(self.k_codes), ptr(self.v_codes), ptr(self.k_sz), ptr(self.v_sz),
+                                      ptr(self.ks_codes), ptr(self.vs_codes), ptr(self.ks_sz), ptr(self.vs_sz))
+        self.reset()
+
+    def append(self, k_new, v_new, stream=None) -> None:
+        T = k_new.shape[1]
+        _lib._bf16(k_new, (self.B, T, self.Hkv, self.D), "k_new")
+        _lib._bf16(v_new, (self.B, T, self.Hkv, self.D), "v_new")
+        _lib.duo_kv_append_kv4(self.handle, self.cache, self.kv4, k_new, v_new, T, stream)
+
+    def decode(self, q, out=None, stream=None):
+        import torch
+        _lib._bf16(q, (self.B, self.Hq, self.D), "q")
+        if out is None:
+            out = torch.empty_like(q)
+        _lib._bf16(out, (self.B, self.Hq, self.D), "o")
+        _lib.duo_attn_decode_kv4(self.handle, self.cache, self.kv4, q, out, self.workspace, stream)
+        return out
+
+
 def _check_mscale(mscale, shape):
     import torch
     if mscale is None:

@@ -31,7 +31,8 @@ EXPORTS = (
     "duo_classify_heads", "duo_create", "duo_destroy", "duo_cache_reset", "duo_kv_append",
     "duo_attn_prefill", "duo_attn_prefill_select", "duo_decode_workspace_size", "duo_attn_decode",
     "duo_attn_decode_static", "duo_kv_append_paged", "duo_attn_prefill_paged", "duo_attn_decode_paged",
-    "duo_paged_stream_dead_blocks", "duo_dca_prefill", "duo_dca_decode",
+    "duo_paged_stream_dead_blocks", "duo_dca_prefill", "duo_dca_decode", "duo_kv_append_kv4",
+    "duo_attn_decode_kv4",
     "duo_kv_append_varlen", "duo_attn_decode_varlen", "duo_device_error", "duo_selftest_bounded_wait",
     "duo_last_error", "duo_status_string",
 )
@@ -52,6 +53,11 @@ class duo_config(ctypes.Structure):
 class duo_paged(ctypes.Structure):
     _fields_ = [("block_table", c_void_p), ("block_size", c_int32), ("max_blocks", c_int32),
                 ("num_blocks", c_int64), ("stream_table", c_void_p)]
+
+
+class duo_kv4_cache(ctypes.Structure):
+    _fields_ = [(name, c_void_p) for name in ("k_codes", "v_codes", "k_sz", "v_sz", "ks_codes", "vs_codes", "ks_sz",
+                                              "vs_sz")]
 
 
 class duo_kv_cache(ctypes.Structure):
@@ -93,6 +99,10 @@ def library() -> ctypes.CDLL:
                                             c_void_p, c_void_p, c_size_t, c_void_p]),
         "duo_paged_stream_dead_blocks": (c_int32, [c_int32, c_int32, c_int32, c_int64, POINTER(c_int64),
                                                    POINTER(c_int64)]),
+        "duo_kv_append_kv4": (c_int32, [c_void_p, POINTER(duo_kv_cache), POINTER(duo_kv4_cache), c_void_p, c_void_p,
+                                        c_int32, c_void_p]),
+        "duo_attn_decode_kv4": (c_int32, [c_void_p, POINTER(duo_kv_cache), POINTER(duo_kv4_cache), c_void_p,
+                                          c_void_p, c_void_p, c_size_t, c_void_p]),
         "duo_dca_prefill": (c_int32, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int32,
                                       c_int32, c_void_p, c_void_p]),
         "duo_dca_decode": (c_int32, [c_void_p, POINTER(duo_kv_cache), c_void_p, c_void_p, c_void_p, c_void_p,
@@ -218,6 +228,18 @@ def duo_attn_decode_paged(handle, cache: "duo_kv_cache", paged: "duo_paged", q, 
     nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(library().duo_attn_decode_paged(handle, ctypes.byref(cache), ctypes.byref(paged), _ptr(q), _ptr(o),
                                            _ptr(workspace), nbytes, _stream_ptr(stream)))
+
+
+def duo_kv_append_kv4(handle, cache: "duo_kv_cache", kv4: "duo_kv4_cache", k_new, v_new, T: int,
+                      stream=None) -> None:
+    _check(library().duo_kv_append_kv4(handle, ctypes.byref(cache), ctypes.byref(kv4), _ptr(k_new), _ptr(v_new), T,
+                                       _stream_ptr(stream)))
+
+
+def duo_attn_decode_kv4(handle, cache: "duo_kv_cache", kv4: "duo_kv4_cache", q, o, workspace, stream=None) -> None:
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(library().duo_attn_decode_kv4(handle, ctypes.byref(cache), ctypes.byref(kv4), _ptr(q), _ptr(o),
+                                         _ptr(workspace), nbytes, _stream_ptr(stream)))
 
 
 def duo_dca_prefill(handle, q, q_succ, q_inter, k, v, mscale, T: int, chunk_len: int, o, stream=None) -> None:

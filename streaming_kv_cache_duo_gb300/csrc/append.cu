@@ -15,7 +15,9 @@
 // read-only 128-bit loads from the token-major input and 128-bit stores into the
 // head-major caches. Bytes moved: 2 * 2 * D * (T * n_ret + survivors * n_str) per
 // sequence, plus 4 bytes of pos per surviving token.
-#include "duo_internal.h"
+#include <cuda_fp16.h>
+
+#include "duo_device.cuh"
 
 namespace duo {
 namespace {
@@ -142,7 +144,116 @@ __global__ void __launch_bounds__(256) append_varlen_kernel(const AppendParams p
   }
 }
 
+// 4-bit caches: one warp per (token, head) row of K and V. Each lane holds D / 32
+// values of the row; the row's min and max come from warp shuffles, then
+//   scale = fp16(fp32((max - min) / 15)),  zero = fp16(min),
+//   code  = clamp(rint(fp32(x - zero) / scale), 0, 15)   (0 when scale is 0),
+// every step in fp32 round-to-nearest, so the codes are a fixed function of the
+// row. Codes are packed two per byte (even dim in the low nibble); lane 0 stores
+// the fp16 pair (scale low, zero high). Rows: retrieval rows of all T tokens, then
+// the streaming rows the call keeps (the same two intervals as the bf16 ring).
+template <int D>
+__device__ __forceinline__ void quantize_row(const uint16_t* src, uint8_t* codes, uint32_t* sz, int lane) {
+  constexpr int VPL = D / 32;  // values per lane: 4 (D 128) or 2 (D 64)
+  float x[VPL];
+  if constexpr (VPL == 4) {
+    const uint2 w = __ldg(reinterpret_cast<const uint2*>(src) + lane);
+    x[0] = bf16lo(w.x);
+    x[1] = bf16hi(w.x);
+    x[2] = bf16lo(w.y);
+    x[3] = bf16hi(w.y);
+  } else {
+    const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(src) + lane);
+    x[0] = bf16lo(w);
+    x[1] = bf16hi(w);
+  }
+  float mn = x[0], mx = x[0];
+#pragma unroll
+  for (int i = 1; i < VPL; ++i) {
+    mn = fminf(mn, x[i]);
+    mx = fmaxf(mx, x[i]);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, off));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+  }
+  const __half sh = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), 15.f));
+  const __half zh = __float2half_rn(mn);
+  const float s = __half2float(sh), z = __half2float(zh);
+  uint32_t packed = 0;
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    int c = 0;
+    if (s != 0.f) {
+      c = __float2int_rn(__fdiv_rn(__fsub_rn(x[i], z), s));
+      c = c < 0 ? 0 : (c > 15 ? 15 : c);
+    }
+    packed |= (uint32_t)c << (4 * i);
+  }
+  if constexpr (VPL == 4)
+    reinterpret_cast<uint16_t*>(codes)[lane] = (uint16_t)packed;
+  else
+    codes[lane] = (uint8_t)packed;
+  if (lane == 0) *sz = (uint32_t)__half_as_ushort(sh) | ((uint32_t)__half_as_ushort(zh) << 16);
+}
+
+template <int D>
+__global__ void __launch_bounds__(256) append_kv4_kernel(const AppendParams p) {
+  const int lane = threadIdx.x & 31;
+  const int Hkv = p.sh.Hkv;
+  const int n_ret = p.sh.n_ret, n_str = p.sh.n_str;
+  const int SR = p.sh.S + p.sh.R;
+  const int64_t T = p.T;
+  const int64_t ret_rows = (int64_t)p.sh.B * T * n_ret;
+  const int64_t surv = p.sink_cnt + p.ring_cnt;
+  const int64_t total = ret_rows + (int64_t)p.sh.B * surv * n_str;
+  const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  for (int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < total; r += warps) {
+    int64_t src_row, dst_row;  // row of [B, T, Hkv] input; row of the destination plane
+    bool streaming;
+    if (r < ret_rows) {
+      const int ri = (int)(r % n_ret);
+      const int64_t t = (r / n_ret) % T;
+      const int64_t b = r / n_ret / T;
+      src_row = (b * T + t) * Hkv + p.heads.ret_head[ri];
+      dst_row = (b * n_ret + ri) * p.cap16 + p.n + t;
+      streaming = false;
+    } else {
+      const int64_t q = r - ret_rows;
+      const int si = (int)(q % n_str);
+      const int64_t k = (q / n_str) % surv;
+      const int64_t b = q / n_str / surv;
+      const int64_t t_abs = k < p.sink_cnt ? p.sink_lo + k : p.ring_lo + (k - p.sink_cnt);
+      const int64_t slot = t_abs < p.sh.S ? t_abs : p.sh.S + (t_abs - p.sh.S) % p.sh.R;
+      src_row = (b * T + (t_abs - p.n)) * Hkv + p.heads.str_head[si];
+      dst_row = (b * n_str + si) * p.sr16 + slot;
+      streaming = true;
+      if (si == 0 && lane == 0) p.pos[b * SR + slot] = (int32_t)t_abs;
+    }
+    quantize_row<D>(p.k_new + src_row * D, (streaming ? p.ks4 : p.k4) + dst_row * (D / 2),
+                    (streaming ? p.kssz : p.ksz) + dst_row, lane);
+    quantize_row<D>(p.v_new + src_row * D, (streaming ? p.vs4 : p.v4) + dst_row * (D / 2),
+                    (streaming ? p.vssz : p.vsz) + dst_row, lane);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_append_kv4(const AppendParams& p, int num_sms, cudaStream_t stream) {
+  const int64_t rows = (int64_t)p.sh.B * p.T * p.sh.n_ret + (int64_t)p.sh.B * (p.sink_cnt + p.ring_cnt) * p.sh.n_str;
+  if (rows == 0) return cudaSuccess;
+  int64_t blocks = (rows + 7) / 8;
+  const int64_t cap = (int64_t)num_sms * 8;
+  if (blocks > cap) blocks = cap;
+  if (p.sh.D == 128)
+    append_kv4_kernel<128><<<(unsigned)blocks, 256, 0, stream>>>(p);
+  else if (p.sh.D == 64)
+    append_kv4_kernel<64><<<(unsigned)blocks, 256, 0, stream>>>(p);
+  else
+    return cudaErrorInvalidValue;
+  return cudaGetLastError();
+}
 
 cudaError_t launch_append_varlen(const AppendParams& p, int32_t* seq_lens, cudaStream_t stream) {
   const int work = p.sh.Hkv * (p.sh.D / 8);

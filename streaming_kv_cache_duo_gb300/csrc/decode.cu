@@ -58,11 +58,12 @@ constexpr int kModePlain = 0;  // contiguous retrieval caches, ring caches for s
 constexpr int kModePaged = 1;  // retrieval caches in a paged pool (block table), ring caches
 constexpr int kModePool = 2;   // both head kinds in the paged pool
 constexpr int kModeDca = 3;    // Dual Chunk Attention: the query vector depends on the key's chunk
+constexpr int kModeKv4 = 4;    // 4-bit caches: codes + fp16 (scale, zero) per row
 
 // retrieval caches (and maybe streaming ones) in the paged pool
 __host__ __device__ constexpr bool is_paged_mode(int mode) { return mode == kModePaged || mode == kModePool; }
 
-template <int D, int G>
+template <int D, int G, bool KV4 = false>
 struct Cfg {
   static constexpr int DPL = (G * 16 <= 64) ? 16 : 8;  // dims per lane
   static constexpr int LPK = D / DPL;                  // lanes per key
@@ -71,13 +72,17 @@ struct Cfg {
   static constexpr int KPI = 32 / LPK;                 // keys per warp iteration
   static constexpr int IT = kKPW / KPI;                // iterations per tile
   static constexpr int CH = DPL / 8;                   // 16-byte chunks per lane
-  static constexpr int ROW = D * 2;                    // bytes per key row
+  // 4-bit rows are a quarter of the bytes, so the per-warp ring is deeper
+  static constexpr int NSW = KV4 ? 8 : kNSW;           // pipeline stages per warp
+  static constexpr int ROW = KV4 ? D / 2 : D * 2;      // bytes per key row (codes or bf16)
   static constexpr int SLICE = kKPW * ROW;             // one warp's K (or V) rows of a tile
-  static constexpr int WSTAGE = 2 * SLICE;             // K slice then V slice
-  static constexpr int RING = kWarps * kNSW * WSTAGE;
+  static constexpr int PSLICE = KV4 ? kKPW * 4 : 0;    // their (scale, zero) pairs
+  static constexpr int WSTAGE = 2 * SLICE + 2 * PSLICE;  // K, V (then K, V pairs)
+  static constexpr int RING = kWarps * NSW * WSTAGE;
   static constexpr int RED = kWarps * G * (D + 2);
   static constexpr int PS = D + 4;  // floats per head of a partial in the workspace (16-byte multiple)
-  static constexpr size_t SMEM = (size_t)RING + (size_t)RED * 4 + 512;
+  // after the reduction buffer: NSW mbarriers per warp, the segment barrier, flag, maxima
+  static constexpr size_t SMEM = (size_t)RING + (size_t)RED * 4 + (KV4 ? kWarps * NSW * 8 + 256 : 512);
   static_assert(IT >= 1 && kKPW % KPI == 0, "tile split");
   static_assert(G <= LPK, "every head needs a lane of each key group");
 };
@@ -132,6 +137,7 @@ __device__ __forceinline__ Unit unit_info(const DecodeParams& p, int u) {
     x.streaming = true;
     x.pq = seq_len(p, x.b) - 1;
     x.keys = x.pq + 1 < (int64_t)(p.sh.S + p.sh.R) ? x.pq + 1 : (int64_t)(p.sh.S + p.sh.R);
+    if (kMode == kModeKv4) x.plane = us;  // its ring plane in the 4-bit arrays
     if (kMode == kModePool) {  // rows [0, n) of its pool blocks, of which only some tiles are read
       x.plane = us;
       x.keys = x.pq + 1;
@@ -256,7 +262,28 @@ struct Cursor {
 template <int D, int G, int kMode>
 __device__ __forceinline__ bool issue_slice(const DecodeParams& p, const Cursor<kMode>& cur, int w,
                                             uint8_t* stage, uint64_t* bar) {
-  using C = Cfg<D, G>;
+  using C = Cfg<D, G, kMode == kModeKv4>;
+  if constexpr (kMode == kModeKv4) {
+    // whole 16-row chunks of codes and (scale, zero) pairs: the planes' row pitches are
+    // multiples of 16, so the chunk stays inside its plane; rows past the keys are
+    // copied but never used
+    const int rows = warp_rows(cur.x.keys, cur.lt, w);
+    if (rows <= 0) {
+      mbar_arrive_expect_tx(bar, 0);
+      return false;
+    }
+    const int64_t r = cur.x.plane * (cur.x.streaming ? (int64_t)p.sr16 : p.cap16) + cur.lt * kTK + (int64_t)w * kKPW;
+    const uint8_t* kc = (cur.x.streaming ? p.ks4 : p.k4) + r * (D / 2);
+    const uint8_t* vc = (cur.x.streaming ? p.vs4 : p.v4) + r * (D / 2);
+    const uint32_t* kz = (cur.x.streaming ? p.kssz : p.ksz) + r;
+    const uint32_t* vz = (cur.x.streaming ? p.vssz : p.vsz) + r;
+    mbar_arrive_expect_tx(bar, 2 * C::SLICE + 2 * C::PSLICE);
+    bulk_g2s(stage, kc, C::SLICE, bar);
+    bulk_g2s(stage + C::SLICE, vc, C::SLICE, bar);
+    bulk_g2s(stage + 2 * C::SLICE, kz, C::PSLICE, bar);
+    bulk_g2s(stage + 2 * C::SLICE + C::PSLICE, vz, C::PSLICE, bar);
+    return false;
+  }
   const bool pool = is_paged_mode(kMode) && cur.in_pool();
   int rows = warp_rows(cur.x.keys, kMode == kModePool ? cur.row_tile() : cur.lt, w);
   const uint16_t* kp;
@@ -287,6 +314,21 @@ __device__ __forceinline__ bool issue_slice(const DecodeParams& p, const Cursor<
 
 __device__ __forceinline__ float2 unpack2(uint32_t w) { return make_float2(bf16lo(w), bf16hi(w)); }
 
+// 4-bit codes of dims 2e, 2e+1 of an 8-dim chunk as floats: lo / hi hold the low /
+// high nibbles of the chunk's four bytes; a code c becomes the float 2^23 + c by
+// placing it under the exponent bits of 2^23, then 2^23 is subtracted (exact).
+__device__ __forceinline__ float2 codes2(uint32_t lo, uint32_t hi, int e) {
+  const float a = __uint_as_float(__byte_perm(lo, 0x4B000000u, 0x7540u | (uint32_t)e));
+  const float b = __uint_as_float(__byte_perm(hi, 0x4B000000u, 0x7540u | (uint32_t)e));
+  return __fadd2_rn(make_float2(a, b), make_float2(-8388608.f, -8388608.f));
+}
+
+// fp16 (scale, zero) pair of a 4-bit row, widened to fp32
+__device__ __forceinline__ float2 scale_zero(uint32_t w) {
+  return make_float2(__half2float(__ushort_as_half((unsigned short)(w & 0xFFFFu))),
+                     __half2float(__ushort_as_half((unsigned short)(w >> 16))));
+}
+
 // Synchronisation of the eight warps through an mbarrier (bounded wait).
 struct WarpSync {
   uint64_t* bar;
@@ -303,11 +345,11 @@ struct WarpSync {
 
 template <int D, int G, int kMode>
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams p) {
-  using C = Cfg<D, G>;
+  using C = Cfg<D, G, kMode == kModeKv4>;
   extern __shared__ __align__(1024) uint8_t smem[];
   float* red = reinterpret_cast<float*>(smem + C::RING);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::RING + (size_t)C::RED * 4);  // [kWarps][kNSW]
-  uint64_t* segbar = full + kWarps * kNSW;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::RING + (size_t)C::RED * 4);  // [kWarps][C::NSW]
+  uint64_t* segbar = full + kWarps * C::NSW;
   int* flag = reinterpret_cast<int*>(segbar + 1);
 
   const DevError err{&g_decode_err};
@@ -318,23 +360,23 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
   // After any CTA of this kernel gave up a wait, later CTAs do no work.
   const bool live = *(volatile unsigned int*)err.word == 0u;
   const int64_t t1 = live && c < p.Cr ? (int64_t)(c + 1) * p.W / p.Cr : t0;
-  uint8_t* ring = smem + (size_t)warp * kNSW * C::WSTAGE;
-  uint64_t* wfull = full + warp * kNSW;
+  uint8_t* ring = smem + (size_t)warp * C::NSW * C::WSTAGE;
+  uint64_t* wfull = full + warp * C::NSW;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kWarps * kNSW; ++s) mbar_init(&full[s], 1);
+    for (int s = 0; s < kWarps * C::NSW; ++s) mbar_init(&full[s], 1);
     mbar_init(segbar, kWarps);
     fence_mbarrier_init();
   }
   __syncthreads();
 
-  // refill cursor (warp-uniform); the prologue issues the first kNSW - 1 slices
+  // refill cursor (warp-uniform); the prologue issues the first C::NSW - 1 slices
   constexpr bool kPaged = is_paged_mode(kMode);
   Cursor<kMode> cur;
   cur.init(p, c, t0, t1, live);
   int64_t issued = 0;
   uint32_t badmask = 0;  // lane 0: bit s set when stage s holds a skipped (bad-block) slice
-  for (int s = 0; s < kNSW - 1 && cur.live; ++s) {
+  for (int s = 0; s < C::NSW - 1 && cur.live; ++s) {
     if (lane == 0) {
       const bool bad = issue_slice<D, G, kMode>(p, cur, warp, ring + s * C::WSTAGE, &wfull[s]);
       if (kPaged) badmask = bad ? (badmask | (1u << s)) : (badmask & ~(1u << s));
@@ -394,6 +436,31 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
     } else {
       load_q(p.q, qfactor);
     }
+    // 4-bit caches: q.k^ = scale (q.c) + zero sum(q), so each lane needs sum(q) of its
+    // head hme, reduced over the key group like a score
+    float qsum = 0.f;
+    float zacc[G];  // 4-bit caches: sum of p * zero(v) per head slot (added to every dim)
+#pragma unroll
+    for (int l = 0; l < G; ++l) zacc[l] = 0.f;
+    if constexpr (kMode == kModeKv4) {
+      float d[G];
+#pragma unroll
+      for (int l = 0; l < G; ++l) {
+        d[l] = 0.f;
+#pragma unroll
+        for (int e = 0; e < C::DPL / 2; ++e) d[l] += q2[l][e].x + q2[l][e].y;
+      }
+#pragma unroll
+      for (int k = 1; k <= C::GB; ++k) {
+        const int half = G >> k;
+        const int bit = 1 << (C::LB - k);
+#pragma unroll
+        for (int l = 0; l < half; ++l) d[l] += __shfl_xor_sync(0xffffffffu, d[l + half], bit);
+      }
+#pragma unroll
+      for (int b = C::LB - C::GB - 1; b >= 0; --b) d[0] += __shfl_xor_sync(0xffffffffu, d[0], 1 << b);
+      qsum = d[0];
+    }
     float2 o2[G][C::DPL / 2];
 #pragma unroll
     for (int l = 0; l < G; ++l)
@@ -402,7 +469,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
     float l_run = 0.f, m_run = -INFINITY;  // of head hme
 
     for (int64_t lt = lt_begin; lt < lt_end; ++lt, ++j) {
-      const int s = (int)(j % kNSW);
+      const int s = (int)(j % C::NSW);
       if (kMode == kModeDca) {
         const int v = dca_var(lt);
         if (v != qv) {  // at most twice per unit
@@ -412,7 +479,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
       }
       // refill: the stage used by tile j - 1 is free now (this warp finished it)
       if (cur.live) {
-        const int sn = (int)((j + kNSW - 1) % kNSW);
+        const int sn = (int)((j + C::NSW - 1) % C::NSW);
         if (lane == 0) {
           const bool bad = issue_slice<D, G, kMode>(p, cur, warp, ring + sn * C::WSTAGE, &wfull[sn]);
           if (kPaged) badmask = bad ? (badmask | (1u << sn)) : (badmask & ~(1u << sn));
@@ -420,7 +487,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
         cur.advance(p, c, t1, live);
         ++issued;
       }
-      if (!mbar_wait(&wfull[s], (uint32_t)((j / kNSW) & 1), err, kErrDecodeConsumer)) {
+      if (!mbar_wait(&wfull[s], (uint32_t)((j / C::NSW) & 1), err, kErrDecodeConsumer)) {
         ok = false;
         break;
       }
@@ -453,13 +520,24 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
         for (int l = 0; l < G; ++l) acc[l] = make_float2(0.f, 0.f);
 #pragma unroll
         for (int ch = 0; ch < C::CH; ++ch) {
-          const uint4 kv = *reinterpret_cast<const uint4*>(sk + key * C::ROW + (cl + ch * C::LPK) * 16);
-          const uint32_t w4[4] = {kv.x, kv.y, kv.z, kv.w};
+          if constexpr (kMode == kModeKv4) {
+            const uint32_t w = *reinterpret_cast<const uint32_t*>(sk + key * C::ROW + (cl + ch * C::LPK) * 4);
+            const uint32_t lo = w & 0x0F0F0F0Fu, hi = (w >> 4) & 0x0F0F0F0Fu;
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float2 k2 = unpack2(w4[e]);
+            for (int e = 0; e < 4; ++e) {
+              const float2 k2 = codes2(lo, hi, e);
 #pragma unroll
-            for (int l = 0; l < G; ++l) acc[l] = __ffma2_rn(q2[l][ch * 4 + e], k2, acc[l]);
+              for (int l = 0; l < G; ++l) acc[l] = __ffma2_rn(q2[l][ch * 4 + e], k2, acc[l]);
+            }
+          } else {
+            const uint4 kv = *reinterpret_cast<const uint4*>(sk + key * C::ROW + (cl + ch * C::LPK) * 16);
+            const uint32_t w4[4] = {kv.x, kv.y, kv.z, kv.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 k2 = unpack2(w4[e]);
+#pragma unroll
+              for (int l = 0; l < G; ++l) acc[l] = __ffma2_rn(q2[l][ch * 4 + e], k2, acc[l]);
+            }
           }
         }
         float dot[G];
@@ -476,6 +554,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
         // butterfly over the remaining lane bits
 #pragma unroll
         for (int b = C::LB - C::GB - 1; b >= 0; --b) dot[0] += __shfl_xor_sync(0xffffffffu, dot[0], 1 << b);
+        if constexpr (kMode == kModeKv4) {
+          const float2 sz = scale_zero(*reinterpret_cast<const uint32_t*>(sk + 2 * C::SLICE + key * 4));
+          dot[0] = fmaf(sz.x, dot[0], sz.y * qsum);
+        }
         sc[it] = valid ? dot[0] : -INFINITY;
       }
 
@@ -498,6 +580,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
           const float2 f2 = make_float2(fl, fl);
 #pragma unroll
           for (int e = 0; e < C::DPL / 2; ++e) o2[l][e] = __fmul2_rn(o2[l][e], f2);
+          if (kMode == kModeKv4) zacc[l] *= fl;
         }
       }
 #pragma unroll
@@ -514,16 +597,39 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
         for (int l = 1; l < G; ++l) pl[l] = __shfl_xor_sync(0xffffffffu, sc[it], l << (C::LB - C::GB));
         if (full_tile || vis[it]) {
           const int key = it * C::KPI + kg;
+          if constexpr (kMode == kModeKv4) {
+            // p v^ = (p scale) c + p zero: the zero part summed per head, added at the end
+            const float2 sz = scale_zero(*reinterpret_cast<const uint32_t*>(sk + 2 * C::SLICE + C::PSLICE + key * 4));
+            float ps[G];
 #pragma unroll
-          for (int ch = 0; ch < C::CH; ++ch) {
-            const uint4 vv = *reinterpret_cast<const uint4*>(sv + key * C::ROW + (cl + ch * C::LPK) * 16);
-            const uint32_t w4[4] = {vv.x, vv.y, vv.z, vv.w};
+            for (int l = 0; l < G; ++l) {
+              ps[l] = pl[l] * sz.x;
+              zacc[l] = fmaf(pl[l], sz.y, zacc[l]);
+            }
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float2 v2 = unpack2(w4[e]);
+            for (int ch = 0; ch < C::CH; ++ch) {
+              const uint32_t w = *reinterpret_cast<const uint32_t*>(sv + key * C::ROW + (cl + ch * C::LPK) * 4);
+              const uint32_t lo = w & 0x0F0F0F0Fu, hi = (w >> 4) & 0x0F0F0F0Fu;
 #pragma unroll
-              for (int l = 0; l < G; ++l)
-                o2[l][ch * 4 + e] = __ffma2_rn(make_float2(pl[l], pl[l]), v2, o2[l][ch * 4 + e]);
+              for (int e = 0; e < 4; ++e) {
+                const float2 v2 = codes2(lo, hi, e);
+#pragma unroll
+                for (int l = 0; l < G; ++l)
+                  o2[l][ch * 4 + e] = __ffma2_rn(make_float2(ps[l], ps[l]), v2, o2[l][ch * 4 + e]);
+              }
+            }
+          } else {
+#pragma unroll
+            for (int ch = 0; ch < C::CH; ++ch) {
+              const uint4 vv = *reinterpret_cast<const uint4*>(sv + key * C::ROW + (cl + ch * C::LPK) * 16);
+              const uint32_t w4[4] = {vv.x, vv.y, vv.z, vv.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float2 v2 = unpack2(w4[e]);
+#pragma unroll
+                for (int l = 0; l < G; ++l)
+                  o2[l][ch * 4 + e] = __ffma2_rn(make_float2(pl[l], pl[l]), v2, o2[l][ch * 4 + e]);
+              }
             }
           }
         }
@@ -533,6 +639,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
     if (!ok) break;
 
     // ---------------------------------------------------- segment merge
+    if constexpr (kMode == kModeKv4) {
+#pragma unroll
+      for (int l = 0; l < G; ++l)
+#pragma unroll
+        for (int e = 0; e < C::DPL / 2; ++e) o2[l][e] = __fadd2_rn(o2[l][e], make_float2(zacc[l], zacc[l]));
+    }
     // sum over the key groups of the warp (each holds other keys)
 #pragma unroll
     for (int off = C::LPK; off < 32; off <<= 1) {
@@ -697,14 +809,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
   // Copies still in flight (only after an early exit) land before the CTA ends.
   if (lane == 0) {
     for (int64_t jj = j; jj < issued; ++jj)
-      mbar_wait(&wfull[jj % kNSW], (uint32_t)((jj / kNSW) & 1), err, kErrDecodeConsumer);
+      mbar_wait(&wfull[jj % C::NSW], (uint32_t)((jj / C::NSW) & 1), err, kErrDecodeConsumer);
   }
   __syncthreads();
 }
 
 template <int D, int G, int kMode>
 cudaError_t launch_v(const DecodeParams& p, cudaStream_t stream) {
-  using C = Cfg<D, G>;
+  using C = Cfg<D, G, kMode == kModeKv4>;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e =
@@ -720,6 +832,7 @@ cudaError_t launch_v(const DecodeParams& p, cudaStream_t stream) {
 // bookkeeping costs the contiguous kernel nothing
 template <int D, int G>
 cudaError_t launch_t(const DecodeParams& p, cudaStream_t stream) {
+  if (p.k4) return launch_v<D, G, kModeKv4>(p, stream);
   if (p.chunk_len > 0) return launch_v<D, G, kModeDca>(p, stream);
   if (p.pg.stream_table) return launch_v<D, G, kModePool>(p, stream);
   return p.pg.table ? launch_v<D, G, kModePaged>(p, stream) : launch_v<D, G, kModePlain>(p, stream);

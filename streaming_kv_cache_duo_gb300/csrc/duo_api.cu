@@ -281,13 +281,39 @@ duo_status duo_cache_reset(duo_handle* h, duo_kv_cache* c, void* stream) {
   return ok();
 }
 
+// 4-bit caches: every array present for the head kinds the handle has, 16-byte
+// aligned; the row pitches are the capacities rounded up to 16 rows.
+static int64_t pitch16(int64_t rows) { return (rows + 15) / 16 * 16; }
+
+static duo_status check_kv4(const duo_handle* h, const duo_kv_cache* c, const duo_kv4_cache* kv) {
+  if (!kv) return fail(DUO_ERR_INVALID_ARG, "kv4 is NULL");
+  if (!c) return fail(DUO_ERR_INVALID_ARG, "cache is NULL");
+  if (c->n < 0) return fail(DUO_ERR_INVALID_ARG, "cache->n < 0");
+  if (h->sh.n_ret > 0) {
+    const void* a[] = {kv->k_codes, kv->v_codes, kv->k_sz, kv->v_sz};
+    for (const void* x : a)
+      if (!x || !aligned16(x)) return fail(DUO_ERR_INVALID_ARG, "retrieval 4-bit arrays NULL or not 16-byte aligned");
+  }
+  if (h->sh.n_str > 0) {
+    const void* a[] = {kv->ks_codes, kv->vs_codes, kv->ks_sz, kv->vs_sz};
+    for (const void* x : a)
+      if (!x || !aligned16(x)) return fail(DUO_ERR_INVALID_ARG, "streaming 4-bit arrays NULL or not 16-byte aligned");
+    if (!c->pos || !aligned16(c->pos)) return fail(DUO_ERR_INVALID_ARG, "pos NULL or not 16-byte aligned");
+  }
+  return DUO_OK;
+}
+
 static duo_status append_impl(duo_handle* h, duo_kv_cache* c, const duo_paged* pgd, const void* k_new,
-                              const void* v_new, int32_t T, void* stream) {
+                              const void* v_new, int32_t T, void* stream, const duo_kv4_cache* kv4 = nullptr) {
   duo_status st = check_handle(h);
   if (st != DUO_OK) return st;
   PagedLayout pg;
   if ((st = check_paged(h, pgd, &pg)) != DUO_OK) return st;
-  if ((st = check_cache(h, c, true, !pg.stream_table)) != DUO_OK) return st;
+  if (kv4) {
+    if ((st = check_kv4(h, c, kv4)) != DUO_OK) return st;
+  } else if ((st = check_cache(h, c, true, !pg.stream_table)) != DUO_OK) {
+    return st;
+  }
   if (T < 1) return fail(DUO_ERR_INVALID_ARG, "T = %d < 1", T);
   if (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new))
     return fail(DUO_ERR_INVALID_ARG, "k_new / v_new NULL or not 16-byte aligned");
@@ -325,7 +351,22 @@ static duo_status append_impl(duo_handle* h, duo_kv_cache* c, const duo_paged* p
   p.ring_cnt = e > r0 ? e - r0 : 0;
   p.sh = sh;
   p.heads = h->heads;
-  cudaError_t ce = launch_append(p, h->num_sms, (cudaStream_t)stream);
+  cudaError_t ce;
+  if (kv4) {
+    p.k4 = static_cast<uint8_t*>(kv4->k_codes);
+    p.v4 = static_cast<uint8_t*>(kv4->v_codes);
+    p.ks4 = static_cast<uint8_t*>(kv4->ks_codes);
+    p.vs4 = static_cast<uint8_t*>(kv4->vs_codes);
+    p.ksz = static_cast<uint32_t*>(kv4->k_sz);
+    p.vsz = static_cast<uint32_t*>(kv4->v_sz);
+    p.kssz = static_cast<uint32_t*>(kv4->ks_sz);
+    p.vssz = static_cast<uint32_t*>(kv4->vs_sz);
+    p.cap16 = pitch16(sh.cap);
+    p.sr16 = (int)pitch16((int64_t)sh.S + sh.R);
+    ce = launch_append_kv4(p, h->num_sms, (cudaStream_t)stream);
+  } else {
+    ce = launch_append(p, h->num_sms, (cudaStream_t)stream);
+  }
   if (ce != cudaSuccess) return cuda_fail(ce, "append launch");
   c->n += T;
   return ok();
@@ -433,6 +474,10 @@ static void decode_plan(const duo_handle* h, int64_t n, DecodeParams* p) {
   p->q_succ = p->q_inter = nullptr;  // not Dual Chunk Attention unless a caller sets chunk_len
   p->mscale = nullptr;
   p->chunk_len = 0;
+  p->k4 = p->v4 = p->ks4 = p->vs4 = nullptr;  // bf16 caches unless a caller sets 4-bit ones
+  p->ksz = p->vsz = p->kssz = p->vssz = nullptr;
+  p->cap16 = 0;
+  p->sr16 = 0;
   const int64_t SR = (int64_t)sh.S + sh.R;
   p->n = n;
   p->nvalid = (int)(n < SR ? n : SR);
@@ -476,9 +521,11 @@ static duo_status check_dca(const duo_handle* h, int32_t chunk_len, const float*
 }
 
 static duo_status decode_impl(duo_handle* h, const duo_kv_cache* c, const duo_paged* pgd, const void* q, void* o,
-                              void* workspace, size_t ws_bytes, void* stream, const DcaDecode* dca = nullptr) {
+                              void* workspace, size_t ws_bytes, void* stream, const DcaDecode* dca = nullptr,
+                              const duo_kv4_cache* kv4 = nullptr) {
   duo_status st = check_handle(h);
   if (st != DUO_OK) return st;
+  if (kv4 && (st = check_kv4(h, c, kv4)) != DUO_OK) return st;
   if (dca) {
     if ((st = check_dca(h, dca->chunk_len, dca->mscale)) != DUO_OK) return st;
     if (!dca->q_succ || !dca->q_inter || !aligned16(dca->q_succ) || !aligned16(dca->q_inter))
@@ -486,7 +533,7 @@ static duo_status decode_impl(duo_handle* h, const duo_kv_cache* c, const duo_pa
   }
   PagedLayout pg;
   if ((st = check_paged(h, pgd, &pg)) != DUO_OK) return st;
-  if ((st = check_cache(h, c, true, !pg.stream_table)) != DUO_OK) return st;
+  if (!kv4 && (st = check_cache(h, c, true, !pg.stream_table)) != DUO_OK) return st;
   if (c->n < 1) return fail(DUO_ERR_INVALID_ARG, "decode needs the query token appended first (cache->n >= 1)");
   if ((st = check_capacity(h, pg, c->n, DUO_ERR_INVALID_ARG)) != DUO_OK) return st;
   if (!q || !o || !aligned16(q) || !aligned16(o))
@@ -522,6 +569,18 @@ static duo_status decode_impl(duo_handle* h, const duo_kv_cache* c, const duo_pa
   p.sh = sh;
   p.heads = h->heads;
   p.pg = pg;
+  if (kv4) {
+    p.k4 = static_cast<const uint8_t*>(kv4->k_codes);
+    p.v4 = static_cast<const uint8_t*>(kv4->v_codes);
+    p.ks4 = static_cast<const uint8_t*>(kv4->ks_codes);
+    p.vs4 = static_cast<const uint8_t*>(kv4->vs_codes);
+    p.ksz = static_cast<const uint32_t*>(kv4->k_sz);
+    p.vsz = static_cast<const uint32_t*>(kv4->v_sz);
+    p.kssz = static_cast<const uint32_t*>(kv4->ks_sz);
+    p.vssz = static_cast<const uint32_t*>(kv4->vs_sz);
+    p.cap16 = pitch16(sh.cap);
+    p.sr16 = (int)pitch16((int64_t)sh.S + sh.R);
+  }
   if (dca) {
     p.q_succ = static_cast<const uint16_t*>(dca->q_succ);
     p.q_inter = static_cast<const uint16_t*>(dca->q_inter);
@@ -604,6 +663,18 @@ duo_status duo_dca_prefill(duo_handle* h, const void* q, const void* q_succ, con
   cudaError_t ce = launch_prefill(p, (cudaStream_t)stream);
   if (ce != cudaSuccess) return cuda_fail(ce, "DCA prefill launch");
   return ok();
+}
+
+duo_status duo_kv_append_kv4(duo_handle* h, duo_kv_cache* c, const duo_kv4_cache* kv4, const void* k_new,
+                             const void* v_new, int32_t T, void* stream) {
+  if (!kv4) return fail(DUO_ERR_INVALID_ARG, "kv4 is NULL");
+  return append_impl(h, c, nullptr, k_new, v_new, T, stream, kv4);
+}
+
+duo_status duo_attn_decode_kv4(duo_handle* h, const duo_kv_cache* c, const duo_kv4_cache* kv4, const void* q,
+                               void* o, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!kv4) return fail(DUO_ERR_INVALID_ARG, "kv4 is NULL");
+  return decode_impl(h, c, nullptr, q, o, workspace, workspace_bytes, stream, nullptr, kv4);
 }
 
 duo_status duo_dca_decode(duo_handle* h, const duo_kv_cache* c, const void* q, const void* q_succ,

@@ -84,8 +84,21 @@ struct AppendParams {
   Shape sh;
   HeadTable heads;
   PagedLayout pg;
+  // 4-bit caches (k4 != nullptr), laid out as in DecodeParams
+  uint8_t* k4;
+  uint8_t* v4;
+  uint8_t* ks4;
+  uint8_t* vs4;
+  uint32_t* ksz;
+  uint32_t* vsz;
+  uint32_t* kssz;
+  uint32_t* vssz;
+  int64_t cap16;
+  int sr16;
 };
 cudaError_t launch_append(const AppendParams& p, int num_sms, cudaStream_t stream);
+// 4-bit caches: quantizes and writes the rows the call keeps (same intervals).
+cudaError_t launch_append_kv4(const AppendParams& p, int num_sms, cudaStream_t stream);
 // One token per sequence at the position held in seq_lens[b] (device), which is
 // then advanced; T is 1 and n is unused.
 cudaError_t launch_append_varlen(const AppendParams& p, int32_t* seq_lens, cudaStream_t stream);
@@ -127,6 +140,19 @@ struct DecodeParams {
   const uint16_t* q_inter;
   const float* mscale;     // fp32 [B] or nullptr (1)
   int chunk_len;           // 0: not DCA; else a multiple of 256
+  // 4-bit caches (k4 != nullptr): codes u8 [planes, pitch, D/2] and per-row fp16
+  // (scale, zero) pairs u32 [planes, pitch]; pitch = cap16 for retrieval planes
+  // (B * n_ret), sr16 for ring planes (B * n_str), both multiples of 16
+  const uint8_t* k4;
+  const uint8_t* v4;
+  const uint8_t* ks4;
+  const uint8_t* vs4;
+  const uint32_t* ksz;
+  const uint32_t* vsz;
+  const uint32_t* kssz;
+  const uint32_t* vssz;
+  int64_t cap16;
+  int sr16;
 };
 size_t decode_workspace_bytes(const Shape& sh, int num_ctas);
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream);

@@ -52,6 +52,15 @@ def decode_bytes(B, Hq, Hkv, D, S, R, is_retrieval, n):
     return B * n_ret * n * row, B * n_str * min(n, S + R) * (row + 4), 2 * B * Hq * D * 2
 
 
+def decode_bytes_kv4(B, Hq, Hkv, D, S, R, is_retrieval, n):
+    """decode_bytes for 4-bit caches: a K or V row is D / 2 bytes of codes plus a
+    4-byte (scale, zero) pair."""
+    n_ret = sum(1 for x in is_retrieval if x)
+    n_str = Hkv - n_ret
+    row = 2 * (D // 2 + 4)
+    return B * n_ret * n * row, B * n_str * min(n, S + R) * (row + 4), 2 * B * Hq * D * 2
+
+
 def append_bytes(B, Hkv, D, S, R, is_retrieval, n, T):
     """Bytes read plus written by one append of T tokens after n stored ones."""
     n_ret = sum(1 for x in is_retrieval if x)

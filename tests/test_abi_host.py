@@ -21,7 +21,7 @@ def lib():
 def _declared_functions():
     text = open(os.path.join(ROOT, "include", "duo_attn.h")).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(duo_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(duo_[a-z_0-9]+)\s*\(", text)))
 
 
 def test_every_declared_function_is_exported(lib):
