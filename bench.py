@@ -48,10 +48,10 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 L2_BYTES = 129e6  # GB300 L2 capacity
 
 MEASURED_TRAFFIC = {
-    "prefill": {"src": ("prefill.cu", "duo_device.cuh", "duo_internal.h"), "sha1": "7c856ada46c1f9c3",
-                "bytes": 573.733888e6 + 231.971328e6},
-    "decode": {"src": ("decode.cu", "duo_device.cuh", "duo_internal.h"), "sha1": "628f17d75ffd331f",
-               "bytes": 1.074878e9 + 3.413504e6},
+    "prefill": {"src": ("prefill.cu", "duo_device.cuh", "duo_internal.h"), "sha1": "4c47b1ff38f5bc76",
+                "bytes": 572.764160e6 + 232.516864e6},
+    "decode": {"src": ("decode.cu", "duo_device.cuh", "duo_internal.h"), "sha1": "b797d77f75ed0bf9",
+               "bytes": 1.074980e9 + 3.506944e6},
 }
 
 

@@ -243,6 +243,9 @@ WORKLOADS = {
     # attention), 131072-token prompt in chunks of 32768, then decode steps
     "qwen2_72b_dca_prefill128k": Workload("qwen2_72b_dca_prefill128k", 6, 1, 64, 8, 128, 0, 1, 8,
                                           prefill_len=131072, decode_steps=16, dca_chunk=32768),
+    # the same layer at 32768 tokens in chunks of 8192 (a size ncu can capture in full)
+    "qwen2_72b_dca_prefill32k": Workload("qwen2_72b_dca_prefill32k", 7, 1, 64, 8, 128, 0, 1, 8,
+                                         prefill_len=32768, decode_steps=16, dca_chunk=8192),
 }
 
 
