@@ -832,7 +832,7 @@ cudaError_t launch_v(const DecodeParams& p, cudaStream_t stream) {
 // bookkeeping costs the contiguous kernel nothing
 template <int D, int G>
 cudaError_t launch_t(const DecodeParams& p, cudaStream_t stream) {
-  if (p.k4) return launch_v<D, G, kModeKv4>(p, stream);
+  if (p.kv4) return launch_v<D, G, kModeKv4>(p, stream);
   if (p.chunk_len > 0) return launch_v<D, G, kModeDca>(p, stream);
   if (p.pg.stream_table) return launch_v<D, G, kModePool>(p, stream);
   return p.pg.table ? launch_v<D, G, kModePaged>(p, stream) : launch_v<D, G, kModePlain>(p, stream);

@@ -478,6 +478,7 @@ static void decode_plan(const duo_handle* h, int64_t n, DecodeParams* p) {
   p->ksz = p->vsz = p->kssz = p->vssz = nullptr;
   p->cap16 = 0;
   p->sr16 = 0;
+  p->kv4 = 0;
   const int64_t SR = (int64_t)sh.S + sh.R;
   p->n = n;
   p->nvalid = (int)(n < SR ? n : SR);
@@ -580,6 +581,7 @@ static duo_status decode_impl(duo_handle* h, const duo_kv_cache* c, const duo_pa
     p.vssz = static_cast<const uint32_t*>(kv4->vs_sz);
     p.cap16 = pitch16(sh.cap);
     p.sr16 = (int)pitch16((int64_t)sh.S + sh.R);
+    p.kv4 = 1;
   }
   if (dca) {
     p.q_succ = static_cast<const uint16_t*>(dca->q_succ);

@@ -153,6 +153,7 @@ struct DecodeParams {
   const uint32_t* vssz;
   int64_t cap16;
   int sr16;
+  int kv4;  // 4-bit caches (the retrieval arrays are null when there is no retrieval head)
 };
 size_t decode_workspace_bytes(const Shape& sh, int num_ctas);
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream);

@@ -50,6 +50,7 @@ CASES = [
     (1, 32, 8, 128, 64, 256, [1, 0, 0, 0, 0, 0, 1, 0], 3000, 2, 1024),
     (1, 16, 2, 128, 8, 40, [0, 1], 1000, 2, None),              # GQA 8
     (2, 2, 2, 128, 3, 5, [1, 1], 5, 4, None),                   # all retrieval, tiny context
+    (1, 16, 2, 128, 35, 115, [0, 0], 600, 2, 250),              # no retrieval head at all
 ]
 
 
