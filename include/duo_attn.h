@@ -107,6 +107,14 @@ duo_status duo_classify_heads(const uint8_t* is_retrieval, int32_t num_kv_heads,
 duo_status duo_create(const duo_config* config, const uint8_t* is_retrieval, duo_handle** out);
 void duo_destroy(duo_handle* handle);
 
+/* Re-classify the KV heads of an existing handle (host array of num_kv_heads flags,
+ * copied), e.g. after loading another head pattern. The caches are laid out by kind
+ * ([B, n_ret, ...] and [B, n_str, ...]), so the caller must re-lay them out (or reset
+ * and refill them) for the new counts before the next call that uses them; the shape
+ * of the handle is otherwise unchanged. The DuoAttention README's patch applies a
+ * loaded head pattern the same way: one mask per layer. */
+duo_status duo_set_head_mask(duo_handle* handle, const uint8_t* is_retrieval);
+
 /* Empty the cache: pos[] := -1 on `stream`, cache->n := 0. */
 duo_status duo_cache_reset(duo_handle* handle, duo_kv_cache* cache, void* stream);
 

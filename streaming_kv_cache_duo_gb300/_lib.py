@@ -28,7 +28,7 @@ DUO_RETRIEVAL = 1
 
 # exported names of include/duo_attn.h (checked against the library by the tests)
 EXPORTS = (
-    "duo_classify_heads", "duo_create", "duo_destroy", "duo_cache_reset", "duo_kv_append",
+    "duo_classify_heads", "duo_create", "duo_destroy", "duo_set_head_mask", "duo_cache_reset", "duo_kv_append",
     "duo_attn_prefill", "duo_attn_prefill_select", "duo_decode_workspace_size", "duo_attn_decode",
     "duo_attn_decode_static", "duo_kv_append_paged", "duo_attn_prefill_paged", "duo_attn_decode_paged",
     "duo_paged_stream_dead_blocks", "duo_dca_prefill", "duo_dca_decode", "duo_kv_append_kv4",
@@ -81,6 +81,7 @@ def library() -> ctypes.CDLL:
         "duo_classify_heads": (c_int32, [POINTER(c_uint8), c_int32, POINTER(c_int32), POINTER(c_int32)]),
         "duo_create": (c_int32, [POINTER(duo_config), POINTER(c_uint8), POINTER(c_void_p)]),
         "duo_destroy": (None, [c_void_p]),
+        "duo_set_head_mask": (c_int32, [c_void_p, POINTER(c_uint8)]),
         "duo_cache_reset": (c_int32, [c_void_p, POINTER(duo_kv_cache), c_void_p]),
         "duo_kv_append": (c_int32, [c_void_p, POINTER(duo_kv_cache), c_void_p, c_void_p, c_int32, c_void_p]),
         "duo_attn_prefill": (c_int32, [c_void_p, POINTER(duo_kv_cache), c_void_p, c_void_p, c_void_p, c_int32,
@@ -175,6 +176,11 @@ def duo_create(batch, num_q_heads, num_kv_heads, head_dim, sink_size, recent_siz
 
 def duo_destroy(handle) -> None:
     library().duo_destroy(handle)
+
+
+def duo_set_head_mask(handle, is_retrieval) -> None:
+    mask = (c_uint8 * len(is_retrieval))(*[1 if x else 0 for x in is_retrieval])
+    _check(library().duo_set_head_mask(handle, mask))
 
 
 def duo_cache_reset(handle, cache: "duo_kv_cache", stream=None) -> None:

@@ -196,6 +196,34 @@ duo_status duo_classify_heads(const uint8_t* is_retrieval, int32_t num_kv_heads,
   return ok();
 }
 
+// Head table and shape of a handle for a per-KV-head retrieval mask.
+static void set_heads(duo_handle* h, const uint8_t* is_retrieval) {
+  const duo_config& c = h->cfg;
+  int nr = 0, ns = 0;
+  for (int k = 0; k < c.num_kv_heads; ++k) {
+    if (is_retrieval[k]) {
+      h->heads.ret_head[nr] = (uint8_t)k;
+      h->heads.kind[k] = DUO_RETRIEVAL;
+      h->heads.kidx[k] = (uint8_t)nr++;
+    } else {
+      h->heads.str_head[ns] = (uint8_t)k;
+      h->heads.kind[k] = DUO_STREAMING;
+      h->heads.kidx[k] = (uint8_t)ns++;
+    }
+  }
+  h->sh = Shape{c.batch, c.num_q_heads, c.num_kv_heads, c.head_dim, c.sink_size, c.recent_size,
+                c.num_q_heads / c.num_kv_heads, nr, ns, c.max_seq_len};
+}
+
+duo_status duo_set_head_mask(duo_handle* h, const uint8_t* is_retrieval) {
+  duo_status st = check_handle(h);
+  if (st != DUO_OK) return st;
+  if (!is_retrieval) return fail(DUO_ERR_INVALID_ARG, "is_retrieval is NULL");
+  set_heads(h, is_retrieval);
+  h->workspace_dirty = true;  // the number of units may have changed
+  return ok();
+}
+
 duo_status duo_create(const duo_config* cfg, const uint8_t* is_retrieval, duo_handle** out) {
   if (!cfg || !is_retrieval || !out) return fail(DUO_ERR_INVALID_ARG, "NULL argument");
   *out = nullptr;
@@ -221,20 +249,7 @@ duo_status duo_create(const duo_config* cfg, const uint8_t* is_retrieval, duo_ha
   duo_handle* h = new (std::nothrow) duo_handle();
   if (!h) return fail(DUO_ERR_INVALID_ARG, "out of host memory");
   h->cfg = c;
-  int nr = 0, ns = 0;
-  for (int k = 0; k < c.num_kv_heads; ++k) {
-    if (is_retrieval[k]) {
-      h->heads.ret_head[nr] = (uint8_t)k;
-      h->heads.kind[k] = DUO_RETRIEVAL;
-      h->heads.kidx[k] = (uint8_t)nr++;
-    } else {
-      h->heads.str_head[ns] = (uint8_t)k;
-      h->heads.kind[k] = DUO_STREAMING;
-      h->heads.kidx[k] = (uint8_t)ns++;
-    }
-  }
-  h->sh = Shape{c.batch, c.num_q_heads, c.num_kv_heads, c.head_dim, c.sink_size, c.recent_size, g, nr, ns,
-                c.max_seq_len};
+  set_heads(h, is_retrieval);
   h->last_workspace = nullptr;
   h->workspace_dirty = true;
   h->epoch = g_error_epoch.load();

@@ -90,3 +90,8 @@ def test_paged_stream_dead_blocks_match_the_oracle(lib):
 def test_paged_stream_dead_blocks_rejects_bad_arguments(lib, args, status):
     with pytest.raises(lib.DuoError, match=status):
         lib.duo_paged_stream_dead_blocks(*args)
+
+
+def test_set_head_mask_rejects_a_null_handle(lib):
+    with pytest.raises(lib.DuoError, match="DUO_ERR_INVALID_ARG"):
+        lib.duo_set_head_mask(None, [1, 0])
