@@ -278,12 +278,15 @@ duo_status duo_attn_decode_kv4(duo_handle* handle, const duo_kv_cache* cache, co
  * of 256 (DUO_ERR_UNSUPPORTED otherwise) so that chunk boundaries fall on the
  * kernels' 256-row query blocks and 128-key tiles.
  *
- * duo_dca_prefill: one-shot prefill of T tokens at positions 0 ... T-1 (no cache).
- * q, q_succ, q_inter: bf16 [B, T, Hq, D]; k, v: bf16 [B, T, Hkv, D]; mscale: fp32
- * [B, T] device memory or NULL; o: bf16 [B, T, Hq, D]; all device, 16-byte aligned.
- * Append k and v with duo_kv_append to decode afterwards. */
-duo_status duo_dca_prefill(duo_handle* handle, const void* q, const void* q_succ, const void* q_inter, const void* k,
-                           const void* v, const float* mscale, int32_t T, int32_t chunk_len, void* o, void* stream);
+ * duo_dca_prefill: prefill of T tokens at positions n ... n+T-1 against the cache as it
+ * is before them (cache NULL or cache->n = 0: one-shot; else a chunk of a chunked
+ * prefill, cache->n a multiple of 256, keys of rows [0, n) read from cache->k_full /
+ * v_full). q, q_succ, q_inter: bf16 [B, T, Hq, D]; k, v: bf16 [B, T, Hkv, D]; mscale:
+ * fp32 [B, T] (the chunk's positions) device memory or NULL; o: bf16 [B, T, Hq, D];
+ * all device, 16-byte aligned. Append k and v with duo_kv_append afterwards. */
+duo_status duo_dca_prefill(duo_handle* handle, const duo_kv_cache* cache, const void* q, const void* q_succ,
+                           const void* q_inter, const void* k, const void* v, const float* mscale, int32_t T,
+                           int32_t chunk_len, void* o, void* stream);
 
 /* duo_dca_decode: one decode step at position cache->n - 1 (the token appended first)
  * over the retrieval caches. q, q_succ, q_inter: bf16 [B, Hq, D]; mscale: fp32 [B] or

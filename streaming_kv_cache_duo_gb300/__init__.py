@@ -86,8 +86,9 @@ class DuoLayer:
         return out
 
     def dca_prefill(self, q, q_succ, q_inter, k, v, chunk_len, mscale=None, out=None, stream=None):
-        """Dual Chunk Attention prefill of T tokens at positions 0 ... T-1 (every head full
-        attention); mscale: fp32 [B, T] on the device or None."""
+        """Dual Chunk Attention prefill of T tokens at positions n ... n+T-1 against the cache
+        (n = tokens appended so far, a multiple of 256; every head full attention); mscale:
+        fp32 [B, T] on the device or None."""
         import torch
         T = q.shape[1]
         for name, t in (("q", q), ("q_succ", q_succ), ("q_inter", q_inter)):
@@ -98,7 +99,7 @@ class DuoLayer:
         if out is None:
             out = torch.empty_like(q)
         _lib._bf16(out, (self.B, T, self.Hq, self.D), "o")
-        _lib.duo_dca_prefill(self.handle, q, q_succ, q_inter, k, v, mscale, T, chunk_len, out, stream)
+        _lib.duo_dca_prefill(self.handle, self.cache, q, q_succ, q_inter, k, v, mscale, T, chunk_len, out, stream)
         return out
 
     def dca_decode(self, q, q_succ, q_inter, chunk_len, mscale=None, out=None, stream=None):

@@ -104,8 +104,8 @@ def library() -> ctypes.CDLL:
                                         c_int32, c_void_p]),
         "duo_attn_decode_kv4": (c_int32, [c_void_p, POINTER(duo_kv_cache), POINTER(duo_kv4_cache), c_void_p,
                                           c_void_p, c_void_p, c_size_t, c_void_p]),
-        "duo_dca_prefill": (c_int32, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int32,
-                                      c_int32, c_void_p, c_void_p]),
+        "duo_dca_prefill": (c_int32, [c_void_p, POINTER(duo_kv_cache), c_void_p, c_void_p, c_void_p, c_void_p,
+                                      c_void_p, c_void_p, c_int32, c_int32, c_void_p, c_void_p]),
         "duo_dca_decode": (c_int32, [c_void_p, POINTER(duo_kv_cache), c_void_p, c_void_p, c_void_p, c_void_p,
                                      c_int32, c_void_p, c_void_p, c_size_t, c_void_p]),
         "duo_kv_append_varlen": (c_int32, [c_void_p, POINTER(duo_kv_cache), c_void_p, c_void_p, c_void_p,
@@ -248,9 +248,11 @@ def duo_attn_decode_kv4(handle, cache: "duo_kv_cache", kv4: "duo_kv4_cache", q, 
                                          _ptr(workspace), nbytes, _stream_ptr(stream)))
 
 
-def duo_dca_prefill(handle, q, q_succ, q_inter, k, v, mscale, T: int, chunk_len: int, o, stream=None) -> None:
-    _check(library().duo_dca_prefill(handle, _ptr(q), _ptr(q_succ), _ptr(q_inter), _ptr(k), _ptr(v), _ptr(mscale), T,
-                                     chunk_len, _ptr(o), _stream_ptr(stream)))
+def duo_dca_prefill(handle, cache, q, q_succ, q_inter, k, v, mscale, T: int, chunk_len: int, o,
+                    stream=None) -> None:
+    _check(library().duo_dca_prefill(handle, None if cache is None else ctypes.byref(cache), _ptr(q), _ptr(q_succ),
+                                     _ptr(q_inter), _ptr(k), _ptr(v), _ptr(mscale), T, chunk_len, _ptr(o),
+                                     _stream_ptr(stream)))
 
 
 def duo_dca_decode(handle, cache: "duo_kv_cache", q, q_succ, q_inter, mscale, chunk_len: int, o, workspace,

@@ -647,12 +647,21 @@ duo_status duo_paged_stream_dead_blocks(int32_t sink_size, int32_t recent_size, 
   return ok();
 }
 
-duo_status duo_dca_prefill(duo_handle* h, const void* q, const void* q_succ, const void* q_inter, const void* k,
-                           const void* v, const float* mscale, int32_t T, int32_t chunk_len, void* o, void* stream) {
+duo_status duo_dca_prefill(duo_handle* h, const duo_kv_cache* c, const void* q, const void* q_succ,
+                           const void* q_inter, const void* k, const void* v, const float* mscale, int32_t T,
+                           int32_t chunk_len, void* o, void* stream) {
   duo_status st = check_handle(h);
   if (st != DUO_OK) return st;
   if ((st = check_dca(h, chunk_len, mscale)) != DUO_OK) return st;
   if (T < 1) return fail(DUO_ERR_INVALID_ARG, "T = %d < 1", T);
+  const int64_t n = c ? c->n : 0;
+  if (n > 0) {
+    if ((st = check_cache(h, c, true, false)) != DUO_OK) return st;
+    if (n % kPrefillRowsPerCta != 0)
+      return fail(DUO_ERR_UNSUPPORTED, "cache->n = %lld is not a multiple of %d", (long long)n, kPrefillRowsPerCta);
+    if (n > h->sh.cap) return fail(DUO_ERR_INVALID_ARG, "cache->n exceeds the retrieval capacity");
+  }
+  if (n + T > 0x7fffffffLL) return fail(DUO_ERR_INVALID_ARG, "positions would reach 2^31");
   const void* ptrs[] = {q, q_succ, q_inter, k, v, o};
   for (const void* ptr : ptrs)
     if (!ptr || !aligned16(ptr)) return fail(DUO_ERR_INVALID_ARG, "q / q_succ / q_inter / k / v / o NULL or not 16-byte aligned");
@@ -664,8 +673,12 @@ duo_status duo_dca_prefill(duo_handle* h, const void* q, const void* q_succ, con
   if ((st = encode_tokens(h, &p.tm_qi, q_inter, sh.B, T, sh.Hq, sh.D)) != DUO_OK) return st;
   if ((st = encode_tokens(h, &p.tm_k, k, sh.B, T, sh.Hkv, sh.D)) != DUO_OK) return st;
   if ((st = encode_tokens(h, &p.tm_v, v, sh.B, T, sh.Hkv, sh.D)) != DUO_OK) return st;
+  if (n > 0) {
+    if ((st = encode_cache(h, &p.tm_kfull, c->k_full, (int64_t)sh.B * sh.n_ret, sh.cap, n, sh.D)) != DUO_OK) return st;
+    if ((st = encode_cache(h, &p.tm_vfull, c->v_full, (int64_t)sh.B * sh.n_ret, sh.cap, n, sh.D)) != DUO_OK) return st;
+  }
   p.o = static_cast<uint16_t*>(o);
-  p.n = 0;
+  p.n = n;
   p.T = T;
   p.num_qt = (T + kPrefillRowsPerCta - 1) / kPrefillRowsPerCta;
   const int64_t items = (int64_t)sh.B * sh.g * p.num_qt * sh.n_ret;

@@ -106,3 +106,42 @@ def test_dca_argument_checks():
         full.dca_prefill(Q, QS, QI, K, V, 384)
     with pytest.raises(DuoError, match="DUO_ERR_UNSUPPORTED"):
         full.dca_prefill(Q, QS, QI, K, V, 128)
+
+
+@pytest.mark.parametrize("chunks,chunk_len", [([512, 768, 300], 256), ([1024, 256, 517], 512)])
+def test_dca_chunked_prefill_matches_oracle(chunks, chunk_len):
+    """Dual Chunk Attention prefill chunk by chunk against the growing cache (the pull
+    request's demo runs with chunked prefill): every chunk's rows equal the one-shot
+    definition at their absolute positions."""
+    from streaming_kv_cache_duo_gb300 import DuoLayer, duo_device_error
+    B, Hq, Hkv, D = 1, 8, 2, 128
+    total = sum(chunks)
+    seed = 901
+    Q, QS, QI, K, V = _inputs(seed, B, Hq, Hkv, D, total)
+    Qh, QSh, QIh, Kh, Vh = _inputs(seed, B, Hq, Hkv, D, total, dev=False)
+    ms = ds.dca_mscale(B, total, chunk_len)
+    msd = torch.from_numpy(ms).cuda()
+    layer = DuoLayer(B, Hq, Hkv, D, 0, 1, total, [1] * Hkv)
+    t = 0
+    for T in chunks:
+        sl = slice(t, t + T)
+        o = layer.dca_prefill(*(x[:, sl].contiguous() for x in (Q, QS, QI, K, V)), chunk_len,
+                              mscale=msd[:, sl].contiguous())
+        torch.cuda.synchronize()
+        assert duo_device_error() == 0
+        rows = np.array(sorted({0, 1, T // 2, T - 2, T - 1} | {r for r in range(0, T, 97)}))
+        ref = dca.attention(Qh[0, :t + T], QSh[0, :t + T], QIh[0, :t + T], Kh[0, :t + T], Vh[0, :t + T],
+                            ms[0, :t + T], chunk_len, rows=rows + t)
+        assert_close(to_np(o)[0, rows], ref, f"chunk at {t}")
+        layer.append(K[:, sl].contiguous(), V[:, sl].contiguous())
+        t += T
+
+
+def test_dca_chunked_prefill_needs_an_aligned_cache():
+    from streaming_kv_cache_duo_gb300 import DuoError, DuoLayer
+    Q, QS, QI, K, V = _inputs(3, 1, 2, 2, 64, 400)
+    layer = DuoLayer(1, 2, 2, 64, 0, 1, 400, [1, 1])
+    layer.append(K[:, :100].contiguous(), V[:, :100].contiguous())
+    sl = slice(100, 400)
+    with pytest.raises(DuoError, match="DUO_ERR_UNSUPPORTED"):
+        layer.dca_prefill(*(x[:, sl].contiguous() for x in (Q, QS, QI, K, V)), 256)
