@@ -3,8 +3,9 @@
 This module holds no attention, mask or cache arithmetic. It defines one
 counter-based generator, so that any element of any input stream can be
 regenerated on its own (the CPU oracle regenerates only the tokens it needs,
-for example the keys of one head of a million-token context), plus the five
-workload shapes and the seeded retrieval/streaming head choice.
+for example the keys of one head of a million-token context), plus the
+workload shapes (five mixed-head, two Dual Chunk Attention) and the seeded
+retrieval/streaming head choice.
 
 Generator definition (one value per element, no state carried between elements):
 
@@ -202,7 +203,7 @@ def retrieval_mask(seed: int, H_kv: int, n_retrieval: int, fixed=None) -> list:
 
 @dataclass(frozen=True)
 class Workload:
-    """One of the five synthetic workloads (shapes, head kinds, schedule)."""
+    """One synthetic workload (shapes, head kinds, schedule)."""
     name: str
     seed: int
     B: int

@@ -185,8 +185,9 @@ struct PrefillParams {
   Shape sh;
   HeadTable heads;
   PagedLayout pg;
-  // Dual Chunk Attention (chunk_len > 0; every head full attention, no cache): the
-  // query vectors for keys one chunk back and further back, and a per-position scale
+  // Dual Chunk Attention (chunk_len > 0; every head full attention; cache length n a
+  // multiple of 256): the query vectors for keys one chunk back and further back, and a
+  // per-position scale
   CUtensorMap tm_qs;     // 4-D over q_succ [B, T, Hq, D], as tm_q
   CUtensorMap tm_qi;     // 4-D over q_inter [B, T, Hq, D]
   const float* mscale;   // fp32 [B, T] or nullptr (1)

@@ -145,3 +145,100 @@ def test_dca_chunked_prefill_needs_an_aligned_cache():
     sl = slice(100, 400)
     with pytest.raises(DuoError, match="DUO_ERR_UNSUPPORTED"):
         layer.dca_prefill(*(x[:, sl].contiguous() for x in (Q, QS, QI, K, V)), 256)
+
+
+def _row_ref(q, qs, qi, K, V, ms_i, i, chunk_len):
+    """Oracle prefill row i of one query head: the three query vectors broadcast to [i + 1,
+    1, D] views (only row i is read), the head's keys and values [i + 1, 1, D]."""
+    D = q.shape[-1]
+    Q3 = [np.broadcast_to(np.asarray(x, np.float64), (i + 1, 1, D)) for x in (q, qs, qi)]
+    ms = np.full(i + 1, ms_i, np.float64)
+    return dca.attention(*Q3, K[:i + 1, None], V[:i + 1, None], ms, chunk_len, rows=[i], heads=[0])[0, 0]
+
+
+def _check_rows(w, o, rows, heads, pos0, ms, keys):
+    """Sampled rows (absolute positions) of the output o [B, T, Hq, D] of a call that
+    started at position pos0, for the given query heads."""
+    g = w.Hq // w.Hkv
+    got = to_np(o[0, [r - pos0 for r in rows]][:, heads])
+    ref = np.empty_like(got)
+    for a, i in enumerate(rows):
+        q, qs, qi = (host_stream(w.seed, s, 1, i, 1, w.Hq, w.D)[0, 0]
+                     for s in (ds.STREAM_Q, ds.STREAM_Q_SUCC, ds.STREAM_Q_INTER))
+        for c, h in enumerate(heads):
+            K, V = keys[h // g]
+            ref[a, c] = _row_ref(q[h], qs[h], qi[h], K, V, ms[0, i], i, w.dca_chunk)
+    assert_close(got, ref, f"{w.name} rows {rows} heads {heads}")
+
+
+def test_full_size_dca_prefill128k_and_decode_sampled():
+    """The 131072-token Qwen2-72B-shaped layer (64 query / 8 KV heads, chunk 32768) in the
+    benchmark's launch: one-shot prefill, then the prompt appended and decode steps from
+    position 131072 (the first token of a new chunk); sampled rows at every chunk
+    boundary and sampled heads of three KV heads against the oracle."""
+    from streaming_kv_cache_duo_gb300 import DuoLayer, duo_device_error
+    from gpu_util import head_keys
+    w = ds.WORKLOADS["qwen2_72b_dca_prefill128k"]
+    L, CL, steps = w.prefill_len, w.dca_chunk, 2
+    total = L + steps
+    gen = lambda s, pos0, T, H: device_stream(w.seed, s, 1, pos0, T, H, w.D, "cuda")
+    q, qs, qi = (gen(s, 0, L, w.Hq) for s in (ds.STREAM_Q, ds.STREAM_Q_SUCC, ds.STREAM_Q_INTER))
+    k, v = gen(ds.STREAM_K, 0, L, w.Hkv), gen(ds.STREAM_V, 0, L, w.Hkv)
+    ms = ds.dca_mscale(1, total, CL)
+    msd = torch.from_numpy(ms).cuda()
+    layer = DuoLayer(1, w.Hq, w.Hkv, w.D, w.S, w.R, total, [1] * w.Hkv)
+    o = layer.dca_prefill(q, qs, qi, k, v, CL, mscale=msd[:, :L].contiguous())
+    torch.cuda.synchronize()
+    assert duo_device_error() == 0
+    del q, qs, qi
+    heads = [0, 37, 63]
+    g = w.Hq // w.Hkv
+    keys = {h // g: head_keys(w.seed, 0, h // g, 0, total, w.D) for h in heads + [5]}
+    rng = np.random.default_rng(6)
+    rows = sorted({0, 255, 256, L - 2, L - 1} | {c + d for c in range(CL, L, CL) for d in (-1, 0)}
+                  | set(rng.integers(0, L, 3).tolist()))
+    _check_rows(w, o, rows, heads, 0, ms, keys)
+    del o
+    layer.append(k, v)
+    for s in range(steps):
+        p = L + s
+        layer.append(gen(ds.STREAM_K, p, 1, w.Hkv), gen(ds.STREAM_V, p, 1, w.Hkv))
+        qd = [gen(x, p, 1, w.Hq)[:, 0].contiguous() for x in (ds.STREAM_Q, ds.STREAM_Q_SUCC, ds.STREAM_Q_INTER)]
+        od = layer.dca_decode(*qd, CL, mscale=msd[:, p].contiguous())
+        torch.cuda.synchronize()
+        assert duo_device_error() == 0
+    p = total - 1
+    qh = [host_stream(w.seed, x, 1, p, 1, w.Hq, w.D)[0, 0] for x in (ds.STREAM_Q, ds.STREAM_Q_SUCC, ds.STREAM_Q_INTER)]
+    dh = [5, 63]
+    ref = np.stack([dca.decode(qh[0][h], qh[1][h], qh[2][h], keys[h // g][0][:p + 1], keys[h // g][1][:p + 1],
+                               ms[0, p], p, CL) for h in dh])
+    assert_close(to_np(od[0, dh]), ref, "decode at 131073")
+
+
+def test_full_size_dca_prefill32k_chunked_sampled():
+    """The 32768-token layer (chunk 8192) prefilled in calls of 12288, 12288 and 8192
+    tokens against the growing cache, so that calls start and end inside DCA chunks;
+    sampled rows of each call against the one-shot definition."""
+    from streaming_kv_cache_duo_gb300 import DuoLayer, duo_device_error
+    from gpu_util import head_keys
+    w = ds.WORKLOADS["qwen2_72b_dca_prefill32k"]
+    L, CL = w.prefill_len, w.dca_chunk
+    gen = lambda s, pos0, T, H: device_stream(w.seed, s, 1, pos0, T, H, w.D, "cuda")
+    ms = ds.dca_mscale(1, L, CL)
+    msd = torch.from_numpy(ms).cuda()
+    layer = DuoLayer(1, w.Hq, w.Hkv, w.D, w.S, w.R, L, [1] * w.Hkv)
+    heads = [3, 30, 60]
+    g = w.Hq // w.Hkv
+    keys = {h // g: head_keys(w.seed, 0, h // g, 0, L, w.D) for h in heads}
+    t = 0
+    for T in (12288, 12288, 8192):
+        q, qs, qi = (gen(s, t, T, w.Hq) for s in (ds.STREAM_Q, ds.STREAM_Q_SUCC, ds.STREAM_Q_INTER))
+        k, v = gen(ds.STREAM_K, t, T, w.Hkv), gen(ds.STREAM_V, t, T, w.Hkv)
+        o = layer.dca_prefill(q, qs, qi, k, v, CL, mscale=msd[:, t:t + T].contiguous())
+        torch.cuda.synchronize()
+        assert duo_device_error() == 0
+        rows = sorted(r for r in {t, t + 1, t + T - 1} | {c + d for c in range(CL, L, CL) for d in (-1, 0)}
+                      if t <= r < t + T)
+        _check_rows(w, o, rows, heads, t, ms, keys)
+        layer.append(k, v)
+        t += T
