@@ -147,7 +147,9 @@ duo_status duo_attn_prefill(duo_handle* handle, const duo_kv_cache* cache, const
 duo_status duo_attn_prefill_select(duo_handle* handle, const duo_kv_cache* cache, const void* q, const void* k,
                                    const void* v, int32_t T, void* o, int32_t kind_mask, void* stream);
 
-/* Bytes of device workspace duo_attn_decode needs for a cache of n tokens. */
+/* Bytes of device workspace the decode entry points (duo_attn_decode, _paged, _varlen,
+ * duo_dca_decode, duo_attn_decode_kv4) need for a cache of n tokens; the size covers
+ * the largest grid any of them launches, so one workspace serves them all. */
 size_t duo_decode_workspace_size(const duo_handle* handle, int64_t n);
 
 /* One decode step for the token at position p = cache->n - 1, which must already have
@@ -169,8 +171,9 @@ duo_status duo_attn_decode(duo_handle* handle, const duo_kv_cache* cache, const 
  * a runtime whose allocator owns every allocation). The pages have no counterpart:
  * it is an interface variant of the decode step above and computes the same result.
  * Scratch lives in a 2 MiB array inside the library (every GPU that loads the library
- * holds it until the process exits); shapes whose scratch
- * (duo_decode_workspace_size) exceeds 2 MiB get DUO_ERR_WORKSPACE. Nothing is
+ * holds it until the process exits); shapes whose bf16 decode scratch (one partial
+ * of g (D + 4) floats per CTA and per (sequence, KV head), with one CTA per SM, plus
+ * the counters) exceeds 2 MiB get DUO_ERR_WORKSPACE. Nothing is
  * allocated: no cudaMalloc, cudaFree or allocating library call. The first call on
  * each device looks up the array's device address (cudaGetSymbolAddress); make that
  * first call before any stream capture. Each call clears the array's counters with

@@ -28,7 +28,10 @@
 // step a plain add). The softmax then runs once per (key, head), the online
 // state (running max with lazy rescaling: it moves only when a score exceeds it
 // by 2^8, and running sum) is per lane for its head, and p of the other heads is
-// fetched by shuffles for the packed p.v FMAs.
+// fetched by shuffles for the packed p.v FMAs. With eight query heads per KV head,
+// and for 4-bit caches, a warp's slice is instead two warp-level tensor-core MMAs
+// (S = Q K^T, then O^T += V^T P^T; see MmaSlice), which takes the per-element FMAs
+// off the CUDA cores that bound those cases.
 //
 // Merge. The part of a unit a CTA covers ("segment") ends with a cross-warp merge
 // in shared memory. A unit covered by one CTA is written out directly; otherwise
@@ -37,6 +40,8 @@
 //     O = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s,
 // the merge the vLLM Dual Chunk Attention pull request applies to its partial
 // softmax outputs.
+#include <type_traits>
+
 #include "duo_device.cuh"
 
 namespace duo {
@@ -49,6 +54,9 @@ constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
 constexpr int kKPW = kTK / kWarps;  // keys of a tile per warp
 constexpr int kNSW = 3;             // pipeline stages per warp
+// query heads per KV head from which bf16 decode runs its slices on the tensor cores
+// (4-bit caches always do)
+constexpr int kMmaMinG = 4;
 
 constexpr int ilog2(int v) { return v <= 1 ? 0 : 1 + ilog2(v / 2); }
 
@@ -72,8 +80,9 @@ struct Cfg {
   static constexpr int KPI = 32 / LPK;                 // keys per warp iteration
   static constexpr int IT = kKPW / KPI;                // iterations per tile
   static constexpr int CH = DPL / 8;                   // 16-byte chunks per lane
-  // 4-bit rows are a quarter of the bytes, so the per-warp ring is deeper
-  static constexpr int NSW = KV4 ? 8 : kNSW;           // pipeline stages per warp
+  // 4-bit rows are a quarter of the bytes: a ring as deep as the bf16 one in bytes
+  // would be 12 stages, but two CTAs share an SM, so each warp keeps 4
+  static constexpr int NSW = KV4 ? 4 : kNSW;           // pipeline stages per warp
   static constexpr int ROW = KV4 ? D / 2 : D * 2;      // bytes per key row (codes or bf16)
   static constexpr int SLICE = kKPW * ROW;             // one warp's K (or V) rows of a tile
   static constexpr int PSLICE = KV4 ? kKPW * 4 : 0;    // their (scale, zero) pairs
@@ -314,20 +323,352 @@ __device__ __forceinline__ bool issue_slice(const DecodeParams& p, const Cursor<
 
 __device__ __forceinline__ float2 unpack2(uint32_t w) { return make_float2(bf16lo(w), bf16hi(w)); }
 
-// 4-bit codes of dims 2e, 2e+1 of an 8-dim chunk as floats: lo / hi hold the low /
-// high nibbles of the chunk's four bytes; a code c becomes the float 2^23 + c by
-// placing it under the exponent bits of 2^23, then 2^23 is subtracted (exact).
-__device__ __forceinline__ float2 codes2(uint32_t lo, uint32_t hi, int e) {
-  const float a = __uint_as_float(__byte_perm(lo, 0x4B000000u, 0x7540u | (uint32_t)e));
-  const float b = __uint_as_float(__byte_perm(hi, 0x4B000000u, 0x7540u | (uint32_t)e));
-  return __fadd2_rn(make_float2(a, b), make_float2(-8388608.f, -8388608.f));
-}
-
 // fp16 (scale, zero) pair of a 4-bit row, widened to fp32
 __device__ __forceinline__ float2 scale_zero(uint32_t w) {
   return make_float2(__half2float(__ushort_as_half((unsigned short)(w & 0xFFFFu))),
                      __half2float(__ushort_as_half((unsigned short)(w >> 16))));
 }
+
+// ------------------------------------------------------------ warp-MMA consumer
+// Warp-level m16n8k16 tensor-core MMA with fp32 accumulation (A row-major, B
+// column-major). Fragment layout (lane = 4 gid + tig): a0 (row gid, cols 2 tig, +1),
+// a1 (row gid + 8, same cols), a2 (row gid, cols 2 tig + 8, +9), a3 (row gid + 8,
+// cols 2 tig + 8, +9); b0 (rows 2 tig, +1, col gid), b1 (rows 2 tig + 8, +9, col
+// gid); c0 c1 (row gid, cols 2 tig, +1), c2 c3 (row gid + 8, same cols); the lower
+// column (row) index sits in the low 16 bits of a register.
+template <bool F16>
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  if constexpr (F16) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  } else {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  }
+}
+
+__device__ __forceinline__ uint32_t hsub2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// 4-bit codes as fp16 without a conversion instruction: a code c in bits 0-3 of a
+// 16-bit half under the exponent of 1024 (0x6400) reads as 1024 + c, a code in bits
+// 4-7 under the exponent of 64 (0x5400, unit in the last place 1/16) as 64 + c.
+constexpr uint32_t kLoMagic = 0x64006400u, kHiMagic = 0x54005400u;
+
+// The per-warp consumer used when the query heads of a KV head are many (and for
+// 4-bit caches): a warp's 16-key slice is two tensor-core products instead of one
+// packed FMA per (element, head pair).
+//   S = Q K^T   rows = the g query heads (rows g ... 15 zero), cols = 8 keys per
+//               n-tile (keys gid and gid + 8 are the columns lane gid loads), k = dims
+//   O^T += V^T P^T   rows = 16 dims per m-tile, cols = the heads, k = the 16 keys
+// The dims inside a k-step may be taken in any order as long as Q and K use the same
+// one, and the rows of O^T in any order as long as the output is written back with
+// it; both orders below are chosen so that each lane reads whole 16-byte (4-byte)
+// pieces of shared memory and needs no shuffles to build its fragments:
+//   bf16 K: k-step 2u + e, k-index 2 tig + i (+ 8) <-> dim 8 (tig + 4u) + 4e + i (+ 2)
+//   4-bit K: lane tig reads code word w = (D / 32) tig + u (dims 8w ... 8w + 7), and
+//     k-step 2u + e, k-index 2 tig + i (+ 8) <-> dim 8w + 2e + 4i (+ 1)
+//   O^T: m-tile i, row gid (gid + 8) <-> dim (D / 8) gid + 2i (+ 1)
+// After S the softmax of the slice runs in the accumulator layout: lane (gid, tig)
+// holds head gid's scores of keys 2 tig, 2 tig + 1, 2 tig + 8, 2 tig + 9, which are
+// exactly the keys of its P^T fragment. For 4-bit K the magic offsets are folded
+// into one per-head constant (sum of q times the offsets of its dims), removed from
+// each slice's fresh fp32 accumulator; then q.k^ = scale (q.c) + zero sum(q). 4-bit V
+// codes are made exact by subtracting the magic (fp16, exact), so the long-lived O
+// accumulator carries no offset; p v^ = (p scale) c + p zero with p scale rounded to
+// fp16 and the zero part summed per head in fp32. q goes through fp16 on this path,
+// so its values must lie within the fp16 range (bf16 values there convert exactly).
+// One slice as the consumer sees it: its K and V rows (codes) in shared memory, for
+// 4-bit caches their (scale, zero) pairs, and the bits of keys 2 tig, 2 tig + 1,
+// 2 tig + 8, 2 tig + 9 that hold a visible key (hvalid: the same, cleared on the zero
+// rows gid >= G).
+struct SliceIn {
+  const uint8_t* k;
+  const uint8_t* v;
+  const uint8_t* kz;
+  const uint8_t* vz;
+  uint32_t kvalid, hvalid;
+};
+
+struct NoMma {};  // stands in for MmaSlice in the kernels that do not use it
+
+template <int D, int G, bool KV4>
+struct MmaSlice {
+  static constexpr int KS = D / 16;   // k-steps of S over the dims
+  static constexpr int MT = D / 16;   // 16-dim m-tiles of O^T
+  static constexpr int DT = D / 8;    // output dims of a lane: DT gid ... DT gid + DT - 1
+  static constexpr int ROW = KV4 ? D / 2 : D * 2;
+  // 4-bit V: p (at most 2^8 under the lazy rescale) times the row scale is stored in
+  // fp16 as p scale 2^-6, so that no row within the fp16 range can overflow it
+  static constexpr float kOScale = KV4 ? 64.f : 1.f;
+  uint32_t qa[KS][2];  // a0, a2 of every k-step (a1 = a3 = 0: rows 8 ... 15)
+  float o[MT][4];
+  float m_run, l_part, qfac;
+  float off, qsum, z_part;  // 4-bit caches
+
+  __device__ __forceinline__ void reset() {
+#pragma unroll
+    for (int i = 0; i < MT; ++i)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) o[i][k] = 0.f;
+    m_run = -INFINITY;
+    l_part = 0.f;
+    z_part = 0.f;
+  }
+
+  // q row of head gid (nullptr for the zero rows gid >= G) into A fragments; factor is
+  // the softmax scale (times the DCA mscale) applied to the fp32 product
+  __device__ __forceinline__ void load_q(const uint16_t* qh, float factor, int tig) {
+    qfac = factor;
+    if constexpr (!KV4) {
+#pragma unroll
+      for (int u = 0; u < D / 32; ++u) {
+        const uint4 v = qh ? __ldg(reinterpret_cast<const uint4*>(qh + (tig + 4 * u) * 8)) : make_uint4(0, 0, 0, 0);
+        qa[2 * u][0] = v.x;
+        qa[2 * u][1] = v.y;
+        qa[2 * u + 1][0] = v.z;
+        qa[2 * u + 1][1] = v.w;
+      }
+    } else {
+      constexpr int WPT = D / 32;  // code words of a lane per K row
+      float so = 0.f, ss = 0.f;
+#pragma unroll
+      for (int u = 0; u < WPT; ++u) {
+        const int w = WPT * tig + u;
+        const uint4 v = qh ? __ldg(reinterpret_cast<const uint4*>(qh + w * 8)) : make_uint4(0, 0, 0, 0);
+        const uint32_t b[4] = {v.x, v.y, v.z, v.w};
+        float h[8];  // dims 8w ... 8w + 7 rounded to fp16 (exact for bf16 values in its range)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          h[2 * k] = __half2float(__float2half_rn(bf16lo(b[k])));
+          h[2 * k + 1] = __half2float(__float2half_rn(bf16hi(b[k])));
+        }
+        qa[2 * u][0] = pack_half2(h[0], h[4]);
+        qa[2 * u][1] = pack_half2(h[1], h[5]);
+        qa[2 * u + 1][0] = pack_half2(h[2], h[6]);
+        qa[2 * u + 1][1] = pack_half2(h[3], h[7]);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          ss += h[k];
+          so = fmaf(h[k], (k & 1) ? 64.f : 1024.f, so);
+        }
+      }
+#pragma unroll
+      for (int m = 1; m <= 2; m <<= 1) {
+        ss += __shfl_xor_sync(0xffffffffu, ss, m);
+        so += __shfl_xor_sync(0xffffffffu, so, m);
+      }
+      qsum = ss;
+      off = so;
+    }
+  }
+
+  // Consumes NS 16-key slices (consecutive tiles of the segment) at once: their
+  // instruction streams interleave and they share one max reduction and rescale.
+  template <int NS>
+  __device__ __forceinline__ void slices(const SliceIn (&in)[2], int gid, int tig) {
+    float x[NS][4];  // keys 2 tig, 2 tig + 1, 2 tig + 8, 2 tig + 9 of each slice
+#pragma unroll
+    for (int q = 0; q < NS; ++q) {
+      float sc[2][2][4];  // [n-tile][chain][fragment]: two independent accumulation chains
+#pragma unroll
+      for (int j = 0; j < 2; ++j)
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+#pragma unroll
+          for (int k = 0; k < 4; ++k) sc[j][c][k] = 0.f;
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const uint8_t* row = in[q].k + (gid + 8 * j) * ROW;
+        if constexpr (KV4) {
+          constexpr int WPT = D / 32;  // code words of a lane per K row
+          uint32_t w[WPT];
+          if constexpr (WPT == 4) {
+            const uint4 v = *reinterpret_cast<const uint4*>(row + tig * 16);
+            w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+          } else {
+            const uint2 v = *reinterpret_cast<const uint2*>(row + tig * 8);
+            w[0] = v.x; w[1] = v.y;
+          }
+#pragma unroll
+          for (int u = 0; u < WPT; ++u) {
+            const uint32_t xw = w[u], x8 = w[u] >> 8;
+            mma16816<true>(sc[j][u & 1], qa[2 * u][0], 0u, qa[2 * u][1], 0u, (xw & 0x000F000Fu) | kLoMagic,
+                           (xw & 0x00F000F0u) | kHiMagic);
+            mma16816<true>(sc[j][u & 1], qa[2 * u + 1][0], 0u, qa[2 * u + 1][1], 0u,
+                           (x8 & 0x000F000Fu) | kLoMagic, (x8 & 0x00F000F0u) | kHiMagic);
+          }
+        } else {
+#pragma unroll
+          for (int u = 0; u < D / 32; ++u) {
+            const uint4 v = *reinterpret_cast<const uint4*>(row + (tig + 4 * u) * 16);
+            mma16816<false>(sc[j][u & 1], qa[2 * u][0], 0u, qa[2 * u][1], 0u, v.x, v.y);
+            mma16816<false>(sc[j][u & 1], qa[2 * u + 1][0], 0u, qa[2 * u + 1][1], 0u, v.z, v.w);
+          }
+        }
+      }
+      x[q][0] = sc[0][0][0] + sc[0][1][0];
+      x[q][1] = sc[0][0][1] + sc[0][1][1];
+      x[q][2] = sc[1][0][0] + sc[1][1][0];
+      x[q][3] = sc[1][0][1] + sc[1][1][1];
+      if constexpr (KV4) {
+        const uint2 z01 = *reinterpret_cast<const uint2*>(in[q].kz + tig * 8);
+        const uint2 z89 = *reinterpret_cast<const uint2*>(in[q].kz + 32 + tig * 8);
+        const uint32_t zz[4] = {z01.x, z01.y, z89.x, z89.y};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float2 sz = scale_zero(zz[k]);
+          x[q][k] = fmaf(sz.x, x[q][k] - off, sz.y * qsum);
+        }
+      }
+    }
+    float mx = -INFINITY;
+#pragma unroll
+    for (int q = 0; q < NS; ++q)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        x[q][k] = ((in[q].hvalid >> k) & 1u) ? x[q][k] * qfac : -INFINITY;
+        mx = fmaxf(mx, x[q][k]);
+      }
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    const bool grow = mx > m_run + 8.f;  // lazy rescale, as in the CUDA-core path
+    if (__any_sync(0xffffffffu, grow)) {
+      const float f = grow ? ex2_approx(m_run - mx) : 1.f;
+      if (grow) {
+        m_run = mx;
+        l_part *= f;
+        if constexpr (KV4) z_part *= f;
+      }
+      const float f0 = __shfl_sync(0xffffffffu, f, 8 * tig);      // head 2 tig
+      const float f1 = __shfl_sync(0xffffffffu, f, 8 * tig + 4);  // head 2 tig + 1
+#pragma unroll
+      for (int i = 0; i < MT; ++i) {
+        o[i][0] *= f0;
+        o[i][1] *= f1;
+        o[i][2] *= f0;
+        o[i][3] *= f1;
+      }
+    }
+    const int kr[4] = {2 * tig, 2 * tig + 1, 2 * tig + 8, 2 * tig + 9};
+#pragma unroll
+    for (int q = 0; q < NS; ++q) {
+      float pr[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        pr[k] = ((in[q].hvalid >> k) & 1u) ? ex2_approx(x[q][k] - m_run) : 0.f;
+        l_part += pr[k];
+      }
+      uint32_t pb0, pb1;
+      if constexpr (KV4) {
+        const uint2 z01 = *reinterpret_cast<const uint2*>(in[q].vz + tig * 8);
+        const uint2 z89 = *reinterpret_cast<const uint2*>(in[q].vz + 32 + tig * 8);
+        const uint32_t zz[4] = {z01.x, z01.y, z89.x, z89.y};
+        float b[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float2 sz = scale_zero(zz[k]);
+          const bool ok = (in[q].hvalid >> k) & 1u;  // the pair of an unused row may be anything
+          b[k] = ok ? pr[k] * (sz.x * (1.f / kOScale)) : 0.f;
+          z_part += ok ? pr[k] * sz.y : 0.f;
+        }
+        pb0 = pack_half2(b[0], b[1]);
+        pb1 = pack_half2(b[2], b[3]);
+        constexpr int VB = D / 16;  // code bytes of a lane per V row (one per m-tile)
+        uint32_t w[4][(VB + 3) / 4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint8_t* r = in[q].v + kr[k] * ROW + VB * gid;
+          if constexpr (VB == 8) {
+            const uint2 v = *reinterpret_cast<const uint2*>(r);
+            w[k][0] = v.x;
+            w[k][1] = v.y;
+          } else {
+            w[k][0] = *reinterpret_cast<const uint32_t*>(r);
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < MT; ++i) {
+          // bytes i of keys (2 tig, 2 tig + 1) side by side in the two halves
+          const uint32_t sel = (uint32_t)(i & 3) * 0x11u + (uint32_t)(4 + (i & 3)) * 0x1100u;
+          const uint32_t y01 = __byte_perm(w[0][i >> 2], w[1][i >> 2], sel);
+          const uint32_t y89 = __byte_perm(w[2][i >> 2], w[3][i >> 2], sel);
+          mma16816<true>(o[i], hsub2((y01 & 0x000F000Fu) | kLoMagic, kLoMagic),
+                         hsub2((y01 & 0x00F000F0u) | kHiMagic, kHiMagic),
+                         hsub2((y89 & 0x000F000Fu) | kLoMagic, kLoMagic),
+                         hsub2((y89 & 0x00F000F0u) | kHiMagic, kHiMagic), pb0, pb1);
+        }
+      } else {
+        pb0 = pack_bf16x2(pr[0], pr[1]);
+        pb1 = pack_bf16x2(pr[2], pr[3]);
+        uint32_t w[4][MT];  // MT words = this lane's DT dims of each key
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const bool ok = (in[q].kvalid >> k) & 1u;  // rows not copied in this stage may hold anything
+#pragma unroll
+          for (int c = 0; c < MT / 4; ++c) {
+            const uint4 v = *reinterpret_cast<const uint4*>(in[q].v + kr[k] * ROW + DT * 2 * gid + c * 16);
+            w[k][4 * c] = ok ? v.x : 0u;
+            w[k][4 * c + 1] = ok ? v.y : 0u;
+            w[k][4 * c + 2] = ok ? v.z : 0u;
+            w[k][4 * c + 3] = ok ? v.w : 0u;
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < MT; ++i)
+          mma16816<false>(o[i], __byte_perm(w[0][i], w[1][i], 0x5410), __byte_perm(w[0][i], w[1][i], 0x7632),
+                          __byte_perm(w[2][i], w[3][i], 0x5410), __byte_perm(w[2][i], w[3][i], 0x7632), pb0, pb1);
+      }
+    }
+  }
+
+  // The warp's (o, max, sum) per head into the reduction buffer, as the CUDA-core path
+  // leaves them: red[(warp G + h) (D + 2) + d], then max and sum at D and D + 1.
+  __device__ __forceinline__ void write(float* red, int warp, int gid, int tig) {
+    float l = l_part;
+    l += __shfl_xor_sync(0xffffffffu, l, 1);
+    l += __shfl_xor_sync(0xffffffffu, l, 2);
+    float z0 = 0.f, z1 = 0.f;
+    if constexpr (KV4) {
+      float z = z_part;
+      z += __shfl_xor_sync(0xffffffffu, z, 1);
+      z += __shfl_xor_sync(0xffffffffu, z, 2);
+      z0 = __shfl_sync(0xffffffffu, z, 8 * tig);
+      z1 = __shfl_sync(0xffffffffu, z, 8 * tig + 4);
+    }
+    const int h0 = 2 * tig, h1 = 2 * tig + 1;
+#pragma unroll
+    for (int i = 0; i < MT; ++i) {
+      const int d = DT * gid + 2 * i;
+      if (h0 < G) {
+        float* r = red + (warp * G + h0) * (D + 2) + d;
+        r[0] = fmaf(o[i][0], kOScale, z0);
+        r[1] = fmaf(o[i][2], kOScale, z0);
+      }
+      if (h1 < G) {
+        float* r = red + (warp * G + h1) * (D + 2) + d;
+        r[0] = fmaf(o[i][1], kOScale, z1);
+        r[1] = fmaf(o[i][3], kOScale, z1);
+      }
+    }
+    if (tig == 0 && gid < G) {
+      float* r = red + (warp * G + gid) * (D + 2);
+      r[D] = m_run;
+      r[D + 1] = l;
+    }
+  }
+};
 
 // Synchronisation of the eight warps through an mbarrier (bounded wait).
 struct WarpSync {
@@ -344,7 +685,8 @@ struct WarpSync {
 };
 
 template <int D, int G, int kMode>
-__global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(kThreads, kMode == kModeKv4 ? kDecodeCtasPerSmKv4 : 1)
+    decode_kernel(const DecodeParams p) {
   using C = Cfg<D, G, kMode == kModeKv4>;
   extern __shared__ __align__(1024) uint8_t smem[];
   float* red = reinterpret_cast<float*>(smem + C::RING);
@@ -388,6 +730,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
   const int kg = lane / C::LPK;           // key within the warp iteration
   const int cl = lane % C::LPK;           // dims slot of this lane within its key group
   const int hme = cl >> (C::LB - C::GB);  // the head this lane ends up owning
+  constexpr bool kMma = kMode == kModeKv4 || G >= kMmaMinG;
+  const int gid = lane >> 2, tig = lane & 3;  // tensor-core slices: fragment row group, thread in group
+  std::conditional_t<kMma, MmaSlice<D, G, kMode == kModeKv4>, NoMma> mm;
   const int SR = p.sh.S + p.sh.R;
   WarpSync ws{segbar, 0};
   int64_t j = 0;  // tiles consumed
@@ -429,37 +774,20 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
     }
     auto dca_var = [&](int64_t lt) { return lt >= t_intra ? 0 : (lt >= t_succ ? 1 : 2); };
     auto dca_q = [&](int v) { return v == 0 ? p.q : (v == 1 ? p.q_succ : p.q_inter); };
+    // tensor-core slices: lane (gid, tig) holds head gid's row of the A fragments
+    auto set_q = [&](const uint16_t* qsrc) {
+      if constexpr (kMma)
+        mm.load_q(gid < G ? qsrc + ((int64_t)x.b * p.sh.Hq + (int64_t)x.kvh * G + gid) * D : nullptr, qfactor, tig);
+      else
+        load_q(qsrc, qfactor);
+    };
+    if constexpr (kMma) mm.reset();
     if (kMode == kModeDca) {
       if (p.mscale) qfactor *= __ldg(p.mscale + x.b);
       qv = dca_var(lt_begin);
-      load_q(dca_q(qv), qfactor);
+      set_q(dca_q(qv));
     } else {
-      load_q(p.q, qfactor);
-    }
-    // 4-bit caches: q.k^ = scale (q.c) + zero sum(q), so each lane needs sum(q) of its
-    // head hme, reduced over the key group like a score
-    float qsum = 0.f;
-    float zacc[G];  // 4-bit caches: sum of p * zero(v) per head slot (added to every dim)
-#pragma unroll
-    for (int l = 0; l < G; ++l) zacc[l] = 0.f;
-    if constexpr (kMode == kModeKv4) {
-      float d[G];
-#pragma unroll
-      for (int l = 0; l < G; ++l) {
-        d[l] = 0.f;
-#pragma unroll
-        for (int e = 0; e < C::DPL / 2; ++e) d[l] += q2[l][e].x + q2[l][e].y;
-      }
-#pragma unroll
-      for (int k = 1; k <= C::GB; ++k) {
-        const int half = G >> k;
-        const int bit = 1 << (C::LB - k);
-#pragma unroll
-        for (int l = 0; l < half; ++l) d[l] += __shfl_xor_sync(0xffffffffu, d[l + half], bit);
-      }
-#pragma unroll
-      for (int b = C::LB - C::GB - 1; b >= 0; --b) d[0] += __shfl_xor_sync(0xffffffffu, d[0], 1 << b);
-      qsum = d[0];
+      set_q(p.q);
     }
     float2 o2[G][C::DPL / 2];
 #pragma unroll
@@ -468,13 +796,77 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
       for (int e = 0; e < C::DPL / 2; ++e) o2[l][e] = make_float2(0.f, 0.f);
     float l_run = 0.f, m_run = -INFINITY;  // of head hme
 
-    for (int64_t lt = lt_begin; lt < lt_end; ++lt, ++j) {
+    if constexpr (kMma) {
+      // two tiles per step where the ring is deep enough to hold a pair and the next
+      // tiles in flight
+      constexpr int kPair = C::NSW >= 8 ? 2 : 1;
+      for (int64_t lt = lt_begin; lt < lt_end;) {
+        int np = (kPair == 2 && lt + 1 < lt_end) ? 2 : 1;
+        if (kMode == kModeDca) {
+          const int v = dca_var(lt);
+          if (v != qv) {  // at most twice per unit
+            qv = v;
+            set_q(dca_q(v));
+          }
+          if (np == 2 && dca_var(lt + 1) != v) np = 1;
+        }
+        // refill: the stage of tile `issued` is free once tile issued - NSW is consumed
+        while (cur.live && issued < j + C::NSW) {
+          const int sn = (int)(issued % C::NSW);
+          if (lane == 0) {
+            const bool bad = issue_slice<D, G, kMode>(p, cur, warp, ring + sn * C::WSTAGE, &wfull[sn]);
+            if (kPaged) badmask = bad ? (badmask | (1u << sn)) : (badmask & ~(1u << sn));
+          }
+          cur.advance(p, c, t1, live);
+          ++issued;
+        }
+        SliceIn in[2];
+        for (int q = 0; q < np; ++q) {
+          const int s = (int)((j + q) % C::NSW);
+          if (!mbar_wait(&wfull[s], (uint32_t)(((j + q) / C::NSW) & 1), err, kErrDecodeConsumer)) {
+            ok = false;
+            break;
+          }
+          const bool str_pool = kMode == kModePool && x.streaming;
+          const int64_t kt = str_pool ? stream_tile(p, lt + q) : lt + q;
+          int rows = warp_rows(x.keys, kt, warp);
+          if (kPaged && ((__shfl_sync(0xffffffffu, badmask, 0) >> s) & 1u)) rows = 0;
+          uint32_t kvalid = 0xFu;  // keys 2 tig, 2 tig + 1, 2 tig + 8, 2 tig + 9 of the slice
+          if (rows != kKPW || x.streaming) {
+            kvalid = 0u;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const int key = 2 * tig + (k & 1) + 8 * (k >> 1);
+              bool valid = key < rows;
+              if (x.streaming && valid) {
+                const int64_t slot = kt * kTK + (int64_t)warp * kKPW + key;
+                const int jp = str_pool ? (int)slot : __ldg(p.pos + (int64_t)x.b * SR + slot);
+                valid = jp >= 0 && jp <= x.pq && (jp < p.sh.S || x.pq - jp < p.sh.R);
+              }
+              kvalid |= (uint32_t)valid << k;
+            }
+          }
+          const uint8_t* sk = ring + s * C::WSTAGE;
+          in[q] = SliceIn{sk, sk + C::SLICE, sk + 2 * C::SLICE, sk + 2 * C::SLICE + C::PSLICE, kvalid,
+                          gid < G ? kvalid : 0u};
+        }
+        if (!ok) break;
+        if (np == 2)
+          mm.template slices<2>(in, gid, tig);
+        else
+          mm.template slices<1>(in, gid, tig);
+        __syncwarp();
+        lt += np;
+        j += np;
+      }
+    }
+    for (int64_t lt = lt_begin; lt < lt_end && !kMma; ++lt, ++j) {
       const int s = (int)(j % C::NSW);
       if (kMode == kModeDca) {
         const int v = dca_var(lt);
         if (v != qv) {  // at most twice per unit
           qv = v;
-          load_q(dca_q(v), qfactor);
+          set_q(dca_q(v));
         }
       }
       // refill: the stage used by tile j - 1 is free now (this warp finished it)
@@ -520,24 +912,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
         for (int l = 0; l < G; ++l) acc[l] = make_float2(0.f, 0.f);
 #pragma unroll
         for (int ch = 0; ch < C::CH; ++ch) {
-          if constexpr (kMode == kModeKv4) {
-            const uint32_t w = *reinterpret_cast<const uint32_t*>(sk + key * C::ROW + (cl + ch * C::LPK) * 4);
-            const uint32_t lo = w & 0x0F0F0F0Fu, hi = (w >> 4) & 0x0F0F0F0Fu;
+          const uint4 kv = *reinterpret_cast<const uint4*>(sk + key * C::ROW + (cl + ch * C::LPK) * 16);
+          const uint32_t w4[4] = {kv.x, kv.y, kv.z, kv.w};
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float2 k2 = codes2(lo, hi, e);
+          for (int e = 0; e < 4; ++e) {
+            const float2 k2 = unpack2(w4[e]);
 #pragma unroll
-              for (int l = 0; l < G; ++l) acc[l] = __ffma2_rn(q2[l][ch * 4 + e], k2, acc[l]);
-            }
-          } else {
-            const uint4 kv = *reinterpret_cast<const uint4*>(sk + key * C::ROW + (cl + ch * C::LPK) * 16);
-            const uint32_t w4[4] = {kv.x, kv.y, kv.z, kv.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float2 k2 = unpack2(w4[e]);
-#pragma unroll
-              for (int l = 0; l < G; ++l) acc[l] = __ffma2_rn(q2[l][ch * 4 + e], k2, acc[l]);
-            }
+            for (int l = 0; l < G; ++l) acc[l] = __ffma2_rn(q2[l][ch * 4 + e], k2, acc[l]);
           }
         }
         float dot[G];
@@ -554,10 +935,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
         // butterfly over the remaining lane bits
 #pragma unroll
         for (int b = C::LB - C::GB - 1; b >= 0; --b) dot[0] += __shfl_xor_sync(0xffffffffu, dot[0], 1 << b);
-        if constexpr (kMode == kModeKv4) {
-          const float2 sz = scale_zero(*reinterpret_cast<const uint32_t*>(sk + 2 * C::SLICE + key * 4));
-          dot[0] = fmaf(sz.x, dot[0], sz.y * qsum);
-        }
         sc[it] = valid ? dot[0] : -INFINITY;
       }
 
@@ -580,7 +957,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
           const float2 f2 = make_float2(fl, fl);
 #pragma unroll
           for (int e = 0; e < C::DPL / 2; ++e) o2[l][e] = __fmul2_rn(o2[l][e], f2);
-          if (kMode == kModeKv4) zacc[l] *= fl;
         }
       }
 #pragma unroll
@@ -597,39 +973,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
         for (int l = 1; l < G; ++l) pl[l] = __shfl_xor_sync(0xffffffffu, sc[it], l << (C::LB - C::GB));
         if (full_tile || vis[it]) {
           const int key = it * C::KPI + kg;
-          if constexpr (kMode == kModeKv4) {
-            // p v^ = (p scale) c + p zero: the zero part summed per head, added at the end
-            const float2 sz = scale_zero(*reinterpret_cast<const uint32_t*>(sk + 2 * C::SLICE + C::PSLICE + key * 4));
-            float ps[G];
 #pragma unroll
-            for (int l = 0; l < G; ++l) {
-              ps[l] = pl[l] * sz.x;
-              zacc[l] = fmaf(pl[l], sz.y, zacc[l]);
-            }
+          for (int ch = 0; ch < C::CH; ++ch) {
+            const uint4 vv = *reinterpret_cast<const uint4*>(sv + key * C::ROW + (cl + ch * C::LPK) * 16);
+            const uint32_t w4[4] = {vv.x, vv.y, vv.z, vv.w};
 #pragma unroll
-            for (int ch = 0; ch < C::CH; ++ch) {
-              const uint32_t w = *reinterpret_cast<const uint32_t*>(sv + key * C::ROW + (cl + ch * C::LPK) * 4);
-              const uint32_t lo = w & 0x0F0F0F0Fu, hi = (w >> 4) & 0x0F0F0F0Fu;
+            for (int e = 0; e < 4; ++e) {
+              const float2 v2 = unpack2(w4[e]);
 #pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const float2 v2 = codes2(lo, hi, e);
-#pragma unroll
-                for (int l = 0; l < G; ++l)
-                  o2[l][ch * 4 + e] = __ffma2_rn(make_float2(ps[l], ps[l]), v2, o2[l][ch * 4 + e]);
-              }
-            }
-          } else {
-#pragma unroll
-            for (int ch = 0; ch < C::CH; ++ch) {
-              const uint4 vv = *reinterpret_cast<const uint4*>(sv + key * C::ROW + (cl + ch * C::LPK) * 16);
-              const uint32_t w4[4] = {vv.x, vv.y, vv.z, vv.w};
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const float2 v2 = unpack2(w4[e]);
-#pragma unroll
-                for (int l = 0; l < G; ++l)
-                  o2[l][ch * 4 + e] = __ffma2_rn(make_float2(pl[l], pl[l]), v2, o2[l][ch * 4 + e]);
-              }
+              for (int l = 0; l < G; ++l)
+                o2[l][ch * 4 + e] = __ffma2_rn(make_float2(pl[l], pl[l]), v2, o2[l][ch * 4 + e]);
             }
           }
         }
@@ -639,15 +992,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
     if (!ok) break;
 
     // ---------------------------------------------------- segment merge
-    if constexpr (kMode == kModeKv4) {
-#pragma unroll
-      for (int l = 0; l < G; ++l)
-#pragma unroll
-        for (int e = 0; e < C::DPL / 2; ++e) o2[l][e] = __fadd2_rn(o2[l][e], make_float2(zacc[l], zacc[l]));
-    }
+    if constexpr (kMma) mm.write(red, warp, gid, tig);
     // sum over the key groups of the warp (each holds other keys)
 #pragma unroll
-    for (int off = C::LPK; off < 32; off <<= 1) {
+    for (int off = C::LPK; off < 32 && !kMma; off <<= 1) {
       l_run += __shfl_xor_sync(0xffffffffu, l_run, off);
 #pragma unroll
       for (int l = 0; l < G; ++l)
@@ -658,7 +1006,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
           o2[l][e] = __fadd2_rn(o2[l][e], o);
         }
     }
-    if (kg == 0) {
+    if (kg == 0 && !kMma) {
 #pragma unroll
       for (int l = 0; l < G; ++l) {
         float* r = red + (warp * G + (hme ^ l)) * (D + 2);

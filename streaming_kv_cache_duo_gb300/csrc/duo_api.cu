@@ -481,7 +481,7 @@ duo_status duo_attn_prefill_paged(duo_handle* h, const duo_kv_cache* c, const du
   return prefill_impl(h, c, paged, q, k, v, T, o, 3, stream);
 }
 
-static void decode_plan(const duo_handle* h, int64_t n, DecodeParams* p) {
+static void decode_plan(const duo_handle* h, int64_t n, DecodeParams* p, int ctas_per_sm = 1) {
   const Shape& sh = h->sh;
   p->seq_lens = nullptr;  // uniform length n unless a caller sets device lengths
   p->pg = PagedLayout{nullptr, 0, 0, 0, nullptr};  // contiguous retrieval caches unless paged
@@ -503,7 +503,8 @@ static void decode_plan(const duo_handle* h, int64_t n, DecodeParams* p) {
   p->tiles_s = (p->nvalid + kDecodeTK - 1) / kDecodeTK;
   p->W = (int64_t)p->U_r * p->tiles_r;  // retrieval tiles; streaming units are dealt whole
   const int64_t work = p->W + p->U_s;
-  p->C = (int)(work < h->num_sms ? work : h->num_sms);
+  const int64_t cmax = (int64_t)h->num_sms * ctas_per_sm;
+  p->C = (int)(work < cmax ? work : cmax);
   p->Cr = (int)(p->W < p->C ? p->W : p->C);
 }
 
@@ -512,8 +513,8 @@ size_t duo_decode_workspace_size(const duo_handle* h, int64_t n) {
   DecodeParams p;
   decode_plan(h, n < 1 ? 1 : n, &p);
   (void)p;
-  // sized for the largest grid so that one workspace serves every n
-  return decode_workspace_bytes(h->sh, h->num_sms);
+  // sized for the largest grid (the 4-bit decode's) so that one workspace serves every n
+  return decode_workspace_bytes(h->sh, h->num_sms * kDecodeCtasPerSmKv4);
 }
 
 // Dual Chunk Attention arguments of a decode step (nullptr: plain decode).
@@ -554,14 +555,15 @@ static duo_status decode_impl(duo_handle* h, const duo_kv_cache* c, const duo_pa
   if ((st = check_capacity(h, pg, c->n, DUO_ERR_INVALID_ARG)) != DUO_OK) return st;
   if (!q || !o || !aligned16(q) || !aligned16(o))
     return fail(DUO_ERR_INVALID_ARG, "q / o NULL or not 16-byte aligned");
-  const size_t need = decode_workspace_bytes(h->sh, h->num_sms);
+  const int ctas_per_sm = kv4 ? kDecodeCtasPerSmKv4 : 1;
+  const size_t need = decode_workspace_bytes(h->sh, h->num_sms * ctas_per_sm);
   if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
     return fail(DUO_ERR_INVALID_ARG, "workspace not 256-byte aligned");
   if (!workspace || ws_bytes < need)
     return fail(DUO_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need, workspace ? ws_bytes : 0);
   const Shape& sh = h->sh;
   DecodeParams p;
-  decode_plan(h, c->n, &p);
+  decode_plan(h, c->n, &p, ctas_per_sm);
   const int64_t U = (int64_t)sh.B * sh.Hkv;
   const size_t counter_bytes = ((size_t)U * 4 + 255) / 256 * 256;
   const unsigned epoch = g_error_epoch.load();

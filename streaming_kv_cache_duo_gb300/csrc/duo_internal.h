@@ -106,6 +106,9 @@ cudaError_t append_read_clear_error(uint32_t* code);
 
 // ------------------------------------------------------------------ decode
 constexpr int kDecodeTK = 128;  // keys per decode tile
+// CTAs per SM of the 4-bit decode (its rings are small enough for two; more warps hide
+// the latency of its per-slice dependency chains); the bf16 decode runs one
+constexpr int kDecodeCtasPerSmKv4 = 2;
 
 struct DecodeParams {
   const uint16_t* q;  // bf16 [B, Hq, D]
