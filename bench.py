@@ -48,10 +48,10 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 L2_BYTES = 129e6  # GB300 L2 capacity
 
 MEASURED_TRAFFIC = {
-    "prefill": {"src": ("prefill.cu", "duo_device.cuh", "duo_internal.h"), "sha1": "74e603c0b5b91dfc",
-                "bytes": 571.204352e6 + 232.534272e6},
-    "decode": {"src": ("decode.cu", "duo_device.cuh", "duo_internal.h"), "sha1": "9403eb347eb033b9",
-               "bytes": 1.074880e9 + 3.595008e6},
+    "prefill": {"src": ("prefill.cu", "duo_device.cuh", "duo_internal.h"), "sha1": "b9fb41cf8dafa854",
+                "bytes": 573.076992e6 + 232.428800e6},
+    "decode": {"src": ("decode.cu", "duo_device.cuh", "duo_internal.h"), "sha1": "c73b23450733dbb9",
+               "bytes": 1.074862e9 + 3.666176e6},
 }
 
 

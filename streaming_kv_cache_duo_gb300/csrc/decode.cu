@@ -474,13 +474,10 @@ struct MmaSlice {
     }
   }
 
-  // Consumes NS 16-key slices (consecutive tiles of the segment) at once: their
-  // instruction streams interleave and they share one max reduction and rescale.
-  template <int NS>
-  __device__ __forceinline__ void slices(const SliceIn (&in)[2], int gid, int tig) {
-    float x[NS][4];  // keys 2 tig, 2 tig + 1, 2 tig + 8, 2 tig + 9 of each slice
-#pragma unroll
-    for (int q = 0; q < NS; ++q) {
+  // One 16-key slice.
+  __device__ __forceinline__ void slice(const SliceIn& in, int gid, int tig) {
+    float x[4];  // scores of keys 2 tig, 2 tig + 1, 2 tig + 8, 2 tig + 9
+    {
       float sc[2][2][4];  // [n-tile][chain][fragment]: two independent accumulation chains
 #pragma unroll
       for (int j = 0; j < 2; ++j)
@@ -490,7 +487,7 @@ struct MmaSlice {
           for (int k = 0; k < 4; ++k) sc[j][c][k] = 0.f;
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
-        const uint8_t* row = in[q].k + (gid + 8 * j) * ROW;
+        const uint8_t* row = in.k + (gid + 8 * j) * ROW;
         if constexpr (KV4) {
           constexpr int WPT = D / 32;  // code words of a lane per K row
           uint32_t w[WPT];
@@ -518,29 +515,27 @@ struct MmaSlice {
           }
         }
       }
-      x[q][0] = sc[0][0][0] + sc[0][1][0];
-      x[q][1] = sc[0][0][1] + sc[0][1][1];
-      x[q][2] = sc[1][0][0] + sc[1][1][0];
-      x[q][3] = sc[1][0][1] + sc[1][1][1];
+      x[0] = sc[0][0][0] + sc[0][1][0];
+      x[1] = sc[0][0][1] + sc[0][1][1];
+      x[2] = sc[1][0][0] + sc[1][1][0];
+      x[3] = sc[1][0][1] + sc[1][1][1];
       if constexpr (KV4) {
-        const uint2 z01 = *reinterpret_cast<const uint2*>(in[q].kz + tig * 8);
-        const uint2 z89 = *reinterpret_cast<const uint2*>(in[q].kz + 32 + tig * 8);
+        const uint2 z01 = *reinterpret_cast<const uint2*>(in.kz + tig * 8);
+        const uint2 z89 = *reinterpret_cast<const uint2*>(in.kz + 32 + tig * 8);
         const uint32_t zz[4] = {z01.x, z01.y, z89.x, z89.y};
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const float2 sz = scale_zero(zz[k]);
-          x[q][k] = fmaf(sz.x, x[q][k] - off, sz.y * qsum);
+          x[k] = fmaf(sz.x, x[k] - off, sz.y * qsum);
         }
       }
     }
     float mx = -INFINITY;
 #pragma unroll
-    for (int q = 0; q < NS; ++q)
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        x[q][k] = ((in[q].hvalid >> k) & 1u) ? x[q][k] * qfac : -INFINITY;
-        mx = fmaxf(mx, x[q][k]);
-      }
+    for (int k = 0; k < 4; ++k) {
+      x[k] = ((in.hvalid >> k) & 1u) ? x[k] * qfac : -INFINITY;
+      mx = fmaxf(mx, x[k]);
+    }
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
     const bool grow = mx > m_run + 8.f;  // lazy rescale, as in the CUDA-core path
@@ -562,24 +557,23 @@ struct MmaSlice {
       }
     }
     const int kr[4] = {2 * tig, 2 * tig + 1, 2 * tig + 8, 2 * tig + 9};
-#pragma unroll
-    for (int q = 0; q < NS; ++q) {
+    {
       float pr[4];
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        pr[k] = ((in[q].hvalid >> k) & 1u) ? ex2_approx(x[q][k] - m_run) : 0.f;
+        pr[k] = ((in.hvalid >> k) & 1u) ? ex2_approx(x[k] - m_run) : 0.f;
         l_part += pr[k];
       }
       uint32_t pb0, pb1;
       if constexpr (KV4) {
-        const uint2 z01 = *reinterpret_cast<const uint2*>(in[q].vz + tig * 8);
-        const uint2 z89 = *reinterpret_cast<const uint2*>(in[q].vz + 32 + tig * 8);
+        const uint2 z01 = *reinterpret_cast<const uint2*>(in.vz + tig * 8);
+        const uint2 z89 = *reinterpret_cast<const uint2*>(in.vz + 32 + tig * 8);
         const uint32_t zz[4] = {z01.x, z01.y, z89.x, z89.y};
         float b[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const float2 sz = scale_zero(zz[k]);
-          const bool ok = (in[q].hvalid >> k) & 1u;  // the pair of an unused row may be anything
+          const bool ok = (in.hvalid >> k) & 1u;  // the pair of an unused row may be anything
           b[k] = ok ? pr[k] * (sz.x * (1.f / kOScale)) : 0.f;
           z_part += ok ? pr[k] * sz.y : 0.f;
         }
@@ -589,7 +583,7 @@ struct MmaSlice {
         uint32_t w[4][(VB + 3) / 4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          const uint8_t* r = in[q].v + kr[k] * ROW + VB * gid;
+          const uint8_t* r = in.v + kr[k] * ROW + VB * gid;
           if constexpr (VB == 8) {
             const uint2 v = *reinterpret_cast<const uint2*>(r);
             w[k][0] = v.x;
@@ -615,10 +609,10 @@ struct MmaSlice {
         uint32_t w[4][MT];  // MT words = this lane's DT dims of each key
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          const bool ok = (in[q].kvalid >> k) & 1u;  // rows not copied in this stage may hold anything
+          const bool ok = (in.kvalid >> k) & 1u;  // rows not copied in this stage may hold anything
 #pragma unroll
           for (int c = 0; c < MT / 4; ++c) {
-            const uint4 v = *reinterpret_cast<const uint4*>(in[q].v + kr[k] * ROW + DT * 2 * gid + c * 16);
+            const uint4 v = *reinterpret_cast<const uint4*>(in.v + kr[k] * ROW + DT * 2 * gid + c * 16);
             w[k][4 * c] = ok ? v.x : 0u;
             w[k][4 * c + 1] = ok ? v.y : 0u;
             w[k][4 * c + 2] = ok ? v.z : 0u;
@@ -796,71 +790,7 @@ __global__ void __launch_bounds__(kThreads, kMode == kModeKv4 ? kDecodeCtasPerSm
       for (int e = 0; e < C::DPL / 2; ++e) o2[l][e] = make_float2(0.f, 0.f);
     float l_run = 0.f, m_run = -INFINITY;  // of head hme
 
-    if constexpr (kMma) {
-      // two tiles per step where the ring is deep enough to hold a pair and the next
-      // tiles in flight
-      constexpr int kPair = C::NSW >= 8 ? 2 : 1;
-      for (int64_t lt = lt_begin; lt < lt_end;) {
-        int np = (kPair == 2 && lt + 1 < lt_end) ? 2 : 1;
-        if (kMode == kModeDca) {
-          const int v = dca_var(lt);
-          if (v != qv) {  // at most twice per unit
-            qv = v;
-            set_q(dca_q(v));
-          }
-          if (np == 2 && dca_var(lt + 1) != v) np = 1;
-        }
-        // refill: the stage of tile `issued` is free once tile issued - NSW is consumed
-        while (cur.live && issued < j + C::NSW) {
-          const int sn = (int)(issued % C::NSW);
-          if (lane == 0) {
-            const bool bad = issue_slice<D, G, kMode>(p, cur, warp, ring + sn * C::WSTAGE, &wfull[sn]);
-            if (kPaged) badmask = bad ? (badmask | (1u << sn)) : (badmask & ~(1u << sn));
-          }
-          cur.advance(p, c, t1, live);
-          ++issued;
-        }
-        SliceIn in[2];
-        for (int q = 0; q < np; ++q) {
-          const int s = (int)((j + q) % C::NSW);
-          if (!mbar_wait(&wfull[s], (uint32_t)(((j + q) / C::NSW) & 1), err, kErrDecodeConsumer)) {
-            ok = false;
-            break;
-          }
-          const bool str_pool = kMode == kModePool && x.streaming;
-          const int64_t kt = str_pool ? stream_tile(p, lt + q) : lt + q;
-          int rows = warp_rows(x.keys, kt, warp);
-          if (kPaged && ((__shfl_sync(0xffffffffu, badmask, 0) >> s) & 1u)) rows = 0;
-          uint32_t kvalid = 0xFu;  // keys 2 tig, 2 tig + 1, 2 tig + 8, 2 tig + 9 of the slice
-          if (rows != kKPW || x.streaming) {
-            kvalid = 0u;
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const int key = 2 * tig + (k & 1) + 8 * (k >> 1);
-              bool valid = key < rows;
-              if (x.streaming && valid) {
-                const int64_t slot = kt * kTK + (int64_t)warp * kKPW + key;
-                const int jp = str_pool ? (int)slot : __ldg(p.pos + (int64_t)x.b * SR + slot);
-                valid = jp >= 0 && jp <= x.pq && (jp < p.sh.S || x.pq - jp < p.sh.R);
-              }
-              kvalid |= (uint32_t)valid << k;
-            }
-          }
-          const uint8_t* sk = ring + s * C::WSTAGE;
-          in[q] = SliceIn{sk, sk + C::SLICE, sk + 2 * C::SLICE, sk + 2 * C::SLICE + C::PSLICE, kvalid,
-                          gid < G ? kvalid : 0u};
-        }
-        if (!ok) break;
-        if (np == 2)
-          mm.template slices<2>(in, gid, tig);
-        else
-          mm.template slices<1>(in, gid, tig);
-        __syncwarp();
-        lt += np;
-        j += np;
-      }
-    }
-    for (int64_t lt = lt_begin; lt < lt_end && !kMma; ++lt, ++j) {
+    for (int64_t lt = lt_begin; lt < lt_end; ++lt, ++j) {
       const int s = (int)(j % C::NSW);
       if (kMode == kModeDca) {
         const int v = dca_var(lt);
@@ -892,97 +822,117 @@ __global__ void __launch_bounds__(kThreads, kMode == kModeKv4 ? kDecodeCtasPerSm
       const uint8_t* sv = sk + C::SLICE;
       const bool full_tile = rows == kKPW && !x.streaming;
 
-      float sc[C::IT];
-      bool vis[C::IT];
-#pragma unroll
-      for (int it = 0; it < C::IT; ++it) {
-        const int key = it * C::KPI + kg;  // row within this warp's slice
-        bool valid = true;
+      if constexpr (kMma) {
+        uint32_t kvalid = 0xFu;  // keys 2 tig, 2 tig + 1, 2 tig + 8, 2 tig + 9 of the slice
         if (!full_tile) {
-          valid = key < rows;
-          if (x.streaming && valid) {
-            const int64_t slot = kt * kTK + (int64_t)warp * kKPW + key;
-            const int jp = str_pool ? (int)slot : __ldg(p.pos + (int64_t)x.b * SR + slot);
-            valid = jp >= 0 && jp <= x.pq && (jp < p.sh.S || x.pq - jp < p.sh.R);
+          kvalid = 0u;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int key = 2 * tig + (k & 1) + 8 * (k >> 1);
+            bool valid = key < rows;
+            if (x.streaming && valid) {
+              const int64_t slot = kt * kTK + (int64_t)warp * kKPW + key;
+              const int jp = str_pool ? (int)slot : __ldg(p.pos + (int64_t)x.b * SR + slot);
+              valid = jp >= 0 && jp <= x.pq && (jp < p.sh.S || x.pq - jp < p.sh.R);
+            }
+            kvalid |= (uint32_t)valid << k;
           }
         }
-        vis[it] = valid;
-        float2 acc[G];
+        mm.slice(SliceIn{sk, sv, sk + 2 * C::SLICE, sk + 2 * C::SLICE + C::PSLICE, kvalid, gid < G ? kvalid : 0u},
+                 gid, tig);
+      } else {
+        float sc[C::IT];
+        bool vis[C::IT];
 #pragma unroll
-        for (int l = 0; l < G; ++l) acc[l] = make_float2(0.f, 0.f);
-#pragma unroll
-        for (int ch = 0; ch < C::CH; ++ch) {
-          const uint4 kv = *reinterpret_cast<const uint4*>(sk + key * C::ROW + (cl + ch * C::LPK) * 16);
-          const uint32_t w4[4] = {kv.x, kv.y, kv.z, kv.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float2 k2 = unpack2(w4[e]);
-#pragma unroll
-            for (int l = 0; l < G; ++l) acc[l] = __ffma2_rn(q2[l][ch * 4 + e], k2, acc[l]);
+        for (int it = 0; it < C::IT; ++it) {
+          const int key = it * C::KPI + kg;  // row within this warp's slice
+          bool valid = true;
+          if (!full_tile) {
+            valid = key < rows;
+            if (x.streaming && valid) {
+              const int64_t slot = kt * kTK + (int64_t)warp * kKPW + key;
+              const int jp = str_pool ? (int)slot : __ldg(p.pos + (int64_t)x.b * SR + slot);
+              valid = jp >= 0 && jp <= x.pq && (jp < p.sh.S || x.pq - jp < p.sh.R);
+            }
           }
-        }
-        float dot[G];
+          vis[it] = valid;
+          float2 acc[G];
 #pragma unroll
-        for (int l = 0; l < G; ++l) dot[l] = acc[l].x + acc[l].y;
-        // reduce-scatter over the high lane bits: keep the low half of the slots
-#pragma unroll
-        for (int k = 1; k <= C::GB; ++k) {
-          const int half = G >> k;
-          const int bit = 1 << (C::LB - k);
-#pragma unroll
-          for (int l = 0; l < half; ++l) dot[l] += __shfl_xor_sync(0xffffffffu, dot[l + half], bit);
-        }
-        // butterfly over the remaining lane bits
-#pragma unroll
-        for (int b = C::LB - C::GB - 1; b >= 0; --b) dot[0] += __shfl_xor_sync(0xffffffffu, dot[0], 1 << b);
-        sc[it] = valid ? dot[0] : -INFINITY;
-      }
-
-      // tile max of this lane's head over the warp, lazy rescale
-      float mx = sc[0];
-#pragma unroll
-      for (int it = 1; it < C::IT; ++it) mx = fmaxf(mx, sc[it]);
-#pragma unroll
-      for (int off = C::LPK; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-      const bool grow = mx > m_run + 8.f;
-      if (__any_sync(0xffffffffu, grow)) {
-        const float f = grow ? ex2_approx(m_run - mx) : 1.f;  // 0 when m was -inf
-        if (grow) {
-          l_run *= f;
-          m_run = mx;
-        }
-#pragma unroll
-        for (int l = 0; l < G; ++l) {
-          const float fl = __shfl_xor_sync(0xffffffffu, f, l << (C::LB - C::GB));
-          const float2 f2 = make_float2(fl, fl);
-#pragma unroll
-          for (int e = 0; e < C::DPL / 2; ++e) o2[l][e] = __fmul2_rn(o2[l][e], f2);
-        }
-      }
-#pragma unroll
-      for (int it = 0; it < C::IT; ++it) {
-        const float pv = vis[it] ? ex2_approx(sc[it] - m_run) : 0.f;
-        sc[it] = pv;
-        l_run += pv;
-      }
-#pragma unroll
-      for (int it = 0; it < C::IT; ++it) {
-        float pl[G];
-        pl[0] = sc[it];
-#pragma unroll
-        for (int l = 1; l < G; ++l) pl[l] = __shfl_xor_sync(0xffffffffu, sc[it], l << (C::LB - C::GB));
-        if (full_tile || vis[it]) {
-          const int key = it * C::KPI + kg;
+          for (int l = 0; l < G; ++l) acc[l] = make_float2(0.f, 0.f);
 #pragma unroll
           for (int ch = 0; ch < C::CH; ++ch) {
-            const uint4 vv = *reinterpret_cast<const uint4*>(sv + key * C::ROW + (cl + ch * C::LPK) * 16);
-            const uint32_t w4[4] = {vv.x, vv.y, vv.z, vv.w};
+            const uint4 kv = *reinterpret_cast<const uint4*>(sk + key * C::ROW + (cl + ch * C::LPK) * 16);
+            const uint32_t w4[4] = {kv.x, kv.y, kv.z, kv.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const float2 v2 = unpack2(w4[e]);
+              const float2 k2 = unpack2(w4[e]);
 #pragma unroll
-              for (int l = 0; l < G; ++l)
-                o2[l][ch * 4 + e] = __ffma2_rn(make_float2(pl[l], pl[l]), v2, o2[l][ch * 4 + e]);
+              for (int l = 0; l < G; ++l) acc[l] = __ffma2_rn(q2[l][ch * 4 + e], k2, acc[l]);
+            }
+          }
+          float dot[G];
+#pragma unroll
+          for (int l = 0; l < G; ++l) dot[l] = acc[l].x + acc[l].y;
+          // reduce-scatter over the high lane bits: keep the low half of the slots
+#pragma unroll
+          for (int k = 1; k <= C::GB; ++k) {
+            const int half = G >> k;
+            const int bit = 1 << (C::LB - k);
+#pragma unroll
+            for (int l = 0; l < half; ++l) dot[l] += __shfl_xor_sync(0xffffffffu, dot[l + half], bit);
+          }
+          // butterfly over the remaining lane bits
+#pragma unroll
+          for (int b = C::LB - C::GB - 1; b >= 0; --b) dot[0] += __shfl_xor_sync(0xffffffffu, dot[0], 1 << b);
+          sc[it] = valid ? dot[0] : -INFINITY;
+        }
+
+        // tile max of this lane's head over the warp, lazy rescale
+        float mx = sc[0];
+#pragma unroll
+        for (int it = 1; it < C::IT; ++it) mx = fmaxf(mx, sc[it]);
+#pragma unroll
+        for (int off = C::LPK; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+        const bool grow = mx > m_run + 8.f;
+        if (__any_sync(0xffffffffu, grow)) {
+          const float f = grow ? ex2_approx(m_run - mx) : 1.f;  // 0 when m was -inf
+          if (grow) {
+            l_run *= f;
+            m_run = mx;
+          }
+#pragma unroll
+          for (int l = 0; l < G; ++l) {
+            const float fl = __shfl_xor_sync(0xffffffffu, f, l << (C::LB - C::GB));
+            const float2 f2 = make_float2(fl, fl);
+#pragma unroll
+            for (int e = 0; e < C::DPL / 2; ++e) o2[l][e] = __fmul2_rn(o2[l][e], f2);
+          }
+        }
+#pragma unroll
+        for (int it = 0; it < C::IT; ++it) {
+          const float pv = vis[it] ? ex2_approx(sc[it] - m_run) : 0.f;
+          sc[it] = pv;
+          l_run += pv;
+        }
+#pragma unroll
+        for (int it = 0; it < C::IT; ++it) {
+          float pl[G];
+          pl[0] = sc[it];
+#pragma unroll
+          for (int l = 1; l < G; ++l) pl[l] = __shfl_xor_sync(0xffffffffu, sc[it], l << (C::LB - C::GB));
+          if (full_tile || vis[it]) {
+            const int key = it * C::KPI + kg;
+#pragma unroll
+            for (int ch = 0; ch < C::CH; ++ch) {
+              const uint4 vv = *reinterpret_cast<const uint4*>(sv + key * C::ROW + (cl + ch * C::LPK) * 16);
+              const uint32_t w4[4] = {vv.x, vv.y, vv.z, vv.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float2 v2 = unpack2(w4[e]);
+#pragma unroll
+                for (int l = 0; l < G; ++l)
+                  o2[l][ch * 4 + e] = __ffma2_rn(make_float2(pl[l], pl[l]), v2, o2[l][ch * 4 + e]);
+              }
             }
           }
         }

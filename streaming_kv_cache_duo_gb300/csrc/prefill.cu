@@ -225,22 +225,20 @@ struct PagedWalk {
 // Dual Chunk Attention: which query vectors (0 query, 1 query_succ, 2 query_inter)
 // the 256 query rows of a block use against a key tile. chunk_len and the cache
 // length n are multiples of 256, so the block and every tile lie in one chunk each;
-// the block's chunk gives two thresholds on the absolute key tile (cache tile k is
-// tile k, new-token tile k is tile n / 128 + k), worked out once per CTA.
+// the block's chunk gives two thresholds on the absolute key tile, worked out once
+// per CTA. Every head is a retrieval head here, so an item's tiles are the cache
+// tiles 0 ... n / 128 - 1 followed by the new-token tiles, and the j-th tile of the
+// item is absolute key tile j: the variant needs no tile lookup (the MMA thread
+// evaluates it for every tile, on the critical path).
 struct DcaTiles {
   int t_intra;  // first key tile of the query block's chunk
   int t_succ;   // first key tile of the chunk before it
-  int base;     // absolute tile of the first new token
   __device__ __forceinline__ void init(const PrefillParams& p, int qp) {
     const int tpc = p.chunk_len / BN;
-    base = (int)(p.n / BN);
     t_intra = (int)((p.n + (int64_t)qp * kRows) / p.chunk_len) * tpc;
     t_succ = t_intra - tpc;
   }
-  __device__ __forceinline__ int var(const Tile& t) const {
-    const int kt = t.phase == 0 ? t.k : base + t.k;
-    return kt >= t_intra ? 0 : (kt >= t_succ ? 1 : 2);
-  }
+  __device__ __forceinline__ int var(int j) const { return j >= t_intra ? 0 : (j >= t_succ ? 1 : 2); }
 };
 
 __device__ __forceinline__ const CUtensorMap* dca_map(const PrefillParams& p, int v) {
@@ -359,7 +357,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         DcaTiles dt;
         if (kMode == kModeDca) {
           dt.init(p, it.qp);
-          qvar = ntiles > 0 ? dt.var(tile_at<kMode>(pl, 0)) : 0;
+          qvar = ntiles > 0 ? dt.var(0) : 0;
           qmap = dca_map(p, qvar);
         }
         prefetch_tmap(qmap);
@@ -385,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         for (; j < ntiles && ok; ++j) {
           const Tile t = tile_at<kMode>(pl, j);
           if (kMode == kModeDca) {
-            const int v = dt.var(t);
+            const int v = dt.var(j);
             if (v != qvar) {
               // the S MMAs that read the previous query vectors have completed
               if (!mbar_wait(&bars->q_free, (uint32_t)((q_loads - 1) & 1), err, kErrPrefillProducer)) {
@@ -514,7 +512,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         int qv = 0;
         if (kMode == kModeDca) {
           dt.init(p, it.qp);
-          qv = ntiles > 0 ? dt.var(tile_at<kMode>(pl, 0)) : 0;
+          qv = ntiles > 0 ? dt.var(0) : 0;
         }
         uint32_t qph = 0;
         for (int j = 0; j < ntiles && ok; ++j) {
@@ -522,7 +520,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
           const bool more = j + 1 < ntiles;
           bool qswitch = false;
           if (kMode == kModeDca && more) {
-            const int v = dt.var(tile_at<kMode>(pl, j + 1));
+            const int v = dt.var(j + 1);
             if (v != qv) {
               // S_0(j) and S_1(j), issued before this commit, were the last reads of
               // the current vectors; the producer reloads the buffer once they finish
