@@ -235,7 +235,9 @@ struct DcaTiles {
   int t_succ;   // first key tile of the chunk before it
   __device__ __forceinline__ void init(const PrefillParams& p, int qp) {
     const int tpc = p.chunk_len / BN;
-    t_intra = (int)((p.n + (int64_t)qp * kRows) / p.chunk_len) * tpc;
+    // 32-bit: positions stay below 2^31 (checked on the host); a 64-bit division here
+    // made the whole DCA prefill 7 % slower
+    t_intra = (((int)p.n + qp * kRows) / p.chunk_len) * tpc;
     t_succ = t_intra - tpc;
   }
   __device__ __forceinline__ int var(int j) const { return j >= t_intra ? 0 : (j >= t_succ ? 1 : 2); }
