@@ -76,8 +76,12 @@ def test_decode_matches_oracle(case):
             assert_close(got[b, s], ref, f"b{b} step {s}")
 
 
-def test_poisoned_cache_tail_is_never_read():
-    case = (2, 8, 4, 128, 4, 64, [0, 1, 1, 0], 150, 6)
+@pytest.mark.parametrize("case", [
+    (2, 8, 4, 128, 4, 64, [0, 1, 1, 0], 150, 6),     # g = 2: CUDA-core consumer
+    (2, 16, 4, 128, 4, 64, [0, 1, 1, 0], 150, 6),    # g = 4: tensor-core slices
+    (1, 16, 2, 64, 5, 27, [1, 0], 333, 4),           # g = 8, D 64, partial tiles
+], ids=["g2", "g4", "g8"])
+def test_poisoned_cache_tail_is_never_read(case):
     clean, _ = _decode_run(3, *case)
     dirty, _ = _decode_run(3, *case, poison=True)
     assert torch.isfinite(dirty.float()).all()

@@ -22,10 +22,15 @@ def _bits(sz):
     return (u & 0xFFFF).astype(np.uint16).view(np.float16), (u >> 16).astype(np.uint16).view(np.float16)
 
 
-def _run(seed, B, Hq, Hkv, D, S, R, kinds, ctx, steps, chunk=None):
+def _run(seed, B, Hq, Hkv, D, S, R, kinds, ctx, steps, chunk=None, poison=False):
     from streaming_kv_cache_duo_gb300 import DuoKv4Layer, duo_device_error
     total = ctx + steps
     layer = DuoKv4Layer(B, Hq, Hkv, D, S, R, total, kinds)
+    if poison:  # codes 0xFF and (NaN, NaN) pairs wherever nothing has been appended
+        for t in (layer.k_codes, layer.v_codes, layer.ks_codes, layer.vs_codes):
+            t.fill_(0xFF)
+        for t in (layer.k_sz, layer.v_sz, layer.ks_sz, layer.vs_sz):
+            t.fill_(0x7E007E00)
     K = device_stream(seed, ds.STREAM_K, B, 0, total, Hkv, D, "cuda")
     V = device_stream(seed, ds.STREAM_V, B, 0, total, Hkv, D, "cuda")
     Q = device_stream(seed, ds.STREAM_Q, B, 0, total, Hq, D, "cuda")
@@ -127,3 +132,45 @@ def test_kv4_argument_checks():
     with pytest.raises(DuoError, match="DUO_ERR_CAPACITY"):
         layer.append(torch.zeros((1, 33, 2, 64), dtype=torch.bfloat16, device="cuda"),
                      torch.zeros((1, 33, 2, 64), dtype=torch.bfloat16, device="cuda"))
+
+
+def test_kv4_poisoned_tail_is_never_used():
+    """Decode copies whole 16-row chunks, so rows past the tokens held (and empty ring
+    slots) reach shared memory: their codes and NaN (scale, zero) pairs must not reach
+    the output. Every GQA grouping and both head dims, against an unpoisoned run."""
+    for case in [(2, 8, 4, 128, 4, 64, [1, 0, 1, 0], 150, 3, None),     # g = 2
+                 (1, 16, 4, 64, 3, 29, [0, 1, 1, 0], 301, 3, 100),      # g = 4, D 64
+                 (2, 16, 2, 128, 8, 40, [1, 0], 77, 4, None)]:          # g = 8
+        _, clean = _run(31, *case)
+        _, dirty = _run(31, *case, poison=True)
+        for a, b in zip(clean, dirty):
+            assert torch.isfinite(b.float()).all()
+            assert torch.equal(a, b)
+
+
+def test_kv4_wide_value_rows_do_not_overflow_fp16():
+    """V rows 1024 times wider than the generator's (exact in bf16; |v| up to ~5000, row
+    scales ~650): p (up to 2^8 under the lazy rescale) times the row scale would pass
+    the fp16 maximum if stored unscaled; the decode must still match the oracle."""
+    from streaming_kv_cache_duo_gb300 import DuoKv4Layer, duo_device_error
+    B, Hq, Hkv, D, S, R, kinds, ctx, steps = 1, 16, 4, 128, 4, 64, [1, 0, 1, 1], 900, 3
+    seed = 77
+    total = ctx + steps
+    layer = DuoKv4Layer(B, Hq, Hkv, D, S, R, total, kinds)
+    K = device_stream(seed, ds.STREAM_K, B, 0, total, Hkv, D, "cuda")
+    V = device_stream(seed, ds.STREAM_V, B, 0, total, Hkv, D, "cuda") * 1024
+    Q = device_stream(seed, ds.STREAM_Q, B, 0, total, Hq, D, "cuda")
+    layer.append(K[:, :ctx].contiguous(), V[:, :ctx].contiguous())
+    Kq = kv4.roundtrip(host_stream(seed, ds.STREAM_K, B, 0, total, Hkv, D).astype(np.float32))
+    Vq = kv4.roundtrip((host_stream(seed, ds.STREAM_V, B, 0, total, Hkv, D) * 1024).astype(np.float32))
+    Qh = host_stream(seed, ds.STREAM_Q, B, 0, total, Hq, D)
+    for s in range(steps):
+        p = ctx + s
+        layer.append(K[:, p:p + 1].contiguous(), V[:, p:p + 1].contiguous())
+        o = layer.decode(Q[:, p].contiguous())
+        torch.cuda.synchronize()
+        assert duo_device_error() == 0
+        cache = OracleCache(kinds, S, R, D)
+        cache.append(Kq[0, :p + 1], Vq[0, :p + 1])
+        ref = decode_from_cache(Qh[0, p], p, cache)
+        assert_close(to_np(o[0]) / 1024, ref / 1024, f"step {s}")
