@@ -249,7 +249,14 @@ duo_status duo_attn_decode_paged(duo_handle* handle, const duo_kv_cache* cache, 
  * used. duo_kv_append_kv4 quantizes and stores the new tokens (same slot rule as
  * duo_kv_append); duo_attn_decode_kv4 is duo_attn_decode over these arrays, with the
  * dequantization folded into the dot products (q . k = scale (q . codes) + zero sum(q)).
- * Prefill never reads a cache in this form: chunked prefill needs the bf16 caches. */
+ * Prefill never reads a cache in this form: chunked prefill needs the bf16 caches.
+ *
+ * duo_attn_decode_kv4 runs its dot products on the tensor cores with fp16 operands
+ * (codes, q, and p times the row scale, stored as p scale / 64) and fp32 accumulation,
+ * so q must lie within the fp16 range as well (bf16 values there convert exactly).
+ * Its workspace is the one duo_decode_workspace_size gives; it launches two CTAs per
+ * SM. Errors: as duo_attn_decode, plus DUO_ERR_INVALID_ARG for a NULL or misaligned
+ * array the handle's head kinds need (every array 16-byte aligned). */
 typedef struct {
   void* k_codes;
   void* v_codes;
