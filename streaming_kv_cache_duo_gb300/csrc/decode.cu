@@ -16,7 +16,8 @@
 // streams its own rows of K and V into a private 3-stage shared-memory ring with
 // 1-D bulk copies (cp.async.bulk, completion on the warp's mbarrier). A warp
 // refills a stage as soon as it has finished with it, so no producer warp and no
-// cross-warp hand-off is needed, and each thread keeps up to 255 registers.
+// cross-warp hand-off is needed, and each thread keeps up to 255 registers. The
+// 4-bit decode keeps 4 stages per warp and runs two CTAs per SM (128 registers).
 //
 // Inside a warp, LPK lanes share a key row and each owns 16 (or 8) of its dims:
 // 128-bit shared loads, fp32 q pre-scaled by log2(e)/sqrt(D), packed fp32x2 FMAs
@@ -28,10 +29,10 @@
 // step a plain add). The softmax then runs once per (key, head), the online
 // state (running max with lazy rescaling: it moves only when a score exceeds it
 // by 2^8, and running sum) is per lane for its head, and p of the other heads is
-// fetched by shuffles for the packed p.v FMAs. With eight query heads per KV head,
-// and for 4-bit caches, a warp's slice is instead two warp-level tensor-core MMAs
-// (S = Q K^T, then O^T += V^T P^T; see MmaSlice), which takes the per-element FMAs
-// off the CUDA cores that bound those cases.
+// fetched by shuffles for the packed p.v FMAs. With four or more query heads per KV
+// head, and for 4-bit caches, a warp's slice is instead two warp-level tensor-core
+// MMAs (S = Q K^T, then O^T += V^T P^T; see MmaSlice), which takes the per-element
+// FMAs off the CUDA cores that bound those cases.
 //
 // Merge. The part of a unit a CTA covers ("segment") ends with a cross-warp merge
 // in shared memory. A unit covered by one CTA is written out directly; otherwise
