@@ -48,8 +48,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 L2_BYTES = 129e6  # GB300 L2 capacity
 
 MEASURED_TRAFFIC = {
-    "prefill": {"src": ("prefill.cu", "duo_device.cuh", "duo_internal.h"), "sha1": "219447b8fbd07302",
-                "bytes": 572.471040e6 + 232.317440e6},
+    "prefill": {"src": ("prefill.cu", "duo_device.cuh", "duo_internal.h"), "sha1": "62c17fdf8e6b211d",
+                "bytes": 570.448896e6 + 231.574272e6},
     "decode": {"src": ("decode.cu", "duo_device.cuh", "duo_internal.h"), "sha1": "5ae6c083af1a8e30",
                "bytes": 1.074862e9 + 3.666176e6},
 }

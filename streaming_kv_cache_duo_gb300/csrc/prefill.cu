@@ -253,44 +253,43 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
   return r;
 }
 
+// Bits [0, hi) of a 32-bit word (hi clamped to 0 ... 32).
+__device__ __forceinline__ uint32_t bits_below(int hi) {
+  return hi <= 0 ? 0u : (hi >= 32 ? 0xffffffffu : (1u << hi) - 1u);
+}
+
 // Sets masked scores of one 32-column chunk to -inf (columns c0 ... c0+31 of tile t).
+// Where the chunk's keys are consecutive positions j0 ... j0+31, the keys row i_abs
+// sees form at most two runs (the sinks j < S, and j in (i - R, i]), so the chunk's
+// visibility is a 32-bit mask built from a few shifts, applied with one bit test per
+// score; ring-cache slots are looked up one by one.
 template <int kMode>
 __device__ __forceinline__ void mask_chunk(float* v, const PrefillParams& p, const Item& it, const Tile& t, int c0,
                                            int i_abs) {
   const int S = p.sh.S, R = p.sh.R;
-  if (t.phase == 1) {
-    const int j0 = (int)p.n + t.k * BN + c0;
-#pragma unroll
-    for (int e = 0; e < 32; ++e) {
-      const int jp = j0 + e;
-      const int d = i_abs - jp;
-      const bool vis = d >= 0 && (!it.streaming || jp < S || d < R);
-      if (!vis) v[e] = -INFINITY;
-    }
+  uint32_t vis;
+  if (t.phase == 1 || (kMode == kModePool && it.streaming)) {
+    // new tokens (j0 = n + tile start), or a streaming head in the pool (row = position)
+    const int j0 = t.phase == 1 ? (int)p.n + t.k * BN + c0 : t.k * BN + c0;
+    const int d0 = i_abs - j0;  // column e is the key d0 - e positions back
+    vis = bits_below(d0 + 1);   // causal: e <= d0
+    if (it.streaming) vis &= bits_below(S - j0) | ~bits_below(d0 - R + 1);  // sink, or inside the window
+    if (t.phase == 0) vis &= bits_below((int)p.n - j0);                        // rows >= n hold no token
   } else if (!it.streaming) {
-    const int lim = (int)p.n - t.k * BN - c0;  // rows >= n hold no token
-#pragma unroll
-    for (int e = 0; e < 32; ++e)
-      if (e >= lim) v[e] = -INFINITY;
-  } else if (kMode == kModePool) {
-    // a streaming head in the pool: row = position; rows >= n hold no token
-    const int j0 = t.k * BN + c0;
-#pragma unroll
-    for (int e = 0; e < 32; ++e) {
-      const int jp = j0 + e;
-      const bool vis = jp < p.n && jp <= i_abs && (jp < S || i_abs - jp < R);
-      if (!vis) v[e] = -INFINITY;
-    }
+    vis = bits_below((int)p.n - t.k * BN - c0);  // rows >= n hold no token
   } else {
     const int32_t* prow = p.pos + (int64_t)it.b * (S + R);
+    vis = 0u;
 #pragma unroll
     for (int e = 0; e < 32; ++e) {
       const int slot = t.k * BN + c0 + e;
       const int jp = slot < p.nvalid ? __ldg(prow + slot) : -1;
-      const bool vis = jp >= 0 && jp <= i_abs && (jp < S || i_abs - jp < R);
-      if (!vis) v[e] = -INFINITY;
+      vis |= (uint32_t)(jp >= 0 && jp <= i_abs && (jp < S || i_abs - jp < R)) << e;
     }
   }
+#pragma unroll
+  for (int e = 0; e < 32; ++e)
+    if (!((vis >> e) & 1u)) v[e] = -INFINITY;
 }
 
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
