@@ -17,10 +17,14 @@ from gpu_util import assert_close, device_stream, to_np
 pytestmark = pytest.mark.gpu
 
 
-def test_static_scratch_decode_matches_workspace_decode():
+@pytest.mark.parametrize("B,Hq,Hkv,kinds", [
+    (2, 8, 4, [1, 0, 0, 1]),             # g = 2: CUDA-core consumer
+    (1, 32, 8, [1, 0, 0, 0, 0, 0, 1, 0]),  # g = 4: tensor-core slices
+    (2, 16, 2, [0, 1]),                  # g = 8
+], ids=["g2", "g4", "g8"])
+def test_static_scratch_decode_matches_workspace_decode(B, Hq, Hkv, kinds):
     from streaming_kv_cache_duo_gb300 import DuoLayer, _lib, duo_device_error
-    B, Hq, Hkv, D, S, R, ctx = 2, 8, 4, 128, 4, 64, 3000
-    kinds = [1, 0, 0, 1]
+    D, S, R, ctx = 128, 4, 64, 3000
     layer = DuoLayer(B, Hq, Hkv, D, S, R, ctx + 2, kinds)
     seed = 31
     layer.append(device_stream(seed, ds.STREAM_K, B, 0, ctx, Hkv, D, "cuda"),
