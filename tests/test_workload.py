@@ -33,3 +33,35 @@ def test_append_survivors(S, R):
     for n in [0, 1, S, S + R, 1000]:
         for T in [1, 3, R, R + 7, 5000]:
             assert wl.append_survivors(n, T, S, R) == len(oracle.append_survivors(n, T, S, R))
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,D,S,R,kinds,n", [
+    (1, 32, 8, 128, 64, 256, [1, 0, 0, 0, 0, 0, 1, 0], 1 << 20),
+    (8, 32, 8, 128, 64, 256, [0, 1, 0, 0, 1, 0, 0, 0], 131073),
+    (1, 4, 4, 64, 4, 32, [1, 0, 1, 0], 17),       # ring not yet full
+    (2, 16, 2, 128, 0, 1, [0, 1], 5),             # window of one
+    (1, 8, 4, 64, 8, 40, [0, 0, 0, 0], 1000),     # no retrieval head
+])
+def test_decode_bytes_count_what_the_cache_holds(B, Hq, Hkv, D, S, R, kinds, n):
+    """Decode reads each held K and V row once per KV head: a retrieval head holds n
+    rows, a streaming head the slots the ring model has filled after n appends (each
+    with its int32 position), plus q and o; 4-bit rows are D / 2 bytes of codes and a
+    4-byte (scale, zero) pair."""
+    sim = oracle.RingCacheSim(S, R)
+    sim.append(n)
+    held = sum(1 for x in sim.positions() if x >= 0)
+    n_ret = sum(kinds)
+    n_str = Hkv - n_ret
+    qo = 2 * B * Hq * D * 2
+    assert wl.decode_bytes(B, Hq, Hkv, D, S, R, kinds, n) == (
+        B * n_ret * n * 2 * D * 2, B * n_str * held * (2 * D * 2 + 4), qo)
+    assert wl.decode_bytes_kv4(B, Hq, Hkv, D, S, R, kinds, n) == (
+        B * n_ret * n * 2 * (D // 2 + 4), B * n_str * held * (2 * (D // 2 + 4) + 4), qo)
+
+
+def test_decode_bytes_of_the_million_token_step():
+    # 2 retrieval KV heads of 1,048,577 rows x 512 bytes (K + V, bf16, D 128) ~ 1.074 GB
+    br, bs, bq = wl.decode_bytes(1, 32, 8, 128, 64, 256, [1, 1, 0, 0, 0, 0, 0, 0], 1048577)
+    assert br == 2 * 1048577 * 512
+    assert bs == 6 * 320 * 516 and bq == 2 * 32 * 128 * 2
+    assert abs(br + bs + bq - 1.0748e9) < 1e6
