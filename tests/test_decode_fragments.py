@@ -1,0 +1,160 @@
+"""The fragment layouts of the decode's tensor-core slices, emulated lane by lane on
+the CPU (no GPU, no library code). The kernel builds its m16n8k16 operands so that
+every lane reads whole pieces of shared memory with no shuffles, which requires
+permuting the head dims inside a k-step and the rows of O^T; these tests rebuild the
+A / B / C matrices from the per-lane fragment contents exactly as the PTX ISA defines
+the m16n8k16 .row.col layout, and check that the products equal q . k and p . v for
+both cache formats (bf16 rows, and 4-bit codes placed under fp16 magic exponents)."""
+
+import numpy as np
+import pytest
+
+LANES = [(l >> 2, l & 3) for l in range(32)]  # (gid, tig)
+
+
+def mma(afr, bfr):
+    """C (16 x 8) = A (16 x 16) B (16 x 8) from per-lane fragments: afr[lane] =
+    (a0, a1, a2, a3), each a pair (low, high) of values; bfr[lane] = (b0, b1)."""
+    A = np.full((16, 16), np.nan)
+    B = np.full((16, 8), np.nan)
+    for lane, (g, t) in enumerate(LANES):
+        a0, a1, a2, a3 = afr[lane]
+        for e in range(2):
+            A[g, 2 * t + e], A[g + 8, 2 * t + e] = a0[e], a1[e]
+            A[g, 2 * t + 8 + e], A[g + 8, 2 * t + 8 + e] = a2[e], a3[e]
+        b0, b1 = bfr[lane]
+        for e in range(2):
+            B[2 * t + e, g], B[2 * t + 8 + e, g] = b0[e], b1[e]
+    assert not np.isnan(A).any() and not np.isnan(B).any()
+    C = A @ B
+    return [((C[g, 2 * t], C[g, 2 * t + 1]), (C[g + 8, 2 * t], C[g + 8, 2 * t + 1])) for g, t in LANES]
+
+
+def half_bits_value(bits):
+    return float(np.array([bits], np.uint16).view(np.float16)[0])
+
+
+def fp16_pair(word):
+    return half_bits_value(word & 0xFFFF), half_bits_value(word >> 16)
+
+
+def byte_perm(x, y, sel):
+    src = [(x >> (8 * i)) & 0xFF for i in range(4)] + [(y >> (8 * i)) & 0xFF for i in range(4)]
+    return sum(src[(sel >> (4 * i)) & 7] << (8 * i) for i in range(4))
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("G", [1, 2, 4, 8])
+def test_bf16_scores(D, G):
+    """S = Q K^T: lane tig takes 16-byte chunk tig + 4u of a row, i.e. k-index 2 tig + i
+    (+ 8) of k-step 2u + e is dim 8 (tig + 4u) + 4e + i (+ 2)."""
+    rng = np.random.default_rng(D + G)
+    q = rng.standard_normal((G, D))
+    k = rng.standard_normal((16, D))
+    S = np.zeros((G, 16))
+    for j in range(2):  # n-tiles: keys gid, gid + 8
+        acc = np.zeros((16, 8))
+        for s in range(D // 16):
+            u, e = divmod(s, 2)
+            afr, bfr = [], []
+            for g, t in LANES:
+                c = t + 4 * u
+                d = [8 * c + 4 * e + i for i in range(4)]  # the chunk's words 2e and 2e + 1
+                qrow = q[g] if g < G else np.zeros(D)
+                afr.append(((qrow[d[0]], qrow[d[1]]), (0, 0), (qrow[d[2]], qrow[d[3]]), (0, 0)))
+                krow = k[g + 8 * j]
+                bfr.append(((krow[d[0]], krow[d[1]]), (krow[d[2]], krow[d[3]])))
+            out = mma(afr, bfr)
+            for lane, (g, t) in enumerate(LANES):
+                (c0, c1), _ = out[lane]
+                acc[g, 2 * t] += c0
+                acc[g, 2 * t + 1] += c1
+        S[:, 8 * j:8 * j + 8] = acc[:G]
+    assert np.allclose(S, q @ k.T)
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_kv4_scores_with_folded_offsets(D):
+    """4-bit K: word w = (D/32) tig + u of a row holds dims 8w ... 8w+7 (nibble n = dim
+    8w + n); k-index 2 tig + i (+ 8) of k-step 2u + e is dim 8w + 2e + 4i (+ 1); codes
+    read as 1024 + c (bits 0-3) or 64 + c (bits 4-7), so q . c = S - sum q_d off_d."""
+    G = 8
+    rng = np.random.default_rng(D)
+    q = np.round(rng.standard_normal((G, D)) * 64) / 64  # exact in fp16
+    codes = rng.integers(0, 16, (16, D))
+    packed = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)  # [16, D/2]
+    words = np.ascontiguousarray(packed).view("<u4")  # [16, D/8]: word w = bytes 4w ... 4w+3
+    WPT = D // 32
+    lo, hi = 0x64006400, 0x54005400
+    S = np.zeros((G, 16))
+    for j in range(2):
+        acc = np.zeros((16, 8))
+        for s in range(D // 16):
+            u, e = divmod(s, 2)
+            afr, bfr = [], []
+            for g, t in LANES:
+                w = WPT * t + u
+                dims = [8 * w + 2 * e + 4 * i for i in range(2)]  # k = 2 tig + i
+                dims8 = [d + 1 for d in dims]                       # k = 2 tig + 8 + i
+                afr.append(((q[g, dims[0]], q[g, dims[1]]), (0, 0), (q[g, dims8[0]], q[g, dims8[1]]), (0, 0)))
+                x = int(words[g + 8 * j, w]) >> (8 * e)
+                bfr.append((fp16_pair((x & 0x000F000F) | lo), fp16_pair((x & 0x00F000F0) | hi)))
+            out = mma(afr, bfr)
+            for lane, (g, t) in enumerate(LANES):
+                (c0, c1), _ = out[lane]
+                acc[g, 2 * t] += c0
+                acc[g, 2 * t + 1] += c1
+        S[:, 8 * j:8 * j + 8] = acc[:G]
+    off = (q[:, 0::2] * 1024).sum(1) + (q[:, 1::2] * 64).sum(1)
+    assert np.allclose(S - off[:, None], q @ codes.T)
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("G", [1, 4, 8])
+@pytest.mark.parametrize("kv4", [False, True])
+def test_output_rows(D, G, kv4):
+    """O^T += V^T P^T: m-tile i, row gid (gid + 8) is dim (D/8) gid + 2i (+ 1); the P^T
+    fragment of lane (gid, tig) holds head gid's p of keys 2 tig, 2 tig + 1, 2 tig + 8,
+    2 tig + 9; every (head < G, dim) comes out of exactly one lane and fragment slot."""
+    rng = np.random.default_rng(D * G + kv4)
+    DT = D // 8
+    p = rng.random((8, 16))
+    p[G:] = 0
+    if kv4:
+        codes = rng.integers(0, 16, (16, D))
+        packed = np.ascontiguousarray((codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8))
+        V = codes.astype(float)
+    else:
+        V = rng.standard_normal((16, D))
+    O = np.full((G, D), np.nan)
+    kr = lambda t: [2 * t, 2 * t + 1, 2 * t + 8, 2 * t + 9]
+    for i in range(D // 16):
+        afr, bfr = [], []
+        for g, t in LANES:
+            k0, k1, k2, k3 = kr(t)
+            if kv4:
+                VB = D // 16  # bytes of a lane per row: byte i is this m-tile's
+                sel = (i & 3) * 0x11 + (4 + (i & 3)) * 0x1100
+                word = lambda key: int(np.ascontiguousarray(packed[key, VB * g:VB * g + VB]).view("<u4")[i >> 2])
+                y01 = byte_perm(word(k0), word(k1), sel)
+                y89 = byte_perm(word(k2), word(k3), sel)
+                a0 = tuple(v - 1024 for v in fp16_pair((y01 & 0x000F000F) | 0x64006400))
+                a1 = tuple(v - 64 for v in fp16_pair((y01 & 0x00F000F0) | 0x54005400))
+                a2 = tuple(v - 1024 for v in fp16_pair((y89 & 0x000F000F) | 0x64006400))
+                a3 = tuple(v - 64 for v in fp16_pair((y89 & 0x00F000F0) | 0x54005400))
+            else:
+                d0 = DT * g + 2 * i
+                a0, a1 = (V[k0, d0], V[k1, d0]), (V[k0, d0 + 1], V[k1, d0 + 1])
+                a2, a3 = (V[k2, d0], V[k3, d0]), (V[k2, d0 + 1], V[k3, d0 + 1])
+            afr.append((a0, a1, a2, a3))
+            bfr.append(((p[g, k0], p[g, k1]), (p[g, k2], p[g, k3])))
+        out = mma(afr, bfr)
+        for lane, (g, t) in enumerate(LANES):
+            (c0, c1), (c2, c3) = out[lane]
+            d = DT * g + 2 * i
+            for h, (v_even, v_odd) in ((2 * t, (c0, c2)), (2 * t + 1, (c1, c3))):
+                if h < G:
+                    assert np.isnan(O[h, d]) and np.isnan(O[h, d + 1])
+                    O[h, d], O[h, d + 1] = v_even, v_odd
+    assert not np.isnan(O).any()
+    assert np.allclose(O, p[:G] @ V)
