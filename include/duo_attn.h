@@ -159,9 +159,10 @@ size_t duo_decode_workspace_size(const duo_handle* handle, int64_t n);
  * KV head for all its query heads. The keys are split over the GPU's SMs; partial
  * softmaxes (o, max, sum) go to `workspace` and are merged by log-sum-exp.
  * workspace: device memory of at least duo_decode_workspace_size(handle, n) bytes,
- * 256-byte aligned. It keeps per-head counters that each call leaves at zero; the
- * library clears them itself the first time it sees a workspace address and after any
- * error. Calls sharing one workspace must be ordered on the GPU (same stream). */
+ * 256-byte aligned. Its first bytes are per-(sequence, KV head) arrival counters,
+ * which every call clears on `stream` before its kernel (one cudaMemsetAsync of
+ * ceil(B Hkv 4 / 256) 256 bytes), so the memory may hold anything between calls.
+ * Calls sharing one workspace must be ordered on the GPU (same stream). */
 duo_status duo_attn_decode(duo_handle* handle, const duo_kv_cache* cache, const void* q, void* o, void* workspace,
                            size_t workspace_bytes, void* stream);
 
@@ -175,8 +176,9 @@ duo_status duo_attn_decode(duo_handle* handle, const duo_kv_cache* cache, const 
  * of g (D + 4) floats per CTA and per (sequence, KV head), with one CTA per SM, plus
  * the counters) exceeds 2 MiB get DUO_ERR_WORKSPACE. Nothing is
  * allocated: no cudaMalloc, cudaFree or allocating library call. The first call on
- * each device looks up the array's device address (cudaGetSymbolAddress); make that
- * first call before any stream capture. Each call clears the array's counters with
+ * each device, and the first in any other CUDA context made current there later (after
+ * cudaDeviceReset, say), looks up the array's device address (cudaGetSymbolAddress);
+ * make that first call before any stream capture. Each call clears the array's counters with
  * cudaMemsetAsync on `stream`. All calls on a device share the one array, so calls
  * that overlap on the GPU (different streams, or several host threads) race: order
  * them on one stream. */

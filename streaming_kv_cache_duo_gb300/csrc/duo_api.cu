@@ -4,7 +4,6 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
-#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -21,10 +20,6 @@ using namespace duo;
 namespace {
 
 thread_local std::string g_last_error;
-
-// Bumped whenever duo_device_error() finds that a kernel gave up a wait: decode
-// counters may then be left nonzero, so every handle clears them again.
-std::atomic<unsigned> g_error_epoch{0};
 
 duo_status fail(duo_status st, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
 duo_status fail(duo_status st, const char* fmt, ...) {
@@ -61,9 +56,6 @@ struct duo_handle {
   int device;
   int num_sms;
   EncodeTiledFn encode;
-  const void* last_workspace;  // counters known to be zero for this address
-  bool workspace_dirty;
-  unsigned epoch;
 };
 
 namespace {
@@ -220,7 +212,6 @@ duo_status duo_set_head_mask(duo_handle* h, const uint8_t* is_retrieval) {
   if (st != DUO_OK) return st;
   if (!is_retrieval) return fail(DUO_ERR_INVALID_ARG, "is_retrieval is NULL");
   set_heads(h, is_retrieval);
-  h->workspace_dirty = true;  // the number of units may have changed
   return ok();
 }
 
@@ -250,9 +241,6 @@ duo_status duo_create(const duo_config* cfg, const uint8_t* is_retrieval, duo_ha
   if (!h) return fail(DUO_ERR_INVALID_ARG, "out of host memory");
   h->cfg = c;
   set_heads(h, is_retrieval);
-  h->last_workspace = nullptr;
-  h->workspace_dirty = true;
-  h->epoch = g_error_epoch.load();
 
   cudaError_t e = cudaGetDevice(&h->device);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device);
@@ -566,14 +554,11 @@ static duo_status decode_impl(duo_handle* h, const duo_kv_cache* c, const duo_pa
   decode_plan(h, c->n, &p, ctas_per_sm);
   const int64_t U = (int64_t)sh.B * sh.Hkv;
   const size_t counter_bytes = ((size_t)U * 4 + 255) / 256 * 256;
-  const unsigned epoch = g_error_epoch.load();
-  if (workspace != h->last_workspace || h->workspace_dirty || epoch != h->epoch) {
-    cudaError_t e = cudaMemsetAsync(workspace, 0, counter_bytes, (cudaStream_t)stream);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(workspace counters)");
-    h->last_workspace = workspace;
-    h->workspace_dirty = false;
-    h->epoch = epoch;
-  }
+  // The arrival counters must start at zero. The kernel leaves them at zero, but the
+  // caller may have lent the workspace's memory to other data since the last call (a
+  // caching allocator does), so every call clears them: U x 4 bytes, on the stream.
+  cudaError_t me = cudaMemsetAsync(workspace, 0, counter_bytes, (cudaStream_t)stream);
+  if (me != cudaSuccess) return cuda_fail(me, "cudaMemsetAsync(workspace counters)");
   p.q = static_cast<const uint16_t*>(q);
   p.o = static_cast<uint16_t*>(o);
   p.k_full = static_cast<const uint16_t*>(c->k_full);
@@ -620,10 +605,7 @@ static duo_status decode_impl(duo_handle* h, const duo_kv_cache* c, const duo_pa
     p.tiles_s = (int)(st_tiles + (te > wl ? te - wl : 0));
   }
   cudaError_t ce = launch_decode(p, (cudaStream_t)stream);
-  if (ce != cudaSuccess) {
-    h->workspace_dirty = true;
-    return cuda_fail(ce, "decode launch");
-  }
+  if (ce != cudaSuccess) return cuda_fail(ce, "decode launch");
   return ok();
 }
 
@@ -761,14 +743,11 @@ duo_status duo_attn_decode_varlen(duo_handle* h, const duo_kv_cache* c, const in
   decode_plan(h, max_len, &p);
   const int64_t U = (int64_t)sh.B * sh.Hkv;
   const size_t counter_bytes = ((size_t)U * 4 + 255) / 256 * 256;
-  const unsigned epoch = g_error_epoch.load();
-  if (workspace != h->last_workspace || h->workspace_dirty || epoch != h->epoch) {
-    cudaError_t e = cudaMemsetAsync(workspace, 0, counter_bytes, (cudaStream_t)stream);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(workspace counters)");
-    h->last_workspace = workspace;
-    h->workspace_dirty = false;
-    h->epoch = epoch;
-  }
+  // The arrival counters must start at zero. The kernel leaves them at zero, but the
+  // caller may have lent the workspace's memory to other data since the last call (a
+  // caching allocator does), so every call clears them: U x 4 bytes, on the stream.
+  cudaError_t me = cudaMemsetAsync(workspace, 0, counter_bytes, (cudaStream_t)stream);
+  if (me != cudaSuccess) return cuda_fail(me, "cudaMemsetAsync(workspace counters)");
   p.seq_lens = seq_lens;
   p.q = static_cast<const uint16_t*>(q);
   p.o = static_cast<uint16_t*>(o);
@@ -783,10 +762,7 @@ duo_status duo_attn_decode_varlen(duo_handle* h, const duo_kv_cache* c, const in
   p.sh = sh;
   p.heads = h->heads;
   cudaError_t ce = launch_decode(p, (cudaStream_t)stream);
-  if (ce != cudaSuccess) {
-    h->workspace_dirty = true;
-    return cuda_fail(ce, "decode launch (device lengths)");
-  }
+  if (ce != cudaSuccess) return cuda_fail(ce, "decode launch (device lengths)");
   return ok();
 }
 
@@ -800,7 +776,6 @@ duo_status duo_device_error(uint32_t* code) {
   if ((e = selftest_read_clear_error(&t)) != cudaSuccess) return cuda_fail(e, "read self-test error word");
   if ((e = append_read_clear_error(&ap)) != cudaSuccess) return cuda_fail(e, "read append error word");
   *code = a | b | t | ap;
-  if ((a | b | t) & ~kErrBadBlock) g_error_epoch.fetch_add(1);
   if ((*code & kErrBadBlock) && !(*code & ~(kErrBadBlock | kErrAppendCapacity)))
     return fail(DUO_ERR_INVALID_ARG, "a block table held an id outside [0, num_blocks) (code 0x%x)", *code);
   if (ap && !(a | b | t))
@@ -837,21 +812,43 @@ static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBy
 
 constexpr int kMaxDevices = 64;
 std::mutex g_static_scratch_mu;
-void* g_static_scratch_addr[kMaxDevices];  // device address of the array, per device
+// Device address of the array per device, and the CUDA context it was looked up in: a
+// module loaded into another context (after cudaDeviceReset, or under a context the
+// caller made current) may sit at another address, so a new context looks it up again.
+struct StaticScratchAddr {
+  CUcontext ctx;
+  void* ptr;
+};
+StaticScratchAddr g_static_scratch_addr[kMaxDevices];
 
-// Looks up the array's device address once per device. The name of a __device__
-// variable is only a host-side stand-in; kernels must be given this address.
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+
+// Looks up the array's device address once per device and context. The name of a
+// __device__ variable is only a host-side stand-in; kernels must be given this address.
 duo_status static_scratch_address(int device, void** out) {
   if (device < 0 || device >= kMaxDevices) return fail(DUO_ERR_UNSUPPORTED, "device index %d >= %d", device, kMaxDevices);
+  static CtxGetCurrentFn get_ctx = nullptr;
   std::lock_guard<std::mutex> lock(g_static_scratch_mu);
-  if (!g_static_scratch_addr[device]) {
+  if (!get_ctx) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+      return fail(DUO_ERR_CUDA, "cuCtxGetCurrent entry point unavailable");
+    get_ctx = reinterpret_cast<CtxGetCurrentFn>(fn);
+  }
+  CUcontext ctx = nullptr;
+  if (get_ctx(&ctx) != CUDA_SUCCESS || !ctx) return fail(DUO_ERR_CUDA, "no current CUDA context");
+  StaticScratchAddr& slot = g_static_scratch_addr[device];
+  if (!slot.ptr || slot.ctx != ctx) {
     void* ptr = nullptr;
     cudaError_t e = cudaGetSymbolAddress(&ptr, g_static_scratch);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static decode scratch)");
     if (!ptr) return fail(DUO_ERR_CUDA, "cudaGetSymbolAddress returned NULL for the static decode scratch");
-    g_static_scratch_addr[device] = ptr;
+    slot.ctx = ctx;
+    slot.ptr = ptr;
   }
-  *out = g_static_scratch_addr[device];
+  *out = slot.ptr;
   return DUO_OK;
 }
 

@@ -42,3 +42,100 @@ def head_keys(seed, b, h, pos0, T, D):
     """float64 K and V [T, D] of one (sequence, KV head)."""
     return (ds.head_stream_f64(seed, ds.STREAM_K, b, h, pos0, T, D, workers=8),
             ds.head_stream_f64(seed, ds.STREAM_V, b, h, pos0, T, D, workers=8))
+
+
+# ------------------------------------------------------------------ peaked inputs
+# Real attention rows are dominated by a few keys (the sinks and a few recent or
+# retrieved tokens). The seeded generator is bounded (|x| <= 4.9), so on its own it
+# never makes a later key tile's best score beat the running maximum by more than
+# 2^8, which is when the kernels rescale the running output. These recipes make
+# such rows; both sides receive the same bf16 values.
+
+LOG2E = 1.4426950408889634
+SPIKE_DIM = 3     # the direction every query row is shifted along, and spike keys point
+SPIKE_SHIFT = 3.0
+
+
+def bf16_pair(x):
+    """float64 array -> (torch bf16 CPU tensor, float64 array of exactly its values)."""
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(torch.bfloat16)
+    return t, t.to(torch.float64).numpy()
+
+
+def spike_value(jump_log2, D, base=3.6):
+    """K entry along SPIKE_DIM whose score, for a query shifted by SPIKE_SHIFT, sits about
+    `jump_log2` log2-units above a baseline row maximum of `base` (in score units)."""
+    return (base + jump_log2 / LOG2E) * np.sqrt(D) / SPIKE_SHIFT
+
+
+def plant(Q, K, spikes, D):
+    """Shift every query row along SPIKE_DIM and set K[:, p, h, SPIKE_DIM] for each
+    (p, h, jump) in `spikes` (in place on float64 arrays)."""
+    Q[..., SPIKE_DIM] += SPIKE_SHIFT
+    for p, h, jump in spikes:
+        K[:, p, h, SPIKE_DIM] = spike_value(jump, D)
+
+
+def lazy_rescale_hits(scores, tile_of_key, limit=8.0):
+    """scores: float64 [rows, keys] in log2 units (-inf = not visible), keys in the order
+    a kernel visits them; tile_of_key: non-decreasing tile index of each key. Applies the
+    kernels' lazy rule (the running max moves only when a tile's max exceeds it by more
+    than `limit`) and returns, per row, (rescales after the row's first tile with a finite
+    running max, largest softmax share of the keys before such a tile)."""
+    tile_of_key = np.asarray(tile_of_key)
+    starts = np.flatnonzero(np.r_[True, np.diff(tile_of_key) != 0])
+    tmax = np.maximum.reduceat(scores, starts, axis=1)
+    top = scores.max(axis=1, keepdims=True)
+    w = np.where(np.isfinite(scores), np.exp2(scores - top), 0.0)
+    cum = np.cumsum(np.add.reduceat(w, starts, axis=1), axis=1)
+    rows = scores.shape[0]
+    m = np.full(rows, -np.inf)
+    hits = np.zeros(rows, np.int64)
+    share = np.zeros(rows)
+    for j in range(len(starts)):
+        grow = tmax[:, j] > m + limit
+        if j > 0:
+            hit = grow & np.isfinite(m)
+            hits += hit
+            share = np.where(hit, np.maximum(share, cum[:, j - 1] / cum[:, -1]), share)
+        m = np.where(grow, tmax[:, j], m)
+    return hits, share
+
+
+def decode_rescale_hits(scores_by_unit, n, num_ctas, streaming_units, tile=128, warps=8, limit=8.0):
+    """Lazy-rule rescales inside the decode kernel's per-warp streams for retrieval
+    units, following its documented work split: W = units x tiles retrieval tiles,
+    C = min(num_ctas, W + streaming units) CTAs, the first Cr = min(C, W) of them taking
+    tiles [c W / Cr, (c + 1) W / Cr), a unit's share cut at unit boundaries, and warp w
+    of a CTA owning keys [w 16, w 16 + 16) of every tile. scores_by_unit: list of
+    float64 [heads, n] in log2 units. Returns the number of (segment, warp, head)
+    streams that rescale after their first slice with a finite running max."""
+    U = len(scores_by_unit)
+    tiles = -(-n // tile)
+    W = U * tiles
+    C = min(num_ctas, W + streaming_units)
+    Cr = min(C, W)
+    kpw = tile // warps
+    count = 0
+    for c in range(Cr):
+        t0, t1 = c * W // Cr, (c + 1) * W // Cr
+        t = t0
+        while t < t1:
+            u = t // tiles
+            te = min((u + 1) * tiles, t1)
+            sc = scores_by_unit[u]
+            for w in range(warps):
+                m = np.full(sc.shape[0], -np.inf)
+                for j, lt in enumerate(range(t - u * tiles, te - u * tiles)):
+                    k0 = lt * tile + w * kpw
+                    seg = sc[:, k0:min(k0 + kpw, n)]
+                    if seg.shape[1] == 0:
+                        continue
+                    mx = seg.max(axis=1)
+                    grow = mx > m + limit
+                    if j > 0:
+                        count += int((grow & np.isfinite(m)).sum())
+                    m = np.where(grow, mx, m)
+            t = te
+    return count

@@ -152,3 +152,35 @@ def test_full_size_decode_1m_sampled():
     strh = [h for h in range(w.Hkv) if not w.is_retrieval[h]]
     _check_sampled(w, out, [w.decode_steps - 1], [0], ret[:1] + strh)
     _check_sampled(w, out, [0], [0], strh[:2])
+
+
+@pytest.mark.parametrize("Hq", [4, 8], ids=["g2", "g4"])
+def test_workspace_holding_other_data_between_calls(Hq):
+    """A caller may lend the workspace's memory to other data between decode calls (a
+    caching allocator does): with the same handle and address, a workspace filled with
+    0xFF bytes between two steps still gives the oracle's output (every call clears its
+    arrival counters). The context is long enough that one unit spans many CTAs."""
+    from streaming_kv_cache_duo_gb300 import DuoLayer, duo_device_error
+    B, Hkv, D, S, R, kinds, ctx = 1, 2, 128, 4, 64, [1, 0], 20000
+    seed = 41
+    layer = DuoLayer(B, Hq, Hkv, D, S, R, ctx + 2, kinds)
+    layer.append(device_stream(seed, ds.STREAM_K, B, 0, ctx, Hkv, D, "cuda"),
+                 device_stream(seed, ds.STREAM_V, B, 0, ctx, Hkv, D, "cuda"))
+    K = host_stream(seed, ds.STREAM_K, B, 0, ctx + 2, Hkv, D)
+    V = host_stream(seed, ds.STREAM_V, B, 0, ctx + 2, Hkv, D)
+    cache = OracleCache(kinds, S, R, D)
+    cache.append(K[0, :ctx], V[0, :ctx])
+    addr = layer.workspace.data_ptr()
+    for step in range(2):
+        p = ctx + step
+        layer.append(device_stream(seed, ds.STREAM_K, B, p, 1, Hkv, D, "cuda"),
+                     device_stream(seed, ds.STREAM_V, B, p, 1, Hkv, D, "cuda"))
+        q = device_stream(seed, ds.STREAM_Q, B, p, 1, Hq, D, "cuda")[:, 0].contiguous()
+        o = layer.decode(q)
+        torch.cuda.synchronize()
+        assert duo_device_error() == 0
+        cache.append(K[0, p:p + 1], V[0, p:p + 1])
+        ref = decode_from_cache(host_stream(seed, ds.STREAM_Q, B, p, 1, Hq, D)[0, 0], p, cache)
+        assert_close(to_np(o[0]), ref, f"step {step}")
+        layer.workspace.fill_(0xFF)  # the memory used for something else until the next call
+    assert layer.workspace.data_ptr() == addr
