@@ -50,6 +50,12 @@ L2_BYTES = 129e6  # GB300 L2 capacity
 MEASURED_TRAFFIC = {
     "prefill": {"src": ("prefill.cu", "duo_device.cuh", "duo_internal.h"), "sha1": "62c17fdf8e6b211d",
                 "bytes": 570.448896e6 + 231.574272e6},
+    # the 8 prefill launches of one chunked-prefill step (Llama-2-7B shape, 8 x 4096 tokens)
+    "prefill_chunked": {"src": ("prefill.cu", "duo_device.cuh", "duo_internal.h"), "sha1": "62c17fdf8e6b211d",
+                        "bytes": 1305.383e6 + 102.669e6},
+    # one decode launch of the batched 8 x 128K workload (device lengths, graph replay)
+    "decode_batched": {"src": ("decode.cu", "duo_device.cuh", "duo_internal.h"), "sha1": "5ae6c083af1a8e30",
+                       "bytes": 1.081976e9 + 1.811712e6},
     "decode": {"src": ("decode.cu", "duo_device.cuh", "duo_internal.h"), "sha1": "5ae6c083af1a8e30",
                "bytes": 1.074862e9 + 3.666176e6},
 }
@@ -58,7 +64,9 @@ MEASURED_TRAFFIC = {
 def measured_traffic(kernel):
     """Traffic of the last ncu capture of `kernel`, or None if its sources changed since."""
     import hashlib
-    rec = MEASURED_TRAFFIC[kernel]
+    rec = MEASURED_TRAFFIC.get(kernel)
+    if rec is None:
+        return None
     m = hashlib.sha1()
     for f in rec["src"]:
         with open(os.path.join(ROOT, "streaming_kv_cache_duo_gb300", "csrc", f), "rb") as fh:
@@ -77,8 +85,8 @@ def load_peaks():
 
 # ----------------------------------------------------------------------------- clocks
 class ClockSampler:
-    """SM clock and throttle reasons sampled every 10 ms (NVML through ctypes) while the
-    timed region runs; falls back to `nvidia-smi -lms 200`."""
+    """SM clock and throttle reasons sampled every 5 ms (NVML through ctypes) while a
+    timed region runs, with one sample as it starts and one as it ends."""
 
     REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
                0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
@@ -122,10 +130,12 @@ class ClockSampler:
         rs = ctypes.c_ulonglong()
         get_r = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
             getattr(nv, "nvmlDeviceGetCurrentClocksThrottleReasons")
-        while not self.stop_flag.is_set():
+        while True:
             if nv.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0 and get_r(h, ctypes.byref(rs)) == 0:
                 self.samples.append((float(clk.value), int(rs.value)))
-            time.sleep(0.01)
+            if self.stop_flag.is_set():  # one last sample after the region ends
+                break
+            time.sleep(0.005)
 
     def start(self):
         try:
@@ -359,17 +369,20 @@ def e2e_prefill(w, layer, q, k, v, o, flops, steps, warmup, world):
     run(warmup)
     torch.cuda.synchronize()
     barrier(world)
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record(comp)
     run(steps)
     b.record(comp)
     torch.cuda.synchronize()
+    clk = clocks.stop()
     ms = dist_max(a.elapsed_time(b), world) / steps
     h2d = (hq.numel() + hk.numel() + hv.numel()) * 2
     return {"value": round(flops * world / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s", "ms_per_step": round(ms, 4),
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": ho[0].numel() * 2,
             "how": "pinned host Q/K/V in, O out, every step; copies on two side streams, double-buffered, "
-                   "overlapping the neighbouring steps' kernels"}
+                   "overlapping the neighbouring steps' kernels", "clocks": clk}
 
 
 def make_layer(w, cap, dev, paged_block, pool=False, kv4=False):
@@ -425,6 +438,8 @@ def bench_decode(w, steps_cap, peaks, paged_block=0, pool=False, kv4=False):
     stream = torch.cuda.current_stream()
     torch.cuda.synchronize()
     ev = []
+    clocks = ClockSampler(dev.index)
+    clocks.start()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t0.record(stream)
     for s in range(steps):
@@ -436,6 +451,7 @@ def bench_decode(w, steps_cap, peaks, paged_block=0, pool=False, kv4=False):
         ev.append((a, b, layer.n))
     t1.record(stream)
     torch.cuda.synchronize()
+    clk = clocks.stop()
     if duo_device_error():
         raise RuntimeError("a kernel gave up a bounded wait")
     # the first steps warm up; report the rest
@@ -455,7 +471,7 @@ def bench_decode(w, steps_cap, peaks, paged_block=0, pool=False, kv4=False):
                          "frac": round(gbs / peak, 4),
                          "traffic": None if (kv4 or paged_block) else measured_traffic("decode"),
                          "kernel": f"decode_kernel<{w.D},{w.Hq // w.Hkv},{'kv4' if kv4 else 'plain'}>"},
-            "tokens_per_s": round(1e3 / (sum(times) / len(times)), 1)}
+            "tokens_per_s": round(1e3 / (sum(times) / len(times)), 1), "clocks": clk}
 
 
 def bench_decode_graph(w, peaks):
@@ -498,6 +514,8 @@ def bench_decode_graph(w, peaks):
         layer.decode_varlen(sq, seq_lens, max_len, out=so)
     stream = torch.cuda.current_stream()
     steps = w.decode_steps - 1
+    clocks = ClockSampler(dev.index)
+    clocks.start()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t0.record(stream)
     for s_ in range(1, w.decode_steps):
@@ -507,6 +525,7 @@ def bench_decode_graph(w, peaks):
         graph.replay()
     t1.record(stream)
     torch.cuda.synchronize()
+    clk = clocks.stop()
     if duo_device_error():
         raise RuntimeError("a kernel reported an error")
     ms = t0.elapsed_time(t1) / steps
@@ -518,7 +537,11 @@ def bench_decode_graph(w, peaks):
             "bytes_per_step": int(nbytes), "steps_timed": steps,
             "how": "device-held sequence lengths; (append + decode) captured once in a CUDA graph and "
                    "replayed; step time includes the three 1-token input copies",
-            "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 4)}
+            "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 4), "clocks": clk,
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(gbs / peaks["hbm_gbs"], 4), "traffic": measured_traffic("decode_batched"),
+                         "kernel": f"decode_kernel<{w.D},{w.Hq // w.Hkv},plain> (device lengths)"},
+            "gpu_launches_per_step": 2}
 
 
 def bench_chunked(w, steps, warmup, peaks, paged_block=0, pool=False):
@@ -562,23 +585,147 @@ def bench_chunked(w, steps, warmup, peaks, paged_block=0, pool=False):
     for _ in range(warmup):
         step(False)
     torch.cuda.synchronize()
+    clocks = ClockSampler(dev.index)
+    clocks.start()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t0.record(stream)
     for _ in range(steps):
         step(True)
     t1.record(stream)
     torch.cuda.synchronize()
+    clk = clocks.stop()
     if duo_device_error():
         raise RuntimeError("a kernel reported an error")
     ms = t0.elapsed_time(t1) / steps
     pre_ms = sum(a.elapsed_time(b) for a, b in pre) / steps
     layer.close()
+    # traffic of one step's prefill launches, from the ncu capture of the unpaged layout
+    traffic = measured_traffic("prefill_chunked") if not paged_block else None
     return {"value": flops / (ms * 1e-3) / 1e12, "ms_per_step": ms, "flops": flops, "retrieval_flops": fr,
-            "prefill_ms": pre_ms, "launches": 2 * len(chunks) * steps,
+            "prefill_ms": pre_ms, "append_ms": ms - pre_ms, "launches": 2 * len(chunks) * steps, "clocks": clk,
             "roofline": {"bound": "tensor", "achieved": round(flops / (pre_ms * 1e-3) / 1e12, 2),
                          "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                          "frac": round(flops / (pre_ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
-                         "traffic": None, "kernel": "prefill_kernel<128> (8 launches per step)"}}
+                         "traffic": traffic, "traffic_is": "sum over the step's 8 prefill launches",
+                         "kernel": f"prefill_kernel<{w.D}> ({len(chunks)} launches per step)",
+                         "flops_per_step": flops}}
+
+
+def bench_tiny(w, steps, warmup, peaks):
+    """The tiny workload end to end on the device: one step = reset the caches, prefill
+    the 256-token prompt (all heads, one launch), append it, then 16 decode steps (append
+    one token, decode it). Timed eagerly (every call launched from the host) and as one
+    CUDA graph of the whole step replayed; both are launch-bound, so the figure of
+    merit is microseconds per step."""
+    import torch
+
+    import duo_synth as ds
+    from streaming_kv_cache_duo_gb300 import DuoLayer, duo_device_error, workload as wl
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+    L, n_dec = w.prefill_len, w.decode_steps
+    kinds = w.is_retrieval
+    layer = DuoLayer(w.B, w.Hq, w.Hkv, w.D, w.S, w.R, L + n_dec, kinds, device=dev)
+    gen = lambda st, H: ds.stream_torch(w.seed, st, w.B, 0, L + n_dec, H, w.D, device=dev)
+    q, k, v = gen(ds.STREAM_Q, w.Hq), gen(ds.STREAM_K, w.Hkv), gen(ds.STREAM_V, w.Hkv)
+    qp, kp, vp = (x[:, :L].contiguous() for x in (q, k, v))
+    qd = [q[:, L + s].contiguous() for s in range(n_dec)]
+    kd = [k[:, L + s:L + s + 1].contiguous() for s in range(n_dec)]
+    vd = [v[:, L + s:L + s + 1].contiguous() for s in range(n_dec)]
+    op = torch.empty_like(qp)
+    od = torch.empty_like(qd[0])
+
+    def step():
+        stream = torch.cuda.current_stream()  # the capture stream while a graph is captured
+        layer.reset(stream=stream)
+        layer.prefill(qp, kp, vp, out=op, stream=stream)
+        layer.append(kp, vp, stream=stream)
+        for s_ in range(n_dec):
+            layer.append(kd[s_], vd[s_], stream=stream)
+            layer.decode(qd[s_], out=od, stream=stream)
+
+    stream = torch.cuda.current_stream()
+
+    def timed(fn, n):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        clocks = ClockSampler(dev.index)
+        clocks.start()
+        a.record(stream)
+        for _ in range(n):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) * 1e3 / n, clocks.stop()
+
+    n = max(steps, 20)
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    eager_us, clk = timed(step, n)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    for _ in range(warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    graph_us, clk_g = timed(graph.replay, n)
+    if duo_device_error():
+        raise RuntimeError("a kernel reported an error")
+    layer.close()
+    fr, fs = wl.prefill_flops(w.B, w.Hq, w.Hkv, w.D, w.S, w.R, kinds, L)
+    dec_bytes = sum(sum(wl.decode_bytes(w.B, w.Hq, w.Hkv, w.D, w.S, w.R, kinds, L + s_ + 1)) for s_ in range(n_dec))
+    return {"workload": w.name, "us_per_step": round(eager_us, 2), "us_per_step_graph": round(graph_us, 2),
+            "steps_timed": n, "prefill_flops": fr + fs, "decode_bytes_per_step": dec_bytes,
+            "gpu_launches_per_step": 3 + 2 * n_dec, "clocks": clk, "clocks_graph": clk_g,
+            "how": "reset + prefill (256 tokens) + append + 16 x (append 1, decode 1); eager launches, and the "
+                   "same step captured once as a CUDA graph and replayed; launch-bound"}
+
+
+def oracle_decode_sample(w, steps_pick, batches, budget_s):
+    """Time the CPU oracle's decode (what the caches hold after the step's append, the
+    float64 softmax over it) for the picked decode steps and sequences, every KV head:
+    retrieval heads read every stored key, streaming heads their sink + ring slots.
+    Inputs are regenerated on the host (excluded from the time). Stops after the step
+    that passes `budget_s` of oracle time."""
+    import numpy as np
+
+    import duo_synth as ds
+    import oracle
+    from streaming_kv_cache_duo_gb300 import workload as wl
+
+    g = w.Hq // w.Hkv
+    kinds = w.is_retrieval
+    spent, nbytes, done = 0.0, 0, []
+    for s_ in steps_pick:
+        p = w.context + s_
+        for b in batches:
+            Qp = ds.stream_f64(w.seed, ds.STREAM_Q, w.B, p, 1, w.Hq, w.D, batches=[b])[0, 0]
+            for h in range(w.Hkv):
+                if kinds[h]:
+                    K = ds.head_stream_f64(w.seed, ds.STREAM_K, b, h, 0, p + 1, w.D, workers=8)
+                    V = ds.head_stream_f64(w.seed, ds.STREAM_V, b, h, 0, p + 1, w.D, workers=8)
+                    kpos = np.arange(p + 1)
+                else:
+                    sim = oracle.RingCacheSim(w.S, w.R)
+                    sim.append(p + 1)
+                    kpos = np.array([x for x in sim.positions() if x >= 0])
+                    K = np.stack([ds.stream_f64(w.seed, ds.STREAM_K, w.B, int(t), 1, w.Hkv, w.D,
+                                                heads=[h], batches=[b])[0, 0, 0] for t in kpos])
+                    V = np.stack([ds.stream_f64(w.seed, ds.STREAM_V, w.B, int(t), 1, w.Hkv, w.D,
+                                                heads=[h], batches=[b])[0, 0, 0] for t in kpos])
+                t0 = time.perf_counter()
+                oracle.attend_rows(Qp[h * g:(h + 1) * g], [p] * g, K, V, kpos, kinds[h], w.S, w.R)
+                spent += time.perf_counter() - t0
+            r, st, _ = wl.decode_bytes(1, w.Hq, w.Hkv, w.D, w.S, w.R, kinds, p + 1)
+            nbytes += r + st
+            done.append((s_, b))
+        if spent > budget_s:
+            break
+    return {"value": round(nbytes / spent / 1e9, 3), "unit": "GB/s", "cores": _threads_used(), "kind": "oracle",
+            "s_per_sequence_step": round(spent / len(done), 3),
+            "sample": f"{len(done)} (step, sequence) decodes of {w.name}, steps {sorted({d[0] for d in done})}, "
+                      f"sequences {sorted({d[1] for d in done})}, every KV head ({spent:.1f} s of attention "
+                      f"work, input generation excluded); GB/s = KV bytes the method reads / oracle time"}
 
 
 # ----------------------------------------------------------------------------- oracle arm
@@ -631,6 +778,19 @@ def _threads_used():
         return int(v) if v else (os.cpu_count() or 1)
 
 
+def prefill_config(w, world):
+    """`config` of the one-shot prefill line, the same for both arms."""
+    in_bytes = w.B * w.prefill_len * (w.Hq + 2 * w.Hkv) * w.D * 2
+    l2 = ((f"L2 flushed before every step (inputs {in_bytes / 2**20:.1f} MiB fit in the 129 MB L2; "
+           "256 MiB write outside the step's events)") if in_bytes < L2_BYTES else
+          (f"no flush: per-step inputs (Q {w.B * w.prefill_len * w.Hq * w.D * 2 / 2**20:.0f} MiB, K/V "
+           f"{w.B * w.prefill_len * w.Hkv * w.D * 2 / 2**20:.0f} MiB each) exceed the 129 MB L2"))
+    return {"workload": w.name, "batch": w.B, "seq_len": w.prefill_len, "q_heads": w.Hq,
+            "kv_heads": w.Hkv, "head_dim": w.D, "retrieval_kv_heads": sum(w.is_retrieval),
+            "sink": w.S, "recent": w.R, "parallelism": f"replicas{world}", "l2": l2,
+            "step": f"prefill (all heads, one launch) + append of the {w.prefill_len} tokens"}
+
+
 def run_reference(args, w, world, rank):
     if rank != 0:
         return
@@ -651,9 +811,7 @@ def run_reference(args, w, world, rank):
             "ms_per_step": round(full / (value * 1e12) * 1e3, 1), "ms_per_step_is": "extrapolated from the sample",
             "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded counter-based generator)",
-            "config": {"workload": w.name, "batch": w.B, "seq_len": w.prefill_len, "q_heads": w.Hq,
-                       "kv_heads": w.Hkv, "head_dim": w.D, "retrieval_kv_heads": sum(w.is_retrieval), "sink": w.S,
-                       "recent": w.R, "parallelism": f"replicas{world}"},
+            "config": prefill_config(w, world),
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": r["cores"], "kind": "oracle",
                              "sample": f"each step: {r['sample']}"},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -822,15 +980,30 @@ def main():
         other_workload(args, w, world, rank, peaks)
         return
     res = bench_prefill(w, args.steps, args.warmup, world, peaks, not args.no_e2e)
-    dec = dec_graph = None
+    dec = dec_graph = chunked = tiny = None
     if not args.no_decode:
+        # the other workloads, each in its own timed region with its own clock record
         dec = bench_decode(ds.WORKLOADS["decode_ctx1m"], 64, peaks)
         dec_graph = bench_decode_graph(ds.WORKLOADS["batched_decode_ctx128k"], peaks)
+        wc = ds.WORKLOADS["llama2_7b_chunked_prefill32k"]
+        r = bench_chunked(wc, args.steps, args.warmup, peaks)
+        chunked = {"workload": wc.name, "value": round(r["value"], 2), "unit": "TFLOP/s",
+                   "ms_per_step": round(r["ms_per_step"], 4), "prefill_ms": round(r["prefill_ms"], 4),
+                   "append_ms": round(r["append_ms"], 4), "roofline": r["roofline"],
+                   "retrieval_flops": r["retrieval_flops"], "gpu_launches": r["launches"], "clocks": r["clocks"],
+                   "step": "8 x (prefill of a 4096-token chunk against the cache, append)"}
+        tiny = bench_tiny(ds.WORKLOADS["tiny_prefill256_decode16"], args.steps, args.warmup, peaks)
     if rank != 0:
         return
     cpu = None
     if not args.no_cpu_baseline and world == 1:
         cpu = oracle_prefill_sample(w, args.cpu_budget)
+        if not args.no_decode:
+            w5, w3 = ds.WORKLOADS["decode_ctx1m"], ds.WORKLOADS["batched_decode_ctx128k"]
+            cpu["decode"] = {
+                w5.name: oracle_decode_sample(w5, [0, w5.decode_steps - 1, 17], [0], args.cpu_budget / 3),
+                w3.name: oracle_decode_sample(w3, [0, w3.decode_steps - 1, 101], [0, w3.B - 1, 3],
+                                              args.cpu_budget / 3)}
     res["roofline"]["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json bf16_tflops, burst)" \
         if peak_src == "measured" else "fallback 1.9 PFLOP/s"
     line = {
@@ -838,19 +1011,18 @@ def main():
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(res["ms_per_step"], 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded counter-based generator, bf16 values of mean 0, variance 1)",
-        "config": {"workload": w.name, "batch": w.B, "seq_len": w.prefill_len, "q_heads": w.Hq,
-                   "kv_heads": w.Hkv, "head_dim": w.D, "retrieval_kv_heads": sum(w.is_retrieval),
-                   "sink": w.S, "recent": w.R, "parallelism": f"replicas{world}",
-                   "l2": res["l2"],
-                   "step": f"prefill (all heads, one launch) + append of the {w.prefill_len} tokens"},
+        "config": prefill_config(w, world),
         "roofline": res["roofline"],
         "prefill_retrieval_only": res["prefill_retrieval_only"],
         "decode": dec,
         "decode_batched_graph": dec_graph,
+        "chunked_prefill": chunked,
+        "tiny": tiny,
         "cpu_baseline": cpu,
         "e2e": res.get("e2e"),
         "clocks": res["clocks"],
         "gpu_launches": res["launches"],
+        "gpu_launches_is": "prefill + append launches of the main timed region; each sub-record counts its own",
         "breakdown_ms": {"prefill": round(res["prefill_ms"], 4), "append": round(res["append_ms"], 4)},
     }
     print(json.dumps(line))
