@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -445,6 +446,9 @@ static duo_status prefill_impl(duo_handle* h, const duo_kv_cache* c, const duo_p
   if (ir + is > 0x7fffffffLL) return fail(DUO_ERR_UNSUPPORTED, "too many query tiles for one launch");
   p.items_r = (int)ir;
   p.items_s = (int)is;
+  // about one wave of CTAs per KV head; at most num_qt, so qp_group x (items per block)
+  // stays within the item count (an int)
+  p.qp_group = std::max(1, std::min(h->num_sms / sh.g, p.num_qt));
   p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)sh.D));
   p.sh = sh;
   p.heads = h->heads;
@@ -669,6 +673,7 @@ duo_status duo_dca_prefill(duo_handle* h, const duo_kv_cache* c, const void* q, 
   if (items > 0x7fffffffLL) return fail(DUO_ERR_UNSUPPORTED, "too many query tiles for one launch");
   p.items_r = (int)items;
   p.items_s = 0;
+  p.qp_group = std::max(1, std::min(h->num_sms / sh.g, p.num_qt));
   p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)sh.D));
   p.sh = sh;
   p.heads = h->heads;

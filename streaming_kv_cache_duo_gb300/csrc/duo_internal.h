@@ -184,6 +184,7 @@ struct PrefillParams {
   int num_qt;            // 256-row query blocks per head: ceil(T / 256)
   int items_r;           // work items of retrieval heads: B * n_ret * g * num_qt
   int items_s;           // work items of streaming heads
+  int qp_group;          // query blocks per group in the retrieval work order (>= 1)
   float scale_log2;
   Shape sh;
   HeadTable heads;

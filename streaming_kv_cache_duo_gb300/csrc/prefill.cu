@@ -109,6 +109,24 @@ __device__ __forceinline__ Item item_of(const PrefillParams& p, int idx) {
     nk = p.sh.n_str;
   }
   const int per_qp = p.sh.B * nk * g;
+  if (!it.streaming) {
+    // longest query blocks first, in groups of qp_group blocks (about one wave of CTAs
+    // per KV head); inside a group, one (sequence, KV head) after the other, so that the
+    // CTAs in flight together read the same K/V tiles and each tile comes from DRAM
+    // about once (with evict-last loads keeping it in L2 for the CTAs that follow)
+    const int GQ = p.qp_group;
+    const int grp = idx / (GQ * per_qp);
+    const int gs = min(GQ, p.num_qt - grp * GQ);
+    int r = idx - grp * GQ * per_qp;
+    const int bc = r / (gs * g);
+    r %= gs * g;
+    it.qp = p.num_qt - 1 - (grp * GQ + r / g);
+    it.b = bc / nk;
+    it.cidx = bc % nk;
+    it.kvh = p.heads.ret_head[it.cidx];
+    it.hq = it.kvh * g + (r % g);
+    return it;
+  }
   const int qp_rev = idx / per_qp;  // longest query blocks first
   int r = idx % per_qp;
   it.qp = p.num_qt - 1 - qp_rev;
@@ -362,6 +380,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
           qmap = dca_map(p, qvar);
         }
         prefetch_tmap(qmap);
+        // each query tile is read by this CTA alone; K/V tiles by every CTA of the KV head
+        const uint64_t pol_kv = l2_policy_evict_last();
         mbar_arrive_expect_tx(&bars->q_full, kQT * C::Q_BYTES);
   #pragma unroll
         for (int x = 0; x < kQT; ++x)
@@ -433,13 +453,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   #pragma unroll
           for (int bx = 0; bx < C::NBOX; ++bx) {
             if (t.phase == 1)
-              tma_load_4d(dk + bx * kBox, &p.tm_k, bx * 64, it.kvh, t.k * BN, it.b, &bars->k_full[s]);
+              tma_load_4d_hint(dk + bx * kBox, &p.tm_k, bx * 64, it.kvh, t.k * BN, it.b, &bars->k_full[s], pol_kv);
             else if (paged)
-              tma_load_3d(dk + bx * kBox, map_k, bx * 64, prow, blk, &bars->k_full[s]);
+              tma_load_3d_hint(dk + bx * kBox, map_k, bx * 64, prow, blk, &bars->k_full[s], pol_kv);
             else if (!it.streaming)
-              tma_load_3d(dk + bx * kBox, &p.tm_kfull, bx * 64, t.k * BN, it.b * p.sh.n_ret + it.cidx, &bars->k_full[s]);
+              tma_load_3d_hint(dk + bx * kBox, &p.tm_kfull, bx * 64, t.k * BN, it.b * p.sh.n_ret + it.cidx,
+                               &bars->k_full[s], pol_kv);
             else
-              tma_load_3d(dk + bx * kBox, &p.tm_ksr, bx * 64, t.k * BN, it.b * p.sh.n_str + it.cidx, &bars->k_full[s]);
+              tma_load_3d_hint(dk + bx * kBox, &p.tm_ksr, bx * 64, t.k * BN, it.b * p.sh.n_str + it.cidx,
+                               &bars->k_full[s], pol_kv);
           }
           if (!mbar_wait(&bars->v_empty[s], ph ^ 1u, err, kErrPrefillProducer)) {
             ok = false;
@@ -451,13 +473,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   #pragma unroll
           for (int bx = 0; bx < C::NBOX; ++bx) {
             if (t.phase == 1)
-              tma_load_4d(dv + bx * kBox, &p.tm_v, bx * 64, it.kvh, t.k * BN, it.b, &bars->v_full[s]);
+              tma_load_4d_hint(dv + bx * kBox, &p.tm_v, bx * 64, it.kvh, t.k * BN, it.b, &bars->v_full[s], pol_kv);
             else if (paged)
-              tma_load_3d(dv + bx * kBox, map_v, bx * 64, prow, blk, &bars->v_full[s]);
+              tma_load_3d_hint(dv + bx * kBox, map_v, bx * 64, prow, blk, &bars->v_full[s], pol_kv);
             else if (!it.streaming)
-              tma_load_3d(dv + bx * kBox, &p.tm_vfull, bx * 64, t.k * BN, it.b * p.sh.n_ret + it.cidx, &bars->v_full[s]);
+              tma_load_3d_hint(dv + bx * kBox, &p.tm_vfull, bx * 64, t.k * BN, it.b * p.sh.n_ret + it.cidx,
+                               &bars->v_full[s], pol_kv);
             else
-              tma_load_3d(dv + bx * kBox, &p.tm_vsr, bx * 64, t.k * BN, it.b * p.sh.n_str + it.cidx, &bars->v_full[s]);
+              tma_load_3d_hint(dv + bx * kBox, &p.tm_vsr, bx * 64, t.k * BN, it.b * p.sh.n_str + it.cidx,
+                               &bars->v_full[s], pol_kv);
           }
         }
         if (!ok) {
@@ -669,7 +693,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             pk[e] = pack_bf16x2(__uint_as_float(ov[2 * e]) * inv, __uint_as_float(ov[2 * e + 1]) * inv);
           uint4* dst = reinterpret_cast<uint4*>(orow + q4 * 32);
 #pragma unroll
-          for (int e = 0; e < 4; ++e) dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+          for (int e = 0; e < 4; ++e)
+            dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
         }
       }
     }
