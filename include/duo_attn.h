@@ -241,6 +241,13 @@ duo_status duo_attn_decode_paged(duo_handle* handle, const duo_kv_cache* cache, 
  * scale is 0), value = code * scale + zero. Codes are packed two per byte, the even
  * dim in the low nibble. Rows must stay within the fp16 range.
  *
+ * K codes are stored row by row (D / 2 bytes per row). V codes are stored in groups of
+ * 16 rows (rows 16 m ... 16 m + 15 of a plane, 8 D bytes), ordered for the decode's
+ * tensor-core fragments: the byte with the codes of dims 2 dp (low nibble) and 2 dp + 1
+ * (high nibble) of row k of the group sits at byte
+ *     4 ((4 (dp / MT) + (k % 8) / 2) MT + dp % MT) + 2 (k % 2) + k / 8,   MT = D / 16,
+ * of the group. Each byte belongs to one row, so appending a row writes only its bytes.
+ *
  * Layout (all device memory, caller-owned, 16-byte aligned), with cap16 = max_seq_len
  * and sr16 = S + R each rounded up to a multiple of 16 rows:
  *   k_codes, v_codes    u8  [B, n_ret, cap16, D / 2]   retrieval heads, row t = token t

@@ -152,8 +152,23 @@ __global__ void __launch_bounds__(256) append_varlen_kernel(const AppendParams p
 // row. Codes are packed two per byte (even dim in the low nibble); lane 0 stores
 // the fp16 pair (scale low, zero high). Rows: retrieval rows of all T tokens, then
 // the streaming rows the call keeps (the same two intervals as the bf16 ring).
+// V codes are stored in the order the decode's tensor-core fragments take them (no
+// byte permutes there): within each group of 16 rows, the byte holding the codes of
+// row k for dims (2 dp, 2 dp + 1) (low nibble, high nibble) sits at
+//     4 ((4 (dp / MT) + ((k & 7) >> 1)) MT + dp % MT) + 2 (k & 1) + (k >> 3),  MT = D / 16,
+// so the 32-bit word a lane reads per 16-dim m-tile holds the codes of rows 2t, 2t + 8,
+// 2t + 1, 2t + 9 (bytes 0 ... 3) for its two dims. Every byte belongs to one row, so a
+// row is written without touching the other rows of its group.
 template <int D>
-__device__ __forceinline__ void quantize_row(const uint16_t* src, uint8_t* codes, uint32_t* sz, int lane) {
+__device__ __forceinline__ int v_code_byte(int k, int dp) {
+  constexpr int MT = D / 16;
+  return 4 * ((4 * (dp / MT) + ((k & 7) >> 1)) * MT + dp % MT) + 2 * (k & 1) + (k >> 3);
+}
+
+// VT = false: `codes` is the row (D / 2 bytes, row-major nibbles); VT = true: `codes` is
+// the base of the row's 16-row group and k its row within the group (the V layout).
+template <int D, bool VT>
+__device__ __forceinline__ void quantize_row(const uint16_t* src, uint8_t* codes, int k, uint32_t* sz, int lane) {
   constexpr int VPL = D / 32;  // values per lane: 4 (D 128) or 2 (D 64)
   float x[VPL];
   if constexpr (VPL == 4) {
@@ -191,10 +206,15 @@ __device__ __forceinline__ void quantize_row(const uint16_t* src, uint8_t* codes
     }
     packed |= (uint32_t)c << (4 * i);
   }
-  if constexpr (VPL == 4)
+  if constexpr (VT) {
+#pragma unroll
+    for (int m = 0; m < VPL / 2; ++m)  // dims (4 lane + 2 m, +1) or (2 lane, +1): pair lane VPL / 2 + m
+      codes[v_code_byte<D>(k, lane * (VPL / 2) + m)] = (uint8_t)(packed >> (8 * m));
+  } else if constexpr (VPL == 4) {
     reinterpret_cast<uint16_t*>(codes)[lane] = (uint16_t)packed;
-  else
+  } else {
     codes[lane] = (uint8_t)packed;
+  }
   if (lane == 0) *sz = (uint32_t)__half_as_ushort(sh) | ((uint32_t)__half_as_ushort(zh) << 16);
 }
 
@@ -231,10 +251,11 @@ __global__ void __launch_bounds__(256) append_kv4_kernel(const AppendParams p) {
       streaming = true;
       if (si == 0 && lane == 0) p.pos[b * SR + slot] = (int32_t)t_abs;
     }
-    quantize_row<D>(p.k_new + src_row * D, (streaming ? p.ks4 : p.k4) + dst_row * (D / 2),
-                    (streaming ? p.kssz : p.ksz) + dst_row, lane);
-    quantize_row<D>(p.v_new + src_row * D, (streaming ? p.vs4 : p.v4) + dst_row * (D / 2),
-                    (streaming ? p.vssz : p.vsz) + dst_row, lane);
+    quantize_row<D, false>(p.k_new + src_row * D, (streaming ? p.ks4 : p.k4) + dst_row * (D / 2), 0,
+                           (streaming ? p.kssz : p.ksz) + dst_row, lane);
+    // plane pitches are multiples of 16 rows, so dst_row's 16-row group starts at dst_row & ~15
+    quantize_row<D, true>(p.v_new + src_row * D, (streaming ? p.vs4 : p.v4) + (dst_row & ~int64_t(15)) * (D / 2),
+                          (int)(dst_row & 15), (streaming ? p.vssz : p.vsz) + dst_row, lane);
   }
 }
 

@@ -367,6 +367,13 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
 // 4-7 under the exponent of 64 (0x5400, unit in the last place 1/16) as 64 + c.
 constexpr uint32_t kLoMagic = 0x64006400u, kHiMagic = 0x54005400u;
 
+// (x & mask) | magic in one instruction
+__device__ __forceinline__ uint32_t and_or(uint32_t x, uint32_t mask, uint32_t magic) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(x), "r"(mask), "r"(magic));
+  return d;
+}
+
 // The per-warp consumer used when the query heads of a KV head are many (and for
 // 4-bit caches): a warp's 16-key slice is two tensor-core products instead of one
 // packed FMA per (element, head pair).
@@ -475,7 +482,10 @@ struct MmaSlice {
     }
   }
 
-  // One 16-key slice.
+  // One 16-key slice. kFull: every key of the slice is a stored, visible key (an interior
+  // tile of a retrieval unit), so no key needs masking; the rows gid >= G then hold
+  // finite values for heads that do not exist, whose columns of O^T are never written out.
+  template <bool kFull>
   __device__ __forceinline__ void slice(const SliceIn& in, int gid, int tig) {
     float x[4];  // scores of keys 2 tig, 2 tig + 1, 2 tig + 8, 2 tig + 9
     {
@@ -502,10 +512,10 @@ struct MmaSlice {
 #pragma unroll
           for (int u = 0; u < WPT; ++u) {
             const uint32_t xw = w[u], x8 = w[u] >> 8;
-            mma16816<true>(sc[j][u & 1], qa[2 * u][0], 0u, qa[2 * u][1], 0u, (xw & 0x000F000Fu) | kLoMagic,
-                           (xw & 0x00F000F0u) | kHiMagic);
+            mma16816<true>(sc[j][u & 1], qa[2 * u][0], 0u, qa[2 * u][1], 0u, and_or(xw, 0x000F000Fu, kLoMagic),
+                           and_or(xw, 0x00F000F0u, kHiMagic));
             mma16816<true>(sc[j][u & 1], qa[2 * u + 1][0], 0u, qa[2 * u + 1][1], 0u,
-                           (x8 & 0x000F000Fu) | kLoMagic, (x8 & 0x00F000F0u) | kHiMagic);
+                           and_or(x8, 0x000F000Fu, kLoMagic), and_or(x8, 0x00F000F0u, kHiMagic));
           }
         } else {
 #pragma unroll
@@ -534,7 +544,7 @@ struct MmaSlice {
     float mx = -INFINITY;
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      x[k] = ((in.hvalid >> k) & 1u) ? x[k] * qfac : -INFINITY;
+      x[k] = (kFull || ((in.hvalid >> k) & 1u)) ? x[k] * qfac : -INFINITY;
       mx = fmaxf(mx, x[k]);
     }
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
@@ -562,7 +572,7 @@ struct MmaSlice {
       float pr[4];
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        pr[k] = ((in.hvalid >> k) & 1u) ? ex2_approx(x[k] - m_run) : 0.f;
+        pr[k] = (kFull || ((in.hvalid >> k) & 1u)) ? ex2_approx(x[k] - m_run) : 0.f;
         l_part += pr[k];
       }
       uint32_t pb0, pb1;
@@ -574,35 +584,30 @@ struct MmaSlice {
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const float2 sz = scale_zero(zz[k]);
-          const bool ok = (in.hvalid >> k) & 1u;  // the pair of an unused row may be anything
+          const bool ok = kFull || ((in.hvalid >> k) & 1u);  // the pair of an unused row may be anything
           b[k] = ok ? pr[k] * (sz.x * (1.f / kOScale)) : 0.f;
           z_part += ok ? pr[k] * sz.y : 0.f;
         }
         pb0 = pack_half2(b[0], b[1]);
         pb1 = pack_half2(b[2], b[3]);
-        constexpr int VB = D / 16;  // code bytes of a lane per V row (one per m-tile)
-        uint32_t w[4][(VB + 3) / 4];
+        // V codes in fragment order (see the 4-bit append): the lane's word i holds, for
+        // its dims of m-tile i, the codes of keys 2 tig, 2 tig + 8, 2 tig + 1, 2 tig + 9
+        uint32_t w[MT];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const uint8_t* r = in.v + kr[k] * ROW + VB * gid;
-          if constexpr (VB == 8) {
-            const uint2 v = *reinterpret_cast<const uint2*>(r);
-            w[k][0] = v.x;
-            w[k][1] = v.y;
-          } else {
-            w[k][0] = *reinterpret_cast<const uint32_t*>(r);
-          }
+        for (int c = 0; c < MT / 4; ++c) {
+          const uint4 v = *reinterpret_cast<const uint4*>(in.v + (4 * gid + tig) * MT * 4 + 16 * c);
+          w[4 * c] = v.x;
+          w[4 * c + 1] = v.y;
+          w[4 * c + 2] = v.z;
+          w[4 * c + 3] = v.w;
         }
 #pragma unroll
         for (int i = 0; i < MT; ++i) {
-          // bytes i of keys (2 tig, 2 tig + 1) side by side in the two halves
-          const uint32_t sel = (uint32_t)(i & 3) * 0x11u + (uint32_t)(4 + (i & 3)) * 0x1100u;
-          const uint32_t y01 = __byte_perm(w[0][i >> 2], w[1][i >> 2], sel);
-          const uint32_t y89 = __byte_perm(w[2][i >> 2], w[3][i >> 2], sel);
-          mma16816<true>(o[i], hsub2((y01 & 0x000F000Fu) | kLoMagic, kLoMagic),
-                         hsub2((y01 & 0x00F000F0u) | kHiMagic, kHiMagic),
-                         hsub2((y89 & 0x000F000Fu) | kLoMagic, kLoMagic),
-                         hsub2((y89 & 0x00F000F0u) | kHiMagic, kHiMagic), pb0, pb1);
+          const uint32_t x8 = w[i] >> 8;
+          mma16816<true>(o[i], hsub2(and_or(w[i], 0x000F000Fu, kLoMagic), kLoMagic),
+                         hsub2(and_or(w[i], 0x00F000F0u, kHiMagic), kHiMagic),
+                         hsub2(and_or(x8, 0x000F000Fu, kLoMagic), kLoMagic),
+                         hsub2(and_or(x8, 0x00F000F0u, kHiMagic), kHiMagic), pb0, pb1);
         }
       } else {
         pb0 = pack_bf16x2(pr[0], pr[1]);
@@ -610,7 +615,7 @@ struct MmaSlice {
         uint32_t w[4][MT];  // MT words = this lane's DT dims of each key
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          const bool ok = (in.kvalid >> k) & 1u;  // rows not copied in this stage may hold anything
+          const bool ok = kFull || ((in.kvalid >> k) & 1u);  // rows not copied in this stage may hold anything
 #pragma unroll
           for (int c = 0; c < MT / 4; ++c) {
             const uint4 v = *reinterpret_cast<const uint4*>(in.v + kr[k] * ROW + DT * 2 * gid + c * 16);
@@ -839,8 +844,11 @@ __global__ void __launch_bounds__(kThreads, kMode == kModeKv4 ? kDecodeCtasPerSm
             kvalid |= (uint32_t)valid << k;
           }
         }
-        mm.slice(SliceIn{sk, sv, sk + 2 * C::SLICE, sk + 2 * C::SLICE + C::PSLICE, kvalid, gid < G ? kvalid : 0u},
-                 gid, tig);
+        const SliceIn in{sk, sv, sk + 2 * C::SLICE, sk + 2 * C::SLICE + C::PSLICE, kvalid, gid < G ? kvalid : 0u};
+        if (full_tile)
+          mm.template slice<true>(in, gid, tig);
+        else
+          mm.template slice<false>(in, gid, tig);
       } else {
         float sc[C::IT];
         bool vis[C::IT];

@@ -139,3 +139,19 @@ def decode_rescale_hits(scores_by_unit, n, num_ctas, streaming_units, tile=128, 
                     m = np.where(grow, mx, m)
             t = te
     return count
+
+
+def kv4_v_rows(groups, D):
+    """4-bit V codes as the library stores them (16-row groups in fragment order, as
+    include/duo_attn.h states: row k, dims (2 dp, 2 dp + 1) at byte 4 ((4 (dp / MT) +
+    (k % 8) / 2) MT + dp % MT) + 2 (k % 2) + k / 8 of its group, MT = D / 16) -> rows of
+    D / 2 bytes, even dim in the low nibble. groups: uint8 [..., rows (multiple of 16), D / 2]."""
+    groups = np.asarray(groups)
+    MT = D // 16
+    k = np.arange(16)[:, None]
+    dp = np.arange(D // 2)[None, :]
+    addr = 4 * ((4 * (dp // MT) + (k % 8) // 2) * MT + dp % MT) + 2 * (k % 2) + k // 8  # [16, D/2]
+    lead = groups.shape[:-2]
+    rows = groups.shape[-2]
+    g = groups.reshape(lead + (rows // 16, 16 * (D // 2)))
+    return g[..., addr].reshape(lead + (rows, D // 2))

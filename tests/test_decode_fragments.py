@@ -38,9 +38,19 @@ def fp16_pair(word):
     return half_bits_value(word & 0xFFFF), half_bits_value(word >> 16)
 
 
-def byte_perm(x, y, sel):
-    src = [(x >> (8 * i)) & 0xFF for i in range(4)] + [(y >> (8 * i)) & 0xFF for i in range(4)]
-    return sum(src[(sel >> (4 * i)) & 7] << (8 * i) for i in range(4))
+def v_group_bytes(codes, D):
+    """The 4-bit V layout of one 16-row group as include/duo_attn.h states it: the byte of
+    row k and dims (2 dp, 2 dp + 1) (low, high nibble) at 4 ((4 (dp / MT) + (k % 8) / 2)
+    MT + dp % MT) + 2 (k % 2) + k / 8, MT = D / 16."""
+    MT = D // 16
+    out = np.full(16 * D // 2, -1, np.int64)
+    for k in range(16):
+        for dp in range(D // 2):
+            a = 4 * ((4 * (dp // MT) + (k % 8) // 2) * MT + dp % MT) + 2 * (k % 2) + k // 8
+            assert out[a] < 0  # each byte holds one row's pair of codes
+            out[a] = codes[k, 2 * dp] | (codes[k, 2 * dp + 1] << 4)
+    assert (out >= 0).all()
+    return out.astype(np.uint8)
 
 
 @pytest.mark.parametrize("D", [64, 128])
@@ -122,7 +132,7 @@ def test_output_rows(D, G, kv4):
     p[G:] = 0
     if kv4:
         codes = rng.integers(0, 16, (16, D))
-        packed = np.ascontiguousarray((codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8))
+        words = v_group_bytes(codes, D).view("<u4")  # the group's 32-bit words
         V = codes.astype(float)
     else:
         V = rng.standard_normal((16, D))
@@ -133,15 +143,14 @@ def test_output_rows(D, G, kv4):
         for g, t in LANES:
             k0, k1, k2, k3 = kr(t)
             if kv4:
-                VB = D // 16  # bytes of a lane per row: byte i is this m-tile's
-                sel = (i & 3) * 0x11 + (4 + (i & 3)) * 0x1100
-                word = lambda key: int(np.ascontiguousarray(packed[key, VB * g:VB * g + VB]).view("<u4")[i >> 2])
-                y01 = byte_perm(word(k0), word(k1), sel)
-                y89 = byte_perm(word(k2), word(k3), sel)
-                a0 = tuple(v - 1024 for v in fp16_pair((y01 & 0x000F000F) | 0x64006400))
-                a1 = tuple(v - 64 for v in fp16_pair((y01 & 0x00F000F0) | 0x54005400))
-                a2 = tuple(v - 1024 for v in fp16_pair((y89 & 0x000F000F) | 0x64006400))
-                a3 = tuple(v - 64 for v in fp16_pair((y89 & 0x00F000F0) | 0x54005400))
+                # word i of lane (g, t): bytes = keys 2t, 2t + 8, 2t + 1, 2t + 9 (low nibble
+                # dim d, high nibble dim d + 1); the shift by 8 brings keys 2t + 8, 2t + 9 down
+                w = int(words[(4 * g + t) * (D // 16) + i])
+                x8 = w >> 8
+                a0 = tuple(v - 1024 for v in fp16_pair((w & 0x000F000F) | 0x64006400))
+                a1 = tuple(v - 64 for v in fp16_pair((w & 0x00F000F0) | 0x54005400))
+                a2 = tuple(v - 1024 for v in fp16_pair((x8 & 0x000F000F) | 0x64006400))
+                a3 = tuple(v - 64 for v in fp16_pair((x8 & 0x00F000F0) | 0x54005400))
             else:
                 d0 = DT * g + 2 * i
                 a0, a1 = (V[k0, d0], V[k1, d0]), (V[k0, d0 + 1], V[k1, d0 + 1])

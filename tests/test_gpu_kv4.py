@@ -11,7 +11,7 @@ import duo_synth as ds
 import oracle.kv4 as kv4
 from oracle import RingCacheSim
 from oracle.attention import OracleCache, decode_from_cache
-from gpu_util import assert_close, device_stream, host_stream, to_np
+from gpu_util import assert_close, device_stream, host_stream, kv4_v_rows, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -71,13 +71,16 @@ def test_kv4_append_is_bit_exact_and_decode_matches_oracle(case):
     ret = [h for h in range(Hkv) if kinds[h]]
     strm = [h for h in range(Hkv) if not kinds[h]]
     # stored rows, bit for bit
-    for X, codes, sz, scodes, ssz in ((Kh, layer.k_codes, layer.k_sz, layer.ks_codes, layer.ks_sz),
-                                      (Vh, layer.v_codes, layer.v_sz, layer.vs_codes, layer.vs_sz)):
+    rows = lambda t: t.cpu().numpy()
+    v_rows = lambda t: kv4_v_rows(t.cpu().numpy(), D)  # V codes are kept in 16-row groups
+    for X, codes, sz, scodes, ssz, as_rows in ((Kh, layer.k_codes, layer.k_sz, layer.ks_codes, layer.ks_sz, rows),
+                                               (Vh, layer.v_codes, layer.v_sz, layer.vs_codes, layer.vs_sz, v_rows)):
+        codes, scodes = as_rows(codes), as_rows(scodes)
         c_all, s_all, z_all = kv4.quantize_rows(X)  # [B, total, Hkv, ...]
         if ret:
             got_s, got_z = _bits(sz[:, :, :total])
             for ri, h in enumerate(ret):
-                assert np.array_equal(codes[:, ri, :total].cpu().numpy(), kv4.pack_codes(c_all[:, :, h]))
+                assert np.array_equal(codes[:, ri, :total], kv4.pack_codes(c_all[:, :, h]))
                 assert np.array_equal(got_s[:, ri].view(np.uint16), s_all[:, :, h].view(np.uint16))
                 assert np.array_equal(got_z[:, ri].view(np.uint16), z_all[:, :, h].view(np.uint16))
         if strm:
@@ -90,7 +93,7 @@ def test_kv4_append_is_bit_exact_and_decode_matches_oracle(case):
                 for slot, t in enumerate(pos):
                     if t < 0:
                         continue
-                    assert np.array_equal(scodes[:, si, slot].cpu().numpy(), kv4.pack_codes(c_all[:, t, h]))
+                    assert np.array_equal(scodes[:, si, slot], kv4.pack_codes(c_all[:, t, h]))
                     assert np.array_equal(got_s[:, si, slot].view(np.uint16), s_all[:, t, h].view(np.uint16))
                     assert np.array_equal(got_z[:, si, slot].view(np.uint16), z_all[:, t, h].view(np.uint16))
     # decode over what the cache holds: the dequantized rows
