@@ -393,9 +393,9 @@ def make_layer(w, cap, dev, paged_block, pool=False, kv4=False):
     import numpy as np
     import torch
 
-    from streaming_kv_cache_duo_gb300 import DuoKv4Layer, DuoLayer, DuoPagedLayer
+    from streaming_kv_cache_duo_gb300 import DuoKv4Layer, DuoKv4PagedLayer, DuoLayer, DuoPagedLayer
     kinds = w.is_retrieval
-    if kv4:
+    if kv4 and paged_block <= 0:
         return DuoKv4Layer(w.B, w.Hq, w.Hkv, w.D, w.S, w.R, cap, kinds, device=dev)
     if paged_block <= 0:
         return DuoLayer(w.B, w.Hq, w.Hkv, w.D, w.S, w.R, cap, kinds, device=dev)
@@ -406,6 +406,9 @@ def make_layer(w, cap, dev, paged_block, pool=False, kv4=False):
     num_blocks = w.B * planes * max_blocks
     ids = np.random.default_rng(w.seed).permutation(num_blocks).reshape(w.B, planes, max_blocks)
     table = torch.tensor(ids[:, :n_ret], dtype=torch.int32, device=dev) if n_ret else None
+    if kv4:  # 4-bit rows in the pool; streaming heads keep their 4-bit ring arrays
+        return DuoKv4PagedLayer(w.B, w.Hq, w.Hkv, w.D, w.S, w.R, paged_block, max_blocks, num_blocks, table, kinds,
+                                device=dev)
     stream = torch.tensor(ids[:, n_ret:], dtype=torch.int32, device=dev) if pool else None
     return DuoPagedLayer(w.B, w.Hq, w.Hkv, w.D, w.S, w.R, paged_block, max_blocks, num_blocks, table, kinds,
                          device=dev, stream_table=stream)
@@ -470,7 +473,8 @@ def bench_decode(w, steps_cap, peaks, paged_block=0, pool=False, kv4=False):
             "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(gbs / peak, 4),
                          "traffic": None if (kv4 or paged_block) else measured_traffic("decode"),
-                         "kernel": f"decode_kernel<{w.D},{w.Hq // w.Hkv},{'kv4' if kv4 else 'plain'}>"},
+                         "kernel": f"decode_kernel<{w.D},{w.Hq // w.Hkv},"
+                                   f"{('kv4' if kv4 else 'plain') + (' paged' if paged_block else '')}>"},
             "tokens_per_s": round(1e3 / (sum(times) / len(times)), 1), "clocks": clk}
 
 

@@ -282,6 +282,24 @@ duo_status duo_kv_append_kv4(duo_handle* handle, duo_kv_cache* cache, const duo_
 duo_status duo_attn_decode_kv4(duo_handle* handle, const duo_kv_cache* cache, const duo_kv4_cache* kv4,
                                const void* q, void* o, void* workspace, size_t workspace_bytes, void* stream);
 
+/* 4-bit caches with the retrieval rows in a paged pool (the two layouts above combined:
+ * the block allocator of the attention-sink issue holding the 4-bit rows the README
+ * pairs the method with). kv4->k_codes, v_codes are pools u8 [num_blocks, block_size,
+ * D / 2] and kv4->k_sz, v_sz pools u32 [num_blocks, block_size]; row t of retrieval head
+ * r of sequence b is row t % block_size of block paged->block_table[(b n_ret + r)
+ * max_blocks + t / block_size] (block_size a multiple of 128, so 16-row V groups never
+ * straddle blocks). The row encoding and the V group order are those of the contiguous
+ * 4-bit arrays. Streaming heads keep their 4-bit sink + ring arrays: paged->stream_table
+ * must be NULL (DUO_ERR_UNSUPPORTED otherwise). Capacity, bad block ids and errors: as
+ * duo_kv_append_paged / duo_attn_decode_paged (a bad id is reported by duo_device_error,
+ * its rows are neither written nor read). */
+duo_status duo_kv_append_kv4_paged(duo_handle* handle, duo_kv_cache* cache, const duo_paged* paged,
+                                   const duo_kv4_cache* kv4, const void* k_new, const void* v_new, int32_t T,
+                                   void* stream);
+duo_status duo_attn_decode_kv4_paged(duo_handle* handle, const duo_kv_cache* cache, const duo_paged* paged,
+                                     const duo_kv4_cache* kv4, const void* q, void* o, void* workspace,
+                                     size_t workspace_bytes, void* stream);
+
 /* Dual Chunk Attention (vLLM pull request "[Model] Implement DualChunkAttention for
  * Qwen2 Models"): the sequence is cut into chunks of chunk_len positions from the start
  * (the last one may be shorter) and every position carries three query vectors made by

@@ -251,6 +251,53 @@ class DuoKv4Layer(DuoLayer):
         return out
 
 
+class DuoKv4PagedLayer(DuoKv4Layer):
+    """4-bit caches whose retrieval rows live in a pool of blocks shared by every sequence
+    and head: codes u8 [num_blocks, block_size, D/2] and (scale, zero) pairs int32
+    [num_blocks, block_size], row t of retrieval head r of sequence b at row t %
+    block_size of block block_table[b, r, t // block_size] (block_table: device int32
+    [B, n_ret, max_blocks]; block_size a multiple of 128). Streaming heads keep their 4-bit
+    sink + ring arrays."""
+
+    def __init__(self, batch, num_q_heads, num_kv_heads, head_dim, sink_size, recent_size, block_size,
+                 max_blocks, num_blocks, block_table, is_retrieval, device="cuda"):
+        import torch
+        super().__init__(batch, num_q_heads, num_kv_heads, head_dim, sink_size, recent_size, 16, is_retrieval,
+                         device=device)
+        u8 = dict(dtype=torch.uint8, device=self.device)
+        i32 = dict(dtype=torch.int32, device=self.device)
+        rows = num_blocks * block_size if self.n_ret else 0
+        self.k_codes = torch.zeros((rows, head_dim // 2), **u8)
+        self.v_codes = torch.zeros_like(self.k_codes)
+        self.k_sz = torch.zeros((rows,), **i32)
+        self.v_sz = torch.zeros_like(self.k_sz)
+        if block_table is not None:
+            assert block_table.dtype == torch.int32 and block_table.is_cuda and block_table.is_contiguous()
+            assert tuple(block_table.shape) == (batch, self.n_ret, max_blocks)
+        self.block_size = block_size
+        self.block_table = block_table
+        self.paged = _lib.duo_paged(block_table.data_ptr() if block_table is not None else None, block_size,
+                                    max_blocks, num_blocks, None)
+        ptr = lambda t: t.data_ptr() if t.numel() else None
+        self.kv4 = _lib.duo_kv4_cache(ptr(self.k_codes), ptr(self.v_codes), ptr(self.k_sz), ptr(self.v_sz),
+                                      ptr(self.ks_codes), ptr(self.vs_codes), ptr(self.ks_sz), ptr(self.vs_sz))
+
+    def append(self, k_new, v_new, stream=None) -> None:
+        T = k_new.shape[1]
+        _lib._bf16(k_new, (self.B, T, self.Hkv, self.D), "k_new")
+        _lib._bf16(v_new, (self.B, T, self.Hkv, self.D), "v_new")
+        _lib.duo_kv_append_kv4_paged(self.handle, self.cache, self.paged, self.kv4, k_new, v_new, T, stream)
+
+    def decode(self, q, out=None, stream=None):
+        import torch
+        _lib._bf16(q, (self.B, self.Hq, self.D), "q")
+        if out is None:
+            out = torch.empty_like(q)
+        _lib._bf16(out, (self.B, self.Hq, self.D), "o")
+        _lib.duo_attn_decode_kv4_paged(self.handle, self.cache, self.paged, self.kv4, q, out, self.workspace, stream)
+        return out
+
+
 def _check_mscale(mscale, shape):
     import torch
     if mscale is None:

@@ -237,7 +237,17 @@ __global__ void __launch_bounds__(256) append_kv4_kernel(const AppendParams p) {
       const int64_t t = (r / n_ret) % T;
       const int64_t b = r / n_ret / T;
       src_row = (b * T + t) * Hkv + p.heads.ret_head[ri];
-      dst_row = (b * n_ret + ri) * p.cap16 + p.n + t;
+      if (p.pg.table) {  // a pool of blocks [num_blocks x block_size rows]
+        const int64_t row = p.n + t;
+        const int64_t blk = p.pg.table[(b * n_ret + ri) * p.pg.max_blocks + row / p.pg.block_size];
+        if (blk < 0 || blk >= p.pg.num_blocks) {
+          if (lane == 0) atomicOr(&g_append_err, kErrBadBlock);
+          continue;
+        }
+        dst_row = blk * p.pg.block_size + row % p.pg.block_size;
+      } else {
+        dst_row = (b * n_ret + ri) * p.cap16 + p.n + t;
+      }
       streaming = false;
     } else {
       const int64_t q = r - ret_rows;

@@ -68,9 +68,12 @@ constexpr int kModePaged = 1;  // retrieval caches in a paged pool (block table)
 constexpr int kModePool = 2;   // both head kinds in the paged pool
 constexpr int kModeDca = 3;    // Dual Chunk Attention: the query vector depends on the key's chunk
 constexpr int kModeKv4 = 4;    // 4-bit caches: codes + fp16 (scale, zero) per row
+constexpr int kModeKv4Paged = 5;  // 4-bit caches, retrieval rows in a paged pool of blocks
 
 // retrieval caches (and maybe streaming ones) in the paged pool
 __host__ __device__ constexpr bool is_paged_mode(int mode) { return mode == kModePaged || mode == kModePool; }
+// 4-bit caches (contiguous or paged retrieval rows)
+__host__ __device__ constexpr bool is_kv4_mode(int mode) { return mode == kModeKv4 || mode == kModeKv4Paged; }
 
 template <int D, int G, bool KV4 = false>
 struct Cfg {
@@ -147,7 +150,7 @@ __device__ __forceinline__ Unit unit_info(const DecodeParams& p, int u) {
     x.streaming = true;
     x.pq = seq_len(p, x.b) - 1;
     x.keys = x.pq + 1 < (int64_t)(p.sh.S + p.sh.R) ? x.pq + 1 : (int64_t)(p.sh.S + p.sh.R);
-    if (kMode == kModeKv4) x.plane = us;  // its ring plane in the 4-bit arrays
+    if (is_kv4_mode(kMode)) x.plane = us;  // its ring plane in the 4-bit arrays
     if (kMode == kModePool) {  // rows [0, n) of its pool blocks, of which only some tiles are read
       x.plane = us;
       x.keys = x.pq + 1;
@@ -221,6 +224,10 @@ struct Cursor {
   int bi;   // paged: index of the block holding the tile in the unit's table row
   int bt;   // paged: the tile's index within that block
   int blk;  // paged: the block id there (as stored, unchecked)
+  // 4-bit retrieval rows in a pool (lane 0 only): the (plane, block index) whose id is in
+  // kv4_blk, and the id of the block after it, loaded ahead so that its latency passes
+  // while the slices of the current block are consumed
+  int kv4_plane = -1, kv4_bi = -1, kv4_blk = 0, kv4_next = 0;
   __device__ __forceinline__ bool in_pool() const { return !x.streaming || kMode == kModePool; }
   // row tile of the current position (= lt except for a streaming unit in the pool)
   __device__ __forceinline__ int64_t row_tile() const { return (int64_t)bi * tpb + bt; }
@@ -270,10 +277,10 @@ struct Cursor {
 // slice lies in a paged block whose id is out of range: then nothing is copied, the
 // error is recorded and the consumer skips the slice's rows.
 template <int D, int G, int kMode>
-__device__ __forceinline__ bool issue_slice(const DecodeParams& p, const Cursor<kMode>& cur, int w,
+__device__ __forceinline__ bool issue_slice(const DecodeParams& p, Cursor<kMode>& cur, int w,
                                             uint8_t* stage, uint64_t* bar) {
-  using C = Cfg<D, G, kMode == kModeKv4>;
-  if constexpr (kMode == kModeKv4) {
+  using C = Cfg<D, G, is_kv4_mode(kMode)>;
+  if constexpr (is_kv4_mode(kMode)) {
     // whole 16-row chunks of codes and (scale, zero) pairs: the planes' row pitches are
     // multiples of 16, so the chunk stays inside its plane; rows past the keys are
     // copied but never used
@@ -282,7 +289,29 @@ __device__ __forceinline__ bool issue_slice(const DecodeParams& p, const Cursor<
       mbar_arrive_expect_tx(bar, 0);
       return false;
     }
-    const int64_t r = cur.x.plane * (cur.x.streaming ? (int64_t)p.sr16 : p.cap16) + cur.lt * kTK + (int64_t)w * kKPW;
+    int64_t r = cur.x.plane * (cur.x.streaming ? (int64_t)p.sr16 : p.cap16) + cur.lt * kTK + (int64_t)w * kKPW;
+    if (kMode == kModeKv4Paged && !cur.x.streaming) {
+      // the slice's 16 rows lie in one block (block sizes are multiples of 128)
+      // rows stay below block_size x max_blocks < 2^31 (checked on the host)
+      const int row = (int)(cur.lt * kTK) + w * kKPW;
+      const int bi = (int)((uint32_t)row / (uint32_t)p.pg.block_size);
+      const int plane = (int)cur.x.plane;
+      if (plane != cur.kv4_plane || bi != cur.kv4_bi) {
+        const int32_t* trow = p.pg.table + (int64_t)plane * p.pg.max_blocks;
+        cur.kv4_blk = (plane == cur.kv4_plane && bi == cur.kv4_bi + 1) ? cur.kv4_next : __ldg(trow + bi);
+        cur.kv4_plane = plane;
+        cur.kv4_bi = bi;
+        // the next block's id, if the unit has rows there (else its entry may not exist)
+        if ((int64_t)(bi + 1) * p.pg.block_size < cur.x.keys) cur.kv4_next = __ldg(trow + bi + 1);
+      }
+      const int64_t blk = cur.kv4_blk;
+      if (blk < 0 || blk >= p.pg.num_blocks) {
+        atomicOr(&g_decode_err, kErrBadBlock);
+        mbar_arrive_expect_tx(bar, 0);
+        return true;  // nothing copied; the consumer skips the slice's rows
+      }
+      r = blk * p.pg.block_size + (row - bi * p.pg.block_size);
+    }
     const uint8_t* kc = (cur.x.streaming ? p.ks4 : p.k4) + r * (D / 2);
     const uint8_t* vc = (cur.x.streaming ? p.vs4 : p.v4) + r * (D / 2);
     const uint32_t* kz = (cur.x.streaming ? p.kssz : p.ksz) + r;
@@ -685,9 +714,9 @@ struct WarpSync {
 };
 
 template <int D, int G, int kMode>
-__global__ void __launch_bounds__(kThreads, kMode == kModeKv4 ? kDecodeCtasPerSmKv4 : 1)
+__global__ void __launch_bounds__(kThreads, is_kv4_mode(kMode) ? kDecodeCtasPerSmKv4 : 1)
     decode_kernel(const DecodeParams p) {
-  using C = Cfg<D, G, kMode == kModeKv4>;
+  using C = Cfg<D, G, is_kv4_mode(kMode)>;
   extern __shared__ __align__(1024) uint8_t smem[];
   float* red = reinterpret_cast<float*>(smem + C::RING);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::RING + (size_t)C::RED * 4);  // [kWarps][C::NSW]
@@ -714,6 +743,7 @@ __global__ void __launch_bounds__(kThreads, kMode == kModeKv4 ? kDecodeCtasPerSm
 
   // refill cursor (warp-uniform); the prologue issues the first C::NSW - 1 slices
   constexpr bool kPaged = is_paged_mode(kMode);
+  constexpr bool kBadBlocks = kPaged || kMode == kModeKv4Paged;  // a slice may come from a bad block id
   Cursor<kMode> cur;
   cur.init(p, c, t0, t1, live);
   int64_t issued = 0;
@@ -721,7 +751,7 @@ __global__ void __launch_bounds__(kThreads, kMode == kModeKv4 ? kDecodeCtasPerSm
   for (int s = 0; s < C::NSW - 1 && cur.live; ++s) {
     if (lane == 0) {
       const bool bad = issue_slice<D, G, kMode>(p, cur, warp, ring + s * C::WSTAGE, &wfull[s]);
-      if (kPaged) badmask = bad ? (badmask | (1u << s)) : (badmask & ~(1u << s));
+      if (kBadBlocks) badmask = bad ? (badmask | (1u << s)) : (badmask & ~(1u << s));
     }
     cur.advance(p, c, t1, live);
     ++issued;
@@ -730,9 +760,9 @@ __global__ void __launch_bounds__(kThreads, kMode == kModeKv4 ? kDecodeCtasPerSm
   const int kg = lane / C::LPK;           // key within the warp iteration
   const int cl = lane % C::LPK;           // dims slot of this lane within its key group
   const int hme = cl >> (C::LB - C::GB);  // the head this lane ends up owning
-  constexpr bool kMma = kMode == kModeKv4 || G >= kMmaMinG;
+  constexpr bool kMma = is_kv4_mode(kMode) || G >= kMmaMinG;
   const int gid = lane >> 2, tig = lane & 3;  // tensor-core slices: fragment row group, thread in group
-  std::conditional_t<kMma, MmaSlice<D, G, kMode == kModeKv4>, NoMma> mm;
+  std::conditional_t<kMma, MmaSlice<D, G, is_kv4_mode(kMode)>, NoMma> mm;
   const int SR = p.sh.S + p.sh.R;
   WarpSync ws{segbar, 0};
   int64_t j = 0;  // tiles consumed
@@ -810,7 +840,7 @@ __global__ void __launch_bounds__(kThreads, kMode == kModeKv4 ? kDecodeCtasPerSm
         const int sn = (int)((j + C::NSW - 1) % C::NSW);
         if (lane == 0) {
           const bool bad = issue_slice<D, G, kMode>(p, cur, warp, ring + sn * C::WSTAGE, &wfull[sn]);
-          if (kPaged) badmask = bad ? (badmask | (1u << sn)) : (badmask & ~(1u << sn));
+          if (kBadBlocks) badmask = bad ? (badmask | (1u << sn)) : (badmask & ~(1u << sn));
         }
         cur.advance(p, c, t1, live);
         ++issued;
@@ -823,7 +853,7 @@ __global__ void __launch_bounds__(kThreads, kMode == kModeKv4 ? kDecodeCtasPerSm
       const bool str_pool = kMode == kModePool && x.streaming;
       const int64_t kt = str_pool ? stream_tile(p, lt) : lt;
       int rows = warp_rows(x.keys, kt, warp);
-      if (kPaged && ((__shfl_sync(0xffffffffu, badmask, 0) >> s) & 1u)) rows = 0;
+      if (kBadBlocks && ((__shfl_sync(0xffffffffu, badmask, 0) >> s) & 1u)) rows = 0;
       const uint8_t* sk = ring + s * C::WSTAGE;
       const uint8_t* sv = sk + C::SLICE;
       const bool full_tile = rows == kKPW && !x.streaming;
@@ -1123,7 +1153,7 @@ __global__ void __launch_bounds__(kThreads, kMode == kModeKv4 ? kDecodeCtasPerSm
 
 template <int D, int G, int kMode>
 cudaError_t launch_v(const DecodeParams& p, cudaStream_t stream) {
-  using C = Cfg<D, G, kMode == kModeKv4>;
+  using C = Cfg<D, G, is_kv4_mode(kMode)>;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e =
@@ -1139,7 +1169,7 @@ cudaError_t launch_v(const DecodeParams& p, cudaStream_t stream) {
 // bookkeeping costs the contiguous kernel nothing
 template <int D, int G>
 cudaError_t launch_t(const DecodeParams& p, cudaStream_t stream) {
-  if (p.kv4) return launch_v<D, G, kModeKv4>(p, stream);
+  if (p.kv4) return p.pg.table ? launch_v<D, G, kModeKv4Paged>(p, stream) : launch_v<D, G, kModeKv4>(p, stream);
   if (p.chunk_len > 0) return launch_v<D, G, kModeDca>(p, stream);
   if (p.pg.stream_table) return launch_v<D, G, kModePool>(p, stream);
   return p.pg.table ? launch_v<D, G, kModePaged>(p, stream) : launch_v<D, G, kModePlain>(p, stream);

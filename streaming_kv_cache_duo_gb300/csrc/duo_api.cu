@@ -315,6 +315,7 @@ static duo_status append_impl(duo_handle* h, duo_kv_cache* c, const duo_paged* p
   if ((st = check_paged(h, pgd, &pg)) != DUO_OK) return st;
   if (kv4) {
     if ((st = check_kv4(h, c, kv4)) != DUO_OK) return st;
+    if (pg.stream_table) return fail(DUO_ERR_UNSUPPORTED, "4-bit caches keep streaming heads in their ring arrays");
   } else if ((st = check_cache(h, c, true, !pg.stream_table)) != DUO_OK) {
     return st;
   }
@@ -535,6 +536,8 @@ static duo_status decode_impl(duo_handle* h, const duo_kv_cache* c, const duo_pa
   duo_status st = check_handle(h);
   if (st != DUO_OK) return st;
   if (kv4 && (st = check_kv4(h, c, kv4)) != DUO_OK) return st;
+  if (kv4 && pgd && pgd->stream_table)
+    return fail(DUO_ERR_UNSUPPORTED, "4-bit caches keep streaming heads in their ring arrays");
   if (dca) {
     if ((st = check_dca(h, dca->chunk_len, dca->mscale)) != DUO_OK) return st;
     if (!dca->q_succ || !dca->q_inter || !aligned16(dca->q_succ) || !aligned16(dca->q_inter))
@@ -694,6 +697,21 @@ duo_status duo_attn_decode_kv4(duo_handle* h, const duo_kv_cache* c, const duo_k
                                void* o, void* workspace, size_t workspace_bytes, void* stream) {
   if (!kv4) return fail(DUO_ERR_INVALID_ARG, "kv4 is NULL");
   return decode_impl(h, c, nullptr, q, o, workspace, workspace_bytes, stream, nullptr, kv4);
+}
+
+duo_status duo_kv_append_kv4_paged(duo_handle* h, duo_kv_cache* c, const duo_paged* paged, const duo_kv4_cache* kv4,
+                                   const void* k_new, const void* v_new, int32_t T, void* stream) {
+  if (!paged) return fail(DUO_ERR_INVALID_ARG, "paged is NULL");
+  if (!kv4) return fail(DUO_ERR_INVALID_ARG, "kv4 is NULL");
+  return append_impl(h, c, paged, k_new, v_new, T, stream, kv4);
+}
+
+duo_status duo_attn_decode_kv4_paged(duo_handle* h, const duo_kv_cache* c, const duo_paged* paged,
+                                     const duo_kv4_cache* kv4, const void* q, void* o, void* workspace,
+                                     size_t workspace_bytes, void* stream) {
+  if (!paged) return fail(DUO_ERR_INVALID_ARG, "paged is NULL");
+  if (!kv4) return fail(DUO_ERR_INVALID_ARG, "kv4 is NULL");
+  return decode_impl(h, c, paged, q, o, workspace, workspace_bytes, stream, nullptr, kv4);
 }
 
 duo_status duo_dca_decode(duo_handle* h, const duo_kv_cache* c, const void* q, const void* q_succ,

@@ -1,6 +1,6 @@
 """Full-size parity in the cache layouts the benchmark also times, each layer built
 exactly as the benchmark builds it (bench.make_layer: paged pools with a seeded
-scattered block order, streaming heads in the pool, 4-bit caches):
+scattered block order, streaming heads in the pool, 4-bit caches, 4-bit caches in a pool):
 - the million-token decode (1 sequence, 1,048,576 context tokens, 32 q / 8 kv heads,
   D 128, 2 retrieval kv heads, sink 64 + ring 256), filled by the same 65536-token
   appends: sampled heads of the last decode step against the oracle;
@@ -73,6 +73,12 @@ def test_full_size_decode_1m_pool_sampled():
     """Both head kinds in the pool (streaming heads' blocks past the window untouched)."""
     w, got = _run(paged_block=256, pool=True)
     _check(w, got, False)
+
+
+def test_full_size_decode_1m_kv4_paged_sampled():
+    """4-bit retrieval rows in a pool of 256-token blocks in a scattered order."""
+    w, got = _run(paged_block=256, use_kv4=True)
+    _check(w, got, True)
 
 
 def test_full_size_decode_1m_kv4_sampled():
