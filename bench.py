@@ -918,7 +918,15 @@ def other_workload(args, w, world, rank, peaks):
     if args.paged:
         base["config"]["paged_block"] = args.paged
         base["config"]["streaming_heads"] = "paged pool" if args.pool else "sink + ring cache"
-    if w.dca_chunk:
+    if w.prefill_len and w.decode_steps and not w.dca_chunk:
+        # the tiny workload: prefill then decode steps, launch-bound, microseconds per step
+        r = bench_tiny(w, args.steps, args.warmup, peaks)
+        base["config"].update(seq_len=w.prefill_len, decode_steps=w.decode_steps,
+                              step="reset, prefill, append, 16 x (append 1, decode 1); one CUDA graph")
+        line = dict(base, value=round(r["us_per_step_graph"], 2), unit="us/step", higher_is_better=False,
+                    ms_per_step=round(r["us_per_step_graph"] / 1e3, 5), tiny=r,
+                    gpu_launches=r["gpu_launches_per_step"] * 2 * r["steps_timed"])
+    elif w.dca_chunk:
         r = bench_dca(w, args.steps, args.warmup, peaks)
         base["config"].update(seq_len=w.prefill_len, dca_chunk_len=w.dca_chunk, decode_steps=w.decode_steps,
                               step="one Dual Chunk Attention prefill launch of the prompt (all heads)")
@@ -969,7 +977,7 @@ def main():
     w = ds.WORKLOADS[args.workload]
     rank, world, local = dist_setup()
     if args.impl == "reference":
-        if w.prefill_len == 0 or w.chunk or w.dca_chunk:
+        if w.prefill_len == 0 or w.chunk or w.dca_chunk or w.decode_steps:
             if rank == 0:
                 print(json.dumps({"impl": "reference", "unavailable": "the oracle arm times the one-shot "
                                   "prefill workloads only"}))
@@ -980,7 +988,7 @@ def main():
     import __graft_entry__
     __graft_entry__.build()
     peaks, peak_src = load_peaks()
-    if w.prefill_len == 0 or w.chunk or w.dca_chunk:
+    if w.prefill_len == 0 or w.chunk or w.dca_chunk or w.decode_steps:
         other_workload(args, w, world, rank, peaks)
         return
     res = bench_prefill(w, args.steps, args.warmup, world, peaks, not args.no_e2e)
