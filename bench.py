@@ -548,7 +548,7 @@ def bench_decode_graph(w, peaks):
             "gpu_launches_per_step": 2}
 
 
-def bench_chunked(w, steps, warmup, peaks, paged_block=0, pool=False):
+def bench_chunked(w, steps, warmup, peaks, paged_block=0, pool=False, kv4=False):
     """Chunked prefill against the growing cache: one step = for each chunk, prefill of
     the chunk (keys: cache before it + the chunk) then its append."""
     import torch
@@ -559,7 +559,7 @@ def bench_chunked(w, steps, warmup, peaks, paged_block=0, pool=False):
     dev = torch.device("cuda", torch.cuda.current_device())
     L, C = w.prefill_len, w.chunk
     kinds = w.is_retrieval
-    layer = make_layer(w, L, dev, paged_block, pool)
+    layer = make_layer(w, L, dev, paged_block, pool, kv4)
     q = ds.stream_torch(w.seed, ds.STREAM_Q, w.B, 0, L, w.Hq, w.D, device=dev)
     k = ds.stream_torch(w.seed, ds.STREAM_K, w.B, 0, L, w.Hkv, w.D, device=dev)
     v = ds.stream_torch(w.seed, ds.STREAM_V, w.B, 0, L, w.Hkv, w.D, device=dev)
@@ -604,7 +604,7 @@ def bench_chunked(w, steps, warmup, peaks, paged_block=0, pool=False):
     pre_ms = sum(a.elapsed_time(b) for a, b in pre) / steps
     layer.close()
     # traffic of one step's prefill launches, from the ncu capture of the unpaged layout
-    traffic = measured_traffic("prefill_chunked") if not paged_block else None
+    traffic = measured_traffic("prefill_chunked") if not (paged_block or kv4) else None
     return {"value": flops / (ms * 1e-3) / 1e12, "ms_per_step": ms, "flops": flops, "retrieval_flops": fr,
             "prefill_ms": pre_ms, "append_ms": ms - pre_ms, "launches": 2 * len(chunks) * steps, "clocks": clk,
             "roofline": {"bound": "tensor", "achieved": round(flops / (pre_ms * 1e-3) / 1e12, 2),
@@ -934,7 +934,7 @@ def other_workload(args, w, world, rank, peaks):
                     roofline=r["roofline"], gpu_launches=r["launches"],
                     plain_causal_prefill_ms=round(r["plain_causal_ms"], 4), decode=r["decode"])
     elif w.chunk:
-        r = bench_chunked(w, args.steps, args.warmup, peaks, args.paged, args.pool)
+        r = bench_chunked(w, args.steps, args.warmup, peaks, args.paged, args.pool, args.kv4)
         base["config"].update(seq_len=w.prefill_len, chunk=w.chunk,
                               step="8 x (prefill of a 4096-token chunk against the cache, append)")
         line = dict(base, value=round(r["value"] * world, 2), unit="TFLOP/s", ms_per_step=round(r["ms_per_step"], 4),
@@ -964,7 +964,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--kv4", action="store_true",
-                    help="decode workloads: caches stored as 4-bit codes with an fp16 (scale, zero) per row")
+                    help="decode and chunked workloads: caches stored as 4-bit codes with an fp16 (scale, zero) "
+                         "per row (chunked prefill then dequantizes the cache tiles in the kernel)")
     ap.add_argument("--pool", action="store_true",
                     help="with --paged: streaming heads in the paged pool too (block-granular eviction)")
     ap.add_argument("--paged", type=int, default=0,

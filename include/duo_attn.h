@@ -258,7 +258,7 @@ duo_status duo_attn_decode_paged(duo_handle* handle, const duo_kv_cache* cache, 
  * used. duo_kv_append_kv4 quantizes and stores the new tokens (same slot rule as
  * duo_kv_append); duo_attn_decode_kv4 is duo_attn_decode over these arrays, with the
  * dequantization folded into the dot products (q . k = scale (q . codes) + zero sum(q)).
- * Prefill never reads a cache in this form: chunked prefill needs the bf16 caches.
+ * duo_attn_prefill_kv4 prefills a chunk against caches in this form.
  *
  * duo_attn_decode_kv4 runs its dot products on the tensor cores with fp16 operands
  * (codes, q, and p times the row scale, stored as p scale / 64) and fp32 accumulation,
@@ -281,6 +281,17 @@ duo_status duo_kv_append_kv4(duo_handle* handle, duo_kv_cache* cache, const duo_
                              const void* v_new, int32_t T, void* stream);
 duo_status duo_attn_decode_kv4(duo_handle* handle, const duo_kv_cache* cache, const duo_kv4_cache* kv4,
                                const void* q, void* o, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Prefill of T new tokens against 4-bit caches (chunked prefill after earlier chunks were
+ * appended with duo_kv_append_kv4): as duo_attn_prefill, with the keys and values of the
+ * cache rows (retrieval rows [0, n), valid sink + ring slots) read from `kv4` and
+ * dequantized (code * scale + zero in fp32, rounded to bf16) into the kernel's shared-memory
+ * tiles, so no bf16 copy of the cache exists anywhere; the T new tokens' k and v are the bf16
+ * inputs as usual. Append the chunk afterwards with duo_kv_append_kv4. cache->k_full,
+ * v_full, k_sr, v_sr are not used. Errors: as duo_attn_prefill, plus those of the 4-bit
+ * arrays (see duo_attn_decode_kv4). */
+duo_status duo_attn_prefill_kv4(duo_handle* handle, const duo_kv_cache* cache, const duo_kv4_cache* kv4,
+                                const void* q, const void* k, const void* v, int32_t T, void* o, void* stream);
 
 /* 4-bit caches with the retrieval rows in a paged pool (the two layouts above combined:
  * the block allocator of the attention-sink issue holding the 4-bit rows the README

@@ -250,6 +250,20 @@ class DuoKv4Layer(DuoLayer):
         _lib.duo_attn_decode_kv4(self.handle, self.cache, self.kv4, q, out, self.workspace, stream)
         return out
 
+    def prefill(self, q, k, v, out=None, kind_mask=3, stream=None):
+        """A chunk of T new tokens against the 4-bit caches (dequantized in the kernel)."""
+        import torch
+        assert kind_mask == 3
+        T = q.shape[1]
+        _lib._bf16(q, (self.B, T, self.Hq, self.D), "q")
+        _lib._bf16(k, (self.B, T, self.Hkv, self.D), "k")
+        _lib._bf16(v, (self.B, T, self.Hkv, self.D), "v")
+        if out is None:
+            out = torch.empty_like(q)
+        _lib._bf16(out, (self.B, T, self.Hq, self.D), "o")
+        _lib.duo_attn_prefill_kv4(self.handle, self.cache, self.kv4, q, k, v, T, out, stream)
+        return out
+
 
 class DuoKv4PagedLayer(DuoKv4Layer):
     """4-bit caches whose retrieval rows live in a pool of blocks shared by every sequence
@@ -287,6 +301,9 @@ class DuoKv4PagedLayer(DuoKv4Layer):
         _lib._bf16(k_new, (self.B, T, self.Hkv, self.D), "k_new")
         _lib._bf16(v_new, (self.B, T, self.Hkv, self.D), "v_new")
         _lib.duo_kv_append_kv4_paged(self.handle, self.cache, self.paged, self.kv4, k_new, v_new, T, stream)
+
+    def prefill(self, *args, **kwargs):
+        raise NotImplementedError("prefill against 4-bit rows in a paged pool is not provided")
 
     def decode(self, q, out=None, stream=None):
         import torch

@@ -32,7 +32,7 @@ EXPORTS = (
     "duo_attn_prefill", "duo_attn_prefill_select", "duo_decode_workspace_size", "duo_attn_decode",
     "duo_attn_decode_static", "duo_kv_append_paged", "duo_attn_prefill_paged", "duo_attn_decode_paged",
     "duo_paged_stream_dead_blocks", "duo_dca_prefill", "duo_dca_decode", "duo_kv_append_kv4",
-    "duo_attn_decode_kv4", "duo_kv_append_kv4_paged", "duo_attn_decode_kv4_paged",
+    "duo_attn_decode_kv4", "duo_kv_append_kv4_paged", "duo_attn_decode_kv4_paged", "duo_attn_prefill_kv4",
     "duo_kv_append_varlen", "duo_attn_decode_varlen", "duo_device_error", "duo_selftest_bounded_wait",
     "duo_last_error", "duo_status_string",
 )
@@ -104,6 +104,8 @@ def library() -> ctypes.CDLL:
                                         c_int32, c_void_p]),
         "duo_attn_decode_kv4": (c_int32, [c_void_p, POINTER(duo_kv_cache), POINTER(duo_kv4_cache), c_void_p,
                                           c_void_p, c_void_p, c_size_t, c_void_p]),
+        "duo_attn_prefill_kv4": (c_int32, [c_void_p, POINTER(duo_kv_cache), POINTER(duo_kv4_cache), c_void_p,
+                                           c_void_p, c_void_p, c_int32, c_void_p, c_void_p]),
         "duo_kv_append_kv4_paged": (c_int32, [c_void_p, POINTER(duo_kv_cache), POINTER(duo_paged),
                                               POINTER(duo_kv4_cache), c_void_p, c_void_p, c_int32, c_void_p]),
         "duo_attn_decode_kv4_paged": (c_int32, [c_void_p, POINTER(duo_kv_cache), POINTER(duo_paged),
@@ -251,6 +253,12 @@ def duo_attn_decode_kv4(handle, cache: "duo_kv_cache", kv4: "duo_kv4_cache", q, 
     nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(library().duo_attn_decode_kv4(handle, ctypes.byref(cache), ctypes.byref(kv4), _ptr(q), _ptr(o),
                                          _ptr(workspace), nbytes, _stream_ptr(stream)))
+
+
+def duo_attn_prefill_kv4(handle, cache: "duo_kv_cache", kv4: "duo_kv4_cache", q, k, v, T: int, o,
+                         stream=None) -> None:
+    _check(library().duo_attn_prefill_kv4(handle, ctypes.byref(cache), ctypes.byref(kv4), _ptr(q), _ptr(k), _ptr(v),
+                                          T, _ptr(o), _stream_ptr(stream)))
 
 
 def duo_kv_append_kv4_paged(handle, cache: "duo_kv_cache", paged: "duo_paged", kv4: "duo_kv4_cache", k_new, v_new,

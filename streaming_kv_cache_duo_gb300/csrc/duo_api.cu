@@ -389,7 +389,8 @@ duo_status duo_kv_append_paged(duo_handle* h, duo_kv_cache* c, const duo_paged* 
 }
 
 static duo_status prefill_impl(duo_handle* h, const duo_kv_cache* c, const duo_paged* pgd, const void* q,
-                               const void* k, const void* v, int32_t T, void* o, int32_t kind_mask, void* stream) {
+                               const void* k, const void* v, int32_t T, void* o, int32_t kind_mask, void* stream,
+                               const duo_kv4_cache* kv4 = nullptr) {
   duo_status st = check_handle(h);
   if (st != DUO_OK) return st;
   if (!c) return fail(DUO_ERR_INVALID_ARG, "cache is NULL");
@@ -397,7 +398,11 @@ static duo_status prefill_impl(duo_handle* h, const duo_kv_cache* c, const duo_p
   const bool use_cache = c->n > 0;
   PagedLayout pg;
   if ((st = check_paged(h, pgd, &pg)) != DUO_OK) return st;
-  if ((st = check_cache(h, c, use_cache, use_cache && !pg.stream_table)) != DUO_OK) return st;
+  if (kv4) {
+    if ((st = check_kv4(h, c, kv4)) != DUO_OK) return st;
+  } else if ((st = check_cache(h, c, use_cache, use_cache && !pg.stream_table)) != DUO_OK) {
+    return st;
+  }
   if (T < 1) return fail(DUO_ERR_INVALID_ARG, "T = %d < 1", T);
   if (!q || !k || !v || !o) return fail(DUO_ERR_INVALID_ARG, "q / k / v / o is NULL");
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o))
@@ -412,7 +417,20 @@ static duo_status prefill_impl(duo_handle* h, const duo_kv_cache* c, const duo_p
   if ((st = encode_tokens(h, &p.tm_v, v, sh.B, T, sh.Hkv, sh.D)) != DUO_OK) return st;
   const int64_t SR = (int64_t)sh.S + sh.R;
   const int nvalid = (int)(c->n < SR ? c->n : SR);
-  if (use_cache && (sh.n_ret > 0 || pg.stream_table)) {
+  if (kv4) {  // cache tiles are dequantized in the kernel; no tensor maps over the caches
+    if ((st = check_capacity(h, pg, c->n, DUO_ERR_INVALID_ARG)) != DUO_OK) return st;
+    p.k4 = static_cast<const uint8_t*>(kv4->k_codes);
+    p.v4 = static_cast<const uint8_t*>(kv4->v_codes);
+    p.ks4 = static_cast<const uint8_t*>(kv4->ks_codes);
+    p.vs4 = static_cast<const uint8_t*>(kv4->vs_codes);
+    p.ksz = static_cast<const uint32_t*>(kv4->k_sz);
+    p.vsz = static_cast<const uint32_t*>(kv4->v_sz);
+    p.kssz = static_cast<const uint32_t*>(kv4->ks_sz);
+    p.vssz = static_cast<const uint32_t*>(kv4->vs_sz);
+    p.cap16 = pitch16(sh.cap);
+    p.sr16 = (int)pitch16(SR);
+    p.kv4 = 1;
+  } else if (use_cache && (sh.n_ret > 0 || pg.stream_table)) {
     if ((st = check_capacity(h, pg, c->n, DUO_ERR_INVALID_ARG)) != DUO_OK) return st;
     if (!is_paged(pg)) {
       if ((st = encode_cache(h, &p.tm_kfull, c->k_full, (int64_t)sh.B * sh.n_ret, sh.cap, c->n, sh.D)) != DUO_OK)
@@ -431,7 +449,7 @@ static duo_status prefill_impl(duo_handle* h, const duo_kv_cache* c, const duo_p
     }
   }
   p.pg = pg;
-  if (use_cache && sh.n_str > 0 && !pg.stream_table) {
+  if (!kv4 && use_cache && sh.n_str > 0 && !pg.stream_table) {
     if ((st = encode_cache(h, &p.tm_ksr, c->k_sr, (int64_t)sh.B * sh.n_str, SR, nvalid, sh.D)) != DUO_OK) return st;
     if ((st = encode_cache(h, &p.tm_vsr, c->v_sr, (int64_t)sh.B * sh.n_str, SR, nvalid, sh.D)) != DUO_OK) return st;
   }
@@ -466,6 +484,12 @@ duo_status duo_attn_prefill(duo_handle* h, const duo_kv_cache* c, const void* q,
 duo_status duo_attn_prefill_select(duo_handle* h, const duo_kv_cache* c, const void* q, const void* k,
                                    const void* v, int32_t T, void* o, int32_t kind_mask, void* stream) {
   return prefill_impl(h, c, nullptr, q, k, v, T, o, kind_mask, stream);
+}
+
+duo_status duo_attn_prefill_kv4(duo_handle* h, const duo_kv_cache* c, const duo_kv4_cache* kv4, const void* q,
+                                const void* k, const void* v, int32_t T, void* o, void* stream) {
+  if (!kv4) return fail(DUO_ERR_INVALID_ARG, "kv4 is NULL");
+  return prefill_impl(h, c, nullptr, q, k, v, T, o, 3, stream, kv4);
 }
 
 duo_status duo_attn_prefill_paged(duo_handle* h, const duo_kv_cache* c, const duo_paged* paged, const void* q,

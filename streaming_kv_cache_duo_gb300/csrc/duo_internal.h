@@ -196,6 +196,19 @@ struct PrefillParams {
   CUtensorMap tm_qi;     // 4-D over q_inter [B, T, Hq, D]
   const float* mscale;   // fp32 [B, T] or nullptr (1)
   int chunk_len;         // 0: not DCA; else a multiple of 256
+  // 4-bit caches (kv4 != 0): the cache tiles are dequantized into the K/V tiles in shared
+  // memory instead of loaded by TMA; arrays laid out as in DecodeParams
+  const uint8_t* k4;
+  const uint8_t* v4;
+  const uint8_t* ks4;
+  const uint8_t* vs4;
+  const uint32_t* ksz;
+  const uint32_t* vsz;
+  const uint32_t* kssz;
+  const uint32_t* vssz;
+  int64_t cap16;
+  int sr16;
+  int kv4;
 };
 cudaError_t launch_prefill(const PrefillParams& p, cudaStream_t stream);
 

@@ -64,6 +64,8 @@ constexpr int kModePlain = 0;  // contiguous retrieval caches, ring caches for s
 constexpr int kModePaged = 1;  // retrieval caches in a paged pool (block table), ring caches
 constexpr int kModePool = 2;   // both head kinds in the paged pool
 constexpr int kModeDca = 3;    // Dual Chunk Attention: one of three query vectors per key tile
+constexpr int kModeKv4 = 4;    // 4-bit caches: cache tiles dequantized into shared memory by warps 10, 11
+constexpr int kWarpDeq = 10;   // first of the two dequantizing warps (4-bit caches)
 constexpr int kBox = 128 * 128;  // bytes of a 128-row x 64-column bf16 box
 
 __host__ __device__ constexpr uint32_t col_s(int x) { return (uint32_t)x * 256u; }
@@ -79,6 +81,11 @@ struct PCfg {
   static constexpr int OFF_V = OFF_K + kNS * KV_BYTES;
   static constexpr int OFF_BAR = OFF_V + kNS * KV_BYTES;
   static constexpr size_t SMEM = (size_t)OFF_BAR + 256 + 1024;  // + alignment slack
+  // 4-bit caches: the raw rows of one cache tile (K codes, V codes, K pairs, V pairs),
+  // staged by the producer and dequantized into a K/V stage by warps 10 and 11
+  static constexpr int RAW_CODES = BN * D / 2;
+  static constexpr int OFF_RAW = OFF_BAR + 256;
+  static constexpr size_t SMEM_KV4 = (size_t)OFF_RAW + 2 * RAW_CODES + 2 * BN * 4 + 1024;
 };
 
 struct Bars {
@@ -89,7 +96,10 @@ struct Bars {
   uint64_t drain;
   uint32_t tmem_base;
   uint64_t q_free;  // DCA: the MMAs reading the current query vectors have completed
+  uint64_t raw_full, raw_empty;  // 4-bit caches: the staged raw rows of a cache tile
+  uint64_t deq_sync;             // 4-bit caches: both dequantizing warps are done with a tile
 };
+static_assert(sizeof(Bars) <= 256, "barrier area");
 
 struct Item {
   bool streaming;
@@ -310,6 +320,53 @@ __device__ __forceinline__ void mask_chunk(float* v, const PrefillParams& p, con
     if (!((vis >> e) & 1u)) v[e] = -INFINITY;
 }
 
+// Row r of a staged 4-bit cache tile into a K or V tile of a stage, laid out as TMA
+// writes the bf16 rows (64-column boxes of 128 rows, 128-byte swizzle): value = code *
+// scale + zero in fp32, rounded to bf16; a row holding no token is written as zeros. K codes
+// are row-major; V codes are in 16-row groups in the decode's fragment order (the byte of
+// row k, dims 2 dp and 2 dp + 1, at 4 ((4 (dp / MT) + (k % 8) / 2) MT + dp % MT) + 2 (k % 2)
+// + k / 8 of its group, MT = D / 16), so the 4 bytes of dims 8c ... 8c + 7 of a row lie in
+// one 16-byte piece, one byte per word.
+template <int D, bool kV>
+__device__ __forceinline__ void dequant_row(uint8_t* tile, const uint8_t* codes, const uint32_t* sz, int r,
+                                            bool valid) {
+  constexpr int MT = D / 16;
+  float sc = 0.f, zr = 0.f;
+  if (valid) {
+    const uint32_t w = sz[r];
+    sc = __half2float(__ushort_as_half((unsigned short)(w & 0xFFFFu)));
+    zr = __half2float(__ushort_as_half((unsigned short)(w >> 16)));
+  }
+  const int k = r & 15;
+  const uint32_t sel = (uint32_t)(2 * (k & 1) + (k >> 3));  // byte of each word (V)
+  uint8_t* row = tile + r * 128;
+#pragma unroll
+  for (int c = 0; c < D / 8; ++c) {  // dims 8c ... 8c + 7: one 16-byte chunk of the row
+    uint32_t w = 0;  // byte i: codes of dims 8c + 2i (low nibble), 8c + 2i + 1
+    if (valid) {
+      if constexpr (kV) {
+        const int seg = 4 * ((4 * ((4 * c) / MT) + ((k & 7) >> 1)) * MT + (4 * c) % MT);
+        const uint4 q = *reinterpret_cast<const uint4*>(codes + (r & ~15) * (D / 2) + seg);
+        w = __byte_perm(__byte_perm(q.x, q.y, sel | ((4u + sel) << 4)), __byte_perm(q.z, q.w, sel | ((4u + sel) << 4)),
+                        0x5410);
+      } else {
+        w = *reinterpret_cast<const uint32_t*>(codes + r * (D / 2) + 4 * c);
+      }
+    }
+    const uint32_t wl = w & 0x0F0F0F0Fu, wh = (w >> 4) & 0x0F0F0F0Fu;
+    uint32_t out[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      // a code under the float exponent of 2^23 reads as 2^23 + code
+      const float lo = __uint_as_float(__byte_perm(wl, 0x4B000000u, 0x7540u | i)) - 8388608.f;
+      const float hi = __uint_as_float(__byte_perm(wh, 0x4B000000u, 0x7540u | i)) - 8388608.f;
+      out[i] = pack_bf16x2(fmaf(lo, sc, zr), fmaf(hi, sc, zr));
+    }
+    const int box = c >> 3, cc = c & 7;
+    *reinterpret_cast<uint4*>(row + box * kBox + ((cc ^ (r & 7)) << 4)) = make_uint4(out[0], out[1], out[2], out[3]);
+  }
+}
+
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
@@ -353,6 +410,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     }
     mbar_init(&bars->drain, 1);
     if (kMode == kModeDca) mbar_init(&bars->q_free, 1);
+    if (kMode == kModeKv4) {
+      mbar_init(&bars->raw_full, 1);
+      mbar_init(&bars->raw_empty, 1);
+      mbar_init(&bars->deq_sync, 64);
+    }
     fence_mbarrier_init();
   }
   if (warp == kWarpMma) {
@@ -401,6 +463,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             blk_next = __ldg(pw.row + (kMode == kModePool ? pw.block_index(tile_at<kMode>(pl, 0).k) : 0));
         }
         int j = 0;
+        int rc = 0;  // 4-bit caches: raw tiles staged so far
         for (; j < ntiles && ok; ++j) {
           const Tile t = tile_at<kMode>(pl, j);
           if (kMode == kModeDca) {
@@ -422,6 +485,32 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                               &bars->q_full);
               ++q_loads;
             }
+          }
+          if (kMode == kModeKv4 && t.phase == 0) {
+            // a cache tile of 4-bit rows: whole 16-row groups of codes and (scale, zero)
+            // pairs into the staging buffer (plane pitches are multiples of 16, so the copy
+            // stays in its plane); warps 10 and 11 dequantize them into stage j % kNS and
+            // complete its k_full / v_full themselves
+            if (!mbar_wait(&bars->raw_empty, (uint32_t)((rc & 1) ^ 1), err, kErrPrefillProducer)) {
+              ok = false;
+              break;
+            }
+            const int64_t r0 = (int64_t)t.k * BN;
+            const int64_t keys = it.streaming ? (int64_t)p.nvalid : p.n;
+            const int64_t left = (keys - r0 + 15) / 16 * 16;
+            const uint32_t rows16 = (uint32_t)(left < BN ? left : BN);
+            const int64_t row = (it.streaming ? ((int64_t)it.b * p.sh.n_str + it.cidx) * p.sr16
+                                              : ((int64_t)it.b * p.sh.n_ret + it.cidx) * p.cap16) + r0;
+            uint8_t* raw = smem + C::OFF_RAW;
+            mbar_arrive_expect_tx(&bars->raw_full, rows16 * (uint32_t)(D + 8));
+            bulk_g2s(raw, (it.streaming ? p.ks4 : p.k4) + row * (D / 2), rows16 * (D / 2), &bars->raw_full);
+            bulk_g2s(raw + C::RAW_CODES, (it.streaming ? p.vs4 : p.v4) + row * (D / 2), rows16 * (D / 2),
+                     &bars->raw_full);
+            bulk_g2s(raw + 2 * C::RAW_CODES, (it.streaming ? p.kssz : p.ksz) + row, rows16 * 4, &bars->raw_full);
+            bulk_g2s(raw + 2 * C::RAW_CODES + BN * 4, (it.streaming ? p.vssz : p.vsz) + row, rows16 * 4,
+                     &bars->raw_full);
+            ++rc;
+            continue;
           }
           // paged cache tile: pool block, first row within it, and the maps to read through
           int blk = 0, prow = 0;
@@ -488,9 +577,56 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
           // after an early exit, let the copies already issued land before the CTA ends
           mbar_wait(&bars->q_full, kMode == kModeDca ? (uint32_t)((q_loads - 1) & 1) : 0u, err, kErrPrefillProducer);
           for (int jj = (j > kNS ? j - kNS : 0); jj < j; ++jj) {
+            if (kMode == kModeKv4 && jj < pl.n_cache) continue;  // filled by the dequantizing warps
             mbar_wait(&bars->k_full[jj % kNS], (uint32_t)((jj / kNS) & 1), err, kErrPrefillProducer);
             mbar_wait(&bars->v_full[jj % kNS], (uint32_t)((jj / kNS) & 1), err, kErrPrefillProducer);
           }
+          if (kMode == kModeKv4 && rc > 0)  // the last staging copy
+            mbar_wait(&bars->raw_full, (uint32_t)((rc - 1) & 1), err, kErrPrefillProducer);
+        }
+      }
+    } else if (kMode == kModeKv4 && (warp == kWarpDeq || warp == kWarpDeq + 1)) {
+      // ------------------------------------------------------------ 4-bit dequantization
+      // The cache tiles come first in an item's tile list; each is staged raw by the
+      // producer, and these 64 threads write it into its K/V stage as TMA would have
+      // written the bf16 rows (two rows of K and two of V per thread), then complete the
+      // stage's k_full and v_full.
+      const int tid = threadIdx.x - kWarpDeq * 32;
+      const uint8_t* raw = smem + C::OFF_RAW;
+      const int64_t keys = it.streaming ? (int64_t)p.nvalid : p.n;
+      bool ok = true;
+      for (int j = 0; j < ntiles && j < pl.n_cache && ok; ++j) {
+        const Tile t = tile_at<kMode>(pl, j);
+        const int s = j % kNS;
+        const uint32_t ph = (uint32_t)((j / kNS) & 1);
+        const int64_t left = keys - (int64_t)t.k * BN;
+        const int rows = left < BN ? (int)left : BN;  // rows of the tile holding a token
+        if (!mbar_wait(&bars->raw_full, (uint32_t)(j & 1), err, kErrPrefillProducer) ||
+            !mbar_wait(&bars->k_empty[s], ph ^ 1u, err, kErrPrefillProducer)) {
+          ok = false;
+          break;
+        }
+        dequant_row<D, false>(sK + s * C::KV_BYTES, raw, reinterpret_cast<const uint32_t*>(raw + 2 * C::RAW_CODES), tid,
+                              tid < rows);
+        dequant_row<D, false>(sK + s * C::KV_BYTES, raw, reinterpret_cast<const uint32_t*>(raw + 2 * C::RAW_CODES),
+                              tid + 64, tid + 64 < rows);
+        if (!mbar_wait(&bars->v_empty[s], ph ^ 1u, err, kErrPrefillProducer)) {
+          ok = false;
+          break;
+        }
+        const uint32_t* vsz = reinterpret_cast<const uint32_t*>(raw + 2 * C::RAW_CODES + BN * 4);
+        dequant_row<D, true>(sV + s * C::KV_BYTES, raw + C::RAW_CODES, vsz, tid, tid < rows);
+        dequant_row<D, true>(sV + s * C::KV_BYTES, raw + C::RAW_CODES, vsz, tid + 64, tid + 64 < rows);
+        fence_proxy_async_shared();  // these generic-proxy writes are read by the tensor cores
+        mbar_arrive(&bars->deq_sync);
+        if (!mbar_wait(&bars->deq_sync, (uint32_t)(j & 1), err, kErrPrefillProducer)) {
+          ok = false;
+          break;
+        }
+        if (tid == 0) {
+          mbar_arrive(&bars->k_full[s]);
+          mbar_arrive(&bars->v_full[s]);
+          mbar_arrive(&bars->raw_empty);  // the staging buffer may take the next tile
         }
       }
     } else if (warp == kWarpMma) {
@@ -710,10 +846,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
 template <int D, int kMode>
 cudaError_t launch_t(const PrefillParams& p, cudaStream_t stream) {
   using C = PCfg<D>;
+  constexpr size_t smem = kMode == kModeKv4 ? C::SMEM_KV4 : C::SMEM;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e =
-        cudaFuncSetAttribute(prefill_kernel<D, kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
+        cudaFuncSetAttribute(prefill_kernel<D, kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
@@ -728,7 +865,7 @@ cudaError_t launch_t(const PrefillParams& p, cudaStream_t stream) {
   if (regs != kLaunchRegs) return cudaErrorInvalidConfiguration;
   const int grid = p.items_r + p.items_s;
   if (grid == 0) return cudaSuccess;
-  prefill_kernel<D, kMode><<<grid, kThreads, C::SMEM, stream>>>(p);
+  prefill_kernel<D, kMode><<<grid, kThreads, smem, stream>>>(p);
   return cudaGetLastError();
 }
 
@@ -742,6 +879,7 @@ cudaError_t launch_mode(const PrefillParams& p, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_prefill(const PrefillParams& p, cudaStream_t stream) {
+  if (p.kv4) return launch_mode<kModeKv4>(p, stream);
   if (p.chunk_len > 0) return launch_mode<kModeDca>(p, stream);
   if (p.pg.stream_table) return launch_mode<kModePool>(p, stream);
   return p.pg.table ? launch_mode<kModePaged>(p, stream) : launch_mode<kModePlain>(p, stream);
