@@ -81,11 +81,13 @@ struct PCfg {
   static constexpr int OFF_V = OFF_K + kNS * KV_BYTES;
   static constexpr int OFF_BAR = OFF_V + kNS * KV_BYTES;
   static constexpr size_t SMEM = (size_t)OFF_BAR + 256 + 1024;  // + alignment slack
-  // 4-bit caches: the raw rows of one cache tile (K codes, V codes, K pairs, V pairs),
-  // staged by the producer and dequantized into a K/V stage by warps 10 and 11
+  // 4-bit caches: the raw rows of one cache tile, K (codes, then pairs) and V (same) in
+  // separate buffers, staged by the producer and dequantized into a K/V stage by warps 10
+  // and 11: the copy of the next tile's K overlaps the dequantization of this tile's V
   static constexpr int RAW_CODES = BN * D / 2;
+  static constexpr int RAW_HALF = RAW_CODES + BN * 4;
   static constexpr int OFF_RAW = OFF_BAR + 256;
-  static constexpr size_t SMEM_KV4 = (size_t)OFF_RAW + 2 * RAW_CODES + 2 * BN * 4 + 1024;
+  static constexpr size_t SMEM_KV4 = (size_t)OFF_RAW + 2 * RAW_HALF + 1024;
 };
 
 struct Bars {
@@ -96,8 +98,8 @@ struct Bars {
   uint64_t drain;
   uint32_t tmem_base;
   uint64_t q_free;  // DCA: the MMAs reading the current query vectors have completed
-  uint64_t raw_full, raw_empty;  // 4-bit caches: the staged raw rows of a cache tile
-  uint64_t deq_sync;             // 4-bit caches: both dequantizing warps are done with a tile
+  uint64_t raw_full[2], raw_empty[2];  // 4-bit caches: the staged raw K (0) and V (1) rows of a cache tile
+  uint64_t deq_sync;                   // 4-bit caches: both dequantizing warps are done with K or V
 };
 static_assert(sizeof(Bars) <= 256, "barrier area");
 
@@ -357,10 +359,12 @@ __device__ __forceinline__ void dequant_row(uint8_t* tile, const uint8_t* codes,
     uint32_t out[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      // a code under the float exponent of 2^23 reads as 2^23 + code
-      const float lo = __uint_as_float(__byte_perm(wl, 0x4B000000u, 0x7540u | i)) - 8388608.f;
-      const float hi = __uint_as_float(__byte_perm(wh, 0x4B000000u, 0x7540u | i)) - 8388608.f;
-      out[i] = pack_bf16x2(fmaf(lo, sc, zr), fmaf(hi, sc, zr));
+      // a code under the float exponent of 2^23 reads as 2^23 + code; dims 8c + 2i, + 1 as a pair
+      float2 c2 = make_float2(__uint_as_float(__byte_perm(wl, 0x4B000000u, 0x7540u | i)),
+                              __uint_as_float(__byte_perm(wh, 0x4B000000u, 0x7540u | i)));
+      c2 = __fadd2_rn(c2, make_float2(-8388608.f, -8388608.f));
+      const float2 val = __ffma2_rn(c2, make_float2(sc, sc), make_float2(zr, zr));
+      out[i] = pack_bf16x2(val.x, val.y);
     }
     const int box = c >> 3, cc = c & 7;
     *reinterpret_cast<uint4*>(row + box * kBox + ((cc ^ (r & 7)) << 4)) = make_uint4(out[0], out[1], out[2], out[3]);
@@ -411,8 +415,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     mbar_init(&bars->drain, 1);
     if (kMode == kModeDca) mbar_init(&bars->q_free, 1);
     if (kMode == kModeKv4) {
-      mbar_init(&bars->raw_full, 1);
-      mbar_init(&bars->raw_empty, 1);
+      for (int h = 0; h < 2; ++h) {
+        mbar_init(&bars->raw_full[h], 1);
+        mbar_init(&bars->raw_empty[h], 1);
+      }
       mbar_init(&bars->deq_sync, 64);
     }
     fence_mbarrier_init();
@@ -491,24 +497,25 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             // pairs into the staging buffer (plane pitches are multiples of 16, so the copy
             // stays in its plane); warps 10 and 11 dequantize them into stage j % kNS and
             // complete its k_full / v_full themselves
-            if (!mbar_wait(&bars->raw_empty, (uint32_t)((rc & 1) ^ 1), err, kErrPrefillProducer)) {
-              ok = false;
-              break;
-            }
             const int64_t r0 = (int64_t)t.k * BN;
             const int64_t keys = it.streaming ? (int64_t)p.nvalid : p.n;
             const int64_t left = (keys - r0 + 15) / 16 * 16;
             const uint32_t rows16 = (uint32_t)(left < BN ? left : BN);
             const int64_t row = (it.streaming ? ((int64_t)it.b * p.sh.n_str + it.cidx) * p.sr16
                                               : ((int64_t)it.b * p.sh.n_ret + it.cidx) * p.cap16) + r0;
-            uint8_t* raw = smem + C::OFF_RAW;
-            mbar_arrive_expect_tx(&bars->raw_full, rows16 * (uint32_t)(D + 8));
-            bulk_g2s(raw, (it.streaming ? p.ks4 : p.k4) + row * (D / 2), rows16 * (D / 2), &bars->raw_full);
-            bulk_g2s(raw + C::RAW_CODES, (it.streaming ? p.vs4 : p.v4) + row * (D / 2), rows16 * (D / 2),
-                     &bars->raw_full);
-            bulk_g2s(raw + 2 * C::RAW_CODES, (it.streaming ? p.kssz : p.ksz) + row, rows16 * 4, &bars->raw_full);
-            bulk_g2s(raw + 2 * C::RAW_CODES + BN * 4, (it.streaming ? p.vssz : p.vsz) + row, rows16 * 4,
-                     &bars->raw_full);
+            for (int h = 0; h < 2 && ok; ++h) {  // K, then V
+              if (!mbar_wait(&bars->raw_empty[h], (uint32_t)((rc & 1) ^ 1), err, kErrPrefillProducer)) {
+                ok = false;
+                break;
+              }
+              uint8_t* raw = smem + C::OFF_RAW + h * C::RAW_HALF;
+              const uint8_t* codes = h == 0 ? (it.streaming ? p.ks4 : p.k4) : (it.streaming ? p.vs4 : p.v4);
+              const uint32_t* pairs = h == 0 ? (it.streaming ? p.kssz : p.ksz) : (it.streaming ? p.vssz : p.vsz);
+              mbar_arrive_expect_tx(&bars->raw_full[h], rows16 * (uint32_t)(D / 2 + 4));
+              bulk_g2s(raw, codes + row * (D / 2), rows16 * (D / 2), &bars->raw_full[h]);
+              bulk_g2s(raw + C::RAW_CODES, pairs + row, rows16 * 4, &bars->raw_full[h]);
+            }
+            if (!ok) break;
             ++rc;
             continue;
           }
@@ -581,8 +588,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             mbar_wait(&bars->k_full[jj % kNS], (uint32_t)((jj / kNS) & 1), err, kErrPrefillProducer);
             mbar_wait(&bars->v_full[jj % kNS], (uint32_t)((jj / kNS) & 1), err, kErrPrefillProducer);
           }
-          if (kMode == kModeKv4 && rc > 0)  // the last staging copy
-            mbar_wait(&bars->raw_full, (uint32_t)((rc - 1) & 1), err, kErrPrefillProducer);
+          if (kMode == kModeKv4 && rc > 0)  // the last staging copies
+            for (int h = 0; h < 2; ++h) mbar_wait(&bars->raw_full[h], (uint32_t)((rc - 1) & 1), err, kErrPrefillProducer);
         }
       }
     } else if (kMode == kModeKv4 && (warp == kWarpDeq || warp == kWarpDeq + 1)) {
@@ -592,7 +599,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       // written the bf16 rows (two rows of K and two of V per thread), then complete the
       // stage's k_full and v_full.
       const int tid = threadIdx.x - kWarpDeq * 32;
-      const uint8_t* raw = smem + C::OFF_RAW;
       const int64_t keys = it.streaming ? (int64_t)p.nvalid : p.n;
       bool ok = true;
       for (int j = 0; j < ntiles && j < pl.n_cache && ok; ++j) {
@@ -601,32 +607,32 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         const uint32_t ph = (uint32_t)((j / kNS) & 1);
         const int64_t left = keys - (int64_t)t.k * BN;
         const int rows = left < BN ? (int)left : BN;  // rows of the tile holding a token
-        if (!mbar_wait(&bars->raw_full, (uint32_t)(j & 1), err, kErrPrefillProducer) ||
-            !mbar_wait(&bars->k_empty[s], ph ^ 1u, err, kErrPrefillProducer)) {
-          ok = false;
-          break;
-        }
-        dequant_row<D, false>(sK + s * C::KV_BYTES, raw, reinterpret_cast<const uint32_t*>(raw + 2 * C::RAW_CODES), tid,
-                              tid < rows);
-        dequant_row<D, false>(sK + s * C::KV_BYTES, raw, reinterpret_cast<const uint32_t*>(raw + 2 * C::RAW_CODES),
-                              tid + 64, tid + 64 < rows);
-        if (!mbar_wait(&bars->v_empty[s], ph ^ 1u, err, kErrPrefillProducer)) {
-          ok = false;
-          break;
-        }
-        const uint32_t* vsz = reinterpret_cast<const uint32_t*>(raw + 2 * C::RAW_CODES + BN * 4);
-        dequant_row<D, true>(sV + s * C::KV_BYTES, raw + C::RAW_CODES, vsz, tid, tid < rows);
-        dequant_row<D, true>(sV + s * C::KV_BYTES, raw + C::RAW_CODES, vsz, tid + 64, tid + 64 < rows);
-        fence_proxy_async_shared();  // these generic-proxy writes are read by the tensor cores
-        mbar_arrive(&bars->deq_sync);
-        if (!mbar_wait(&bars->deq_sync, (uint32_t)(j & 1), err, kErrPrefillProducer)) {
-          ok = false;
-          break;
-        }
-        if (tid == 0) {
-          mbar_arrive(&bars->k_full[s]);
-          mbar_arrive(&bars->v_full[s]);
-          mbar_arrive(&bars->raw_empty);  // the staging buffer may take the next tile
+        for (int h = 0; h < 2 && ok; ++h) {  // K into sK[s], then V into sV[s]
+          const uint8_t* raw = smem + C::OFF_RAW + h * C::RAW_HALF;
+          const uint32_t* pairs = reinterpret_cast<const uint32_t*>(raw + C::RAW_CODES);
+          if (!mbar_wait(&bars->raw_full[h], (uint32_t)(j & 1), err, kErrPrefillProducer) ||
+              !mbar_wait(h == 0 ? &bars->k_empty[s] : &bars->v_empty[s], ph ^ 1u, err, kErrPrefillProducer)) {
+            ok = false;
+            break;
+          }
+          uint8_t* tile = (h == 0 ? sK : sV) + s * C::KV_BYTES;
+          if (h == 0) {
+            dequant_row<D, false>(tile, raw, pairs, tid, tid < rows);
+            dequant_row<D, false>(tile, raw, pairs, tid + 64, tid + 64 < rows);
+          } else {
+            dequant_row<D, true>(tile, raw, pairs, tid, tid < rows);
+            dequant_row<D, true>(tile, raw, pairs, tid + 64, tid + 64 < rows);
+          }
+          fence_proxy_async_shared();  // these generic-proxy writes are read by the tensor cores
+          mbar_arrive(&bars->deq_sync);
+          if (!mbar_wait(&bars->deq_sync, (uint32_t)(h & 1), err, kErrPrefillProducer)) {  // two phases a tile
+            ok = false;
+            break;
+          }
+          if (tid == 0) {
+            mbar_arrive(h == 0 ? &bars->k_full[s] : &bars->v_full[s]);
+            mbar_arrive(&bars->raw_empty[h]);  // the staging buffer may take the next tile's rows
+          }
         }
       }
     } else if (warp == kWarpMma) {
