@@ -48,15 +48,15 @@ constexpr int kRows = BM * kQT;
 constexpr int kNS = 2;  // K/V pipeline stages
 constexpr int kWarpTma = 8;
 constexpr int kWarpMma = 9;
-constexpr int kThreads = 384;  // warpgroups: softmax 0, softmax 1, (TMA, MMA, 2 idle)
-// Register split: the block is launched with kLaunchRegs per thread (384 x 168 =
-// 64512); the third warpgroup drops to kRegsCtl, the softmax warpgroups rise to
-// kRegsSoftmax: 2 x 128 x 200 + 128 x 104 = 64512, exactly the launch total. The
-// host refuses to launch unless the compiled kernel uses kLaunchRegs.
-constexpr int kLaunchRegs = 168;
-constexpr int kRegsSoftmax = 200;
-constexpr int kRegsCtl = 104;
-static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsCtl <= kThreads * kLaunchRegs, "register split");
+// Threads and register split of an instance. Warpgroups: softmax 0, softmax 1, (TMA, MMA,
+// 2 idle) -- the 4-bit instance uses the two idle warps and a fourth warpgroup to
+// dequantize its cache tiles (6 warps). The block is launched with kLaunchRegs per
+// thread; the warpgroups after the softmax ones drop to kRegsCtl, the softmax
+// warpgroups rise to kRegsSoftmax: 2 x 128 x 200 + 128 x 104 = 384 x 168 = 64512, and for
+// the 4-bit instance 2 x 128 x 184 + 2 x 128 x 72 = 512 x 128 = 65536, exactly the launch
+// totals. The host refuses to launch unless the compiled kernel uses kLaunchRegs.
+template <int kMode>
+struct Roles;
 constexpr uint32_t kTmemCols = 512;
 // Kernel variants, compiled separately so that the paged paths leave the register
 // allocation of the kernels that do not use them untouched.
@@ -65,7 +65,17 @@ constexpr int kModePaged = 1;  // retrieval caches in a paged pool (block table)
 constexpr int kModePool = 2;   // both head kinds in the paged pool
 constexpr int kModeDca = 3;    // Dual Chunk Attention: one of three query vectors per key tile
 constexpr int kModeKv4 = 4;    // 4-bit caches: cache tiles dequantized into shared memory by warps 10, 11
-constexpr int kWarpDeq = 10;   // first of the two dequantizing warps (4-bit caches)
+constexpr int kWarpDeq = 10;   // first of the dequantizing warps (4-bit caches): 10 ... 15
+template <int kMode>
+struct Roles {
+  static constexpr bool kKv4 = kMode == kModeKv4;
+  static constexpr int kThreads = kKv4 ? 512 : 384;
+  static constexpr int kLaunchRegs = kKv4 ? 128 : 168;
+  static constexpr int kRegsSoftmax = kKv4 ? 184 : 200;
+  static constexpr int kRegsCtl = kKv4 ? 72 : 104;
+  static constexpr int kDeqThreads = kThreads - kWarpDeq * 32;  // 4-bit instance: 192
+  static_assert(2 * 128 * kRegsSoftmax + (kThreads - 256) * kRegsCtl <= kThreads * kLaunchRegs, "register split");
+};
 constexpr int kBox = 128 * 128;  // bytes of a 128-row x 64-column bf16 box
 
 __host__ __device__ constexpr uint32_t col_s(int x) { return (uint32_t)x * 256u; }
@@ -381,7 +391,7 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
 }
 
 template <int D, int kMode>
-__global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ PrefillParams p) {
+__global__ void __launch_bounds__(Roles<kMode>::kThreads, 1) prefill_kernel(const __grid_constant__ PrefillParams p) {
   using C = PCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -419,7 +429,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         mbar_init(&bars->raw_full[h], 1);
         mbar_init(&bars->raw_empty[h], 1);
       }
-      mbar_init(&bars->deq_sync, 64);
+      mbar_init(&bars->deq_sync, Roles<kMode>::kDeqThreads);
     }
     fence_mbarrier_init();
   }
@@ -433,7 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   const uint32_t tmem = bars->tmem_base;
   if (warp >= 8) {
     // ================================================ warpgroup 2: TMA, MMA, idle
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsCtl));
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(Roles<kMode>::kRegsCtl));
     if (warp == kWarpTma) {
       // ------------------------------------------------------------ TMA producer
       if (lane == 0) {
@@ -592,12 +602,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             for (int h = 0; h < 2; ++h) mbar_wait(&bars->raw_full[h], (uint32_t)((rc - 1) & 1), err, kErrPrefillProducer);
         }
       }
-    } else if (kMode == kModeKv4 && (warp == kWarpDeq || warp == kWarpDeq + 1)) {
+    } else if (kMode == kModeKv4 && warp >= kWarpDeq) {
       // ------------------------------------------------------------ 4-bit dequantization
       // The cache tiles come first in an item's tile list; each is staged raw by the
-      // producer, and these 64 threads write it into its K/V stage as TMA would have
-      // written the bf16 rows (two rows of K and two of V per thread), then complete the
-      // stage's k_full and v_full.
+      // producer, and these 192 threads write it into its K/V stage as TMA would have
+      // written the bf16 rows (one row of K, then one of V, for each of the first 128),
+      // then complete the stage's k_full and v_full.
       const int tid = threadIdx.x - kWarpDeq * 32;
       const int64_t keys = it.streaming ? (int64_t)p.nvalid : p.n;
       bool ok = true;
@@ -616,12 +626,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             break;
           }
           uint8_t* tile = (h == 0 ? sK : sV) + s * C::KV_BYTES;
-          if (h == 0) {
-            dequant_row<D, false>(tile, raw, pairs, tid, tid < rows);
-            dequant_row<D, false>(tile, raw, pairs, tid + 64, tid + 64 < rows);
-          } else {
-            dequant_row<D, true>(tile, raw, pairs, tid, tid < rows);
-            dequant_row<D, true>(tile, raw, pairs, tid + 64, tid + 64 < rows);
+          if (tid < BN) {
+            if (h == 0)
+              dequant_row<D, false>(tile, raw, pairs, tid, tid < rows);
+            else
+              dequant_row<D, true>(tile, raw, pairs, tid, tid < rows);
           }
           fence_proxy_async_shared();  // these generic-proxy writes are read by the tensor cores
           mbar_arrive(&bars->deq_sync);
@@ -735,7 +744,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     }
   } else {
     // ================================================ warpgroups 0, 1: softmax
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(Roles<kMode>::kRegsSoftmax));
     const int x = warp >> 2;                     // query tile of this warpgroup
     const int r = (warp & 3) * 32 + lane;        // row within the tile == TMEM lane
     const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
@@ -868,10 +877,10 @@ cudaError_t launch_t(const PrefillParams& p, cudaStream_t stream) {
     regs = fa.numRegs;
   }
   // the setmaxnreg split is sized for exactly this launch allocation
-  if (regs != kLaunchRegs) return cudaErrorInvalidConfiguration;
+  if (regs != Roles<kMode>::kLaunchRegs) return cudaErrorInvalidConfiguration;
   const int grid = p.items_r + p.items_s;
   if (grid == 0) return cudaSuccess;
-  prefill_kernel<D, kMode><<<grid, kThreads, smem, stream>>>(p);
+  prefill_kernel<D, kMode><<<grid, Roles<kMode>::kThreads, smem, stream>>>(p);
   return cudaGetLastError();
 }
 
