@@ -170,7 +170,8 @@ __device__ __forceinline__ int warp_rows(int64_t keys, int64_t lt, int w) {
 }
 
 // The work of CTA c, in order: its share [t0, t1) of the retrieval tiles (cut into
-// segments at unit boundaries), then streaming units c, c + C, c + 2C, ... whole.
+// segments at unit boundaries), then streaming units c', c' + C, c' + 2C, ... whole,
+// c' = (c - s_first) mod C (short caches deal them to the CTAs after the retrieval ones).
 // Dealing the short streaming units round-robin keeps their fixed per-segment
 // cost (q load, merges) from piling up on the last CTAs.
 struct SegState {
@@ -189,7 +190,7 @@ __device__ __forceinline__ bool next_segment(const DecodeParams& p, int c, int64
     st.rt = te;
     return true;
   }
-  const int64_t sidx = c + (int64_t)st.k * p.C;
+  const int64_t sidx = (c >= p.s_first ? c - p.s_first : c + p.C - p.s_first) + (int64_t)st.k * p.C;
   if (streaming_too && sidx < p.U_s) {
     u = p.U_r + (int)sidx;
     lt0 = 0;

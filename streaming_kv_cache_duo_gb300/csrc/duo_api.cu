@@ -523,7 +523,19 @@ static void decode_plan(const duo_handle* h, int64_t n, DecodeParams* p, int cta
   const int64_t cmax = (int64_t)h->num_sms * ctas_per_sm;
   p->C = (int)(work < cmax ? work : cmax);
   p->Cr = (int)(p->W < p->C ? p->W : p->C);
+  p->s_first = 0;
+  if (p->tiles_r <= kDecodeShortTiles && (int64_t)p->U_r + p->U_s <= cmax) {
+    // short caches: one CTA per unit, the streaming units on the CTAs after the retrieval
+    // ones, so no unit is split and no partial is merged across CTAs (the merge's atomics,
+    // fences and reloads cost more than the few tiles a CTA then walks in sequence)
+    p->C = p->U_r + p->U_s;
+    p->Cr = p->U_r;
+    p->s_first = p->U_r;
+  }
 }
+
+// Every unit lies in one CTA (no arrival counter is used by the launch).
+static bool decode_unsplit(const DecodeParams& p) { return p.W == 0 || p.Cr == p.U_r; }
 
 size_t duo_decode_workspace_size(const duo_handle* h, int64_t n) {
   if (!h) return 0;
@@ -588,8 +600,10 @@ static duo_status decode_impl(duo_handle* h, const duo_kv_cache* c, const duo_pa
   // The arrival counters must start at zero. The kernel leaves them at zero, but the
   // caller may have lent the workspace's memory to other data since the last call (a
   // caching allocator does), so every call clears them: U x 4 bytes, on the stream.
-  cudaError_t me = cudaMemsetAsync(workspace, 0, counter_bytes, (cudaStream_t)stream);
-  if (me != cudaSuccess) return cuda_fail(me, "cudaMemsetAsync(workspace counters)");
+  if (!decode_unsplit(p)) {
+    cudaError_t me = cudaMemsetAsync(workspace, 0, counter_bytes, (cudaStream_t)stream);
+    if (me != cudaSuccess) return cuda_fail(me, "cudaMemsetAsync(workspace counters)");
+  }
   p.q = static_cast<const uint16_t*>(q);
   p.o = static_cast<uint16_t*>(o);
   p.k_full = static_cast<const uint16_t*>(c->k_full);
@@ -793,8 +807,10 @@ duo_status duo_attn_decode_varlen(duo_handle* h, const duo_kv_cache* c, const in
   // The arrival counters must start at zero. The kernel leaves them at zero, but the
   // caller may have lent the workspace's memory to other data since the last call (a
   // caching allocator does), so every call clears them: U x 4 bytes, on the stream.
-  cudaError_t me = cudaMemsetAsync(workspace, 0, counter_bytes, (cudaStream_t)stream);
-  if (me != cudaSuccess) return cuda_fail(me, "cudaMemsetAsync(workspace counters)");
+  if (!decode_unsplit(p)) {
+    cudaError_t me = cudaMemsetAsync(workspace, 0, counter_bytes, (cudaStream_t)stream);
+    if (me != cudaSuccess) return cuda_fail(me, "cudaMemsetAsync(workspace counters)");
+  }
   p.seq_lens = seq_lens;
   p.q = static_cast<const uint16_t*>(q);
   p.o = static_cast<uint16_t*>(o);

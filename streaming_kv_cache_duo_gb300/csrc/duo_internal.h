@@ -106,6 +106,7 @@ cudaError_t append_read_clear_error(uint32_t* code);
 
 // ------------------------------------------------------------------ decode
 constexpr int kDecodeTK = 128;  // keys per decode tile
+constexpr int kDecodeShortTiles = 4;  // caches of at most this many tiles: one CTA per unit
 // CTAs per SM of the 4-bit decode (its rings are small enough for two; more warps hide
 // the latency of its per-slice dependency chains); the bf16 decode runs one
 constexpr int kDecodeCtasPerSmKv4 = 2;
@@ -131,6 +132,7 @@ struct DecodeParams {
                    // every CTA c streaming units c, c + C, ...
   int Cr;          // CTAs sharing the retrieval tiles: min(C, W), so none of them gets an
                    // empty share inside a unit's span (its partial would never arrive)
+  int s_first;     // streaming units are dealt round-robin starting at this CTA
   float scale_log2;    // log2(e) / sqrt(D)
   uint32_t* counters;  // [U_r + U_s] arrival tickets, left at zero
   float* partials;     // [C + U_r + U_s][g][D + 4] (o, max, sum, 2 pad) per segment
