@@ -24,17 +24,22 @@ CASES = [
     (1, 16, 2, 128, 64, 256, [0, 1], [512, 700, 333]),        # GQA 8, window spans chunks
     (1, 32, 32, 128, 64, 256, [1] * 8 + [0] * 24, [1024, 1024, 1024]),  # MHA, 8 retrieval heads
     (1, 4, 4, 128, 70, 90, [0, 1, 0, 1], [50, 40, 300]),      # sinks spread over chunks
+    (1, 8, 2, 128, 16, 200, [0, 0], [333, 444]),              # streaming heads only
+    (2, 4, 4, 64, 0, 1, [1, 1, 1, 1], [128, 129, 255]),       # retrieval heads only, D 64
 ]
 
 
+@pytest.mark.parametrize("qscale", [1, 16], ids=["plain", "q16"])
 @pytest.mark.parametrize("case", CASES, ids=[f"case{i}" for i in range(len(CASES))])
-def test_prefill_against_kv4_cache_matches_oracle(case):
+def test_prefill_against_kv4_cache_matches_oracle(case, qscale):
+    """qscale 16: queries times 16 (exact in bf16), so rows take the kernel's lazy rescale of
+    the running output after their first tile, here with dequantized cache tiles."""
     from streaming_kv_cache_duo_gb300 import DuoKv4Layer, duo_device_error
     B, Hq, Hkv, D, S, R, kinds, chunks = case
     total = sum(chunks) + 1
     seed = 1700 + total % 89
     layer = DuoKv4Layer(B, Hq, Hkv, D, S, R, total, kinds)
-    q = device_stream(seed, ds.STREAM_Q, B, 0, total, Hq, D, "cuda")
+    q = device_stream(seed, ds.STREAM_Q, B, 0, total, Hq, D, "cuda") * qscale
     k = device_stream(seed, ds.STREAM_K, B, 0, total, Hkv, D, "cuda")
     v = device_stream(seed, ds.STREAM_V, B, 0, total, Hkv, D, "cuda")
     outs, t = [], 0
@@ -49,7 +54,7 @@ def test_prefill_against_kv4_cache_matches_oracle(case):
     torch.cuda.synchronize()
     assert duo_device_error() == 0
 
-    Qh = host_stream(seed, ds.STREAM_Q, B, 0, total, Hq, D)
+    Qh = host_stream(seed, ds.STREAM_Q, B, 0, total, Hq, D) * qscale
     Kh = host_stream(seed, ds.STREAM_K, B, 0, total, Hkv, D)
     Vh = host_stream(seed, ds.STREAM_V, B, 0, total, Hkv, D)
     Kq, Vq = kv4.roundtrip(Kh.astype(np.float32)), kv4.roundtrip(Vh.astype(np.float32))
