@@ -42,17 +42,18 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from the ncu
-# captures summarised in profiles/, valid only for the kernel sources they were taken on
-# (the prefill figure was re-keyed after edits to duo_internal.h that touched only the
-# decode and append declarations, not the prefill kernel or its parameters).
+# captures summarised in profiles/, valid only for the kernel sources they were taken on.
 L2_BYTES = 129e6  # GB300 L2 capacity
 
 MEASURED_TRAFFIC = {
-    "prefill": {"src": ("prefill.cu", "duo_device.cuh", "duo_internal.h"), "sha1": "974607b4bf1f590a",
-                "bytes": 471.654e6 + 233.480e6},
+    "prefill": {"src": ("prefill.cu", "duo_device.cuh", "duo_internal.h"), "sha1": "f22a1019c1883353",
+                "bytes": 471.968e6 + 233.300e6},
     # the 8 prefill launches of one chunked-prefill step (Llama-2-7B shape, 8 x 4096 tokens)
-    "prefill_chunked": {"src": ("prefill.cu", "duo_device.cuh", "duo_internal.h"), "sha1": "974607b4bf1f590a",
-                        "bytes": 1305.247e6 + 97.195e6},
+    "prefill_chunked": {"src": ("prefill.cu", "duo_device.cuh", "duo_internal.h"), "sha1": "f22a1019c1883353",
+                        "bytes": 1305.029e6 + 97.706e6},
+    # the same against 4-bit caches (codes + pairs read and dequantized in the kernel)
+    "prefill_chunked_kv4": {"src": ("prefill.cu", "duo_device.cuh", "duo_internal.h"), "sha1": "f22a1019c1883353",
+                            "bytes": 941.062e6 + 85.440e6},
     # one decode launch of the batched 8 x 128K workload (device lengths, graph replay)
     "decode_batched": {"src": ("decode.cu", "duo_device.cuh", "duo_internal.h"), "sha1": "5a13e0b2fd97bf44",
                        "bytes": 1.081999e9 + 1.599e6},
@@ -604,8 +605,8 @@ def bench_chunked(w, steps, warmup, peaks, paged_block=0, pool=False, kv4=False)
     ms = t0.elapsed_time(t1) / steps
     pre_ms = sum(a.elapsed_time(b) for a, b in pre) / steps
     layer.close()
-    # traffic of one step's prefill launches, from the ncu capture of the unpaged layout
-    traffic = measured_traffic("prefill_chunked") if not (paged_block or kv4) else None
+    # traffic of one step's prefill launches, from the ncu capture of the contiguous layouts
+    traffic = None if paged_block else measured_traffic("prefill_chunked_kv4" if kv4 else "prefill_chunked")
     return {"value": flops / (ms * 1e-3) / 1e12, "ms_per_step": ms, "flops": flops, "retrieval_flops": fr,
             "prefill_ms": pre_ms, "append_ms": ms - pre_ms, "launches": 2 * len(chunks) * steps, "clocks": clk,
             "roofline": {"bound": "tensor", "achieved": round(flops / (pre_ms * 1e-3) / 1e12, 2),
