@@ -159,10 +159,12 @@ size_t duo_decode_workspace_size(const duo_handle* handle, int64_t n);
  * KV head for all its query heads. The keys are split over the GPU's SMs; partial
  * softmaxes (o, max, sum) go to `workspace` and are merged by log-sum-exp.
  * workspace: device memory of at least duo_decode_workspace_size(handle, n) bytes,
- * 256-byte aligned. Its first bytes are per-(sequence, KV head) arrival counters,
- * which every call that splits a (sequence, KV head) over several CTAs clears on `stream`
- * before its kernel (one cudaMemsetAsync of ceil(B Hkv 4 / 256) 256 bytes; short caches are
- * planned one CTA per unit and use none), so the memory may hold anything between calls.
+ * 256-byte aligned. Its first bytes are 4-byte arrival counters, one per (sequence, KV
+ * head) and one per partial slot (grid size + B Hkv; a long unit's partials are merged
+ * in groups, then the group results), which every call that splits a (sequence, KV head)
+ * over several CTAs clears on `stream` before its kernel (one cudaMemsetAsync of
+ * ceil((2 B Hkv + grid) 4 / 256) 256 bytes; short caches are planned one CTA per unit and
+ * use none), so the memory may hold anything between calls.
  * Calls sharing one workspace must be ordered on the GPU (same stream). */
 duo_status duo_attn_decode(duo_handle* handle, const duo_kv_cache* cache, const void* q, void* o, void* workspace,
                            size_t workspace_bytes, void* stream);

@@ -94,7 +94,7 @@ struct Cfg {
   static constexpr int RING = kWarps * NSW * WSTAGE;
   static constexpr int RED = kWarps * G * (D + 2);
   static constexpr int PS = D + 4;  // floats per head of a partial in the workspace (16-byte multiple)
-  // after the reduction buffer: NSW mbarriers per warp, the segment barrier, flag, maxima
+  // after the reduction buffer: NSW mbarriers per warp, the segment barrier, flag
   static constexpr size_t SMEM = (size_t)RING + (size_t)RED * 4 + (KV4 ? kWarps * NSW * 8 + 256 : 512);
   static_assert(IT >= 1 && kKPW % KPI == 0, "tile split");
   static_assert(G <= LPK, "every head needs a lane of each key group");
@@ -274,12 +274,12 @@ struct Cursor {
   }
 };
 
-// Copies this warp's slice of the cursor's tile into a stage. Returns true when the
-// slice lies in a paged block whose id is out of range: then nothing is copied, the
-// error is recorded and the consumer skips the slice's rows.
+// Copies this warp's slice of the cursor's tile into a stage, under the L2 policy pol.
+// Returns true when the slice lies in a paged block whose id is out of range: then
+// nothing is copied, the error is recorded and the consumer skips the slice's rows.
 template <int D, int G, int kMode>
 __device__ __forceinline__ bool issue_slice(const DecodeParams& p, Cursor<kMode>& cur, int w,
-                                            uint8_t* stage, uint64_t* bar) {
+                                            uint8_t* stage, uint64_t* bar, uint64_t pol) {
   using C = Cfg<D, G, is_kv4_mode(kMode)>;
   if constexpr (is_kv4_mode(kMode)) {
     // whole 16-row chunks of codes and (scale, zero) pairs: the planes' row pitches are
@@ -318,10 +318,10 @@ __device__ __forceinline__ bool issue_slice(const DecodeParams& p, Cursor<kMode>
     const uint32_t* kz = (cur.x.streaming ? p.kssz : p.ksz) + r;
     const uint32_t* vz = (cur.x.streaming ? p.vssz : p.vsz) + r;
     mbar_arrive_expect_tx(bar, 2 * C::SLICE + 2 * C::PSLICE);
-    bulk_g2s(stage, kc, C::SLICE, bar);
-    bulk_g2s(stage + C::SLICE, vc, C::SLICE, bar);
-    bulk_g2s(stage + 2 * C::SLICE, kz, C::PSLICE, bar);
-    bulk_g2s(stage + 2 * C::SLICE + C::PSLICE, vz, C::PSLICE, bar);
+    bulk_g2s_hint(stage, kc, C::SLICE, bar, pol);
+    bulk_g2s_hint(stage + C::SLICE, vc, C::SLICE, bar, pol);
+    bulk_g2s_hint(stage + 2 * C::SLICE, kz, C::PSLICE, bar, pol);
+    bulk_g2s_hint(stage + 2 * C::SLICE + C::PSLICE, vz, C::PSLICE, bar, pol);
     return false;
   }
   const bool pool = is_paged_mode(kMode) && cur.in_pool();
@@ -346,8 +346,8 @@ __device__ __forceinline__ bool issue_slice(const DecodeParams& p, Cursor<kMode>
   const uint32_t bytes = (uint32_t)rows * C::ROW;
   mbar_arrive_expect_tx(bar, 2 * bytes);
   if (rows > 0) {
-    bulk_g2s(stage, kp, bytes, bar);
-    bulk_g2s(stage + C::SLICE, vp, bytes, bar);
+    bulk_g2s_hint(stage, kp, bytes, bar, pol);
+    bulk_g2s_hint(stage + C::SLICE, vp, bytes, bar, pol);
   }
   return bad;
 }
@@ -742,6 +742,9 @@ __global__ void __launch_bounds__(kThreads, is_kv4_mode(kMode) ? kDecodeCtasPerS
   }
   __syncthreads();
 
+  // The cache rows are read once: L2 lets them go first, keeping q, the partials and
+  // the counters the merges read.
+  const uint64_t pol = l2_policy_evict_first();
   // refill cursor (warp-uniform); the prologue issues the first C::NSW - 1 slices
   constexpr bool kPaged = is_paged_mode(kMode);
   constexpr bool kBadBlocks = kPaged || kMode == kModeKv4Paged;  // a slice may come from a bad block id
@@ -751,7 +754,7 @@ __global__ void __launch_bounds__(kThreads, is_kv4_mode(kMode) ? kDecodeCtasPerS
   uint32_t badmask = 0;  // lane 0: bit s set when stage s holds a skipped (bad-block) slice
   for (int s = 0; s < C::NSW - 1 && cur.live; ++s) {
     if (lane == 0) {
-      const bool bad = issue_slice<D, G, kMode>(p, cur, warp, ring + s * C::WSTAGE, &wfull[s]);
+      const bool bad = issue_slice<D, G, kMode>(p, cur, warp, ring + s * C::WSTAGE, &wfull[s], pol);
       if (kBadBlocks) badmask = bad ? (badmask | (1u << s)) : (badmask & ~(1u << s));
     }
     cur.advance(p, c, t1, live);
@@ -840,7 +843,7 @@ __global__ void __launch_bounds__(kThreads, is_kv4_mode(kMode) ? kDecodeCtasPerS
       if (cur.live) {
         const int sn = (int)((j + C::NSW - 1) % C::NSW);
         if (lane == 0) {
-          const bool bad = issue_slice<D, G, kMode>(p, cur, warp, ring + sn * C::WSTAGE, &wfull[sn]);
+          const bool bad = issue_slice<D, G, kMode>(p, cur, warp, ring + sn * C::WSTAGE, &wfull[sn], pol);
           if (kBadBlocks) badmask = bad ? (badmask | (1u << sn)) : (badmask & ~(1u << sn));
         }
         cur.advance(p, c, t1, live);
@@ -1053,88 +1056,156 @@ __global__ void __launch_bounds__(kThreads, is_kv4_mode(kMode) ? kDecodeCtasPerS
         ok = false;
         break;
       }
-      if (tid == 0) {
-        const unsigned int old = atomicAdd(p.counters + u, 1u);
-        const int last = (old == (unsigned int)(n_parts - 1));
-        if (last) p.counters[u] = 0u;  // leave the counter at zero for the next call
-        *flag = last;
-      }
-      if (!ws.sync(err)) {
-        ok = false;
-        break;
-      }
-      if (*flag) {
-        // Last CTA of the unit: merge its n_parts partials. Warps 0 .. g-1 find
-        // each head's max; then warp w takes partials w, w + 8, ..., each lane
-        // 16 (or more) consecutive outputs of one head with 128-bit loads, so the
-        // loads of all partials are in flight together; a shared-memory sum over
-        // the warps finishes it.
+      // The unit's partials are merged in two levels when there are more than a merge
+      // group's worth: the last CTA to arrive in each group of GS consecutive CTAs merges
+      // the group's partials into the group's first slot, and the last group to finish
+      // merges the group results. Each merge reads one batch of partials per warp, so the
+      // unit's end waits for two short merges instead of one long one.
+      constexpr int EPL = G * D / 32;  // outputs per lane (2 ... 32), all of one head
+      static_assert(EPL % 2 == 0 && D % EPL == 0, "merge split");
+      // partials in flight per warp: their loads take up to 64 registers (32 under the
+      // 4-bit kernels' 128-register budget)
+      constexpr int kLoadRegs = is_kv4_mode(kMode) ? 32 : 64;
+      constexpr int NB = kLoadRegs / EPL < 1 ? 1 : (kLoadRegs / EPL > 8 ? 8 : kLoadRegs / EPL);
+      constexpr int VW = EPL % 4 == 0 ? 4 : 2;  // floats per load
+      constexpr int GS = NB * kWarps;  // CTAs per merge group
+      const int n_groups = (n_parts + GS - 1) / GS;
+      const int g0 = c_first + (c - c_first) / GS * GS;  // first CTA of this CTA's group
+      const int g_n = min(GS, c_first + n_parts - g0);
+      // ticket on one arrival counter: true for the CTA that brings it to n (which
+      // leaves it at zero for the next call)
+      auto ticket = [&](uint32_t* counter, int n) -> bool {
+        if (tid == 0) {
+          const unsigned int old = atomicAdd(counter, 1u);
+          const int last = (old == (unsigned int)(n - 1));
+          if (last) *counter = 0u;
+          *flag = last;
+        }
+        return ws.sync(err);
+      };
+      // Merges the n partials in slots s0, s0 + stride, ...: warp w takes partials w,
+      // w + 8, ..., NB at a time with all their loads in flight; each lane holds EPL
+      // consecutive outputs of one head and a running maximum, rescaling when a batch
+      // raises it; the warps' (max, sum, outputs) are combined through shared memory
+      // into the unit's output (to_out) or back into slot s0 as a partial.
+      auto merge_slots = [&](int s0, int stride, int n, bool to_out) -> bool {
         __threadfence();
-        float* Mh = reinterpret_cast<float*>(flag + 4);  // [G]
-        if (warp < G) {
-          float mm = -INFINITY;
-          for (int cc = c_first + lane; cc < c_first + n_parts; cc += 32)
-            mm = fmaxf(mm, __ldcg(p.partials + ((int64_t)(cc + u) * G + warp) * C::PS + D));
-#pragma unroll
-          for (int off = 16; off > 0; off >>= 1) mm = fmaxf(mm, __shfl_xor_sync(0xffffffffu, mm, off));
-          if (lane == 0) Mh[warp] = mm;
-        }
-        if (!ws.sync(err)) {
-          ok = false;
-          break;
-        }
-        constexpr int EPL = G * D / 32;  // outputs per lane (2 ... 32), all of one head
-        static_assert(EPL % 2 == 0 && D % EPL == 0, "merge split");
         const int e0 = lane * EPL;
         const int hl = e0 / D;
         const int d0 = e0 % D;
-        const float Mhl = Mh[hl];
         float acc[EPL];
 #pragma unroll
         for (int k = 0; k < EPL; ++k) acc[k] = 0.f;
-        float den = 0.f;
-        for (int cc = c_first + warp; cc < c_first + n_parts; cc += kWarps) {
-          const float* r = p.partials + ((int64_t)(cc + u) * G + hl) * C::PS;
-          const float mm = __ldcg(r + D);
-          const float f = mm == -INFINITY ? 0.f : ex2_approx(mm - Mhl);
-          den = fmaf(f, __ldcg(r + D + 1), den);
-          if constexpr (EPL % 4 == 0) {
+        float den = 0.f, mrun = -INFINITY;
+        for (int ib = warp; ib < n; ib += NB * kWarps) {
+          float mb[NB], db[NB], ob[NB][EPL];
 #pragma unroll
-            for (int k = 0; k < EPL; k += 4) {
-              const float4 o4 = __ldcg(reinterpret_cast<const float4*>(r + d0 + k));
-              acc[k] = fmaf(f, o4.x, acc[k]);
-              acc[k + 1] = fmaf(f, o4.y, acc[k + 1]);
-              acc[k + 2] = fmaf(f, o4.z, acc[k + 2]);
-              acc[k + 3] = fmaf(f, o4.w, acc[k + 3]);
-            }
-          } else {
+          for (int i = 0; i < NB; ++i) {
+            const int ii = ib + i * kWarps;
+            if (ii < n) {
+              const float* r = p.partials + ((int64_t)(s0 + ii * stride) * G + hl) * C::PS;
+              mb[i] = __ldcg(r + D);
+              db[i] = __ldcg(r + D + 1);
 #pragma unroll
-            for (int k = 0; k < EPL; k += 2) {
-              const float2 o2v = __ldcg(reinterpret_cast<const float2*>(r + d0 + k));
-              acc[k] = fmaf(f, o2v.x, acc[k]);
-              acc[k + 1] = fmaf(f, o2v.y, acc[k + 1]);
+              for (int k = 0; k < EPL; k += VW) {
+                if constexpr (VW == 4) {
+                  const float4 o4 = __ldcg(reinterpret_cast<const float4*>(r + d0 + k));
+                  ob[i][k] = o4.x;
+                  ob[i][k + 1] = o4.y;
+                  ob[i][k + 2] = o4.z;
+                  ob[i][k + 3] = o4.w;
+                } else {
+                  const float2 o2v = __ldcg(reinterpret_cast<const float2*>(r + d0 + k));
+                  ob[i][k] = o2v.x;
+                  ob[i][k + 1] = o2v.y;
+                }
+              }
+            } else {
+              mb[i] = -INFINITY;
+              db[i] = 0.f;
+#pragma unroll
+              for (int k = 0; k < EPL; ++k) ob[i][k] = 0.f;
             }
           }
+          float mnew = mrun;
+#pragma unroll
+          for (int i = 0; i < NB; ++i) mnew = fmaxf(mnew, mb[i]);
+          if (mnew == -INFINITY) continue;  // no visible key in any partial so far
+          const float fo = mrun == -INFINITY ? 0.f : ex2_approx(mrun - mnew);
+          den *= fo;
+#pragma unroll
+          for (int k = 0; k < EPL; ++k) acc[k] *= fo;
+#pragma unroll
+          for (int i = 0; i < NB; ++i) {
+            const float f = mb[i] == -INFINITY ? 0.f : ex2_approx(mb[i] - mnew);
+            den = fmaf(f, db[i], den);
+#pragma unroll
+            for (int k = 0; k < EPL; ++k) acc[k] = fmaf(f, ob[i][k], acc[k]);
+          }
+          mrun = mnew;
         }
         float* rw = red + (warp * G + hl) * (D + 2);
 #pragma unroll
         for (int k = 0; k < EPL; ++k) rw[d0 + k] = acc[k];
-        if (d0 == 0) rw[D + 1] = den;
-        if (!ws.sync(err)) {
-          ok = false;
-          break;
+        if (d0 == 0) {
+          rw[D] = mrun;
+          rw[D + 1] = den;
         }
+        if (!ws.sync(err)) return false;
+        float* dst = p.partials + (int64_t)s0 * G * C::PS;
         for (int e = tid; e < G * D; e += kThreads) {
           const int h = e / D;
           const int d = e % D;
+          float M = -INFINITY;
+#pragma unroll
+          for (int w = 0; w < kWarps; ++w) M = fmaxf(M, red[(w * G + h) * (D + 2) + D]);
           float num = 0.f, dsum = 0.f;
 #pragma unroll
           for (int w = 0; w < kWarps; ++w) {
-            num += red[(w * G + h) * (D + 2) + d];
-            dsum += red[(w * G + h) * (D + 2) + D + 1];
+            const float* r = red + (w * G + h) * (D + 2);
+            const float f = r[D] == -INFINITY ? 0.f : ex2_approx(r[D] - M);
+            num = fmaf(f, r[d], num);
+            dsum = fmaf(f, r[D + 1], dsum);
           }
-          p.o[((int64_t)x.b * p.sh.Hq + (int64_t)x.kvh * G + h) * D + d] =
-              __bfloat16_as_ushort(__float2bfloat16_rn(dsum > 0.f ? num / dsum : 0.f));
+          if (to_out) {
+            p.o[((int64_t)x.b * p.sh.Hq + (int64_t)x.kvh * G + h) * D + d] =
+                __bfloat16_as_ushort(__float2bfloat16_rn(dsum > 0.f ? num / dsum : 0.f));
+          } else {
+            dst[h * C::PS + d] = num;
+            if (d == 0) {
+              dst[h * C::PS + D] = M;
+              dst[h * C::PS + D + 1] = dsum;
+            }
+          }
+        }
+        if (to_out) return true;
+        __threadfence();  // the group result before the group's ticket
+        return ws.sync(err);
+      };
+      uint32_t* group_counters = p.counters + (p.U_r + p.U_s);  // [C + U], by slot
+      if (n_groups == 1) {
+        if (!ticket(p.counters + u, n_parts)) {
+          ok = false;
+          break;
+        }
+        if (*flag && !merge_slots(c_first + u, 1, n_parts, true)) {
+          ok = false;
+          break;
+        }
+      } else {
+        if (!ticket(group_counters + g0 + u, g_n)) {
+          ok = false;
+          break;
+        }
+        if (*flag) {
+          if (!merge_slots(g0 + u, 1, g_n, false) || !ticket(p.counters + u, n_groups)) {
+            ok = false;
+            break;
+          }
+          if (*flag && !merge_slots(c_first + u, GS, n_groups, true)) {
+            ok = false;
+            break;
+          }
         }
       }
     }
@@ -1178,9 +1249,14 @@ cudaError_t launch_t(const DecodeParams& p, cudaStream_t stream) {
 
 }  // namespace
 
+size_t decode_counter_bytes(const Shape& sh, int num_ctas) {
+  const int64_t U = (int64_t)sh.B * sh.Hkv;
+  return ((size_t)(2 * U + num_ctas) * 4 + 255) / 256 * 256;  // per unit, then per slot
+}
+
 size_t decode_workspace_bytes(const Shape& sh, int num_ctas) {
   const int64_t U = (int64_t)sh.B * sh.Hkv;
-  const size_t counters = ((size_t)U * 4 + 255) / 256 * 256;
+  const size_t counters = decode_counter_bytes(sh, num_ctas);
   const size_t parts = (size_t)(num_ctas + U) * sh.g * (sh.D + 4) * 4;  // Cfg::PS floats per head
   return counters + parts;
 }

@@ -595,11 +595,10 @@ static duo_status decode_impl(duo_handle* h, const duo_kv_cache* c, const duo_pa
   const Shape& sh = h->sh;
   DecodeParams p;
   decode_plan(h, c->n, &p, ctas_per_sm);
-  const int64_t U = (int64_t)sh.B * sh.Hkv;
-  const size_t counter_bytes = ((size_t)U * 4 + 255) / 256 * 256;
+  const size_t counter_bytes = decode_counter_bytes(sh, h->num_sms * ctas_per_sm);
   // The arrival counters must start at zero. The kernel leaves them at zero, but the
   // caller may have lent the workspace's memory to other data since the last call (a
-  // caching allocator does), so every call clears them: U x 4 bytes, on the stream.
+  // caching allocator does), so every call clears them (a few KB), on the stream.
   if (!decode_unsplit(p)) {
     cudaError_t me = cudaMemsetAsync(workspace, 0, counter_bytes, (cudaStream_t)stream);
     if (me != cudaSuccess) return cuda_fail(me, "cudaMemsetAsync(workspace counters)");
@@ -802,11 +801,10 @@ duo_status duo_attn_decode_varlen(duo_handle* h, const duo_kv_cache* c, const in
   const Shape& sh = h->sh;
   DecodeParams p;
   decode_plan(h, max_len, &p);
-  const int64_t U = (int64_t)sh.B * sh.Hkv;
-  const size_t counter_bytes = ((size_t)U * 4 + 255) / 256 * 256;
+  const size_t counter_bytes = decode_counter_bytes(sh, h->num_sms);
   // The arrival counters must start at zero. The kernel leaves them at zero, but the
   // caller may have lent the workspace's memory to other data since the last call (a
-  // caching allocator does), so every call clears them: U x 4 bytes, on the stream.
+  // caching allocator does), so every call clears them (a few KB), on the stream.
   if (!decode_unsplit(p)) {
     cudaError_t me = cudaMemsetAsync(workspace, 0, counter_bytes, (cudaStream_t)stream);
     if (me != cudaSuccess) return cuda_fail(me, "cudaMemsetAsync(workspace counters)");
@@ -937,8 +935,7 @@ extern "C" duo_status duo_attn_decode_static(duo_handle* h, const duo_kv_cache* 
   const Shape& sh = h->sh;
   DecodeParams p;
   decode_plan(h, c->n, &p);
-  const int64_t U = (int64_t)sh.B * sh.Hkv;
-  const size_t counter_bytes = ((size_t)U * 4 + 255) / 256 * 256;
+  const size_t counter_bytes = decode_counter_bytes(sh, h->num_sms);
   // The counters must start at zero; the array keeps whatever the last call left.
   cudaError_t e = cudaMemsetAsync(scratch, 0, counter_bytes, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(static decode scratch counters)");
