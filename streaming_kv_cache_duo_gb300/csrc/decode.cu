@@ -84,12 +84,15 @@ struct Cfg {
   static constexpr int KPI = 32 / LPK;                 // keys per warp iteration
   static constexpr int IT = kKPW / KPI;                // iterations per tile
   static constexpr int CH = DPL / 8;                   // 16-byte chunks per lane
-  // 4-bit rows are a quarter of the bytes: a ring as deep as the bf16 one in bytes
-  // would be 12 stages, but two CTAs share an SM, so each warp keeps 4
-  static constexpr int NSW = KV4 ? 4 : kNSW;           // pipeline stages per warp
+  // 4-bit caches: tiles of 256 keys, 32 per warp (two 16-key tensor-core groups per
+  // slice, so the per-slice costs -- copies, waits, cursor, softmax bookkeeping -- are
+  // paid once per 32 keys); two CTAs share an SM, so each warp keeps 2 stages
+  static constexpr int KPW = KV4 ? kDecodeTKKv4 / kWarps : kKPW;  // keys of a tile per warp
+  static constexpr int TK = KPW * kWarps;              // keys per tile
+  static constexpr int NSW = KV4 ? 2 : kNSW;           // pipeline stages per warp
   static constexpr int ROW = KV4 ? D / 2 : D * 2;      // bytes per key row (codes or bf16)
-  static constexpr int SLICE = kKPW * ROW;             // one warp's K (or V) rows of a tile
-  static constexpr int PSLICE = KV4 ? kKPW * 4 : 0;    // their (scale, zero) pairs
+  static constexpr int SLICE = KPW * ROW;              // one warp's K (or V) rows of a tile
+  static constexpr int PSLICE = KV4 ? KPW * 4 : 0;     // their (scale, zero) pairs
   static constexpr int WSTAGE = 2 * SLICE + 2 * PSLICE;  // K, V (then K, V pairs)
   static constexpr int RING = kWarps * NSW * WSTAGE;
   static constexpr int RED = kWarps * G * (D + 2);
@@ -163,10 +166,11 @@ __device__ __forceinline__ Unit unit_info(const DecodeParams& p, int u) {
   return x;
 }
 
-// Rows of local tile `lt` of a unit with `keys` keys that belong to warp w.
+// Rows of local tile `lt` (KPW keys per warp) of a unit with `keys` keys that belong to warp w.
+template <int KPW = kKPW>
 __device__ __forceinline__ int warp_rows(int64_t keys, int64_t lt, int w) {
-  const int64_t r = keys - lt * kTK - (int64_t)w * kKPW;
-  return r <= 0 ? 0 : (r >= kKPW ? kKPW : (int)r);
+  const int64_t r = keys - lt * (KPW * kWarps) - (int64_t)w * KPW;
+  return r <= 0 ? 0 : (r >= KPW ? KPW : (int)r);
 }
 
 // The work of CTA c, in order: its share [t0, t1) of the retrieval tiles (cut into
@@ -282,19 +286,20 @@ __device__ __forceinline__ bool issue_slice(const DecodeParams& p, Cursor<kMode>
                                             uint8_t* stage, uint64_t* bar, uint64_t pol) {
   using C = Cfg<D, G, is_kv4_mode(kMode)>;
   if constexpr (is_kv4_mode(kMode)) {
-    // whole 16-row chunks of codes and (scale, zero) pairs: the planes' row pitches are
-    // multiples of 16, so the chunk stays inside its plane; rows past the keys are
-    // copied but never used
-    const int rows = warp_rows(cur.x.keys, cur.lt, w);
+    // the slice's rows rounded up to whole 16-row groups of codes and (scale, zero)
+    // pairs: the planes' row pitches are multiples of 16, so the groups stay inside
+    // their plane; rows past the keys are copied but never used
+    const int rows = warp_rows<C::KPW>(cur.x.keys, cur.lt, w);
     if (rows <= 0) {
       mbar_arrive_expect_tx(bar, 0);
       return false;
     }
-    int64_t r = cur.x.plane * (cur.x.streaming ? (int64_t)p.sr16 : p.cap16) + cur.lt * kTK + (int64_t)w * kKPW;
+    const uint32_t r16 = (uint32_t)(rows + 15) & ~15u;
+    int64_t r = cur.x.plane * (cur.x.streaming ? (int64_t)p.sr16 : p.cap16) + cur.lt * C::TK + (int64_t)w * C::KPW;
     if (kMode == kModeKv4Paged && !cur.x.streaming) {
-      // the slice's 16 rows lie in one block (block sizes are multiples of 128)
+      // the slice's 32 rows lie in one block (block sizes are multiples of 128)
       // rows stay below block_size x max_blocks < 2^31 (checked on the host)
-      const int row = (int)(cur.lt * kTK) + w * kKPW;
+      const int row = (int)(cur.lt * C::TK) + w * C::KPW;
       const int bi = (int)((uint32_t)row / (uint32_t)p.pg.block_size);
       const int plane = (int)cur.x.plane;
       if (plane != cur.kv4_plane || bi != cur.kv4_bi) {
@@ -317,11 +322,11 @@ __device__ __forceinline__ bool issue_slice(const DecodeParams& p, Cursor<kMode>
     const uint8_t* vc = (cur.x.streaming ? p.vs4 : p.v4) + r * (D / 2);
     const uint32_t* kz = (cur.x.streaming ? p.kssz : p.ksz) + r;
     const uint32_t* vz = (cur.x.streaming ? p.vssz : p.vsz) + r;
-    mbar_arrive_expect_tx(bar, 2 * C::SLICE + 2 * C::PSLICE);
-    bulk_g2s_hint(stage, kc, C::SLICE, bar, pol);
-    bulk_g2s_hint(stage + C::SLICE, vc, C::SLICE, bar, pol);
-    bulk_g2s_hint(stage + 2 * C::SLICE, kz, C::PSLICE, bar, pol);
-    bulk_g2s_hint(stage + 2 * C::SLICE + C::PSLICE, vz, C::PSLICE, bar, pol);
+    mbar_arrive_expect_tx(bar, r16 * (2 * C::ROW + 8));
+    bulk_g2s_hint(stage, kc, r16 * C::ROW, bar, pol);
+    bulk_g2s_hint(stage + C::SLICE, vc, r16 * C::ROW, bar, pol);
+    bulk_g2s_hint(stage + 2 * C::SLICE, kz, r16 * 4, bar, pol);
+    bulk_g2s_hint(stage + 2 * C::SLICE + C::PSLICE, vz, r16 * 4, bar, pol);
     return false;
   }
   const bool pool = is_paged_mode(kMode) && cur.in_pool();
@@ -512,13 +517,61 @@ struct MmaSlice {
     }
   }
 
-  // One 16-key slice. kFull: every key of the slice is a stored, visible key (an interior
-  // tile of a retrieval unit), so no key needs masking; the rows gid >= G then hold
-  // finite values for heads that do not exist, whose columns of O^T are never written out.
+  // One slice: 16 keys (bf16) or 32 keys (4-bit caches, two 16-key groups). kFull:
+  // every key of the slice is a stored, visible key (an interior tile of a retrieval
+  // unit), so no key needs masking; the rows gid >= G then hold finite values for heads
+  // that do not exist, whose columns of O^T are never written out.
+  static constexpr int NGRP = KV4 ? 2 : 1;  // 16-key groups per slice
+  static constexpr int NX = 4 * NGRP;       // scores per lane
   template <bool kFull>
   __device__ __forceinline__ void slice(const SliceIn& in, int gid, int tig) {
-    float x[4];  // scores of keys 2 tig, 2 tig + 1, 2 tig + 8, 2 tig + 9
-    {
+    // x[4 q + k]: scores of keys 16 q + 2 tig, + 1, + 8, + 9 (q = the 16-key group)
+    float x[NX];
+    if constexpr (KV4) {
+      float sc[2 * NGRP][4];  // [n-tile][fragment]: the n-tiles are independent chains
+#pragma unroll
+      for (int j = 0; j < 2 * NGRP; ++j)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) sc[j][k] = 0.f;
+      constexpr int WPT = D / 32;  // code words of a lane per K row
+#pragma unroll
+      for (int j = 0; j < 2 * NGRP; ++j) {
+        // lane tig: words WPT tig ... of row gid + 8 j
+        uint32_t w[WPT];
+        const uint8_t* row = in.k + (gid + 8 * j) * ROW;
+        if constexpr (WPT == 4) {
+          const uint4 v = *reinterpret_cast<const uint4*>(row + tig * 16);
+          w[0] = v.x;
+          w[1] = v.y;
+          w[2] = v.z;
+          w[3] = v.w;
+        } else {
+          const uint2 v = *reinterpret_cast<const uint2*>(row + tig * 8);
+          w[0] = v.x;
+          w[1] = v.y;
+        }
+#pragma unroll
+        for (int u = 0; u < WPT; ++u) {
+          const uint32_t xw = w[u], x8 = xw >> 8;
+          mma16816<true>(sc[j], qa[2 * u][0], 0u, qa[2 * u][1], 0u, and_or(xw, 0x000F000Fu, kLoMagic),
+                         and_or(xw, 0x00F000F0u, kHiMagic));
+          mma16816<true>(sc[j], qa[2 * u + 1][0], 0u, qa[2 * u + 1][1], 0u, and_or(x8, 0x000F000Fu, kLoMagic),
+                         and_or(x8, 0x00F000F0u, kHiMagic));
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < NGRP; ++q) {
+        const uint2 z01 = *reinterpret_cast<const uint2*>(in.kz + 64 * q + tig * 8);
+        const uint2 z89 = *reinterpret_cast<const uint2*>(in.kz + 64 * q + 32 + tig * 8);
+        const uint32_t zz[4] = {z01.x, z01.y, z89.x, z89.y};
+        const float raw[4] = {sc[2 * q][0], sc[2 * q][1], sc[2 * q + 1][0], sc[2 * q + 1][1]};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float2 sz = scale_zero(zz[k]);
+          x[4 * q + k] = fmaf(sz.x, raw[k] - off, sz.y * qsum);
+        }
+      }
+    } else {
       float sc[2][2][4];  // [n-tile][chain][fragment]: two independent accumulation chains
 #pragma unroll
       for (int j = 0; j < 2; ++j)
@@ -529,51 +582,21 @@ struct MmaSlice {
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
         const uint8_t* row = in.k + (gid + 8 * j) * ROW;
-        if constexpr (KV4) {
-          constexpr int WPT = D / 32;  // code words of a lane per K row
-          uint32_t w[WPT];
-          if constexpr (WPT == 4) {
-            const uint4 v = *reinterpret_cast<const uint4*>(row + tig * 16);
-            w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
-          } else {
-            const uint2 v = *reinterpret_cast<const uint2*>(row + tig * 8);
-            w[0] = v.x; w[1] = v.y;
-          }
 #pragma unroll
-          for (int u = 0; u < WPT; ++u) {
-            const uint32_t xw = w[u], x8 = w[u] >> 8;
-            mma16816<true>(sc[j][u & 1], qa[2 * u][0], 0u, qa[2 * u][1], 0u, and_or(xw, 0x000F000Fu, kLoMagic),
-                           and_or(xw, 0x00F000F0u, kHiMagic));
-            mma16816<true>(sc[j][u & 1], qa[2 * u + 1][0], 0u, qa[2 * u + 1][1], 0u,
-                           and_or(x8, 0x000F000Fu, kLoMagic), and_or(x8, 0x00F000F0u, kHiMagic));
-          }
-        } else {
-#pragma unroll
-          for (int u = 0; u < D / 32; ++u) {
-            const uint4 v = *reinterpret_cast<const uint4*>(row + (tig + 4 * u) * 16);
-            mma16816<false>(sc[j][u & 1], qa[2 * u][0], 0u, qa[2 * u][1], 0u, v.x, v.y);
-            mma16816<false>(sc[j][u & 1], qa[2 * u + 1][0], 0u, qa[2 * u + 1][1], 0u, v.z, v.w);
-          }
+        for (int u = 0; u < D / 32; ++u) {
+          const uint4 v = *reinterpret_cast<const uint4*>(row + (tig + 4 * u) * 16);
+          mma16816<false>(sc[j][u & 1], qa[2 * u][0], 0u, qa[2 * u][1], 0u, v.x, v.y);
+          mma16816<false>(sc[j][u & 1], qa[2 * u + 1][0], 0u, qa[2 * u + 1][1], 0u, v.z, v.w);
         }
       }
       x[0] = sc[0][0][0] + sc[0][1][0];
       x[1] = sc[0][0][1] + sc[0][1][1];
       x[2] = sc[1][0][0] + sc[1][1][0];
       x[3] = sc[1][0][1] + sc[1][1][1];
-      if constexpr (KV4) {
-        const uint2 z01 = *reinterpret_cast<const uint2*>(in.kz + tig * 8);
-        const uint2 z89 = *reinterpret_cast<const uint2*>(in.kz + 32 + tig * 8);
-        const uint32_t zz[4] = {z01.x, z01.y, z89.x, z89.y};
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const float2 sz = scale_zero(zz[k]);
-          x[k] = fmaf(sz.x, x[k] - off, sz.y * qsum);
-        }
-      }
     }
     float mx = -INFINITY;
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
+    for (int k = 0; k < NX; ++k) {
       x[k] = (kFull || ((in.hvalid >> k) & 1u)) ? x[k] * qfac : -INFINITY;
       mx = fmaxf(mx, x[k]);
     }
@@ -597,35 +620,35 @@ struct MmaSlice {
         o[i][3] *= f1;
       }
     }
-    const int kr[4] = {2 * tig, 2 * tig + 1, 2 * tig + 8, 2 * tig + 9};
-    {
-      float pr[4];
+    float pr[NX];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        pr[k] = (kFull || ((in.hvalid >> k) & 1u)) ? ex2_approx(x[k] - m_run) : 0.f;
-        l_part += pr[k];
-      }
-      uint32_t pb0, pb1;
-      if constexpr (KV4) {
-        const uint2 z01 = *reinterpret_cast<const uint2*>(in.vz + tig * 8);
-        const uint2 z89 = *reinterpret_cast<const uint2*>(in.vz + 32 + tig * 8);
+    for (int k = 0; k < NX; ++k) {
+      pr[k] = (kFull || ((in.hvalid >> k) & 1u)) ? ex2_approx(x[k] - m_run) : 0.f;
+      l_part += pr[k];
+    }
+    if constexpr (KV4) {
+#pragma unroll
+      for (int q = 0; q < NGRP; ++q) {
+        const uint2 z01 = *reinterpret_cast<const uint2*>(in.vz + 64 * q + tig * 8);
+        const uint2 z89 = *reinterpret_cast<const uint2*>(in.vz + 64 * q + 32 + tig * 8);
         const uint32_t zz[4] = {z01.x, z01.y, z89.x, z89.y};
         float b[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const float2 sz = scale_zero(zz[k]);
-          const bool ok = kFull || ((in.hvalid >> k) & 1u);  // the pair of an unused row may be anything
-          b[k] = ok ? pr[k] * (sz.x * (1.f / kOScale)) : 0.f;
-          z_part += ok ? pr[k] * sz.y : 0.f;
+          const bool ok = kFull || ((in.hvalid >> (4 * q + k)) & 1u);  // an unused row's pair may be anything
+          b[k] = ok ? pr[4 * q + k] * (sz.x * (1.f / kOScale)) : 0.f;
+          z_part += ok ? pr[4 * q + k] * sz.y : 0.f;
         }
-        pb0 = pack_half2(b[0], b[1]);
-        pb1 = pack_half2(b[2], b[3]);
-        // V codes in fragment order (see the 4-bit append): the lane's word i holds, for
-        // its dims of m-tile i, the codes of keys 2 tig, 2 tig + 8, 2 tig + 1, 2 tig + 9
+        const uint32_t pb0 = pack_half2(b[0], b[1]);
+        const uint32_t pb1 = pack_half2(b[2], b[3]);
+        // V codes in fragment order (see the 4-bit append): in group q, the lane's word i
+        // holds, for its dims of m-tile i, the codes of keys 2 tig, 2 tig + 8, 2 tig + 1,
+        // 2 tig + 9
         uint32_t w[MT];
 #pragma unroll
         for (int c = 0; c < MT / 4; ++c) {
-          const uint4 v = *reinterpret_cast<const uint4*>(in.v + (4 * gid + tig) * MT * 4 + 16 * c);
+          const uint4 v = *reinterpret_cast<const uint4*>(in.v + 16 * ROW * q + (4 * gid + tig) * MT * 4 + 16 * c);
           w[4 * c] = v.x;
           w[4 * c + 1] = v.y;
           w[4 * c + 2] = v.z;
@@ -639,27 +662,28 @@ struct MmaSlice {
                          hsub2(and_or(x8, 0x000F000Fu, kLoMagic), kLoMagic),
                          hsub2(and_or(x8, 0x00F000F0u, kHiMagic), kHiMagic), pb0, pb1);
         }
-      } else {
-        pb0 = pack_bf16x2(pr[0], pr[1]);
-        pb1 = pack_bf16x2(pr[2], pr[3]);
-        uint32_t w[4][MT];  // MT words = this lane's DT dims of each key
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const bool ok = kFull || ((in.kvalid >> k) & 1u);  // rows not copied in this stage may hold anything
-#pragma unroll
-          for (int c = 0; c < MT / 4; ++c) {
-            const uint4 v = *reinterpret_cast<const uint4*>(in.v + kr[k] * ROW + DT * 2 * gid + c * 16);
-            w[k][4 * c] = ok ? v.x : 0u;
-            w[k][4 * c + 1] = ok ? v.y : 0u;
-            w[k][4 * c + 2] = ok ? v.z : 0u;
-            w[k][4 * c + 3] = ok ? v.w : 0u;
-          }
-        }
-#pragma unroll
-        for (int i = 0; i < MT; ++i)
-          mma16816<false>(o[i], __byte_perm(w[0][i], w[1][i], 0x5410), __byte_perm(w[0][i], w[1][i], 0x7632),
-                          __byte_perm(w[2][i], w[3][i], 0x5410), __byte_perm(w[2][i], w[3][i], 0x7632), pb0, pb1);
       }
+    } else {
+      const int kr[4] = {2 * tig, 2 * tig + 1, 2 * tig + 8, 2 * tig + 9};
+      const uint32_t pb0 = pack_bf16x2(pr[0], pr[1]);
+      const uint32_t pb1 = pack_bf16x2(pr[2], pr[3]);
+      uint32_t w[4][MT];  // MT words = this lane's DT dims of each key
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const bool ok = kFull || ((in.kvalid >> k) & 1u);  // rows not copied in this stage may hold anything
+#pragma unroll
+        for (int c = 0; c < MT / 4; ++c) {
+          const uint4 v = *reinterpret_cast<const uint4*>(in.v + kr[k] * ROW + DT * 2 * gid + c * 16);
+          w[k][4 * c] = ok ? v.x : 0u;
+          w[k][4 * c + 1] = ok ? v.y : 0u;
+          w[k][4 * c + 2] = ok ? v.z : 0u;
+          w[k][4 * c + 3] = ok ? v.w : 0u;
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < MT; ++i)
+        mma16816<false>(o[i], __byte_perm(w[0][i], w[1][i], 0x5410), __byte_perm(w[0][i], w[1][i], 0x7632),
+                        __byte_perm(w[2][i], w[3][i], 0x5410), __byte_perm(w[2][i], w[3][i], 0x7632), pb0, pb1);
     }
   }
 
@@ -856,22 +880,24 @@ __global__ void __launch_bounds__(kThreads, is_kv4_mode(kMode) ? kDecodeCtasPerS
       // streaming unit in the pool: keys are rows (= positions) of row tile kt
       const bool str_pool = kMode == kModePool && x.streaming;
       const int64_t kt = str_pool ? stream_tile(p, lt) : lt;
-      int rows = warp_rows(x.keys, kt, warp);
+      int rows = warp_rows<C::KPW>(x.keys, kt, warp);
       if (kBadBlocks && ((__shfl_sync(0xffffffffu, badmask, 0) >> s) & 1u)) rows = 0;
       const uint8_t* sk = ring + s * C::WSTAGE;
       const uint8_t* sv = sk + C::SLICE;
-      const bool full_tile = rows == kKPW && !x.streaming;
+      const bool full_tile = rows == C::KPW && !x.streaming;
 
       if constexpr (kMma) {
-        uint32_t kvalid = 0xFu;  // keys 2 tig, 2 tig + 1, 2 tig + 8, 2 tig + 9 of the slice
+        // keys 16 q + 2 tig, + 1, + 8, + 9 of the slice's 16-key groups q
+        constexpr int NK = 4 * (C::KPW / 16);
+        uint32_t kvalid = (1u << NK) - 1u;
         if (!full_tile) {
           kvalid = 0u;
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const int key = 2 * tig + (k & 1) + 8 * (k >> 1);
+          for (int k = 0; k < NK; ++k) {
+            const int key = 16 * (k >> 2) + 2 * tig + (k & 1) + 8 * ((k >> 1) & 1);
             bool valid = key < rows;
             if (x.streaming && valid) {
-              const int64_t slot = kt * kTK + (int64_t)warp * kKPW + key;
+              const int64_t slot = kt * C::TK + (int64_t)warp * C::KPW + key;
               const int jp = str_pool ? (int)slot : __ldg(p.pos + (int64_t)x.b * SR + slot);
               valid = jp >= 0 && jp <= x.pq && (jp < p.sh.S || x.pq - jp < p.sh.R);
             }
@@ -893,7 +919,7 @@ __global__ void __launch_bounds__(kThreads, is_kv4_mode(kMode) ? kDecodeCtasPerS
           if (!full_tile) {
             valid = key < rows;
             if (x.streaming && valid) {
-              const int64_t slot = kt * kTK + (int64_t)warp * kKPW + key;
+              const int64_t slot = kt * C::TK + (int64_t)warp * C::KPW + key;
               const int jp = str_pool ? (int)slot : __ldg(p.pos + (int64_t)x.b * SR + slot);
               valid = jp >= 0 && jp <= x.pq && (jp < p.sh.S || x.pq - jp < p.sh.R);
             }

@@ -498,7 +498,8 @@ duo_status duo_attn_prefill_paged(duo_handle* h, const duo_kv_cache* c, const du
   return prefill_impl(h, c, paged, q, k, v, T, o, 3, stream);
 }
 
-static void decode_plan(const duo_handle* h, int64_t n, DecodeParams* p, int ctas_per_sm = 1) {
+// tk: keys per tile (kDecodeTK, or kDecodeTKKv4 for 4-bit caches)
+static void decode_plan(const duo_handle* h, int64_t n, DecodeParams* p, int ctas_per_sm = 1, int tk = kDecodeTK) {
   const Shape& sh = h->sh;
   p->seq_lens = nullptr;  // uniform length n unless a caller sets device lengths
   p->pg = PagedLayout{nullptr, 0, 0, 0, nullptr};  // contiguous retrieval caches unless paged
@@ -516,8 +517,8 @@ static void decode_plan(const duo_handle* h, int64_t n, DecodeParams* p, int cta
   p->nvalid = (int)(n < SR ? n : SR);
   p->U_r = sh.B * sh.n_ret;
   p->U_s = sh.B * sh.n_str;
-  p->tiles_r = (n + kDecodeTK - 1) / kDecodeTK;
-  p->tiles_s = (p->nvalid + kDecodeTK - 1) / kDecodeTK;
+  p->tiles_r = (n + tk - 1) / tk;
+  p->tiles_s = (p->nvalid + tk - 1) / tk;
   p->W = (int64_t)p->U_r * p->tiles_r;  // retrieval tiles; streaming units are dealt whole
   const int64_t work = p->W + p->U_s;
   const int64_t cmax = (int64_t)h->num_sms * ctas_per_sm;
@@ -594,7 +595,7 @@ static duo_status decode_impl(duo_handle* h, const duo_kv_cache* c, const duo_pa
     return fail(DUO_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need, workspace ? ws_bytes : 0);
   const Shape& sh = h->sh;
   DecodeParams p;
-  decode_plan(h, c->n, &p, ctas_per_sm);
+  decode_plan(h, c->n, &p, ctas_per_sm, kv4 ? kDecodeTKKv4 : kDecodeTK);
   const size_t counter_bytes = decode_counter_bytes(sh, h->num_sms * ctas_per_sm);
   // The arrival counters must start at zero. The kernel leaves them at zero, but the
   // caller may have lent the workspace's memory to other data since the last call (a

@@ -106,6 +106,7 @@ cudaError_t append_read_clear_error(uint32_t* code);
 
 // ------------------------------------------------------------------ decode
 constexpr int kDecodeTK = 128;  // keys per decode tile
+constexpr int kDecodeTKKv4 = 256;  // keys per decode tile over 4-bit caches (32 per warp)
 constexpr int kDecodeShortTiles = 4;  // caches of at most this many tiles: one CTA per unit
 // CTAs per SM of the 4-bit decode (its rings are small enough for two; more warps hide
 // the latency of its per-slice dependency chains); the bf16 decode runs one
