@@ -386,12 +386,6 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
   }
 }
 
-__device__ __forceinline__ uint32_t hsub2(uint32_t a, uint32_t b) {
-  uint32_t d;
-  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-  return d;
-}
-
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
   const __half2 h = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&h);
@@ -410,8 +404,9 @@ __device__ __forceinline__ uint32_t and_or(uint32_t x, uint32_t mask, uint32_t m
 }
 
 // The per-warp consumer used when the query heads of a KV head are many (and for
-// 4-bit caches): a warp's 16-key slice is two tensor-core products instead of one
-// packed FMA per (element, head pair).
+// 4-bit caches): a warp's slice (16 keys; 32 over 4-bit caches, as two 16-key groups)
+// is two tensor-core products per 16 keys instead of one packed FMA per (element, head
+// pair).
 //   S = Q K^T   rows = the g query heads (rows g ... 15 zero), cols = 8 keys per
 //               n-tile (keys gid and gid + 8 are the columns lane gid loads), k = dims
 //   O^T += V^T P^T   rows = 16 dims per m-tile, cols = the heads, k = the 16 keys
@@ -428,9 +423,10 @@ __device__ __forceinline__ uint32_t and_or(uint32_t x, uint32_t mask, uint32_t m
 // exactly the keys of its P^T fragment. For 4-bit K the magic offsets are folded
 // into one per-head constant (sum of q times the offsets of its dims), removed from
 // each slice's fresh fp32 accumulator; then q.k^ = scale (q.c) + zero sum(q). 4-bit V
-// codes are made exact by subtracting the magic (fp16, exact), so the long-lived O
-// accumulator carries no offset; p v^ = (p scale) c + p zero with p scale rounded to
-// fp16 and the zero part summed per head in fp32. q goes through fp16 on this path,
+// codes enter as fp16 subnormals, masked out of the word with no offset (c 2^-24 from
+// bits 0-3, c 2^-20 from bits 4-7; exact), so the long-lived O accumulator carries no
+// offset and each output dim comes back with its power of two; p v^ = (p scale) c +
+// p zero with p scale rounded to fp16 and the zero part summed per head in fp32. q goes through fp16 on this path,
 // so its values must lie within the fp16 range (bf16 values there convert exactly).
 // One slice as the consumer sees it: its K and V rows (codes) in shared memory, for
 // 4-bit caches their (scale, zero) pairs, and the bits of keys 2 tig, 2 tig + 1,
@@ -455,6 +451,8 @@ struct MmaSlice {
   // 4-bit V: p (at most 2^8 under the lazy rescale) times the row scale is stored in
   // fp16 as p scale 2^-6, so that no row within the fp16 range can overflow it
   static constexpr float kOScale = KV4 ? 64.f : 1.f;
+  // 4-bit V codes enter the products as fp16 subnormals: even dims c 2^-24, odd dims c 2^-20
+  static constexpr float kVLo = KV4 ? 16777216.f : 1.f, kVHi = KV4 ? 1048576.f : 1.f;
   uint32_t qa[KS][2];  // a0, a2 of every k-step (a1 = a3 = 0: rows 8 ... 15)
   float o[MT][4];
   float m_run, l_part, qfac;
@@ -657,10 +655,11 @@ struct MmaSlice {
 #pragma unroll
         for (int i = 0; i < MT; ++i) {
           const uint32_t x8 = w[i] >> 8;
-          mma16816<true>(o[i], hsub2(and_or(w[i], 0x000F000Fu, kLoMagic), kLoMagic),
-                         hsub2(and_or(w[i], 0x00F000F0u, kHiMagic), kHiMagic),
-                         hsub2(and_or(x8, 0x000F000Fu, kLoMagic), kLoMagic),
-                         hsub2(and_or(x8, 0x00F000F0u, kHiMagic), kHiMagic), pb0, pb1);
+          // the codes as fp16 subnormals, exact with no offset: c 2^-24 (bits 0-3, rows
+          // gid: even dims) and c 2^-20 (bits 4-7, rows gid + 8: odd dims); the powers of
+          // two come off per output dim in write()
+          mma16816<true>(o[i], w[i] & 0x000F000Fu, w[i] & 0x00F000F0u, x8 & 0x000F000Fu, x8 & 0x00F000F0u, pb0,
+                         pb1);
         }
       }
     } else {
@@ -707,13 +706,13 @@ struct MmaSlice {
       const int d = DT * gid + 2 * i;
       if (h0 < G) {
         float* r = red + (warp * G + h0) * (D + 2) + d;
-        r[0] = fmaf(o[i][0], kOScale, z0);
-        r[1] = fmaf(o[i][2], kOScale, z0);
+        r[0] = fmaf(o[i][0], kOScale * kVLo, z0);
+        r[1] = fmaf(o[i][2], kOScale * kVHi, z0);
       }
       if (h1 < G) {
         float* r = red + (warp * G + h1) * (D + 2) + d;
-        r[0] = fmaf(o[i][1], kOScale, z1);
-        r[1] = fmaf(o[i][3], kOScale, z1);
+        r[0] = fmaf(o[i][1], kOScale * kVLo, z1);
+        r[1] = fmaf(o[i][3], kOScale * kVHi, z1);
       }
     }
     if (tig == 0 && gid < G) {
