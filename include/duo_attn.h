@@ -162,9 +162,10 @@ size_t duo_decode_workspace_size(const duo_handle* handle, int64_t n);
  * 256-byte aligned. Its first bytes are 4-byte arrival counters, one per (sequence, KV
  * head) and one per partial slot (grid size + B Hkv; a long unit's partials are merged
  * in groups, then the group results), which every call that splits a (sequence, KV head)
- * over several CTAs clears on `stream` before its kernel (one cudaMemsetAsync of
- * ceil((2 B Hkv + grid) 4 / 256) 256 bytes; short caches are planned one CTA per unit and
- * use none), so the memory may hold anything between calls.
+ * over several CTAs clears on `stream` before its kernel (one single-CTA kernel zeroing
+ * ceil((2 B Hkv + grid) 4 / 256) 256 bytes, which the decode kernel, launched as its
+ * programmatic dependent, overlaps; short caches are planned one CTA per unit and use
+ * none), so the memory may hold anything between calls.
  * Calls sharing one workspace must be ordered on the GPU (same stream). */
 duo_status duo_attn_decode(duo_handle* handle, const duo_kv_cache* cache, const void* q, void* o, void* workspace,
                            size_t workspace_bytes, void* stream);
@@ -182,7 +183,7 @@ duo_status duo_attn_decode(duo_handle* handle, const duo_kv_cache* cache, const 
  * each device, and the first in any other CUDA context made current there later (after
  * cudaDeviceReset, say), looks up the array's device address (cudaGetSymbolAddress);
  * make that first call before any stream capture. Each call clears the array's counters with
- * cudaMemsetAsync on `stream`. All calls on a device share the one array, so calls
+ * a small kernel on `stream`. All calls on a device share the one array, so calls
  * that overlap on the GPU (different streams, or several host threads) race: order
  * them on one stream. */
 duo_status duo_attn_decode_static(duo_handle* handle, const duo_kv_cache* cache, const void* q, void* o,

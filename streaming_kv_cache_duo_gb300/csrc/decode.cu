@@ -1076,6 +1076,8 @@ __global__ void __launch_bounds__(kThreads, is_kv4_mode(kMode) ? kDecodeCtasPerS
       }
     }
     if (n_parts > 1) {
+      // the counters were cleared by the grid launched before this one (when it was)
+      asm volatile("griddepcontrol.wait;" ::: "memory");
       __threadfence();
       if (!ws.sync(err)) {
         ok = false;
@@ -1248,6 +1250,14 @@ __global__ void __launch_bounds__(kThreads, is_kv4_mode(kMode) ? kDecodeCtasPerS
   __syncthreads();
 }
 
+// Zeroes the decode's arrival counters. It lets the decode kernel launched after it
+// start at once (programmatic dependent launch); the decode waits for this grid to
+// finish (griddepcontrol.wait) only before its first ticket.
+__global__ void __launch_bounds__(256) decode_clear_counters(uint32_t* counters, int n) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  for (int i = threadIdx.x; i < n; i += blockDim.x) counters[i] = 0u;
+}
+
 template <int D, int G, int kMode>
 cudaError_t launch_v(const DecodeParams& p, cudaStream_t stream) {
   using C = Cfg<D, G, is_kv4_mode(kMode)>;
@@ -1258,8 +1268,24 @@ cudaError_t launch_v(const DecodeParams& p, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  decode_kernel<D, G, kMode><<<p.C, kThreads, C::SMEM, stream>>>(p);
-  return cudaGetLastError();
+  if (p.clear_words <= 0) {
+    decode_kernel<D, G, kMode><<<p.C, kThreads, C::SMEM, stream>>>(p);
+    return cudaGetLastError();
+  }
+  decode_clear_counters<<<1, 256, 0, stream>>>(p.counters, p.clear_words);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)p.C);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_kernel<D, G, kMode>, p);
 }
 
 // contiguous and paged retrieval caches are separate kernels, so the paged block

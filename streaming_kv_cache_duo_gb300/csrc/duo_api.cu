@@ -502,6 +502,7 @@ duo_status duo_attn_prefill_paged(duo_handle* h, const duo_kv_cache* c, const du
 static void decode_plan(const duo_handle* h, int64_t n, DecodeParams* p, int ctas_per_sm = 1, int tk = kDecodeTK) {
   const Shape& sh = h->sh;
   p->seq_lens = nullptr;  // uniform length n unless a caller sets device lengths
+  p->clear_words = 0;     // no counter clearing unless the caller asks
   p->pg = PagedLayout{nullptr, 0, 0, 0, nullptr};  // contiguous retrieval caches unless paged
   p->s_sink_tiles = p->s_win_lo = 0;
   p->q_succ = p->q_inter = nullptr;  // not Dual Chunk Attention unless a caller sets chunk_len
@@ -599,11 +600,9 @@ static duo_status decode_impl(duo_handle* h, const duo_kv_cache* c, const duo_pa
   const size_t counter_bytes = decode_counter_bytes(sh, h->num_sms * ctas_per_sm);
   // The arrival counters must start at zero. The kernel leaves them at zero, but the
   // caller may have lent the workspace's memory to other data since the last call (a
-  // caching allocator does), so every call clears them (a few KB), on the stream.
-  if (!decode_unsplit(p)) {
-    cudaError_t me = cudaMemsetAsync(workspace, 0, counter_bytes, (cudaStream_t)stream);
-    if (me != cudaSuccess) return cuda_fail(me, "cudaMemsetAsync(workspace counters)");
-  }
+  // caching allocator does), so every call clears them (a few KB) with a small kernel on
+  // the stream, which the decode kernel overlaps (programmatic dependent launch).
+  if (!decode_unsplit(p)) p.clear_words = (int)(counter_bytes / 4);
   p.q = static_cast<const uint16_t*>(q);
   p.o = static_cast<uint16_t*>(o);
   p.k_full = static_cast<const uint16_t*>(c->k_full);
@@ -805,11 +804,9 @@ duo_status duo_attn_decode_varlen(duo_handle* h, const duo_kv_cache* c, const in
   const size_t counter_bytes = decode_counter_bytes(sh, h->num_sms);
   // The arrival counters must start at zero. The kernel leaves them at zero, but the
   // caller may have lent the workspace's memory to other data since the last call (a
-  // caching allocator does), so every call clears them (a few KB), on the stream.
-  if (!decode_unsplit(p)) {
-    cudaError_t me = cudaMemsetAsync(workspace, 0, counter_bytes, (cudaStream_t)stream);
-    if (me != cudaSuccess) return cuda_fail(me, "cudaMemsetAsync(workspace counters)");
-  }
+  // caching allocator does), so every call clears them (a few KB) with a small kernel on
+  // the stream, which the decode kernel overlaps (programmatic dependent launch).
+  if (!decode_unsplit(p)) p.clear_words = (int)(counter_bytes / 4);
   p.seq_lens = seq_lens;
   p.q = static_cast<const uint16_t*>(q);
   p.o = static_cast<uint16_t*>(o);
@@ -938,8 +935,7 @@ extern "C" duo_status duo_attn_decode_static(duo_handle* h, const duo_kv_cache* 
   decode_plan(h, c->n, &p);
   const size_t counter_bytes = decode_counter_bytes(sh, h->num_sms);
   // The counters must start at zero; the array keeps whatever the last call left.
-  cudaError_t e = cudaMemsetAsync(scratch, 0, counter_bytes, (cudaStream_t)stream);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(static decode scratch counters)");
+  p.clear_words = (int)(counter_bytes / 4);
   p.q = static_cast<const uint16_t*>(q);
   p.o = static_cast<uint16_t*>(o);
   p.k_full = static_cast<const uint16_t*>(c->k_full);

@@ -136,6 +136,7 @@ struct DecodeParams {
   int s_first;     // streaming units are dealt round-robin starting at this CTA
   float scale_log2;    // log2(e) / sqrt(D)
   uint32_t* counters;  // [U] arrival tickets per unit, then [C + U] per merge group; left at zero
+  int clear_words;     // > 0: counters[0, clear_words) are zeroed by a kernel launched just before
   float* partials;     // [C + U_r + U_s][g][D + 4] (o, max, sum, 2 pad) per segment
   Shape sh;
   HeadTable heads;
