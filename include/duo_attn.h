@@ -159,13 +159,10 @@ size_t duo_decode_workspace_size(const duo_handle* handle, int64_t n);
  * KV head for all its query heads. The keys are split over the GPU's SMs; partial
  * softmaxes (o, max, sum) go to `workspace` and are merged by log-sum-exp.
  * workspace: device memory of at least duo_decode_workspace_size(handle, n) bytes,
- * 256-byte aligned. Its first bytes are 4-byte arrival counters, one per (sequence, KV
- * head) and one per partial slot (grid size + B Hkv; a long unit's partials are merged
- * in groups, then the group results), which every call that splits a (sequence, KV head)
- * over several CTAs clears on `stream` before its kernel (one single-CTA kernel zeroing
- * ceil((2 B Hkv + grid) 4 / 256) 256 bytes, which the decode kernel, launched as its
- * programmatic dependent, overlaps; short caches are planned one CTA per unit and use
- * none), so the memory may hold anything between calls.
+ * 256-byte aligned. It holds the partial softmax results (o, max, sum) of the
+ * (sequence, KV head) pairs split over several CTAs, which a second kernel merges
+ * right after the decode kernel (its programmatic dependent); nothing in it has to
+ * survive between calls, so the memory may hold anything between calls.
  * Calls sharing one workspace must be ordered on the GPU (same stream). */
 duo_status duo_attn_decode(duo_handle* handle, const duo_kv_cache* cache, const void* q, void* o, void* workspace,
                            size_t workspace_bytes, void* stream);
@@ -177,15 +174,14 @@ duo_status duo_attn_decode(duo_handle* handle, const duo_kv_cache* cache, const 
  * it is an interface variant of the decode step above and computes the same result.
  * Scratch lives in a 2 MiB array inside the library (every GPU that loads the library
  * holds it until the process exits); shapes whose bf16 decode scratch (one partial
- * of g (D + 4) floats per CTA and per (sequence, KV head), with one CTA per SM, plus
- * the counters) exceeds 2 MiB get DUO_ERR_WORKSPACE. Nothing is
+ * of g (D + 4) floats per CTA and per (sequence, KV head), with one CTA per SM)
+ * exceeds 2 MiB get DUO_ERR_WORKSPACE. Nothing is
  * allocated: no cudaMalloc, cudaFree or allocating library call. The first call on
  * each device, and the first in any other CUDA context made current there later (after
  * cudaDeviceReset, say), looks up the array's device address (cudaGetSymbolAddress);
- * make that first call before any stream capture. Each call clears the array's counters with
- * a small kernel on `stream`. All calls on a device share the one array, so calls
- * that overlap on the GPU (different streams, or several host threads) race: order
- * them on one stream. */
+ * make that first call before any stream capture. All calls on a device share the
+ * one array, so calls that overlap on the GPU (different streams, or several host
+ * threads) race: order them on one stream. */
 duo_status duo_attn_decode_static(duo_handle* handle, const duo_kv_cache* cache, const void* q, void* o,
                                   void* stream);
 

@@ -36,11 +36,12 @@
 //
 // Merge. The part of a unit a CTA covers ("segment") ends with a cross-warp merge
 // in shared memory. A unit covered by one CTA is written out directly; otherwise
-// each segment stores (o, max, sum) in the workspace and the last CTA to arrive
-// (atomic ticket, no spinning) merges them:
+// each segment stores (o, max, sum) in the workspace and a second kernel, launched as
+// the decode's programmatic dependent, merges them once the decode grid is done:
 //     O = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s,
 // the merge the vLLM Dual Chunk Attention pull request applies to its partial
-// softmax outputs.
+// softmax outputs. No counters, atomics or fences: the grid boundary orders the
+// partials before the merge, whose CTAs are already resident and waiting.
 #include <type_traits>
 
 #include "duo_device.cuh"
@@ -97,7 +98,7 @@ struct Cfg {
   static constexpr int RING = kWarps * NSW * WSTAGE;
   static constexpr int RED = kWarps * G * (D + 2);
   static constexpr int PS = D + 4;  // floats per head of a partial in the workspace (16-byte multiple)
-  // after the reduction buffer: NSW mbarriers per warp, the segment barrier, flag
+  // after the reduction buffer: NSW mbarriers per warp, the segment barrier
   static constexpr size_t SMEM = (size_t)RING + (size_t)RED * 4 + (KV4 ? kWarps * NSW * 8 + 256 : 512);
   static_assert(IT >= 1 && kKPW % KPI == 0, "tile split");
   static_assert(G <= LPK, "every head needs a lane of each key group");
@@ -745,7 +746,6 @@ __global__ void __launch_bounds__(kThreads, is_kv4_mode(kMode) ? kDecodeCtasPerS
   float* red = reinterpret_cast<float*>(smem + C::RING);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::RING + (size_t)C::RED * 4);  // [kWarps][C::NSW]
   uint64_t* segbar = full + kWarps * C::NSW;
-  int* flag = reinterpret_cast<int*>(segbar + 1);
 
   const DevError err{&g_decode_err};
   const int warp = threadIdx.x >> 5;
@@ -765,8 +765,9 @@ __global__ void __launch_bounds__(kThreads, is_kv4_mode(kMode) ? kDecodeCtasPerS
   }
   __syncthreads();
 
-  // The cache rows are read once: L2 lets them go first, keeping q, the partials and
-  // the counters the merges read.
+  // The cache rows are read once: L2 lets them go first, keeping q and the partials the
+  // merge reads. The merge kernel launched after this one may be scheduled now.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const uint64_t pol = l2_policy_evict_first();
   // refill cursor (warp-uniform); the prologue issues the first C::NSW - 1 slices
   constexpr bool kPaged = is_paged_mode(kMode);
@@ -1075,167 +1076,6 @@ __global__ void __launch_bounds__(kThreads, is_kv4_mode(kMode) ? kDecodeCtasPerS
         }
       }
     }
-    if (n_parts > 1) {
-      // the counters were cleared by the grid launched before this one (when it was)
-      asm volatile("griddepcontrol.wait;" ::: "memory");
-      __threadfence();
-      if (!ws.sync(err)) {
-        ok = false;
-        break;
-      }
-      // The unit's partials are merged in two levels when there are more than a merge
-      // group's worth: the last CTA to arrive in each group of GS consecutive CTAs merges
-      // the group's partials into the group's first slot, and the last group to finish
-      // merges the group results. Each merge reads one batch of partials per warp, so the
-      // unit's end waits for two short merges instead of one long one.
-      constexpr int EPL = G * D / 32;  // outputs per lane (2 ... 32), all of one head
-      static_assert(EPL % 2 == 0 && D % EPL == 0, "merge split");
-      // partials in flight per warp: their loads take up to 64 registers (32 under the
-      // 4-bit kernels' 128-register budget)
-      constexpr int kLoadRegs = is_kv4_mode(kMode) ? 32 : 64;
-      constexpr int NB = kLoadRegs / EPL < 1 ? 1 : (kLoadRegs / EPL > 8 ? 8 : kLoadRegs / EPL);
-      constexpr int VW = EPL % 4 == 0 ? 4 : 2;  // floats per load
-      constexpr int GS = NB * kWarps;  // CTAs per merge group
-      const int n_groups = (n_parts + GS - 1) / GS;
-      const int g0 = c_first + (c - c_first) / GS * GS;  // first CTA of this CTA's group
-      const int g_n = min(GS, c_first + n_parts - g0);
-      // ticket on one arrival counter: true for the CTA that brings it to n (which
-      // leaves it at zero for the next call)
-      auto ticket = [&](uint32_t* counter, int n) -> bool {
-        if (tid == 0) {
-          const unsigned int old = atomicAdd(counter, 1u);
-          const int last = (old == (unsigned int)(n - 1));
-          if (last) *counter = 0u;
-          *flag = last;
-        }
-        return ws.sync(err);
-      };
-      // Merges the n partials in slots s0, s0 + stride, ...: warp w takes partials w,
-      // w + 8, ..., NB at a time with all their loads in flight; each lane holds EPL
-      // consecutive outputs of one head and a running maximum, rescaling when a batch
-      // raises it; the warps' (max, sum, outputs) are combined through shared memory
-      // into the unit's output (to_out) or back into slot s0 as a partial.
-      auto merge_slots = [&](int s0, int stride, int n, bool to_out) -> bool {
-        __threadfence();
-        const int e0 = lane * EPL;
-        const int hl = e0 / D;
-        const int d0 = e0 % D;
-        float acc[EPL];
-#pragma unroll
-        for (int k = 0; k < EPL; ++k) acc[k] = 0.f;
-        float den = 0.f, mrun = -INFINITY;
-        for (int ib = warp; ib < n; ib += NB * kWarps) {
-          float mb[NB], db[NB], ob[NB][EPL];
-#pragma unroll
-          for (int i = 0; i < NB; ++i) {
-            const int ii = ib + i * kWarps;
-            if (ii < n) {
-              const float* r = p.partials + ((int64_t)(s0 + ii * stride) * G + hl) * C::PS;
-              mb[i] = __ldcg(r + D);
-              db[i] = __ldcg(r + D + 1);
-#pragma unroll
-              for (int k = 0; k < EPL; k += VW) {
-                if constexpr (VW == 4) {
-                  const float4 o4 = __ldcg(reinterpret_cast<const float4*>(r + d0 + k));
-                  ob[i][k] = o4.x;
-                  ob[i][k + 1] = o4.y;
-                  ob[i][k + 2] = o4.z;
-                  ob[i][k + 3] = o4.w;
-                } else {
-                  const float2 o2v = __ldcg(reinterpret_cast<const float2*>(r + d0 + k));
-                  ob[i][k] = o2v.x;
-                  ob[i][k + 1] = o2v.y;
-                }
-              }
-            } else {
-              mb[i] = -INFINITY;
-              db[i] = 0.f;
-#pragma unroll
-              for (int k = 0; k < EPL; ++k) ob[i][k] = 0.f;
-            }
-          }
-          float mnew = mrun;
-#pragma unroll
-          for (int i = 0; i < NB; ++i) mnew = fmaxf(mnew, mb[i]);
-          if (mnew == -INFINITY) continue;  // no visible key in any partial so far
-          const float fo = mrun == -INFINITY ? 0.f : ex2_approx(mrun - mnew);
-          den *= fo;
-#pragma unroll
-          for (int k = 0; k < EPL; ++k) acc[k] *= fo;
-#pragma unroll
-          for (int i = 0; i < NB; ++i) {
-            const float f = mb[i] == -INFINITY ? 0.f : ex2_approx(mb[i] - mnew);
-            den = fmaf(f, db[i], den);
-#pragma unroll
-            for (int k = 0; k < EPL; ++k) acc[k] = fmaf(f, ob[i][k], acc[k]);
-          }
-          mrun = mnew;
-        }
-        float* rw = red + (warp * G + hl) * (D + 2);
-#pragma unroll
-        for (int k = 0; k < EPL; ++k) rw[d0 + k] = acc[k];
-        if (d0 == 0) {
-          rw[D] = mrun;
-          rw[D + 1] = den;
-        }
-        if (!ws.sync(err)) return false;
-        float* dst = p.partials + (int64_t)s0 * G * C::PS;
-        for (int e = tid; e < G * D; e += kThreads) {
-          const int h = e / D;
-          const int d = e % D;
-          float M = -INFINITY;
-#pragma unroll
-          for (int w = 0; w < kWarps; ++w) M = fmaxf(M, red[(w * G + h) * (D + 2) + D]);
-          float num = 0.f, dsum = 0.f;
-#pragma unroll
-          for (int w = 0; w < kWarps; ++w) {
-            const float* r = red + (w * G + h) * (D + 2);
-            const float f = r[D] == -INFINITY ? 0.f : ex2_approx(r[D] - M);
-            num = fmaf(f, r[d], num);
-            dsum = fmaf(f, r[D + 1], dsum);
-          }
-          if (to_out) {
-            p.o[((int64_t)x.b * p.sh.Hq + (int64_t)x.kvh * G + h) * D + d] =
-                __bfloat16_as_ushort(__float2bfloat16_rn(dsum > 0.f ? num / dsum : 0.f));
-          } else {
-            dst[h * C::PS + d] = num;
-            if (d == 0) {
-              dst[h * C::PS + D] = M;
-              dst[h * C::PS + D + 1] = dsum;
-            }
-          }
-        }
-        if (to_out) return true;
-        __threadfence();  // the group result before the group's ticket
-        return ws.sync(err);
-      };
-      uint32_t* group_counters = p.counters + (p.U_r + p.U_s);  // [C + U], by slot
-      if (n_groups == 1) {
-        if (!ticket(p.counters + u, n_parts)) {
-          ok = false;
-          break;
-        }
-        if (*flag && !merge_slots(c_first + u, 1, n_parts, true)) {
-          ok = false;
-          break;
-        }
-      } else {
-        if (!ticket(group_counters + g0 + u, g_n)) {
-          ok = false;
-          break;
-        }
-        if (*flag) {
-          if (!merge_slots(g0 + u, 1, g_n, false) || !ticket(p.counters + u, n_groups)) {
-            ok = false;
-            break;
-          }
-          if (*flag && !merge_slots(c_first + u, GS, n_groups, true)) {
-            ok = false;
-            break;
-          }
-        }
-      }
-    }
     // the reduction buffer is reused by the next segment
     if (!ws.sync(err)) {
       ok = false;
@@ -1250,12 +1090,88 @@ __global__ void __launch_bounds__(kThreads, is_kv4_mode(kMode) ? kDecodeCtasPerS
   __syncthreads();
 }
 
-// Zeroes the decode's arrival counters. It lets the decode kernel launched after it
-// start at once (programmatic dependent launch); the decode waits for this grid to
-// finish (griddepcontrol.wait) only before its first ticket.
-__global__ void __launch_bounds__(256) decode_clear_counters(uint32_t* counters, int n) {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  for (int i = threadIdx.x; i < n; i += blockDim.x) counters[i] = 0u;
+// Merge of the retrieval units split over several CTAs, launched right after the decode
+// kernel as its programmatic dependent: its CTAs are scheduled while the decode runs
+// (the decode signals griddepcontrol.launch_dependents as it starts) and wait in
+// griddepcontrol.wait until the decode grid has finished and its partials are visible.
+// One CTA per (retrieval unit, head, 32 output dims): lane = output dim, warp w takes
+// partials w, w + 8, ..., up to kMergeNB of them per round with all their loads in
+// flight, so a unit split over 152 CTAs is merged in one round of loads; the eight
+// warps' (max, sum, outputs) are combined through shared memory:
+//     O = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s.
+constexpr int kMergeWarps = 8;
+constexpr int kMergeNB = 20;  // partials in flight per warp
+
+template <int D, int G>
+__global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_kernel(const DecodeParams p) {
+  constexpr int PS = D + 4;  // floats per head of a partial (Cfg::PS)
+  constexpr int DC = D / 32;
+  const int dc = blockIdx.x % DC;
+  const int h = (blockIdx.x / DC) % G;
+  const int u = blockIdx.x / (DC * G);  // retrieval unit
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t us = (int64_t)u * p.tiles_r;
+  const int c_first = cta_of(p, us);
+  const int n_parts = cta_of(p, us + p.tiles_r - 1) - c_first + 1;
+  if (n_parts <= 1) return;  // the decode kernel wrote this unit's output
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int d = dc * 32 + lane;
+  float acc = 0.f, den = 0.f, mrun = -INFINITY;
+  for (int i0 = warp; i0 < n_parts; i0 += kMergeWarps * kMergeNB) {
+    float mb[kMergeNB], lb[kMergeNB], ob[kMergeNB];
+#pragma unroll
+    for (int i = 0; i < kMergeNB; ++i) {
+      const int ii = i0 + i * kMergeWarps;
+      if (ii < n_parts) {
+        const float* r = p.partials + ((int64_t)(c_first + ii + u) * G + h) * PS;
+        mb[i] = __ldcg(r + D);
+        lb[i] = __ldcg(r + D + 1);
+        ob[i] = __ldcg(r + d);
+      } else {
+        mb[i] = -INFINITY;
+        lb[i] = 0.f;
+        ob[i] = 0.f;
+      }
+    }
+    float mnew = mrun;
+#pragma unroll
+    for (int i = 0; i < kMergeNB; ++i) mnew = fmaxf(mnew, mb[i]);
+    if (mnew == -INFINITY) continue;  // no visible key in any partial so far
+    const float fo = mrun == -INFINITY ? 0.f : ex2_approx(mrun - mnew);
+    den *= fo;
+    acc *= fo;
+#pragma unroll
+    for (int i = 0; i < kMergeNB; ++i) {
+      const float f = mb[i] == -INFINITY ? 0.f : ex2_approx(mb[i] - mnew);
+      den = fmaf(f, lb[i], den);
+      acc = fmaf(f, ob[i], acc);
+    }
+    mrun = mnew;
+  }
+  __shared__ float s_acc[kMergeWarps][32];
+  __shared__ float s_m[kMergeWarps], s_l[kMergeWarps];
+  s_acc[warp][lane] = acc;
+  if (lane == 0) {
+    s_m[warp] = mrun;
+    s_l[warp] = den;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kMergeWarps; ++w) M = fmaxf(M, s_m[w]);
+    float num = 0.f, dsum = 0.f;
+#pragma unroll
+    for (int w = 0; w < kMergeWarps; ++w) {
+      const float f = s_m[w] == -INFINITY ? 0.f : ex2_approx(s_m[w] - M);
+      num = fmaf(f, s_acc[w][lane], num);
+      dsum = fmaf(f, s_l[w], dsum);
+    }
+    const int b = u / p.sh.n_ret;
+    const int kvh = p.heads.ret_head[u % p.sh.n_ret];
+    p.o[((int64_t)b * p.sh.Hq + (int64_t)kvh * G + h) * D + d] =
+        __bfloat16_as_ushort(__float2bfloat16_rn(dsum > 0.f ? num / dsum : 0.f));
+  }
 }
 
 template <int D, int G, int kMode>
@@ -1268,24 +1184,19 @@ cudaError_t launch_v(const DecodeParams& p, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  if (p.clear_words <= 0) {
-    decode_kernel<D, G, kMode><<<p.C, kThreads, C::SMEM, stream>>>(p);
-    return cudaGetLastError();
-  }
-  decode_clear_counters<<<1, 256, 0, stream>>>(p.counters, p.clear_words);
+  decode_kernel<D, G, kMode><<<p.C, kThreads, C::SMEM, stream>>>(p);
   cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  if (e != cudaSuccess || p.W == 0 || p.Cr == p.U_r) return e;  // no unit split over CTAs
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)p.C);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.gridDim = dim3((unsigned)(p.U_r * G * (D / 32)));
+  cfg.blockDim = dim3(kMergeWarps * 32);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_kernel<D, G, kMode>, p);
+  return cudaLaunchKernelEx(&cfg, decode_merge_kernel<D, G>, p);
 }
 
 // contiguous and paged retrieval caches are separate kernels, so the paged block
@@ -1300,16 +1211,9 @@ cudaError_t launch_t(const DecodeParams& p, cudaStream_t stream) {
 
 }  // namespace
 
-size_t decode_counter_bytes(const Shape& sh, int num_ctas) {
-  const int64_t U = (int64_t)sh.B * sh.Hkv;
-  return ((size_t)(2 * U + num_ctas) * 4 + 255) / 256 * 256;  // per unit, then per slot
-}
-
 size_t decode_workspace_bytes(const Shape& sh, int num_ctas) {
   const int64_t U = (int64_t)sh.B * sh.Hkv;
-  const size_t counters = decode_counter_bytes(sh, num_ctas);
-  const size_t parts = (size_t)(num_ctas + U) * sh.g * (sh.D + 4) * 4;  // Cfg::PS floats per head
-  return counters + parts;
+  return (size_t)(num_ctas + U) * sh.g * (sh.D + 4) * 4;  // Cfg::PS floats per head and slot
 }
 
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream) {

@@ -502,7 +502,6 @@ duo_status duo_attn_prefill_paged(duo_handle* h, const duo_kv_cache* c, const du
 static void decode_plan(const duo_handle* h, int64_t n, DecodeParams* p, int ctas_per_sm = 1, int tk = kDecodeTK) {
   const Shape& sh = h->sh;
   p->seq_lens = nullptr;  // uniform length n unless a caller sets device lengths
-  p->clear_words = 0;     // no counter clearing unless the caller asks
   p->pg = PagedLayout{nullptr, 0, 0, 0, nullptr};  // contiguous retrieval caches unless paged
   p->s_sink_tiles = p->s_win_lo = 0;
   p->q_succ = p->q_inter = nullptr;  // not Dual Chunk Attention unless a caller sets chunk_len
@@ -535,9 +534,6 @@ static void decode_plan(const duo_handle* h, int64_t n, DecodeParams* p, int cta
     p->s_first = p->U_r;
   }
 }
-
-// Every unit lies in one CTA (no arrival counter is used by the launch).
-static bool decode_unsplit(const DecodeParams& p) { return p.W == 0 || p.Cr == p.U_r; }
 
 size_t duo_decode_workspace_size(const duo_handle* h, int64_t n) {
   if (!h) return 0;
@@ -597,12 +593,6 @@ static duo_status decode_impl(duo_handle* h, const duo_kv_cache* c, const duo_pa
   const Shape& sh = h->sh;
   DecodeParams p;
   decode_plan(h, c->n, &p, ctas_per_sm, kv4 ? kDecodeTKKv4 : kDecodeTK);
-  const size_t counter_bytes = decode_counter_bytes(sh, h->num_sms * ctas_per_sm);
-  // The arrival counters must start at zero. The kernel leaves them at zero, but the
-  // caller may have lent the workspace's memory to other data since the last call (a
-  // caching allocator does), so every call clears them (a few KB) with a small kernel on
-  // the stream, which the decode kernel overlaps (programmatic dependent launch).
-  if (!decode_unsplit(p)) p.clear_words = (int)(counter_bytes / 4);
   p.q = static_cast<const uint16_t*>(q);
   p.o = static_cast<uint16_t*>(o);
   p.k_full = static_cast<const uint16_t*>(c->k_full);
@@ -611,8 +601,7 @@ static duo_status decode_impl(duo_handle* h, const duo_kv_cache* c, const duo_pa
   p.v_sr = static_cast<const uint16_t*>(c->v_sr);
   p.pos = c->pos;
   p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)sh.D));
-  p.counters = static_cast<uint32_t*>(workspace);
-  p.partials = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + counter_bytes);
+  p.partials = static_cast<float*>(workspace);
   p.sh = sh;
   p.heads = h->heads;
   p.pg = pg;
@@ -801,12 +790,6 @@ duo_status duo_attn_decode_varlen(duo_handle* h, const duo_kv_cache* c, const in
   const Shape& sh = h->sh;
   DecodeParams p;
   decode_plan(h, max_len, &p);
-  const size_t counter_bytes = decode_counter_bytes(sh, h->num_sms);
-  // The arrival counters must start at zero. The kernel leaves them at zero, but the
-  // caller may have lent the workspace's memory to other data since the last call (a
-  // caching allocator does), so every call clears them (a few KB) with a small kernel on
-  // the stream, which the decode kernel overlaps (programmatic dependent launch).
-  if (!decode_unsplit(p)) p.clear_words = (int)(counter_bytes / 4);
   p.seq_lens = seq_lens;
   p.q = static_cast<const uint16_t*>(q);
   p.o = static_cast<uint16_t*>(o);
@@ -816,8 +799,7 @@ duo_status duo_attn_decode_varlen(duo_handle* h, const duo_kv_cache* c, const in
   p.v_sr = static_cast<const uint16_t*>(c->v_sr);
   p.pos = c->pos;
   p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)sh.D));
-  p.counters = static_cast<uint32_t*>(workspace);
-  p.partials = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + counter_bytes);
+  p.partials = static_cast<float*>(workspace);
   p.sh = sh;
   p.heads = h->heads;
   cudaError_t ce = launch_decode(p, (cudaStream_t)stream);
@@ -861,7 +843,7 @@ duo_status duo_selftest_bounded_wait(uint32_t limit_us, void* stream) {
 // device or fragment memory in the middle of a latency-critical loop, or a host
 // runtime whose allocator owns every device allocation. For them,
 // duo_attn_decode_static() runs the same decode kernel with its scratch (the
-// per-unit arrival counters and the partial softmax results) in the array below,
+// partial softmax results of units split over CTAs) in the array below,
 // which belongs to this library's module: every GPU that loads the library keeps
 // kStaticScratchBytes of device memory for it until the process exits.
 namespace {
@@ -933,9 +915,6 @@ extern "C" duo_status duo_attn_decode_static(duo_handle* h, const duo_kv_cache* 
   const Shape& sh = h->sh;
   DecodeParams p;
   decode_plan(h, c->n, &p);
-  const size_t counter_bytes = decode_counter_bytes(sh, h->num_sms);
-  // The counters must start at zero; the array keeps whatever the last call left.
-  p.clear_words = (int)(counter_bytes / 4);
   p.q = static_cast<const uint16_t*>(q);
   p.o = static_cast<uint16_t*>(o);
   p.k_full = static_cast<const uint16_t*>(c->k_full);
@@ -944,8 +923,7 @@ extern "C" duo_status duo_attn_decode_static(duo_handle* h, const duo_kv_cache* 
   p.v_sr = static_cast<const uint16_t*>(c->v_sr);
   p.pos = c->pos;
   p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)sh.D));
-  p.counters = static_cast<uint32_t*>(scratch);
-  p.partials = reinterpret_cast<float*>(static_cast<uint8_t*>(scratch) + counter_bytes);
+  p.partials = static_cast<float*>(scratch);
   p.sh = sh;
   p.heads = h->heads;
   cudaError_t ce = launch_decode(p, (cudaStream_t)stream);

@@ -135,8 +135,6 @@ struct DecodeParams {
                    // empty share inside a unit's span (its partial would never arrive)
   int s_first;     // streaming units are dealt round-robin starting at this CTA
   float scale_log2;    // log2(e) / sqrt(D)
-  uint32_t* counters;  // [U] arrival tickets per unit, then [C + U] per merge group; left at zero
-  int clear_words;     // > 0: counters[0, clear_words) are zeroed by a kernel launched just before
   float* partials;     // [C + U_r + U_s][g][D + 4] (o, max, sum, 2 pad) per segment
   Shape sh;
   HeadTable heads;
@@ -163,8 +161,7 @@ struct DecodeParams {
   int kv4;  // 4-bit caches (the retrieval arrays are null when there is no retrieval head)
 };
 size_t decode_workspace_bytes(const Shape& sh, int num_ctas);
-// The leading counter bytes of that workspace (cleared before a split decode).
-size_t decode_counter_bytes(const Shape& sh, int num_ctas);
+
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream);
 
 // ------------------------------------------------------------------ prefill

@@ -23,11 +23,10 @@ STATIC_SCRATCH_BYTES = 2 << 20  # the array's size, as include/duo_attn.h states
 
 
 def _scratch_need(B, Hq, Hkv, D, num_sms):
-    """Decode scratch of a shape as the header defines it: 4-byte counters per (sequence,
-    KV head) and per partial slot (SMs + units), rounded up to 256 bytes, then
-    (SMs + units) x g x (D + 4) floats."""
+    """Decode scratch of a shape as the header defines it: (SMs + units) partial slots of
+    g x (D + 4) floats."""
     U = B * Hkv
-    return -(-(2 * U + num_sms) * 4 // 256) * 256 + (num_sms + U) * (Hq // Hkv) * (D + 4) * 4
+    return (num_sms + U) * (Hq // Hkv) * (D + 4) * 4
 
 
 def _run(B, Hq, Hkv, D, S, R, kinds, ctx, seed, check_batches=None):
