@@ -472,7 +472,7 @@ def bench_decode(w, steps_cap, peaks, paged_block=0, pool=False, kv4=False):
     return {"workload": w.name, "value": round(gbs, 1), "unit": "GB/s", "decode_ms": round(avg_ms, 4),
             "step_ms_with_append": round(step_ms, 4), "bytes_per_step": int(sum(nbytes) / len(nbytes)),
             "steps_timed": len(times), "steps_run": steps,
-            # append, counter clear, decode (a million-token decode is always split over CTAs)
+            # append, decode, merge (a million-token decode is always split over CTAs)
             "gpu_launches": 3 * steps,
             "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(gbs / peak, 4),
@@ -549,7 +549,7 @@ def bench_decode_graph(w, peaks):
             "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": round(gbs / peaks["hbm_gbs"], 4), "traffic": measured_traffic("decode_batched"),
                          "kernel": f"decode_kernel<{w.D},{w.Hq // w.Hkv},plain> (device lengths)"},
-            "gpu_launches_per_step": 3}  # append, counter clear, decode
+            "gpu_launches_per_step": 3}  # append, decode, merge of the split units
 
 
 def bench_chunked(w, steps, warmup, peaks, paged_block=0, pool=False, kv4=False):
@@ -952,7 +952,7 @@ def other_workload(args, w, world, rank, peaks):
         base["config"].update(context=w.context, decode_steps=w.decode_steps)
         line = dict(base, value=round(r["value"] * world, 1), unit="GB/s", ms_per_step=r.get("step_ms",
                     r.get("step_ms_with_append")), decode=r,
-                    gpu_launches=r.get("gpu_launches", 3 * r["steps_timed"]))  # append, counter clear, decode
+                    gpu_launches=r.get("gpu_launches", 3 * r["steps_timed"]))  # append, decode, merge
     if rank == 0:
         print(json.dumps(line))
 
