@@ -619,13 +619,8 @@ struct MmaSlice {
         o[i][3] *= f1;
       }
     }
-    float pr[NX];
-#pragma unroll
-    for (int k = 0; k < NX; ++k) {
-      pr[k] = (kFull || ((in.hvalid >> k) & 1u)) ? ex2_approx(x[k] - m_run) : 0.f;
-      l_part += pr[k];
-    }
     if constexpr (KV4) {
+      // p of a group is computed next to its use, so only its four values are live
 #pragma unroll
       for (int q = 0; q < NGRP; ++q) {
         const uint2 z01 = *reinterpret_cast<const uint2*>(in.vz + 64 * q + tig * 8);
@@ -636,8 +631,10 @@ struct MmaSlice {
         for (int k = 0; k < 4; ++k) {
           const float2 sz = scale_zero(zz[k]);
           const bool ok = kFull || ((in.hvalid >> (4 * q + k)) & 1u);  // an unused row's pair may be anything
-          b[k] = ok ? pr[4 * q + k] * (sz.x * (1.f / kOScale)) : 0.f;
-          z_part += ok ? pr[4 * q + k] * sz.y : 0.f;
+          const float pk = ok ? ex2_approx(x[4 * q + k] - m_run) : 0.f;
+          l_part += pk;
+          b[k] = ok ? pk * (sz.x * (1.f / kOScale)) : 0.f;
+          z_part += ok ? pk * sz.y : 0.f;
         }
         const uint32_t pb0 = pack_half2(b[0], b[1]);
         const uint32_t pb1 = pack_half2(b[2], b[3]);
@@ -664,6 +661,12 @@ struct MmaSlice {
         }
       }
     } else {
+      float pr[NX];
+#pragma unroll
+      for (int k = 0; k < NX; ++k) {
+        pr[k] = (kFull || ((in.hvalid >> k) & 1u)) ? ex2_approx(x[k] - m_run) : 0.f;
+        l_part += pr[k];
+      }
       const int kr[4] = {2 * tig, 2 * tig + 1, 2 * tig + 8, 2 * tig + 9};
       const uint32_t pb0 = pack_bf16x2(pr[0], pr[1]);
       const uint32_t pb1 = pack_bf16x2(pr[2], pr[3]);
@@ -774,7 +777,7 @@ __global__ void __launch_bounds__(kThreads, is_kv4_mode(kMode) ? kDecodeCtasPerS
   constexpr bool kBadBlocks = kPaged || kMode == kModeKv4Paged;  // a slice may come from a bad block id
   Cursor<kMode> cur;
   cur.init(p, c, t0, t1, live);
-  int64_t issued = 0;
+  uint32_t issued = 0;  // slices issued (fewer than 2^32 per CTA)
   uint32_t badmask = 0;  // lane 0: bit s set when stage s holds a skipped (bad-block) slice
   for (int s = 0; s < C::NSW - 1 && cur.live; ++s) {
     if (lane == 0) {
@@ -793,7 +796,7 @@ __global__ void __launch_bounds__(kThreads, is_kv4_mode(kMode) ? kDecodeCtasPerS
   std::conditional_t<kMma, MmaSlice<D, G, is_kv4_mode(kMode)>, NoMma> mm;
   const int SR = p.sh.S + p.sh.R;
   WarpSync ws{segbar, 0};
-  int64_t j = 0;  // tiles consumed
+  uint32_t j = 0;  // tiles consumed
   bool ok = true;
   SegState seg{t0, 0};
   int u;
@@ -1084,7 +1087,7 @@ __global__ void __launch_bounds__(kThreads, is_kv4_mode(kMode) ? kDecodeCtasPerS
   }
   // Copies still in flight (only after an early exit) land before the CTA ends.
   if (lane == 0) {
-    for (int64_t jj = j; jj < issued; ++jj)
+    for (uint32_t jj = j; jj < issued; ++jj)
       mbar_wait(&wfull[jj % C::NSW], (uint32_t)((jj / C::NSW) & 1), err, kErrDecodeConsumer);
   }
   __syncthreads();
