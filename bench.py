@@ -55,10 +55,10 @@ MEASURED_TRAFFIC = {
     "prefill_chunked_kv4": {"src": ("prefill.cu", "duo_device.cuh", "duo_internal.h"), "sha1": "f22a1019c1883353",
                             "bytes": 941.062e6 + 85.440e6},
     # one decode launch of the batched 8 x 128K workload (device lengths, graph replay)
-    "decode_batched": {"src": ("decode.cu", "duo_device.cuh", "duo_internal.h"), "sha1": "5a13e0b2fd97bf44",
-                       "bytes": 1.081999e9 + 1.599e6},
-    "decode": {"src": ("decode.cu", "duo_device.cuh", "duo_internal.h"), "sha1": "5a13e0b2fd97bf44",
-               "bytes": 1.074860e9 + 1.757e6},
+    "decode_batched": {"src": ("decode.cu", "duo_device.cuh", "duo_internal.h"), "sha1": "ab97fd96315e78fa",
+                       "bytes": 1.081930e9 + 1.534e6},
+    "decode": {"src": ("decode.cu", "duo_device.cuh", "duo_internal.h"), "sha1": "ab97fd96315e78fa",
+               "bytes": 1.074806e9 + 1.567e6},
 }
 
 
