@@ -177,3 +177,22 @@ def test_kv4_wide_value_rows_do_not_overflow_fp16():
         cache.append(Kq[0, :p + 1], Vq[0, :p + 1])
         ref = decode_from_cache(Qh[0, p], p, cache)
         assert_close(to_np(o[0]) / 1024, ref / 1024, f"step {s}")
+
+
+def test_kv4_decode_one_unit_split_over_every_cta():
+    """One retrieval unit of 160000 keys spread over the whole 4-bit grid (two CTAs per SM,
+    one partial each), so the merge kernel takes its partials in more than one round of
+    loads per warp; two decode steps against the oracle over the dequantized rows."""
+    B, Hq, Hkv, D, S, R, kinds, ctx, steps = 1, 8, 2, 128, 4, 64, [1, 0], 160000, 2
+    seed = 741
+    layer, outs = _run(seed, B, Hq, Hkv, D, S, R, kinds, ctx, steps, 65536)
+    total = ctx + steps
+    Kq = kv4.roundtrip(host_stream(seed, ds.STREAM_K, B, 0, total, Hkv, D).astype(np.float32))
+    Vq = kv4.roundtrip(host_stream(seed, ds.STREAM_V, B, 0, total, Hkv, D).astype(np.float32))
+    Qh = host_stream(seed, ds.STREAM_Q, B, 0, total, Hq, D)
+    cache = OracleCache(kinds, S, R, D)
+    cache.append(Kq[0, :ctx], Vq[0, :ctx])
+    for s in range(steps):
+        p = ctx + s
+        cache.append(Kq[0, p:p + 1], Vq[0, p:p + 1])
+        assert_close(to_np(outs[s][0]), decode_from_cache(Qh[0, p], p, cache), f"step {s}")
