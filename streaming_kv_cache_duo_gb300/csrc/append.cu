@@ -25,6 +25,9 @@ namespace {
 __device__ unsigned int g_append_err;
 
 __global__ void __launch_bounds__(256) append_kernel(const AppendParams p) {
+  // a decode launched next may have its CTAs scheduled now (it waits for this grid
+  // before it reads anything)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int D = p.sh.D;
   const int Hkv = p.sh.Hkv;
   const int vpr = D / 8;  // 16-byte vectors per row
@@ -100,6 +103,9 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendParams p) {
 // is race-free. A sequence whose retrieval cache is full is left unchanged and
 // the capacity error is recorded.
 __global__ void __launch_bounds__(256) append_varlen_kernel(const AppendParams p, int32_t* seq_lens) {
+  // a decode launched next may have its CTAs scheduled now (it waits for this grid
+  // before it reads anything)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int b = blockIdx.x;
   const int D = p.sh.D;
   const int Hkv = p.sh.Hkv;
@@ -220,6 +226,9 @@ __device__ __forceinline__ void quantize_row(const uint16_t* src, uint8_t* codes
 
 template <int D>
 __global__ void __launch_bounds__(256) append_kv4_kernel(const AppendParams p) {
+  // a decode launched next may have its CTAs scheduled now (it waits for this grid
+  // before it reads anything)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int lane = threadIdx.x & 31;
   const int Hkv = p.sh.Hkv;
   const int n_ret = p.sh.n_ret, n_str = p.sh.n_str;

@@ -767,6 +767,9 @@ __global__ void __launch_bounds__(kThreads, is_kv4_mode(kMode) ? kDecodeCtasPerS
     fence_mbarrier_init();
   }
   __syncthreads();
+  // Launched as a programmatic dependent (of the append before it, say): nothing the
+  // previous grid writes (cache rows, ring slots, positions, lengths) is read before it ends.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   // The cache rows are read once: L2 lets them go first, keeping q and the partials the
   // merge reads. The merge kernel launched after this one may be scheduled now.
@@ -1187,17 +1190,24 @@ cudaError_t launch_v(const DecodeParams& p, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  decode_kernel<D, G, kMode><<<p.C, kThreads, C::SMEM, stream>>>(p);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess || p.W == 0 || p.Cr == p.U_r) return e;  // no unit split over CTAs
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(p.U_r * G * (D / 32)));
-  cfg.blockDim = dim3(kMergeWarps * 32);
-  cfg.stream = stream;
+  // Programmatic dependents of what precedes them on the stream: the decode's CTAs may be
+  // resident before an append before it ends (the decode waits for it first thing; with
+  // lengths on the device, measured slower, so not there), the merge's before the decode ends.
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)p.C);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = stream;
   cfg.attrs = attr;
+  cfg.numAttrs = p.seq_lens ? 0 : 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, decode_kernel<D, G, kMode>, p);
+  if (e != cudaSuccess || p.W == 0 || p.Cr == p.U_r) return e;  // no unit split over CTAs
+  cfg.gridDim = dim3((unsigned)(p.U_r * G * (D / 32)));
+  cfg.blockDim = dim3(kMergeWarps * 32);
+  cfg.dynamicSmemBytes = 0;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, decode_merge_kernel<D, G>, p);
 }
