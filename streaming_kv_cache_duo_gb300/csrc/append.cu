@@ -26,8 +26,10 @@ __device__ unsigned int g_append_err;
 
 __global__ void __launch_bounds__(256) append_kernel(const AppendParams p) {
   // a decode launched next may have its CTAs scheduled now (it waits for this grid
-  // before it reads anything)
+  // before it reads anything); this grid, launched as a programmatic dependent itself,
+  // writes nothing before the grid before it (a decode reading the ring slots) has ended
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int D = p.sh.D;
   const int Hkv = p.sh.Hkv;
   const int vpr = D / 8;  // 16-byte vectors per row
@@ -322,8 +324,16 @@ cudaError_t launch_append(const AppendParams& p, int num_sms, cudaStream_t strea
   int64_t blocks = (total + 255) / 256;
   const int64_t cap = (int64_t)num_sms * 8;
   if (blocks > cap) blocks = cap;
-  append_kernel<<<(unsigned)blocks, 256, 0, stream>>>(p);
-  return cudaGetLastError();
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)blocks);
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, append_kernel, p);
 }
 
 }  // namespace duo
