@@ -31,7 +31,13 @@
  *     and row-major in the index order written; base addresses must be 16-byte
  *     aligned.
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
- *     Every kernel runs on it, asynchronously to the host.
+ *     Every kernel runs on it, asynchronously to the host. The append and decode
+ *     kernels use programmatic dependent launch among themselves (an append lets the
+ *     decode after it start early, each waits for the grid before it before touching
+ *     its data); stream order holds as usual for any kernel launched without the
+ *     cudaLaunchAttributeProgrammaticStreamSerialization attribute. A caller kernel
+ *     launched with that attribute right after an append or a decode must call
+ *     cudaGridDependencySynchronize() before it reads what they wrote.
  *   - Arguments are checked on the host before any launch. On an error nothing is
  *     written, the cache length is unchanged, the status is returned and
  *     duo_last_error() describes it.
