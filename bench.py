@@ -513,7 +513,7 @@ def bench_decode_graph(w, peaks):
     sq.copy_(q[:, 0])
     sk.copy_(kn[:, 0:1])
     sv.copy_(vn[:, 0:1])
-    layer.append_varlen(sk, sv, seq_lens)  # eager step 0 (clears the workspace counters)
+    layer.append_varlen(sk, sv, seq_lens)  # eager step 0 (loads the kernels before capture)
     layer.decode_varlen(sq, seq_lens, max_len, out=so)
     torch.cuda.synchronize()
     graph = torch.cuda.CUDAGraph()

@@ -158,8 +158,8 @@ def test_full_size_decode_1m_sampled():
 def test_workspace_holding_other_data_between_calls(Hq):
     """A caller may lend the workspace's memory to other data between decode calls (a
     caching allocator does): with the same handle and address, a workspace filled with
-    0xFF bytes between two steps still gives the oracle's output (every call clears its
-    arrival counters). The context is long enough that one unit spans many CTAs."""
+    0xFF bytes between two steps still gives the oracle's output (nothing in it has to
+    survive between calls). The context is long enough that one unit spans many CTAs."""
     from streaming_kv_cache_duo_gb300 import DuoLayer, duo_device_error
     B, Hkv, D, S, R, kinds, ctx = 1, 2, 128, 4, 64, [1, 0], 20000
     seed = 41

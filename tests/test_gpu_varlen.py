@@ -132,7 +132,7 @@ def test_decode_step_captured_in_a_cuda_graph():
         sk.copy_(_token(K, posn))
         sv.copy_(_token(V, posn))
 
-    # step 0 eagerly (also clears the workspace counters before capture)
+    # step 0 eagerly (the kernels are loaded before capture)
     feed(0)
     layer.append_varlen(sk, sv, seq_lens)
     layer.decode_varlen(sq, seq_lens, max_len, out=so)
