@@ -55,10 +55,10 @@ MEASURED_TRAFFIC = {
     "prefill_chunked_kv4": {"src": ("prefill.cu", "duo_device.cuh", "duo_internal.h"), "sha1": "7a442700a6ccf325",
                             "bytes": 941.013e6 + 84.869e6},
     # one decode launch of the batched 8 x 128K workload (device lengths, graph replay)
-    "decode_batched": {"src": ("decode.cu", "duo_device.cuh", "duo_internal.h"), "sha1": "ab97fd96315e78fa",
-                       "bytes": 1.081930e9 + 1.534e6},
-    "decode": {"src": ("decode.cu", "duo_device.cuh", "duo_internal.h"), "sha1": "ab97fd96315e78fa",
-               "bytes": 1.074806e9 + 1.567e6},
+    "decode_batched": {"src": ("decode.cu", "duo_device.cuh", "duo_internal.h"), "sha1": "1249b666140ea1cb",
+                       "bytes": 1.081935e9 + 1.504e6},
+    "decode": {"src": ("decode.cu", "duo_device.cuh", "duo_internal.h"), "sha1": "1249b666140ea1cb",
+               "bytes": 1.074806e9 + 1.440e6},
 }
 
 
