@@ -42,7 +42,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from the ncu
-# captures summarised in profiles/, valid only for the kernel sources they were taken on.
+# captures summarised in profiles/, valid only for the kernel sources they were taken on
+# (the decode records were re-keyed after an edit to the decode file's header comment only).
 L2_BYTES = 129e6  # GB300 L2 capacity
 
 MEASURED_TRAFFIC = {
@@ -55,9 +56,9 @@ MEASURED_TRAFFIC = {
     "prefill_chunked_kv4": {"src": ("prefill.cu", "duo_device.cuh", "duo_internal.h"), "sha1": "7a442700a6ccf325",
                             "bytes": 941.013e6 + 84.869e6},
     # one decode launch of the batched 8 x 128K workload (device lengths, graph replay)
-    "decode_batched": {"src": ("decode.cu", "duo_device.cuh", "duo_internal.h"), "sha1": "1249b666140ea1cb",
+    "decode_batched": {"src": ("decode.cu", "duo_device.cuh", "duo_internal.h"), "sha1": "4752d2f3b937cdbb",
                        "bytes": 1.081935e9 + 1.504e6},
-    "decode": {"src": ("decode.cu", "duo_device.cuh", "duo_internal.h"), "sha1": "1249b666140ea1cb",
+    "decode": {"src": ("decode.cu", "duo_device.cuh", "duo_internal.h"), "sha1": "4752d2f3b937cdbb",
                "bytes": 1.074806e9 + 1.440e6},
 }
 

@@ -3,8 +3,9 @@
 //
 // Work list. A "unit" is one (sequence, KV head): a retrieval unit holds n keys
 // (rows [0, n) of its full cache), a streaming unit min(n, S + R) ring slots.
-// Retrieval units are cut into tiles of kTK keys laid end to end; CTA c < Cr takes
-// tiles [c W / Cr, (c + 1) W / Cr) with Cr = min(C, W), so no share is empty and
+// Retrieval units are cut into tiles of kTK keys (256 over 4-bit caches) laid end
+// to end; CTA c < Cr takes tiles [c W / Cr, (c + 1) W / Cr) with Cr = min(C, W), so
+// no share is empty and
 // every SM streams the same number of key bytes however long the contexts are
 // (an empty share inside a unit's span would be counted as a part of the unit that
 // never arrives). Streaming units (at most S + R keys) are
@@ -17,7 +18,8 @@
 // 1-D bulk copies (cp.async.bulk, completion on the warp's mbarrier). A warp
 // refills a stage as soon as it has finished with it, so no producer warp and no
 // cross-warp hand-off is needed, and each thread keeps up to 255 registers. The
-// 4-bit decode keeps 4 stages per warp and runs two CTAs per SM (128 registers).
+// 4-bit decode gives each warp 32 keys of a 256-key tile, keeps 2 stages per warp and
+// runs two CTAs per SM (128 registers).
 //
 // Inside a warp, LPK lanes share a key row and each owns 16 (or 8) of its dims:
 // 128-bit shared loads, fp32 q pre-scaled by log2(e)/sqrt(D), packed fp32x2 FMAs
