@@ -809,13 +809,16 @@ __global__ void __launch_bounds__(Roles<kMode>::kThreads, 1) prefill_kernel(cons
       // P = exp2(s * scale - m), written over the first 64 columns of S
       const float m_use = m_run == -INFINITY ? 0.f : m_run;
       float2 ls = make_float2(0.f, 0.f);
+      const float2 sl2x2 = make_float2(sl2, sl2), negm2 = make_float2(-m_use, -m_use);
 #pragma unroll
       for (int q4 = 0; q4 < BN / 32; ++q4) {
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const float p0 = ex2_approx(fmaf(v[q4 * 32 + 2 * e], sl2, -m_use));
-          const float p1 = ex2_approx(fmaf(v[q4 * 32 + 2 * e + 1], sl2, -m_use));
+          // s scale - m for a pair of keys in one packed fp32x2 FMA
+          const float2 y = __ffma2_rn(make_float2(v[q4 * 32 + 2 * e], v[q4 * 32 + 2 * e + 1]), sl2x2, negm2);
+          const float p0 = ex2_approx(y.x);
+          const float p1 = ex2_approx(y.y);
           ls = __fadd2_rn(ls, make_float2(p0, p1));
           pk[e] = pack_bf16x2(p0, p1);
         }
