@@ -47,14 +47,14 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 L2_BYTES = 129e6  # GB300 L2 capacity
 
 MEASURED_TRAFFIC = {
-    "prefill": {"src": ("prefill.cu", "duo_device.cuh", "duo_internal.h"), "sha1": "7a442700a6ccf325",
-                "bytes": 471.768e6 + 233.384e6},
+    "prefill": {"src": ("prefill.cu", "duo_device.cuh", "duo_internal.h"), "sha1": "7a550e89e096f3fb",
+                "bytes": 471.982e6 + 233.347e6},
     # the 8 prefill launches of one chunked-prefill step (Llama-2-7B shape, 8 x 4096 tokens)
-    "prefill_chunked": {"src": ("prefill.cu", "duo_device.cuh", "duo_internal.h"), "sha1": "7a442700a6ccf325",
-                        "bytes": 1305.138e6 + 97.829e6},
+    "prefill_chunked": {"src": ("prefill.cu", "duo_device.cuh", "duo_internal.h"), "sha1": "7a550e89e096f3fb",
+                        "bytes": 1305.004e6 + 96.197e6},
     # the same against 4-bit caches (codes + pairs read and dequantized in the kernel)
-    "prefill_chunked_kv4": {"src": ("prefill.cu", "duo_device.cuh", "duo_internal.h"), "sha1": "7a442700a6ccf325",
-                            "bytes": 941.013e6 + 84.869e6},
+    "prefill_chunked_kv4": {"src": ("prefill.cu", "duo_device.cuh", "duo_internal.h"), "sha1": "7a550e89e096f3fb",
+                            "bytes": 940.968e6 + 84.545e6},
     # one decode launch of the batched 8 x 128K workload (device lengths, graph replay)
     "decode_batched": {"src": ("decode.cu", "duo_device.cuh", "duo_internal.h"), "sha1": "4752d2f3b937cdbb",
                        "bytes": 1.081935e9 + 1.504e6},
