@@ -32,9 +32,10 @@
 // state (running max with lazy rescaling: it moves only when a score exceeds it
 // by 2^8, and running sum) is per lane for its head, and p of the other heads is
 // fetched by shuffles for the packed p.v FMAs. With four or more query heads per KV
-// head, and for 4-bit caches, a warp's slice is instead two warp-level tensor-core
-// MMAs (S = Q K^T, then O^T += V^T P^T; see MmaSlice), which takes the per-element
-// FMAs off the CUDA cores that bound those cases.
+// head a warp's slice is instead two warp-level tensor-core MMAs (S = Q K^T, then
+// O^T += V^T P^T; see MmaSlice), which takes the per-element FMAs off the CUDA cores
+// that bound those cases; over 4-bit caches the score product has the keys as its
+// rows (S^T = K Q^T; see Kv4Slice).
 //
 // Merge. The part of a unit a CTA covers ("segment") ends with a cross-warp merge
 // in shared memory. A unit covered by one CTA is written out directly; otherwise
@@ -406,35 +407,25 @@ __device__ __forceinline__ uint32_t and_or(uint32_t x, uint32_t mask, uint32_t m
   return d;
 }
 
-// The per-warp consumer used when the query heads of a KV head are many (and for
-// 4-bit caches): a warp's slice (16 keys; 32 over 4-bit caches, as two 16-key groups)
-// is two tensor-core products per 16 keys instead of one packed FMA per (element, head
-// pair).
+// The per-warp consumer of bf16 caches used when the query heads of a KV head are
+// many: a warp's 16-key slice is two tensor-core products instead of one packed FMA
+// per (element, head pair).
 //   S = Q K^T   rows = the g query heads (rows g ... 15 zero), cols = 8 keys per
 //               n-tile (keys gid and gid + 8 are the columns lane gid loads), k = dims
 //   O^T += V^T P^T   rows = 16 dims per m-tile, cols = the heads, k = the 16 keys
 // The dims inside a k-step may be taken in any order as long as Q and K use the same
 // one, and the rows of O^T in any order as long as the output is written back with
-// it; both orders below are chosen so that each lane reads whole 16-byte (4-byte)
-// pieces of shared memory and needs no shuffles to build its fragments:
-//   bf16 K: k-step 2u + e, k-index 2 tig + i (+ 8) <-> dim 8 (tig + 4u) + 4e + i (+ 2)
-//   4-bit K: lane tig reads code word w = (D / 32) tig + u (dims 8w ... 8w + 7), and
-//     k-step 2u + e, k-index 2 tig + i (+ 8) <-> dim 8w + 2e + 4i (+ 1)
+// it; both orders below are chosen so that each lane reads whole 16-byte pieces of
+// shared memory and needs no shuffles to build its fragments:
+//   K: k-step 2u + e, k-index 2 tig + i (+ 8) <-> dim 8 (tig + 4u) + 4e + i (+ 2)
 //   O^T: m-tile i, row gid (gid + 8) <-> dim (D / 8) gid + 2i (+ 1)
 // After S the softmax of the slice runs in the accumulator layout: lane (gid, tig)
 // holds head gid's scores of keys 2 tig, 2 tig + 1, 2 tig + 8, 2 tig + 9, which are
-// exactly the keys of its P^T fragment. For 4-bit K the magic offsets are folded
-// into one per-head constant (sum of q times the offsets of its dims), removed from
-// each slice's fresh fp32 accumulator; then q.k^ = scale (q.c) + zero sum(q). 4-bit V
-// codes enter as fp16 subnormals, masked out of the word with no offset (c 2^-24 from
-// bits 0-3, c 2^-20 from bits 4-7; exact), so the long-lived O accumulator carries no
-// offset and each output dim comes back with its power of two; p v^ = (p scale) c +
-// p zero with p scale rounded to fp16 and the zero part summed per head in fp32. q goes through fp16 on this path,
-// so its values must lie within the fp16 range (bf16 values there convert exactly).
+// exactly the keys of its P^T fragment.
 // One slice as the consumer sees it: its K and V rows (codes) in shared memory, for
-// 4-bit caches their (scale, zero) pairs, and the bits of keys 2 tig, 2 tig + 1,
-// 2 tig + 8, 2 tig + 9 that hold a visible key (hvalid: the same, cleared on the zero
-// rows gid >= G).
+// 4-bit caches their (scale, zero) pairs, and the bits of the slice's values (key_of
+// of each consumer gives their keys) that hold a visible key (hvalid: the same,
+// cleared on the values of heads >= G).
 struct SliceIn {
   const uint8_t* k;
   const uint8_t* v;
@@ -443,23 +434,21 @@ struct SliceIn {
   uint32_t kvalid, hvalid;
 };
 
-struct NoMma {};  // stands in for MmaSlice in the kernels that do not use it
+struct NoMma {};  // stands in for the warp-MMA consumers in the kernels that do not use them
 
-template <int D, int G, bool KV4>
+template <int D, int G>
 struct MmaSlice {
   static constexpr int KS = D / 16;   // k-steps of S over the dims
   static constexpr int MT = D / 16;   // 16-dim m-tiles of O^T
   static constexpr int DT = D / 8;    // output dims of a lane: DT gid ... DT gid + DT - 1
-  static constexpr int ROW = KV4 ? D / 2 : D * 2;
-  // 4-bit V: p (at most 2^8 under the lazy rescale) times the row scale is stored in
-  // fp16 as p scale 2^-6, so that no row within the fp16 range can overflow it
-  static constexpr float kOScale = KV4 ? 64.f : 1.f;
-  // 4-bit V codes enter the products as fp16 subnormals: even dims c 2^-24, odd dims c 2^-20
-  static constexpr float kVLo = KV4 ? 16777216.f : 1.f, kVHi = KV4 ? 1048576.f : 1.f;
+  static constexpr int ROW = D * 2;   // bytes per row
   uint32_t qa[KS][2];  // a0, a2 of every k-step (a1 = a3 = 0: rows 8 ... 15)
   float o[MT][4];
   float m_run, l_part, qfac;
-  float off, qsum, z_part;  // 4-bit caches
+
+  // value k of a slice (0 ... 3): key 2 tig + k % 2 + 8 (k / 2), head gid
+  __device__ static __forceinline__ int key_of(int k, int, int tig) { return 2 * tig + (k & 1) + 8 * ((k >> 1) & 1); }
+  __device__ static __forceinline__ uint32_t head_mask(uint32_t kvalid, int gid, int) { return gid < G ? kvalid : 0u; }
 
   __device__ __forceinline__ void reset() {
 #pragma unroll
@@ -468,136 +457,54 @@ struct MmaSlice {
       for (int k = 0; k < 4; ++k) o[i][k] = 0.f;
     m_run = -INFINITY;
     l_part = 0.f;
-    z_part = 0.f;
   }
 
   // q row of head gid (nullptr for the zero rows gid >= G) into A fragments; factor is
   // the softmax scale (times the DCA mscale) applied to the fp32 product
   __device__ __forceinline__ void load_q(const uint16_t* qh, float factor, int tig) {
     qfac = factor;
-    if constexpr (!KV4) {
 #pragma unroll
-      for (int u = 0; u < D / 32; ++u) {
-        const uint4 v = qh ? __ldg(reinterpret_cast<const uint4*>(qh + (tig + 4 * u) * 8)) : make_uint4(0, 0, 0, 0);
-        qa[2 * u][0] = v.x;
-        qa[2 * u][1] = v.y;
-        qa[2 * u + 1][0] = v.z;
-        qa[2 * u + 1][1] = v.w;
-      }
-    } else {
-      constexpr int WPT = D / 32;  // code words of a lane per K row
-      float so = 0.f, ss = 0.f;
-#pragma unroll
-      for (int u = 0; u < WPT; ++u) {
-        const int w = WPT * tig + u;
-        const uint4 v = qh ? __ldg(reinterpret_cast<const uint4*>(qh + w * 8)) : make_uint4(0, 0, 0, 0);
-        const uint32_t b[4] = {v.x, v.y, v.z, v.w};
-        float h[8];  // dims 8w ... 8w + 7 rounded to fp16 (exact for bf16 values in its range)
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          h[2 * k] = __half2float(__float2half_rn(bf16lo(b[k])));
-          h[2 * k + 1] = __half2float(__float2half_rn(bf16hi(b[k])));
-        }
-        qa[2 * u][0] = pack_half2(h[0], h[4]);
-        qa[2 * u][1] = pack_half2(h[1], h[5]);
-        qa[2 * u + 1][0] = pack_half2(h[2], h[6]);
-        qa[2 * u + 1][1] = pack_half2(h[3], h[7]);
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          ss += h[k];
-          so = fmaf(h[k], (k & 1) ? 64.f : 1024.f, so);
-        }
-      }
-#pragma unroll
-      for (int m = 1; m <= 2; m <<= 1) {
-        ss += __shfl_xor_sync(0xffffffffu, ss, m);
-        so += __shfl_xor_sync(0xffffffffu, so, m);
-      }
-      qsum = ss;
-      off = so;
+    for (int u = 0; u < D / 32; ++u) {
+      const uint4 v = qh ? __ldg(reinterpret_cast<const uint4*>(qh + (tig + 4 * u) * 8)) : make_uint4(0, 0, 0, 0);
+      qa[2 * u][0] = v.x;
+      qa[2 * u][1] = v.y;
+      qa[2 * u + 1][0] = v.z;
+      qa[2 * u + 1][1] = v.w;
     }
   }
 
-  // One slice: 16 keys (bf16) or 32 keys (4-bit caches, two 16-key groups). kFull:
-  // every key of the slice is a stored, visible key (an interior tile of a retrieval
-  // unit), so no key needs masking; the rows gid >= G then hold finite values for heads
-  // that do not exist, whose columns of O^T are never written out.
-  static constexpr int NGRP = KV4 ? 2 : 1;  // 16-key groups per slice
-  static constexpr int NX = 4 * NGRP;       // scores per lane
+  // One 16-key slice. kFull: every key of the slice is a stored, visible key (an
+  // interior tile of a retrieval unit), so no key needs masking; the rows gid >= G then
+  // hold finite values for heads that do not exist, whose columns of O^T are never
+  // written out.
   template <bool kFull>
   __device__ __forceinline__ void slice(const SliceIn& in, int gid, int tig) {
-    // x[4 q + k]: scores of keys 16 q + 2 tig, + 1, + 8, + 9 (q = the 16-key group)
-    float x[NX];
-    if constexpr (KV4) {
-      float sc[2 * NGRP][4];  // [n-tile][fragment]: the n-tiles are independent chains
+    // x[k]: scores of keys 2 tig, 2 tig + 1, 2 tig + 8, 2 tig + 9
+    float x[4];
+    float sc[2][2][4];  // [n-tile][chain][fragment]: two independent accumulation chains
 #pragma unroll
-      for (int j = 0; j < 2 * NGRP; ++j)
+    for (int j = 0; j < 2; ++j)
 #pragma unroll
-        for (int k = 0; k < 4; ++k) sc[j][k] = 0.f;
-      constexpr int WPT = D / 32;  // code words of a lane per K row
+      for (int c = 0; c < 2; ++c)
 #pragma unroll
-      for (int j = 0; j < 2 * NGRP; ++j) {
-        // lane tig: words WPT tig ... of row gid + 8 j
-        uint32_t w[WPT];
-        const uint8_t* row = in.k + (gid + 8 * j) * ROW;
-        if constexpr (WPT == 4) {
-          const uint4 v = *reinterpret_cast<const uint4*>(row + tig * 16);
-          w[0] = v.x;
-          w[1] = v.y;
-          w[2] = v.z;
-          w[3] = v.w;
-        } else {
-          const uint2 v = *reinterpret_cast<const uint2*>(row + tig * 8);
-          w[0] = v.x;
-          w[1] = v.y;
-        }
+        for (int k = 0; k < 4; ++k) sc[j][c][k] = 0.f;
 #pragma unroll
-        for (int u = 0; u < WPT; ++u) {
-          const uint32_t xw = w[u], x8 = xw >> 8;
-          mma16816<true>(sc[j], qa[2 * u][0], 0u, qa[2 * u][1], 0u, and_or(xw, 0x000F000Fu, kLoMagic),
-                         and_or(xw, 0x00F000F0u, kHiMagic));
-          mma16816<true>(sc[j], qa[2 * u + 1][0], 0u, qa[2 * u + 1][1], 0u, and_or(x8, 0x000F000Fu, kLoMagic),
-                         and_or(x8, 0x00F000F0u, kHiMagic));
-        }
+    for (int j = 0; j < 2; ++j) {
+      const uint8_t* row = in.k + (gid + 8 * j) * ROW;
+#pragma unroll
+      for (int u = 0; u < D / 32; ++u) {
+        const uint4 v = *reinterpret_cast<const uint4*>(row + (tig + 4 * u) * 16);
+        mma16816<false>(sc[j][u & 1], qa[2 * u][0], 0u, qa[2 * u][1], 0u, v.x, v.y);
+        mma16816<false>(sc[j][u & 1], qa[2 * u + 1][0], 0u, qa[2 * u + 1][1], 0u, v.z, v.w);
       }
-#pragma unroll
-      for (int q = 0; q < NGRP; ++q) {
-        const uint2 z01 = *reinterpret_cast<const uint2*>(in.kz + 64 * q + tig * 8);
-        const uint2 z89 = *reinterpret_cast<const uint2*>(in.kz + 64 * q + 32 + tig * 8);
-        const uint32_t zz[4] = {z01.x, z01.y, z89.x, z89.y};
-        const float raw[4] = {sc[2 * q][0], sc[2 * q][1], sc[2 * q + 1][0], sc[2 * q + 1][1]};
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const float2 sz = scale_zero(zz[k]);
-          x[4 * q + k] = fmaf(sz.x, raw[k] - off, sz.y * qsum);
-        }
-      }
-    } else {
-      float sc[2][2][4];  // [n-tile][chain][fragment]: two independent accumulation chains
-#pragma unroll
-      for (int j = 0; j < 2; ++j)
-#pragma unroll
-        for (int c = 0; c < 2; ++c)
-#pragma unroll
-          for (int k = 0; k < 4; ++k) sc[j][c][k] = 0.f;
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const uint8_t* row = in.k + (gid + 8 * j) * ROW;
-#pragma unroll
-        for (int u = 0; u < D / 32; ++u) {
-          const uint4 v = *reinterpret_cast<const uint4*>(row + (tig + 4 * u) * 16);
-          mma16816<false>(sc[j][u & 1], qa[2 * u][0], 0u, qa[2 * u][1], 0u, v.x, v.y);
-          mma16816<false>(sc[j][u & 1], qa[2 * u + 1][0], 0u, qa[2 * u + 1][1], 0u, v.z, v.w);
-        }
-      }
-      x[0] = sc[0][0][0] + sc[0][1][0];
-      x[1] = sc[0][0][1] + sc[0][1][1];
-      x[2] = sc[1][0][0] + sc[1][1][0];
-      x[3] = sc[1][0][1] + sc[1][1][1];
     }
+    x[0] = sc[0][0][0] + sc[0][1][0];
+    x[1] = sc[0][0][1] + sc[0][1][1];
+    x[2] = sc[1][0][0] + sc[1][1][0];
+    x[3] = sc[1][0][1] + sc[1][1][1];
     float mx = -INFINITY;
 #pragma unroll
-    for (int k = 0; k < NX; ++k) {
+    for (int k = 0; k < 4; ++k) {
       x[k] = (kFull || ((in.hvalid >> k) & 1u)) ? x[k] * qfac : -INFINITY;
       mx = fmaxf(mx, x[k]);
     }
@@ -609,7 +516,6 @@ struct MmaSlice {
       if (grow) {
         m_run = mx;
         l_part *= f;
-        if constexpr (KV4) z_part *= f;
       }
       const float f0 = __shfl_sync(0xffffffffu, f, 8 * tig);      // head 2 tig
       const float f1 = __shfl_sync(0xffffffffu, f, 8 * tig + 4);  // head 2 tig + 1
@@ -621,75 +527,32 @@ struct MmaSlice {
         o[i][3] *= f1;
       }
     }
-    if constexpr (KV4) {
-      // p of a group is computed next to its use, so only its four values are live
+    float pr[4];
 #pragma unroll
-      for (int q = 0; q < NGRP; ++q) {
-        const uint2 z01 = *reinterpret_cast<const uint2*>(in.vz + 64 * q + tig * 8);
-        const uint2 z89 = *reinterpret_cast<const uint2*>(in.vz + 64 * q + 32 + tig * 8);
-        const uint32_t zz[4] = {z01.x, z01.y, z89.x, z89.y};
-        float b[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const float2 sz = scale_zero(zz[k]);
-          const bool ok = kFull || ((in.hvalid >> (4 * q + k)) & 1u);  // an unused row's pair may be anything
-          const float pk = ok ? ex2_approx(x[4 * q + k] - m_run) : 0.f;
-          l_part += pk;
-          b[k] = ok ? pk * (sz.x * (1.f / kOScale)) : 0.f;
-          z_part += ok ? pk * sz.y : 0.f;
-        }
-        const uint32_t pb0 = pack_half2(b[0], b[1]);
-        const uint32_t pb1 = pack_half2(b[2], b[3]);
-        // V codes in fragment order (see the 4-bit append): in group q, the lane's word i
-        // holds, for its dims of m-tile i, the codes of keys 2 tig, 2 tig + 8, 2 tig + 1,
-        // 2 tig + 9
-        uint32_t w[MT];
-#pragma unroll
-        for (int c = 0; c < MT / 4; ++c) {
-          const uint4 v = *reinterpret_cast<const uint4*>(in.v + 16 * ROW * q + (4 * gid + tig) * MT * 4 + 16 * c);
-          w[4 * c] = v.x;
-          w[4 * c + 1] = v.y;
-          w[4 * c + 2] = v.z;
-          w[4 * c + 3] = v.w;
-        }
-#pragma unroll
-        for (int i = 0; i < MT; ++i) {
-          const uint32_t x8 = w[i] >> 8;
-          // the codes as fp16 subnormals, exact with no offset: c 2^-24 (bits 0-3, rows
-          // gid: even dims) and c 2^-20 (bits 4-7, rows gid + 8: odd dims); the powers of
-          // two come off per output dim in write()
-          mma16816<true>(o[i], w[i] & 0x000F000Fu, w[i] & 0x00F000F0u, x8 & 0x000F000Fu, x8 & 0x00F000F0u, pb0,
-                         pb1);
-        }
-      }
-    } else {
-      float pr[NX];
-#pragma unroll
-      for (int k = 0; k < NX; ++k) {
-        pr[k] = (kFull || ((in.hvalid >> k) & 1u)) ? ex2_approx(x[k] - m_run) : 0.f;
-        l_part += pr[k];
-      }
-      const int kr[4] = {2 * tig, 2 * tig + 1, 2 * tig + 8, 2 * tig + 9};
-      const uint32_t pb0 = pack_bf16x2(pr[0], pr[1]);
-      const uint32_t pb1 = pack_bf16x2(pr[2], pr[3]);
-      uint32_t w[4][MT];  // MT words = this lane's DT dims of each key
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const bool ok = kFull || ((in.kvalid >> k) & 1u);  // rows not copied in this stage may hold anything
-#pragma unroll
-        for (int c = 0; c < MT / 4; ++c) {
-          const uint4 v = *reinterpret_cast<const uint4*>(in.v + kr[k] * ROW + DT * 2 * gid + c * 16);
-          w[k][4 * c] = ok ? v.x : 0u;
-          w[k][4 * c + 1] = ok ? v.y : 0u;
-          w[k][4 * c + 2] = ok ? v.z : 0u;
-          w[k][4 * c + 3] = ok ? v.w : 0u;
-        }
-      }
-#pragma unroll
-      for (int i = 0; i < MT; ++i)
-        mma16816<false>(o[i], __byte_perm(w[0][i], w[1][i], 0x5410), __byte_perm(w[0][i], w[1][i], 0x7632),
-                        __byte_perm(w[2][i], w[3][i], 0x5410), __byte_perm(w[2][i], w[3][i], 0x7632), pb0, pb1);
+    for (int k = 0; k < 4; ++k) {
+      pr[k] = (kFull || ((in.hvalid >> k) & 1u)) ? ex2_approx(x[k] - m_run) : 0.f;
+      l_part += pr[k];
     }
+    const int kr[4] = {2 * tig, 2 * tig + 1, 2 * tig + 8, 2 * tig + 9};
+    const uint32_t pb0 = pack_bf16x2(pr[0], pr[1]);
+    const uint32_t pb1 = pack_bf16x2(pr[2], pr[3]);
+    uint32_t w[4][MT];  // MT words = this lane's DT dims of each key
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const bool ok = kFull || ((in.kvalid >> k) & 1u);  // rows not copied in this stage may hold anything
+#pragma unroll
+      for (int c = 0; c < MT / 4; ++c) {
+        const uint4 v = *reinterpret_cast<const uint4*>(in.v + kr[k] * ROW + DT * 2 * gid + c * 16);
+        w[k][4 * c] = ok ? v.x : 0u;
+        w[k][4 * c + 1] = ok ? v.y : 0u;
+        w[k][4 * c + 2] = ok ? v.z : 0u;
+        w[k][4 * c + 3] = ok ? v.w : 0u;
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < MT; ++i)
+      mma16816<false>(o[i], __byte_perm(w[0][i], w[1][i], 0x5410), __byte_perm(w[0][i], w[1][i], 0x7632),
+                      __byte_perm(w[2][i], w[3][i], 0x5410), __byte_perm(w[2][i], w[3][i], 0x7632), pb0, pb1);
   }
 
   // The warp's (o, max, sum) per head into the reduction buffer, as the CUDA-core path
@@ -698,13 +561,264 @@ struct MmaSlice {
     float l = l_part;
     l += __shfl_xor_sync(0xffffffffu, l, 1);
     l += __shfl_xor_sync(0xffffffffu, l, 2);
-    float z0 = 0.f, z1 = 0.f;
-    if constexpr (KV4) {
-      float z = z_part;
-      z += __shfl_xor_sync(0xffffffffu, z, 1);
-      z += __shfl_xor_sync(0xffffffffu, z, 2);
-      z0 = __shfl_sync(0xffffffffu, z, 8 * tig);
-      z1 = __shfl_sync(0xffffffffu, z, 8 * tig + 4);
+    const int h0 = 2 * tig, h1 = 2 * tig + 1;
+#pragma unroll
+    for (int i = 0; i < MT; ++i) {
+      const int d = DT * gid + 2 * i;
+      if (h0 < G) {
+        float* r = red + (warp * G + h0) * (D + 2) + d;
+        r[0] = o[i][0];
+        r[1] = o[i][2];
+      }
+      if (h1 < G) {
+        float* r = red + (warp * G + h1) * (D + 2) + d;
+        r[0] = o[i][1];
+        r[1] = o[i][3];
+      }
+    }
+    if (tig == 0 && gid < G) {
+      float* r = red + (warp * G + gid) * (D + 2);
+      r[D] = m_run;
+      r[D + 1] = l;
+    }
+  }
+};
+
+// 8x8 transpose of a b16 matrix held in fragment layout (lane 4 gid + tig holds row
+// gid, cols 2 tig and 2 tig + 1); afterwards the lane holds row gid of the transpose.
+__device__ __forceinline__ uint32_t transpose8x8(uint32_t m) {
+  uint32_t d;
+  asm("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(m));
+  return d;
+}
+
+// The consumer over 4-bit caches: a warp's slice is 32 keys, two 16-key groups, and
+// the score product has the keys, not the heads, as its rows:
+//   S^T = K Q^T   rows = the 16 keys of a group, cols = the query heads (8 columns, g
+//                 of them real), k = dims
+//   O^T += V^T P^T   rows = 16 dims per m-tile, cols = the heads, k = the 16 keys
+// The K codes form the A fragments: lane (gid, tig) reads code words w = (D / 32) tig
+// + u (dims 8w ... 8w + 7) of keys 16 q + gid and 16 q + gid + 8, with k-step 2u + e,
+// k-index 2 tig + i (+ 8) <-> dim 8w + 2e + 4i (+ 1); q, rounded to fp16, forms the B
+// fragments in the same order. That is sixteen products per 32 keys, none spent on
+// zero rows, and no zero registers beside q. The codes become fp16 by bit placement
+// (kLoMagic, kHiMagic); their offsets are folded into one constant per head (sum of q
+// times the offsets of its dims), removed from each slice's fresh fp32 accumulator, so
+// that q.k^ = scale (q.c) + zero sum(q). Lane (gid, tig) then holds the scores of keys
+// gid and gid + 8 of each group for heads 2 tig and 2 tig + 1: the running max, sum and
+// zero sum of those two heads live in the lane, and the rescale of its O^T columns (the
+// same two heads) needs no shuffle. P^T is made from the scores with one 8x8 transpose
+// per 8 keys. The V codes enter as fp16 subnormals, masked out of the word with no
+// offset (c 2^-24 from bits 0-3, c 2^-20 from bits 4-7; exact), so the long-lived O
+// accumulator carries no offset and each output dim comes back with its power of two
+// (O^T rows as in MmaSlice); p v^ = (p scale) c + p zero with p scale rounded to fp16
+// and the zero part summed per head in fp32. q goes through fp16 on this path, so its
+// values must lie within the fp16 range (bf16 values there convert exactly).
+template <int D, int G>
+struct Kv4Slice {
+  static constexpr int KS = D / 16;  // k-steps of S over the dims
+  static constexpr int MT = D / 16;  // 16-dim m-tiles of O^T
+  static constexpr int DT = D / 8;   // output dims of a lane: DT gid ... DT gid + DT - 1
+  static constexpr int ROW = D / 2;  // code bytes per row
+  static constexpr int WPT = D / 32;  // code words of a lane per K row
+  static constexpr int NGRP = 2;     // 16-key groups per 32-key slice
+  static constexpr float kOScale = 64.f, kVLo = 16777216.f, kVHi = 1048576.f;
+  uint32_t qb[KS][2];  // b0, b1 of every k-step: head gid's q at k-indices 2 tig (+1), 2 tig + 8 (+9)
+  float o[MT][4];
+  float m_run[2], l_part[2], z_part[2];  // heads 2 tig, 2 tig + 1
+  float off[2], qsum[2];                 // their folded offsets and sums of q
+  float qfac;
+
+  // value k of a slice (0 ... 7): key 16 (k / 4) + gid + 8 ((k / 2) % 2), head 2 tig + k % 2
+  __device__ static __forceinline__ int key_of(int k, int gid, int) { return 16 * (k >> 2) + gid + 8 * ((k >> 1) & 1); }
+  __device__ static __forceinline__ uint32_t head_mask(uint32_t kvalid, int, int tig) {
+    return kvalid & ((2 * tig < G ? 0x55u : 0u) | (2 * tig + 1 < G ? 0xAAu : 0u));
+  }
+
+  __device__ __forceinline__ void reset() {
+#pragma unroll
+    for (int i = 0; i < MT; ++i)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) o[i][k] = 0.f;
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      m_run[e] = -INFINITY;
+      l_part[e] = 0.f;
+      z_part[e] = 0.f;
+    }
+  }
+
+  // q row of head gid (nullptr for the heads gid >= G) into B fragments, rounded to fp16
+  __device__ __forceinline__ void load_q(const uint16_t* qh, float factor, int tig) {
+    qfac = factor;
+    float so = 0.f, ss = 0.f;
+#pragma unroll
+    for (int u = 0; u < WPT; ++u) {
+      const int w = WPT * tig + u;
+      const uint4 v = qh ? __ldg(reinterpret_cast<const uint4*>(qh + w * 8)) : make_uint4(0, 0, 0, 0);
+      const uint32_t b[4] = {v.x, v.y, v.z, v.w};
+      float h[8];  // dims 8w ... 8w + 7 rounded to fp16 (exact for bf16 values in its range)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        h[2 * k] = __half2float(__float2half_rn(bf16lo(b[k])));
+        h[2 * k + 1] = __half2float(__float2half_rn(bf16hi(b[k])));
+      }
+      qb[2 * u][0] = pack_half2(h[0], h[4]);
+      qb[2 * u][1] = pack_half2(h[1], h[5]);
+      qb[2 * u + 1][0] = pack_half2(h[2], h[6]);
+      qb[2 * u + 1][1] = pack_half2(h[3], h[7]);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        ss += h[k];
+        so = fmaf(h[k], (k & 1) ? 64.f : 1024.f, so);
+      }
+    }
+#pragma unroll
+    for (int m = 1; m <= 2; m <<= 1) {
+      ss += __shfl_xor_sync(0xffffffffu, ss, m);
+      so += __shfl_xor_sync(0xffffffffu, so, m);
+    }
+    // lanes 4 h hold head h's sums; this lane wants heads 2 tig and 2 tig + 1
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      off[e] = __shfl_sync(0xffffffffu, so, 4 * (2 * tig + e));
+      qsum[e] = __shfl_sync(0xffffffffu, ss, 4 * (2 * tig + e));
+    }
+  }
+
+  // One 32-key slice (two 16-key groups). kFull: every key is a stored, visible key of
+  // an interior tile; the columns of heads >= G then hold finite values never written out.
+  template <bool kFull>
+  __device__ __forceinline__ void slice(const SliceIn& in, int gid, int tig) {
+    // x[4 q + k]: (key a, head 2 tig), (a, 2 tig + 1), (key b, 2 tig), (b, 2 tig + 1)
+    // with a = 16 q + gid, b = a + 8
+    float x[4 * NGRP];
+#pragma unroll
+    for (int q = 0; q < NGRP; ++q) {
+      float sc[2][4];  // even and odd k-steps: two independent accumulation chains
+#pragma unroll
+      for (int c = 0; c < 2; ++c)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) sc[c][k] = 0.f;
+      uint32_t wa[WPT], wb[WPT];  // lane tig: words WPT tig ... of rows a and b
+      const uint8_t* ra = in.k + (16 * q + gid) * ROW;
+      const uint8_t* rb = ra + 8 * ROW;
+      if constexpr (WPT == 4) {
+        const uint4 va = *reinterpret_cast<const uint4*>(ra + tig * 16);
+        const uint4 vb = *reinterpret_cast<const uint4*>(rb + tig * 16);
+        wa[0] = va.x, wa[1] = va.y, wa[2] = va.z, wa[3] = va.w;
+        wb[0] = vb.x, wb[1] = vb.y, wb[2] = vb.z, wb[3] = vb.w;
+      } else {
+        const uint2 va = *reinterpret_cast<const uint2*>(ra + tig * 8);
+        const uint2 vb = *reinterpret_cast<const uint2*>(rb + tig * 8);
+        wa[0] = va.x, wa[1] = va.y;
+        wb[0] = vb.x, wb[1] = vb.y;
+      }
+#pragma unroll
+      for (int u = 0; u < WPT; ++u) {
+        const uint32_t xa = wa[u], xb = wb[u], xa8 = xa >> 8, xb8 = xb >> 8;
+        mma16816<true>(sc[0], and_or(xa, 0x000F000Fu, kLoMagic), and_or(xb, 0x000F000Fu, kLoMagic),
+                       and_or(xa, 0x00F000F0u, kHiMagic), and_or(xb, 0x00F000F0u, kHiMagic), qb[2 * u][0],
+                       qb[2 * u][1]);
+        mma16816<true>(sc[1], and_or(xa8, 0x000F000Fu, kLoMagic), and_or(xb8, 0x000F000Fu, kLoMagic),
+                       and_or(xa8, 0x00F000F0u, kHiMagic), and_or(xb8, 0x00F000F0u, kHiMagic), qb[2 * u + 1][0],
+                       qb[2 * u + 1][1]);
+      }
+      const float2 sa = scale_zero(*reinterpret_cast<const uint32_t*>(in.kz + 4 * (16 * q + gid)));
+      const float2 sb = scale_zero(*reinterpret_cast<const uint32_t*>(in.kz + 4 * (16 * q + 8 + gid)));
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float2 sz = (k & 2) ? sb : sa;
+        const int e = k & 1;
+        x[4 * q + k] = fmaf(sz.x, (sc[0][k] + sc[1][k]) - off[e], sz.y * qsum[e]);
+      }
+    }
+    // per head: max over the lane's keys, then over the eight row groups
+    float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+    for (int k = 0; k < 4 * NGRP; ++k) {
+      x[k] = (kFull || ((in.hvalid >> k) & 1u)) ? x[k] * qfac : -INFINITY;
+      mx[k & 1] = fmaxf(mx[k & 1], x[k]);
+    }
+#pragma unroll
+    for (int s = 4; s < 32; s <<= 1)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) mx[e] = fmaxf(mx[e], __shfl_xor_sync(0xffffffffu, mx[e], s));
+    const bool g0 = mx[0] > m_run[0] + 8.f, g1 = mx[1] > m_run[1] + 8.f;  // lazy rescale
+    if (__any_sync(0xffffffffu, g0 || g1)) {
+      const float f0 = g0 ? ex2_approx(m_run[0] - mx[0]) : 1.f;
+      const float f1 = g1 ? ex2_approx(m_run[1] - mx[1]) : 1.f;
+      if (g0) {
+        m_run[0] = mx[0];
+        l_part[0] *= f0;
+        z_part[0] *= f0;
+      }
+      if (g1) {
+        m_run[1] = mx[1];
+        l_part[1] *= f1;
+        z_part[1] *= f1;
+      }
+#pragma unroll
+      for (int i = 0; i < MT; ++i) {
+        o[i][0] *= f0;
+        o[i][1] *= f1;
+        o[i][2] *= f0;
+        o[i][3] *= f1;
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < NGRP; ++q) {
+      const float2 va = scale_zero(*reinterpret_cast<const uint32_t*>(in.vz + 4 * (16 * q + gid)));
+      const float2 vb = scale_zero(*reinterpret_cast<const uint32_t*>(in.vz + 4 * (16 * q + 8 + gid)));
+      float b[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float2 sz = (k & 2) ? vb : va;
+        const int e = k & 1;
+        const bool ok = kFull || ((in.hvalid >> (4 * q + k)) & 1u);  // an unused row's pair may be anything
+        const float pk = ok ? ex2_approx(x[4 * q + k] - m_run[e]) : 0.f;
+        l_part[e] += pk;
+        b[k] = ok ? pk * (sz.x * (1.f / kOScale)) : 0.f;
+        z_part[e] += ok ? pk * sz.y : 0.f;
+      }
+      // [key][head] rows a and b, transposed to P^T's fragments: keys 2 tig (+1), 2 tig + 8 (+9) of head gid
+      const uint32_t pb0 = transpose8x8(pack_half2(b[0], b[1]));
+      const uint32_t pb1 = transpose8x8(pack_half2(b[2], b[3]));
+      // V codes in fragment order (see the 4-bit append): in group q, the lane's word i
+      // holds, for its dims of m-tile i, the codes of keys 2 tig, 2 tig + 8, 2 tig + 1,
+      // 2 tig + 9
+      uint32_t w[MT];
+#pragma unroll
+      for (int c = 0; c < MT / 4; ++c) {
+        const uint4 v = *reinterpret_cast<const uint4*>(in.v + 16 * ROW * q + (4 * gid + tig) * MT * 4 + 16 * c);
+        w[4 * c] = v.x;
+        w[4 * c + 1] = v.y;
+        w[4 * c + 2] = v.z;
+        w[4 * c + 3] = v.w;
+      }
+#pragma unroll
+      for (int i = 0; i < MT; ++i) {
+        const uint32_t x8 = w[i] >> 8;
+        // the codes as fp16 subnormals: c 2^-24 (bits 0-3) and c 2^-20 (bits 4-7)
+        mma16816<true>(o[i], w[i] & 0x000F000Fu, w[i] & 0x00F000F0u, x8 & 0x000F000Fu, x8 & 0x00F000F0u, pb0,
+                       pb1);
+      }
+    }
+  }
+
+  // The warp's (o, max, sum) per head into the reduction buffer: red[(warp G + h) (D + 2)
+  // + d], then max and sum at D and D + 1.
+  __device__ __forceinline__ void write(float* red, int warp, int gid, int tig) {
+    float l[2], z[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      l[e] = l_part[e];
+      z[e] = z_part[e];
+#pragma unroll
+      for (int s = 4; s < 32; s <<= 1) {
+        l[e] += __shfl_xor_sync(0xffffffffu, l[e], s);
+        z[e] += __shfl_xor_sync(0xffffffffu, z[e], s);
+      }
     }
     const int h0 = 2 * tig, h1 = 2 * tig + 1;
 #pragma unroll
@@ -712,19 +826,23 @@ struct MmaSlice {
       const int d = DT * gid + 2 * i;
       if (h0 < G) {
         float* r = red + (warp * G + h0) * (D + 2) + d;
-        r[0] = fmaf(o[i][0], kOScale * kVLo, z0);
-        r[1] = fmaf(o[i][2], kOScale * kVHi, z0);
+        r[0] = fmaf(o[i][0], kOScale * kVLo, z[0]);
+        r[1] = fmaf(o[i][2], kOScale * kVHi, z[0]);
       }
       if (h1 < G) {
         float* r = red + (warp * G + h1) * (D + 2) + d;
-        r[0] = fmaf(o[i][1], kOScale * kVLo, z1);
-        r[1] = fmaf(o[i][3], kOScale * kVHi, z1);
+        r[0] = fmaf(o[i][1], kOScale * kVLo, z[1]);
+        r[1] = fmaf(o[i][3], kOScale * kVHi, z[1]);
       }
     }
-    if (tig == 0 && gid < G) {
-      float* r = red + (warp * G + gid) * (D + 2);
-      r[D] = m_run;
-      r[D + 1] = l;
+    if (gid == 0) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e)
+        if (2 * tig + e < G) {
+          float* r = red + (warp * G + 2 * tig + e) * (D + 2);
+          r[D] = m_run[e];
+          r[D + 1] = l[e];
+        }
     }
   }
 };
@@ -798,7 +916,8 @@ __global__ void __launch_bounds__(kThreads, is_kv4_mode(kMode) ? kDecodeCtasPerS
   const int hme = cl >> (C::LB - C::GB);  // the head this lane ends up owning
   constexpr bool kMma = is_kv4_mode(kMode) || G >= kMmaMinG;
   const int gid = lane >> 2, tig = lane & 3;  // tensor-core slices: fragment row group, thread in group
-  std::conditional_t<kMma, MmaSlice<D, G, is_kv4_mode(kMode)>, NoMma> mm;
+  using Mma = std::conditional_t<is_kv4_mode(kMode), Kv4Slice<D, G>, MmaSlice<D, G>>;
+  std::conditional_t<kMma, Mma, NoMma> mm;
   const int SR = p.sh.S + p.sh.R;
   WarpSync ws{segbar, 0};
   uint32_t j = 0;  // tiles consumed
@@ -902,7 +1021,7 @@ __global__ void __launch_bounds__(kThreads, is_kv4_mode(kMode) ? kDecodeCtasPerS
           kvalid = 0u;
 #pragma unroll
           for (int k = 0; k < NK; ++k) {
-            const int key = 16 * (k >> 2) + 2 * tig + (k & 1) + 8 * ((k >> 1) & 1);
+            const int key = Mma::key_of(k, gid, tig);
             bool valid = key < rows;
             if (x.streaming && valid) {
               const int64_t slot = kt * C::TK + (int64_t)warp * C::KPW + key;
@@ -912,7 +1031,7 @@ __global__ void __launch_bounds__(kThreads, is_kv4_mode(kMode) ? kDecodeCtasPerS
             kvalid |= (uint32_t)valid << k;
           }
         }
-        const SliceIn in{sk, sv, sk + 2 * C::SLICE, sk + 2 * C::SLICE + C::PSLICE, kvalid, gid < G ? kvalid : 0u};
+        const SliceIn in{sk, sv, sk + 2 * C::SLICE, sk + 2 * C::SLICE + C::PSLICE, kvalid, Mma::head_mask(kvalid, gid, tig)};
         if (full_tile)
           mm.template slice<true>(in, gid, tig);
         else
