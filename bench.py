@@ -42,8 +42,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from the ncu
-# captures summarised in profiles/, valid only for the kernel sources they were taken on
-# (the decode records were re-keyed after an edit to the decode file's header comment only).
+# captures summarised in profiles/, valid only for the kernel sources they were taken on.
 L2_BYTES = 129e6  # GB300 L2 capacity
 
 MEASURED_TRAFFIC = {
@@ -56,10 +55,13 @@ MEASURED_TRAFFIC = {
     "prefill_chunked_kv4": {"src": ("prefill.cu", "duo_device.cuh", "duo_internal.h"), "sha1": "7a550e89e096f3fb",
                             "bytes": 940.968e6 + 84.545e6},
     # one decode launch of the batched 8 x 128K workload (device lengths, graph replay)
-    "decode_batched": {"src": ("decode.cu", "duo_device.cuh", "duo_internal.h"), "sha1": "4752d2f3b937cdbb",
-                       "bytes": 1.081935e9 + 1.504e6},
-    "decode": {"src": ("decode.cu", "duo_device.cuh", "duo_internal.h"), "sha1": "4752d2f3b937cdbb",
-               "bytes": 1.074806e9 + 1.440e6},
+    "decode_batched": {"src": ("decode.cu", "duo_device.cuh", "duo_internal.h"), "sha1": "1ba35154262e6cb8",
+                       "bytes": 1.081919e9 + 1.479e6},
+    "decode": {"src": ("decode.cu", "duo_device.cuh", "duo_internal.h"), "sha1": "1ba35154262e6cb8",
+               "bytes": 1.074810e9 + 1.485e6},
+    # one decode launch of the million-token decode over 4-bit caches (stored bytes read)
+    "decode_kv4": {"src": ("decode.cu", "duo_device.cuh", "duo_internal.h"), "sha1": "1ba35154262e6cb8",
+                   "bytes": 285.598976e6 + 3.443456e6},
 }
 
 
@@ -477,7 +479,7 @@ def bench_decode(w, steps_cap, peaks, paged_block=0, pool=False, kv4=False):
             "gpu_launches": 3 * steps,
             "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(gbs / peak, 4),
-                         "traffic": None if (kv4 or paged_block) else measured_traffic("decode"),
+                         "traffic": None if paged_block else measured_traffic("decode_kv4" if kv4 else "decode"),
                          "kernel": f"decode_kernel<{w.D},{w.Hq // w.Hkv},"
                                    f"{('kv4' if kv4 else 'plain') + (' paged' if paged_block else '')}>"},
             "tokens_per_s": round(1e3 / (sum(times) / len(times)), 1), "clocks": clk}
