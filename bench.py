@@ -42,7 +42,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from the ncu
-# captures summarised in profiles/, valid only for the kernel sources they were taken on.
+# captures summarised in profiles/, valid only for the kernel sources they were taken on
+# (the decode records were re-keyed after a comment-only edit to the 4-bit consumer).
 L2_BYTES = 129e6  # GB300 L2 capacity
 
 MEASURED_TRAFFIC = {
@@ -55,12 +56,12 @@ MEASURED_TRAFFIC = {
     "prefill_chunked_kv4": {"src": ("prefill.cu", "duo_device.cuh", "duo_internal.h"), "sha1": "7a550e89e096f3fb",
                             "bytes": 940.968e6 + 84.545e6},
     # one decode launch of the batched 8 x 128K workload (device lengths, graph replay)
-    "decode_batched": {"src": ("decode.cu", "duo_device.cuh", "duo_internal.h"), "sha1": "1ba35154262e6cb8",
+    "decode_batched": {"src": ("decode.cu", "duo_device.cuh", "duo_internal.h"), "sha1": "2a2b52e1174c6bc6",
                        "bytes": 1.081919e9 + 1.479e6},
-    "decode": {"src": ("decode.cu", "duo_device.cuh", "duo_internal.h"), "sha1": "1ba35154262e6cb8",
+    "decode": {"src": ("decode.cu", "duo_device.cuh", "duo_internal.h"), "sha1": "2a2b52e1174c6bc6",
                "bytes": 1.074810e9 + 1.485e6},
     # one decode launch of the million-token decode over 4-bit caches (stored bytes read)
-    "decode_kv4": {"src": ("decode.cu", "duo_device.cuh", "duo_internal.h"), "sha1": "1ba35154262e6cb8",
+    "decode_kv4": {"src": ("decode.cu", "duo_device.cuh", "duo_internal.h"), "sha1": "2a2b52e1174c6bc6",
                    "bytes": 285.598976e6 + 3.443456e6},
 }
 

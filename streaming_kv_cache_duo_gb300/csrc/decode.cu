@@ -622,6 +622,9 @@ struct Kv4Slice {
   static constexpr int ROW = D / 2;  // code bytes per row
   static constexpr int WPT = D / 32;  // code words of a lane per K row
   static constexpr int NGRP = 2;     // 16-key groups per 32-key slice
+  // p (at most 2^8 under the lazy rescale) times the row scale enters the V product in
+  // fp16 as p scale 2^-6, so that no row within the fp16 range can overflow it; the V
+  // codes enter as subnormals, c 2^-24 (even dims) and c 2^-20 (odd dims)
   static constexpr float kOScale = 64.f, kVLo = 16777216.f, kVHi = 1048576.f;
   uint32_t qb[KS][2];  // b0, b1 of every k-step: head gid's q at k-indices 2 tig (+1), 2 tig + 8 (+9)
   float o[MT][4];
